@@ -1,0 +1,337 @@
+"""Pins for the CPU oracle (no GPU).
+
+Each test checks the oracle against something other than itself: an exhaustive
+enumeration, a library routine (torch float64 softmax / matmul, NumPy indexing),
+a closed form, or an independent restatement of the quantiser with NumPy's own
+primitives.  A plausible slip in the oracle (wrong head group, dropped scale,
+transposed operand, wrong slot arithmetic, wrong rounding) fails at least one.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+
+BS = 16
+
+
+# ------------------------------------------------------------ 16-bit widening
+def test_f16_widening_exhaustive():
+    bits = np.arange(1 << 16, dtype=np.uint16)
+    ref = bits.view(np.float16).astype(np.float64)
+    got = np.array([oracle.f16_to_f64(int(b)) for b in bits])
+    both_nan = np.isnan(ref) & np.isnan(got)
+    assert np.all(both_nan | (ref == got))
+    assert np.array_equal(np.signbit(ref[~np.isnan(ref)]), np.signbit(got[~np.isnan(got)]))
+
+
+def test_bf16_widening_exhaustive():
+    bits = torch.arange(1 << 16, dtype=torch.int32).to(torch.int16)
+    ref = bits.view(torch.bfloat16).to(torch.float64).numpy()
+    got = np.array([oracle.bf16_to_f64(int(b) & 0xFFFF) for b in bits.tolist()])
+    both_nan = np.isnan(ref) & np.isnan(got)
+    assert np.all(both_nan | (ref == got))
+
+
+# ------------------------------------------------------------ attention helpers
+def _paged_from_dense(K, V, lens, num_blocks, seed, fill=float("nan")):
+    """Place dense per-request K/V [B, Hkv, n, D] into a pool through a random
+    block table using NumPy-style indexing (independent of the oracle)."""
+    B, Hkv, nmax, D = K.shape
+    g = torch.Generator().manual_seed(seed)
+    nblk = [-(-n // BS) for n in lens]
+    perm = torch.randperm(num_blocks, generator=g)
+    mb = max(1, max(nblk))
+    tables = torch.full((B, mb), -1, dtype=torch.int32)
+    kp = torch.full((num_blocks, Hkv, BS, D), fill, dtype=K.dtype)
+    vp = torch.full((num_blocks, Hkv, BS, D), fill, dtype=V.dtype)
+    at = 0
+    for b in range(B):
+        blocks = perm[at:at + nblk[b]]
+        at += nblk[b]
+        tables[b, :nblk[b]] = blocks.to(torch.int32)
+        for i in range(lens[b]):
+            kp[blocks[i // BS], :, i % BS, :] = K[b, :, i, :]
+            vp[blocks[i // BS], :, i % BS, :] = V[b, :, i, :]
+    return kp, vp, tables
+
+
+def _dense_reference(q, K, V, lens, scale):
+    """torch float64: softmax(q K^T scale) V per request, K/V heads repeated
+    for the query-head groups (library routines only)."""
+    B, Hq, D = q.shape
+    Hkv = K.shape[1]
+    out = torch.zeros(B, Hq, D, dtype=torch.float64)
+    for b in range(B):
+        n = lens[b]
+        if n == 0:
+            continue
+        k = K[b, :, :n].double().repeat_interleave(Hq // Hkv, dim=0)  # [Hq, n, D]
+        v = V[b, :, :n].double().repeat_interleave(Hq // Hkv, dim=0)
+        s = torch.einsum("hd,hnd->hn", q[b].double(), k) * scale
+        p = torch.softmax(s, dim=-1)
+        out[b] = torch.einsum("hn,hnd->hd", p, v)
+    return out
+
+
+CASES = [
+    # B, Hq, Hkv, D, lens, dtype
+    (3, 4, 4, 64, [1, 16, 37], torch.float16),
+    (2, 8, 2, 64, [33, 100], torch.float16),
+    (2, 8, 1, 128, [17, 64], torch.bfloat16),
+    (1, 16, 2, 128, [250], torch.float16),
+]
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,D,lens,dtype", CASES)
+def test_dense_equivalence(B, Hq, Hkv, D, lens, dtype):
+    g = torch.Generator().manual_seed(11)
+    nmax = max(lens)
+    q = torch.randn(B, Hq, D, generator=g).to(dtype)
+    K = torch.randn(B, Hkv, nmax, D, generator=g).to(dtype)
+    V = torch.randn(B, Hkv, nmax, D, generator=g).to(dtype)
+    kp, vp, tables = _paged_from_dense(K, V, lens, num_blocks=64, seed=3)
+    scale = 1.0 / math.sqrt(D)
+    got = oracle.attention_decode(q, kp, vp, tables, lens, scale)
+    ref = _dense_reference(q, K, V, lens, scale).numpy()
+    assert np.isfinite(got).all()  # NaN sentinels in unused slots never read
+    np.testing.assert_allclose(got, ref, rtol=1e-12, atol=1e-13)
+
+
+def test_rows_subset_matches_full():
+    g = torch.Generator().manual_seed(5)
+    q = torch.randn(2, 4, 64, generator=g).half()
+    K = torch.randn(2, 2, 40, 64, generator=g).half()
+    V = torch.randn(2, 2, 40, 64, generator=g).half()
+    kp, vp, tables = _paged_from_dense(K, V, [40, 23], 16, seed=1)
+    full = oracle.attention_decode(q, kp, vp, tables, [40, 23], 0.125)
+    rows = [(1, 3), (0, 0), (1, 1)]
+    sub = oracle.attention_decode(q, kp, vp, tables, [40, 23], 0.125, rows=rows)
+    for i, (b, h) in enumerate(rows):
+        assert np.array_equal(sub[i], full[b, h])
+
+
+def test_block_permutation_invariance():
+    g = torch.Generator().manual_seed(21)
+    lens = [50, 7, 128]
+    q = torch.randn(3, 4, 64, generator=g).half()
+    K = torch.randn(3, 2, 128, 64, generator=g).half()
+    V = torch.randn(3, 2, 128, 64, generator=g).half()
+    kp, vp, tables = _paged_from_dense(K, V, lens, 32, seed=2)
+    a = oracle.attention_decode(q, kp, vp, tables, lens, 0.125)
+    pi = torch.randperm(32, generator=g)
+    kp2 = torch.empty_like(kp)
+    vp2 = torch.empty_like(vp)
+    kp2[pi] = kp
+    vp2[pi] = vp
+    t2 = torch.where(tables >= 0, pi[tables.clamp(min=0).long()].to(torch.int32), tables)
+    b = oracle.attention_decode(q, kp2, vp2, t2, lens, 0.125)
+    assert np.array_equal(a, b)
+
+
+def test_single_token_returns_v0_exactly():
+    g = torch.Generator().manual_seed(4)
+    q = torch.randn(2, 4, 64, generator=g).half()
+    K = torch.randn(2, 2, 1, 64, generator=g).half()
+    V = torch.randn(2, 2, 1, 64, generator=g).half()
+    kp, vp, tables = _paged_from_dense(K, V, [1, 1], 8, seed=9)
+    got = oracle.attention_decode(q, kp, vp, tables, [1, 1], 0.125)
+    for b in range(2):
+        for h in range(4):
+            assert np.array_equal(got[b, h], V[b, h // 2, 0].double().numpy())
+
+
+def test_identical_keys_give_mean_of_v():
+    g = torch.Generator().manual_seed(8)
+    n = 45
+    q = torch.randn(1, 2, 64, generator=g).half()
+    k_one = torch.randn(64, generator=g).half()
+    K = k_one.expand(1, 1, n, 64).clone()
+    V = torch.randn(1, 1, n, 64, generator=g).half()
+    kp, vp, tables = _paged_from_dense(K, V, [n], 8, seed=1)
+    got = oracle.attention_decode(q, kp, vp, tables, [n], 0.3)
+    mean = V[0, 0].double().mean(dim=0).numpy()
+    np.testing.assert_allclose(got[0, 0], mean, rtol=0, atol=1e-14)
+    np.testing.assert_allclose(got[0, 1], mean, rtol=0, atol=1e-14)
+
+
+def test_scale_zero_gives_mean_of_v():
+    g = torch.Generator().manual_seed(9)
+    n = 70
+    q = torch.randn(1, 1, 64, generator=g).half()
+    K = torch.randn(1, 1, n, 64, generator=g).half()
+    V = torch.randn(1, 1, n, 64, generator=g).half()
+    kp, vp, tables = _paged_from_dense(K, V, [n], 8, seed=1)
+    got = oracle.attention_decode(q, kp, vp, tables, [n], 0.0)
+    np.testing.assert_allclose(got[0, 0], V[0, 0].double().mean(0).numpy(), rtol=0, atol=1e-14)
+
+
+def test_dominant_key_selects_its_value():
+    g = torch.Generator().manual_seed(10)
+    n = 40
+    q = torch.randn(1, 1, 64, generator=g).half()
+    K = torch.randn(1, 1, n, 64, generator=g).half()
+    V = torch.randn(1, 1, n, 64, generator=g).half()
+    kp, vp, tables = _paged_from_dense(K, V, [n], 8, seed=1)
+    s = (K[0, 0].double() @ q[0, 0].double()).numpy()
+    j = int(np.argmax(s))
+    gap = np.sort(s)[-1] - np.sort(s)[-2]
+    scale = 800.0 / max(gap, 1e-3)  # next-best weight <= e^-800: underflows
+    got = oracle.attention_decode(q, kp, vp, tables, [n], scale)
+    assert np.array_equal(got[0, 0], V[0, 0, j].double().numpy())
+
+
+def test_two_tokens_closed_form():
+    g = torch.Generator().manual_seed(12)
+    q = torch.randn(1, 1, 64, generator=g).half()
+    K = torch.randn(1, 1, 2, 64, generator=g).half()
+    V = torch.randn(1, 1, 2, 64, generator=g).half()
+    kp, vp, tables = _paged_from_dense(K, V, [2], 8, seed=1)
+    sc = 0.2
+    got = oracle.attention_decode(q, kp, vp, tables, [2], sc)[0, 0]
+    qd = q[0, 0].double().numpy()
+    s1 = sc * float(np.dot(qd, K[0, 0, 0].double().numpy()))
+    s2 = sc * float(np.dot(qd, K[0, 0, 1].double().numpy()))
+    w1 = 1.0 / (1.0 + math.exp(s2 - s1))  # logistic form of the 2-way softmax
+    ref = w1 * V[0, 0, 0].double().numpy() + (1.0 - w1) * V[0, 0, 1].double().numpy()
+    np.testing.assert_allclose(got, ref, rtol=1e-13, atol=1e-14)
+
+
+def test_query_group_maps_to_kv_head_by_division():
+    # Hq = 6, Hkv = 3: heads 0,1 -> kv 0; 2,3 -> kv 1; 4,5 -> kv 2.
+    g = torch.Generator().manual_seed(13)
+    n = 20
+    q = torch.randn(1, 6, 64, generator=g).half()
+    K = torch.randn(1, 3, n, 64, generator=g).half()
+    V = torch.empty(1, 3, n, 64, dtype=torch.float16)
+    for kv in range(3):
+        V[0, kv] = float(kv + 1)  # constant value per kv head
+    kp, vp, tables = _paged_from_dense(K, V, [n], 8, seed=1)
+    got = oracle.attention_decode(q, kp, vp, tables, [n], 0.1)
+    for h in range(6):
+        np.testing.assert_allclose(got[0, h], float(h // 2 + 1), rtol=1e-14)
+
+
+def test_zero_length_gives_zero_row_and_bad_block_raises():
+    q = torch.ones(2, 1, 64, dtype=torch.float16)
+    kp = torch.ones(4, 1, BS, 64, dtype=torch.float16)
+    tables = torch.tensor([[0], [5]], dtype=torch.int32)
+    got = oracle.attention_decode(q[:1], kp, kp, tables[:1], [0], 1.0)
+    assert np.array_equal(got, np.zeros((1, 1, 64)))
+    with pytest.raises(ValueError):
+        oracle.attention_decode(q, kp, kp, tables, [0, 3], 1.0)   # block 5 >= 4
+    with pytest.raises(ValueError):
+        oracle.attention_decode(q[:1], kp, kp, tables[:1], [17], 1.0)  # 17 > 1 block
+
+
+def test_int8_decode_equals_dense_on_dequantised_values():
+    g = torch.Generator().manual_seed(14)
+    lens = [33, 90]
+    q = torch.randn(2, 8, 64, generator=g).half()
+    Kc = torch.randint(-127, 128, (2, 2, 90, 64), generator=g, dtype=torch.int8)
+    Vc = torch.randint(-127, 128, (2, 2, 90, 64), generator=g, dtype=torch.int8)
+    Ks = torch.rand(2, 2, 90, generator=g) * 0.05 + 0.001
+    Vs = torch.rand(2, 2, 90, generator=g) * 0.05 + 0.001
+    kp, vp, tables = _paged_from_dense(Kc, Vc, lens, 16, seed=4, fill=0)
+    ksp, vsp, _ = _paged_from_dense(Ks[..., None], Vs[..., None], lens, 16, seed=4, fill=0)
+    got = oracle.attention_decode(q, kp, vp, tables, lens, 0.125,
+                                  k_scale=ksp[..., 0], v_scale=vsp[..., 0])
+    Kd = Kc.double() * Ks.double()[..., None]
+    Vd = Vc.double() * Vs.double()[..., None]
+    ref = _dense_reference(q, Kd, Vd, lens, 0.125).numpy()
+    np.testing.assert_allclose(got, ref, rtol=1e-12, atol=1e-13)
+
+
+# ------------------------------------------------------------ INT8 quantiser
+def _numpy_per_channel_quantiser(x16: np.ndarray):
+    """Restatement of the per-channel branch of the quantiser with NumPy's own
+    primitives: abs-max over the last axis in float32, /127, zero scale -> 1,
+    round (half to even), clip to [-128, 127], cast to int8."""
+    x = x16.astype(np.float32)
+    amax = np.max(np.abs(x), axis=-1, keepdims=True)
+    scale = (amax / np.float32(127.0)).astype(np.float32)
+    scale = np.where(scale > 0, scale, np.float32(1.0)).astype(np.float32)
+    codes = np.clip(np.round(x / scale), -128, 127).astype(np.int8)
+    return codes, scale[..., 0]
+
+
+@pytest.mark.parametrize("dtype", [torch.float16, torch.bfloat16])
+def test_quantiser_matches_numpy_restatement(dtype):
+    g = torch.Generator().manual_seed(15)
+    x = (torch.randn(400, 128, generator=g) * torch.rand(400, 1, generator=g) * 3).to(dtype)
+    x[3] = 0
+    x[4, :7] = 0
+    x[5] = 1e-3
+    codes, scales = oracle.quantize_int8(x)
+    ref_codes, ref_scales = _numpy_per_channel_quantiser(x.float().numpy())
+    assert np.array_equal(codes, ref_codes)
+    assert np.array_equal(scales.view(np.uint32), ref_scales.view(np.uint32))
+
+
+def test_quantiser_special_rows():
+    x = torch.zeros(4, 8, dtype=torch.float16)
+    # row 1: amax 127 -> scale exactly 1.0; x.5 values are ties -> even
+    x[1] = torch.tensor([127.0, 2.5, 3.5, -2.5, -3.5, 0.5, -0.5, 1.5])
+    # row 2: the abs-max element maps to +-127
+    x[2] = torch.tensor([0.1, -3.0, 2.0, 0.0, 1.0, -1.0, 0.25, 2.9])
+    x[3] = torch.tensor([4.0, 1.0, -1.0, 0.0, 0.5, 2.0, -4.0, 3.0])
+    codes, scales = oracle.quantize_int8(x)
+    assert codes[0].tolist() == [0] * 8 and scales[0] == 1.0
+    assert scales[1] == 1.0
+    assert codes[1].tolist() == [127, 2, 4, -2, -4, 0, 0, 2]
+    assert codes[2, 1] == -127 and np.abs(codes[2]).max() == 127
+    assert codes[3, 0] == 127 and codes[3, 6] == -127
+
+
+def test_quantiser_never_reaches_minus_128():
+    g = torch.Generator().manual_seed(16)
+    x = torch.randn(20000, 64, generator=g).half()
+    codes, _ = oracle.quantize_int8(x)
+    assert codes.min() >= -127 and codes.max() <= 127
+    assert (np.abs(codes).max(axis=1) == 127).all()
+
+
+# ------------------------------------------------------------ append / copy
+def test_append_matches_numpy_indexing():
+    g = torch.Generator().manual_seed(17)
+    NB, Hkv, D = 6, 3, 64
+    pool = torch.randn(NB, Hkv, BS, D, generator=g).half()
+    src = torch.randn(5, Hkv, D, generator=g).half()
+    slots = torch.tensor([0, 17, -1, 95, 40], dtype=torch.int32)
+    got = oracle.append(pool, src, slots)
+    ref = pool.clone().numpy()
+    for t, s in enumerate(slots.tolist()):
+        if s >= 0:
+            ref[s // BS, :, s % BS, :] = src[t].numpy()
+    assert np.array_equal(got.view(np.float16), ref)
+    with pytest.raises(ValueError):
+        oracle.append(pool, src[:1], torch.tensor([NB * BS], dtype=torch.int32))
+
+
+def test_copy_blocks_matches_numpy_and_self_copy_is_identity():
+    g = torch.Generator().manual_seed(18)
+    pool = torch.randn(8, 2, BS, 64, generator=g).half()
+    pairs = torch.tensor([[1, 5], [2, 2], [7, 0]], dtype=torch.int32)
+    got = oracle.copy_blocks(pool, pairs).view(np.float16)
+    ref = pool.clone().numpy()
+    ref[5] = ref[1]
+    ref[0] = pool.numpy()[7]
+    assert np.array_equal(got, ref)
+    with pytest.raises(ValueError):
+        oracle.copy_blocks(pool, torch.tensor([[0, 8]], dtype=torch.int32))
+
+
+def test_append_int8_matches_quantise_then_scatter():
+    g = torch.Generator().manual_seed(19)
+    NB, Hkv, D = 4, 2, 64
+    codes = torch.zeros(NB, Hkv, BS, D, dtype=torch.int8)
+    scales = torch.zeros(NB, Hkv, BS)
+    src = torch.randn(3, Hkv, D, generator=g).half()
+    slots = torch.tensor([5, -1, 63], dtype=torch.int32)
+    c, s = oracle.append_int8(codes, scales, src, slots)
+    qc, qs = _numpy_per_channel_quantiser(src.float().numpy())
+    assert np.array_equal(c[0, :, 5], qc[0]) and np.array_equal(c[3, :, 15], qc[2])
+    assert np.array_equal(s[0, :, 5], qs[0]) and np.array_equal(s[3, :, 15], qs[2])
+    assert int(np.count_nonzero(s)) == 2 * Hkv
