@@ -1,0 +1,535 @@
+#!/usr/bin/env python3
+"""Benchmark of the paged-KV decode step on GB300.
+
+One step = the whole hot path over one batch: copy-on-write block copies (when
+the workload has them), append of the step's new tokens (INT8-quantising for the
+INT8 workload), paged decode attention (partition pass + reduce).  Inputs are
+resident in HBM when the timed region starts; `value` is whole-job achieved HBM
+GB/s over the step's algorithmic bytes, timed with CUDA events on the launching
+stream.  Prints ONE JSON line (rank 0).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+  python bench.py --impl reference ...   # the CPU oracle on the host cores
+
+For N > 1 (torchrun) every rank runs an independent replica on its own GPU (the
+decode has no exchange step): value = total bytes of all ranks / max time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import re
+import shutil
+import signal
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+import workloads  # noqa: E402
+
+METRIC = ("paged-attention decode achieved HBM GB/s (% of peak) and attended KV tokens/s")
+L2_BYTES = 129 * 1024 * 1024
+KERNEL_SOURCES = ["kvp_decode.cuh", "kvp_device.cuh", "kvp_decode_simt.cu", "kvp_decode_mma.cu",
+                  "kvp_decode_int8.cu", "kvp_internal.h"]
+
+
+# ------------------------------------------------------------------ byte model
+def kv_bytes_per_layer(Hkv: int, D: int, tokens: int, batch: int, elem_bytes: int) -> int:
+    """2 (K and V) x kv heads x head_dim x tokens x batch x element bytes
+    ("ATB KV Cache management", "KV Cache 的显存需求")."""
+    return 2 * Hkv * D * tokens * batch * elem_bytes
+
+
+def decode_bytes(w, lens) -> dict:
+    """Algorithmic bytes of one decode call: K/V (and INT8 scales) of every
+    attended token, the block-table entries read, q, out and context_lens."""
+    elt = 1 if w.kv_int8 else 2
+    qel = w.q.element_size()
+    kv = sum(kv_bytes_per_layer(w.Hkv, w.D, n, 1, elt) for n in lens)
+    scales = sum(2 * w.Hkv * n * 4 for n in lens) if w.kv_int8 else 0
+    tables = sum(4 * (-(-n // 16)) for n in lens)
+    q = w.B * w.Hq * w.D * qel
+    return {"kv": kv, "scales": scales, "tables": tables, "q": q, "out": q, "lens": 4 * w.B,
+            "partial_pass": kv + scales + tables + q + 4 * w.B,
+            "call": kv + scales + tables + 2 * q + 4 * w.B}
+
+
+def append_bytes(w) -> int:
+    T, Hkv, D = int(w.slot_mapping.numel()), w.Hkv, w.D
+    if w.kv_int8:  # read fp16 K and V, write int8 codes and fp32 scales
+        return 2 * T * Hkv * D * 2 + 2 * T * Hkv * D + 2 * T * Hkv * 4 + 4 * T
+    return 2 * 2 * T * Hkv * D * 2 + 4 * T
+
+
+def copy_bytes(w) -> int:
+    if w.cow_pairs is None:
+        return 0
+    P = int(w.cow_pairs.shape[0])
+    block = w.Hkv * 16 * w.D * (1 if w.kv_int8 else 2)
+    return P * 2 * block * 2 + 8 * P
+
+
+# ------------------------------------------------------------------ helpers
+def measured_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured (MEASURED_PEAKS.json hbm_gbs)"
+    except Exception:
+        return 6800.0, "fallback (6.8 TB/s)"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, "pagedattention_decode_kvp_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(workload: str):
+    """Per-launch DRAM bytes of the decode partition kernel from a committed ncu
+    summary, valid only while the kernel sources are unchanged."""
+    want = kernel_source_hash()
+    pdir = os.path.join(ROOT, "profiles")
+    if not os.path.isdir(pdir):
+        return None
+    pat = re.compile(r"traffic: workload=(\S+) kernel_src_sha=(\S+) bytes_per_launch=(\d+)")
+    for fn in sorted(os.listdir(pdir)):
+        if not fn.endswith((".md", ".txt")):
+            continue
+        with open(os.path.join(pdir, fn)) as fh:
+            for m in pat.finditer(fh.read()):
+                if m.group(1) == workload and m.group(2) == want:
+                    return int(m.group(3))
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples during the timed region."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        if shutil.which("nvidia-smi") is None:
+            return self
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        self.proc = subprocess.Popen(
+            ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}",
+             "--format=csv,noheader,nounits", "-lms", "100"],
+            stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.send_signal(signal.SIGTERM)
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        if not self.path or not os.path.exists(self.path):
+            return None
+        rows = []
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append((float(parts[1]), float(parts[2]), parts[5:9]))
+            except ValueError:
+                continue
+        os.unlink(self.path)
+        if not rows:
+            return None
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for _, _, r in rows for i, v in enumerate(r)
+                          if v.lower() == "active"})
+        sm = [r[0] for r in rows]
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(r[1] for r in rows),
+                "sm_mhz_min": min(sm), "samples": len(rows), "reasons": reasons}
+
+
+# ------------------------------------------------------------------ the GPU arm
+class Step:
+    """Device buffers of one workload and the step through the public API."""
+
+    def __init__(self, w, kvp, dev):
+        self.w, self.kvp, self.dev = w, kvp, dev
+        self.q = w.q.to(dev)
+        self.tables = w.block_tables.to(dev)
+        self.lens = w.context_lens.to(dev)
+        self.slots = w.slot_mapping.to(dev)
+        self.new_k = w.new_k.to(dev)
+        self.new_v = w.new_v.to(dev)
+        self.pairs = w.cow_pairs.to(dev) if w.cow_pairs is not None else None
+        self.out = torch.empty_like(self.q)
+        self.status = torch.zeros(1, dtype=torch.int32, device=dev)
+        if w.kv_int8:
+            self._init_int8()
+        else:
+            self.kp = w.k_pool.to(dev)
+            self.vp = w.v_pool.to(dev)
+        desc = kvp.cache_desc(self.kp)
+        nb = kvp.kvp_decode_workspace_bytes(w.B, w.Hq, desc, w.max_blocks, 0, w.kv_int8)
+        self.ws = torch.empty(max(nb // 4, 1), dtype=torch.float32, device=dev) if nb else None
+        self.split = nb > 0
+        self.part_blocks = kvp.kvp_decode_partition_blocks(w.B, w.Hq, desc, w.max_blocks,
+                                                           w.kv_int8)
+
+    def _init_int8(self):
+        """Quantise the fp16 source pools into the INT8 pools on the GPU: each
+        row is independent, so the pool is appended to itself as
+        NB*Hkv*16 single-head tokens (the long-context prefill)."""
+        w, kvp = self.w, self.kvp
+        NB, Hkv, D = w.num_blocks, w.Hkv, w.D
+        ks, vs = w.k_pool.to(self.dev), w.v_pool.to(self.dev)
+        self.kp = torch.empty(NB, Hkv, 16, D, dtype=torch.int8, device=self.dev)
+        self.vp = torch.empty_like(self.kp)
+        self.ks = torch.empty(NB, Hkv, 16, dtype=torch.float32, device=self.dev)
+        self.vs = torch.empty_like(self.ks)
+        rows = NB * Hkv * 16
+        slots = torch.arange(rows, dtype=torch.int32, device=self.dev)
+        flat = lambda t: t.view(NB * Hkv, 1, 16, *t.shape[3:])  # noqa: E731
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        kvp.kvp_append_int8(ks.view(rows, 1, D), vs.view(rows, 1, D), flat(self.kp),
+                            flat(self.vp), flat(self.ks), flat(self.vs), slots)
+        e1.record()
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1)
+        moved = rows * D * 2 * 2 + rows * D * 2 + rows * 4 * 2
+        self.prefill = {"rows": rows, "ms": ms, "gbs": moved / ms / 1e6}
+        del ks, vs
+
+    def launches_per_step(self) -> int:
+        return (1 if self.pairs is not None else 0) + 1 + 1 + (1 if self.split else 0)
+
+    def run(self, ev=None):
+        """One step; ev = (e_decode_start, e_partial_end) events to record."""
+        kvp, w = self.kvp, self.w
+        if self.pairs is not None:
+            kvp.kvp_copy_blocks(self.kp, self.vp, self.pairs, status=self.status)
+        if w.kv_int8:
+            kvp.kvp_append_int8(self.new_k, self.new_v, self.kp, self.vp, self.ks, self.vs,
+                                self.slots, status=self.status)
+        else:
+            kvp.kvp_append(self.new_k, self.new_v, self.kp, self.vp, self.slots,
+                           status=self.status)
+        if ev is not None:
+            ev[0].record()
+        phases = [kvp.KVP_PHASE_PARTIAL, kvp.KVP_PHASE_REDUCE] if self.split else [kvp.KVP_PHASE_ALL]
+        for i, ph in enumerate(phases):
+            if w.kv_int8:
+                kvp.kvp_attention_decode_int8(self.out, self.q, self.kp, self.vp, self.ks,
+                                              self.vs, self.tables, self.lens, w.scale,
+                                              workspace=self.ws, phases=ph, status=self.status)
+            else:
+                kvp.kvp_attention_decode(self.out, self.q, self.kp, self.vp, self.tables,
+                                         self.lens, w.scale, workspace=self.ws, phases=ph,
+                                         status=self.status)
+            if ev is not None and i == 0:
+                ev[1].record()
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def max_over_ranks(x: float, world: int, device) -> float:
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def sum_over_ranks(x: float, world: int, device) -> float:
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def cpu_oracle_baseline(w, host_k, host_v, host_ks=None, host_vs=None, rows=None):
+    """Time the CPU oracle (as it stands) on a sample of the decode."""
+    import oracle
+    lens = [int(x) for x in w.context_lens]
+    if rows is None:
+        rows = [(b, h) for b in range(w.B) for h in range(w.Hq)]
+    t0 = time.perf_counter()
+    oracle.attention_decode(w.q, host_k, host_v, w.block_tables, w.context_lens, w.scale,
+                            k_scale=host_ks, v_scale=host_vs, rows=rows)
+    dt = time.perf_counter() - t0
+    G = w.Hq // w.Hkv
+    elt = 1 if w.kv_int8 else 2
+    # bytes the sampled rows read: each (b, h) row reads its K/V once per query
+    # head of the group, so count the sample as the fraction of the full call
+    frac = len(rows) / (w.B * w.Hq)
+    sampled_tokens = sum(lens[b] for b, _ in rows)
+    full = decode_bytes(w, lens)["call"]
+    return {"seconds": dt, "bytes": full * frac, "tokens": sampled_tokens / G,
+            "rows": len(rows), "cores": oracle.num_threads(), "elt": elt}
+
+
+def run_ours(args):
+    import pagedattention_decode_kvp_gb300 as kvp
+    from pagedattention_decode_kvp_gb300 import _build
+
+    world, rank, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    if rank == 0 or world == 1:
+        _build.build()
+    barrier(world)
+    kvp.load_library()
+
+    w = workloads.make(args.workload, device=dev, nan_sentinel=False)
+    step = Step(w, kvp, dev)
+    lens = [int(x) for x in w.context_lens]
+    dbytes = decode_bytes(w, lens)
+    sbytes = dbytes["call"] + append_bytes(w) + copy_bytes(w)
+    kv_total = sum(lens)
+    stream = torch.cuda.current_stream()
+
+    for _ in range(args.warmup):
+        step.run()
+    torch.cuda.synchronize()
+    st = kvp.kvp_read_status(step.status)
+    if st != kvp.KVP_OK:
+        raise RuntimeError(f"device status after warm-up: {kvp.kvp_status_string(st)}")
+
+    # ---- timed region: K steps, events on the launching stream
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.steps)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        start.record(stream)
+        for i in range(args.steps):
+            step.run(evs[i])
+        end.record(stream)
+        torch.cuda.synchronize()
+    barrier(world)
+    elapsed_ms = start.elapsed_time(end)
+    partial_ms = statistics.mean(e0.elapsed_time(e1) for e0, e1 in evs)
+    elapsed_ms = max_over_ranks(elapsed_ms, world, dev)
+    ms_per_step = elapsed_ms / args.steps
+    total_bytes = sum_over_ranks(sbytes * args.steps, world, dev)
+    value = total_bytes / (elapsed_ms / 1e3) / 1e9
+    tokens_per_s = sum_over_ranks(kv_total * args.steps, world, dev) / (elapsed_ms / 1e3)
+
+    # ---- end to end through the public API with host buffers
+    e2e = None
+    if not args.no_e2e:
+        host = {k: getattr(step, k).cpu().pin_memory() for k in
+                ("q", "tables", "lens", "slots", "new_k", "new_v")}
+        if step.pairs is not None:
+            host["pairs"] = step.pairs.cpu().pin_memory()
+        out_host = torch.empty(step.out.shape, dtype=step.out.dtype).pin_memory()
+        h2d = sum(t.numel() * t.element_size() for t in host.values())
+        d2h = out_host.numel() * out_host.element_size()
+
+        def e2e_step():
+            for k, t in host.items():
+                getattr(step, k).copy_(t, non_blocking=True)
+            step.run()
+            out_host.copy_(step.out, non_blocking=True)
+            torch.cuda.current_stream().synchronize()
+
+        for _ in range(args.warmup):
+            e2e_step()
+        barrier(world)
+        t0 = time.perf_counter()
+        for _ in range(args.steps):
+            e2e_step()
+        e2e_s = max_over_ranks(time.perf_counter() - t0, world, dev)
+        barrier(world)
+        e2e = {"value": round(total_bytes / e2e_s / 1e9, 2), "unit": "GB/s",
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+               "ms_per_step": round(e2e_s * 1e3 / args.steps, 4)}
+
+    if rank != 0:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+        return
+
+    peak, peak_src = measured_peak()
+    achieved = dbytes["partial_pass"] / (partial_ms / 1e3) / 1e9
+    traffic = profiled_traffic(args.workload)
+    res = {
+        "metric": METRIC,
+        "value": round(value, 2),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_per_step, 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": {torch.float16: "f16", torch.bfloat16: "bf16"}[w.dtype] + (
+            " (int8 KV)" if w.kv_int8 else ""),
+        "data": "synthetic (seeded N(0,1), shapes of the pages' workloads)",
+        "config": {"workload": w.name, "batch": w.B, "q_heads": w.Hq, "kv_heads": w.Hkv,
+                   "head_dim": w.D, "block_size": 16, "num_blocks": w.num_blocks,
+                   "context_tokens": kv_total, "max_context": max(lens),
+                   "new_tokens": int(w.slot_mapping.numel()),
+                   "cow_pairs": int(w.cow_pairs.shape[0]) if w.cow_pairs is not None else 0,
+                   "partition_blocks": step.part_blocks,
+                   "l2": ("inputs larger than L2: {:.2f} GB of K/V per step vs 129 MB L2"
+                          .format(dbytes["kv"] / 1e9)) if dbytes["kv"] > 4 * L2_BYTES else
+                         "inputs partly L2-resident (L2 reuse is part of this workload)",
+                   "parallelism": "replicas" if world > 1 else "single GPU"},
+        "tokens_per_s": round(tokens_per_s, 1),
+        "pct_of_peak": round(100 * value / peak, 2),
+        "step_bytes": sbytes,
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak,
+                     "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": traffic,
+                     "kernel": "decode_partial_kernel", "peak_source": peak_src,
+                     "algorithmic_bytes_per_launch": dbytes["partial_pass"],
+                     "launch_ms": round(partial_ms, 5)},
+        "e2e": e2e,
+        "gpu_launches": step.launches_per_step() * args.steps,
+        "clocks": clk.summary(),
+    }
+    if w.kv_int8:
+        res["prefill_int8"] = step.prefill
+    if w.name == "gqa70b":
+        res["config"]["contiguous_share"] = round(w.info.get("contiguous_share", 0.0), 4)
+
+    if world == 1 and not args.no_cpu_baseline:
+        import oracle
+        oracle.build()
+        w_host = workloads.Workload(**{k: (v.cpu() if isinstance(v, torch.Tensor) else v)
+                                       for k, v in w.__dict__.items()})
+        hk, hv = step.kp.cpu(), step.vp.cpu()
+        hks = step.ks.cpu() if w.kv_int8 else None
+        hvs = step.vs.cpu() if w.kv_int8 else None
+        rows = sample_rows(w, args.cpu_rows)
+        cb = cpu_oracle_baseline(w_host, hk, hv, hks, hvs, rows)
+        res["cpu_baseline"] = {"value": round(cb["bytes"] / cb["seconds"] / 1e9, 4),
+                               "unit": "GB/s", "cores": cb["cores"], "kind": "oracle",
+                               "sample": f"{cb['rows']} of {w.B * w.Hq} (request, query head) "
+                                         f"rows of one decode call, {cb['seconds']:.2f} s"}
+    print(json.dumps(res))
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def sample_rows(w, n):
+    total = w.B * w.Hq
+    if n <= 0 or n >= total:
+        return None
+    stride = total / n
+    return [(int(i * stride) // w.Hq, int(i * stride) % w.Hq) for i in range(n)]
+
+
+# ------------------------------------------------------------------ reference arm
+def run_reference(args):
+    """The CPU oracle as the reference arm, on the host cores."""
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return
+    import oracle
+    oracle.build()
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    w = workloads.make(args.workload, device=dev, nan_sentinel=False)
+    w = workloads.Workload(**{k: (v.cpu() if isinstance(v, torch.Tensor) else v)
+                              for k, v in w.__dict__.items()})
+    kp, vp, ks, vs = w.k_pool, w.v_pool, None, None
+    if w.kv_int8:
+        kc, ksn = oracle.quantize_int8(kp)
+        vc, vsn = oracle.quantize_int8(vp)
+        kp, vp = torch.from_numpy(kc), torch.from_numpy(vc)
+        ks, vs = torch.from_numpy(ksn), torch.from_numpy(vsn)
+    rows = sample_rows(w, args.cpu_rows)
+    for _ in range(args.warmup):
+        cpu_oracle_baseline(w, kp, vp, ks, vs, rows)
+    secs, nbytes, toks = 0.0, 0.0, 0.0
+    for _ in range(args.steps):
+        cb = cpu_oracle_baseline(w, kp, vp, ks, vs, rows)
+        secs += cb["seconds"]
+        nbytes += cb["bytes"]
+        toks += cb["tokens"]
+    value = nbytes / secs / 1e9
+    sample = (f"{cb['rows']} of {w.B * w.Hq} (request, query head) rows of one decode call "
+              "per step")
+    res = {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s",
+           "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+           "ms_per_step": round(secs * 1e3 / args.steps, 3), "higher_is_better": True,
+           "scaling": "weak", "vs_baseline": None,
+           "dtype": "f64 (oracle)", "data": "synthetic (seeded N(0,1))",
+           "config": {"workload": w.name, "batch": w.B, "q_heads": w.Hq, "kv_heads": w.Hkv,
+                      "head_dim": w.D},
+           "tokens_per_s": round(toks / secs, 1),
+           "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": cb["cores"],
+                            "kind": "oracle", "sample": sample},
+           "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                   "d2h_bytes_per_step": 0}}
+    print(json.dumps(res))
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=30)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default="llama7b", choices=workloads.WORKLOAD_NAMES)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--cpu-rows", type=int, default=0,
+                    help="(request, head) rows the CPU oracle times (0 = default sample)")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if args.cpu_rows == 0:
+        args.cpu_rows = 256 if args.impl == "ours" else 64
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

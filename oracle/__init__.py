@@ -190,6 +190,21 @@ def attention_decode(q, k_cache, v_cache, block_tables, context_lens, scale,
     return out
 
 
+def _like(result, template):
+    """Hand raw bytes back as a torch tensor of the template's dtype when the
+    caller passed torch tensors (numpy otherwise)."""
+    try:
+        import torch
+        if isinstance(template, torch.Tensor):
+            t = torch.from_numpy(np.ascontiguousarray(result))
+            if template.dtype in (torch.float16, torch.bfloat16):
+                return t.view(torch.int16).view(template.dtype)
+            return t.view(template.dtype)
+    except ImportError:  # pragma: no cover
+        pass
+    return result
+
+
 def append(cache, src, slot_mapping):
     """Return a copy of ``cache`` [NB, Hkv, bs, D] with rows of ``src`` [T, Hkv, D]
     scattered to their slots (negative slot = skipped).  Raw bytes are moved,
@@ -204,7 +219,7 @@ def append(cache, src, slot_mapping):
                              c.dtype.itemsize, NB, bs)
     if err != 0:
         raise ValueError("oracle append: slot out of range")
-    return c
+    return _like(c, cache)
 
 
 def append_rows(pool, rows, slot_mapping):
@@ -225,14 +240,22 @@ def append_rows(pool, rows, slot_mapping):
 def copy_blocks(pool, pairs):
     """Return a copy of ``pool`` [NB, ...] with block src copied onto block dst for
     each (src, dst) in ``pairs``, in order."""
-    p = np.array(_raw(pool)[0] if not isinstance(pool, np.ndarray) else pool, copy=True)
+    if isinstance(pool, np.ndarray):
+        p = np.array(pool, copy=True)
+    else:
+        try:
+            import torch
+            is_float = isinstance(pool, torch.Tensor) and pool.dtype == torch.float32
+        except ImportError:  # pragma: no cover
+            is_float = False
+        p = np.array(_f32(pool) if is_float else _raw(pool)[0], copy=True)
     pr = _i32(pairs).reshape(-1, 2)
     NB = p.shape[0]
     block_bytes = p.nbytes // NB if NB else 0
     err = _load().orc_copy_blocks(_ptr(p), _ptr(pr), pr.shape[0], block_bytes, NB)
     if err != 0:
         raise ValueError("oracle copy_blocks: block id out of range")
-    return p
+    return _like(p, pool)
 
 
 def quantize_int8(src):
@@ -253,4 +276,6 @@ def append_int8(k_codes, k_scales, src, slot_mapping):
     """Quantise ``src`` [T, Hkv, D] per row, then scatter codes and scales into
     copies of the int8 pool [NB, Hkv, bs, D] and scale pool [NB, Hkv, bs]."""
     q, s = quantize_int8(src)
-    return append(k_codes, q, slot_mapping), append_rows(_f32(k_scales), s, slot_mapping)
+    codes = append(k_codes, q, slot_mapping)
+    scales = _like(append_rows(_f32(k_scales), s, slot_mapping), k_scales)
+    return codes, scales

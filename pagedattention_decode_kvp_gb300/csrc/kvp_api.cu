@@ -1,0 +1,329 @@
+// kvp_api.cu -- the extern "C" entry points declared in include/kvp.h:
+// argument validation, TMA descriptor encoding, split-context sizing and
+// kernel dispatch.  Nothing here allocates device memory.
+#include <cudaTypedefs.h>
+
+#include <cmath>
+#include <cstdint>
+#include <mutex>
+
+#include "kvp_internal.h"
+
+using namespace kvp;
+
+namespace {
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// KVP_OK, or why the cache description is not usable.
+kvp_status check_desc(const kvp_cache_desc& c) {
+  if (c.num_blocks <= 0 || c.num_kv_heads <= 0 || c.block_size <= 0 || c.head_dim <= 0)
+    return KVP_ERR_INVALID_ARG;
+  if (c.block_size != kBlockSize) return KVP_ERR_UNSUPPORTED;
+  if (c.head_dim != 64 && c.head_dim != 128) return KVP_ERR_UNSUPPORTED;
+  // TMA row coordinates are 32-bit signed
+  if (static_cast<long long>(c.num_blocks) * c.num_kv_heads * kBlockSize >= (1ll << 31))
+    return KVP_ERR_UNSUPPORTED;
+  return KVP_OK;
+}
+
+kvp_status from_cuda(cudaError_t e) { return e == cudaSuccess ? KVP_OK : KVP_ERR_CUDA; }
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess) {
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+    }
+  });
+  return fn;
+}
+
+// TMA descriptor over a whole pool viewed as [NB * Hkv * 16 rows][D elements]:
+// a box is 16 token rows by at most 128 bytes, written to shared memory with
+// the 128-byte swizzle (a 256-byte row takes two boxes).
+kvp_status make_pool_map(CUtensorMap* map, const void* base, const kvp_cache_desc& c,
+                         int elem_bytes) {
+  auto fn = encode_fn();
+  if (fn == nullptr) return KVP_ERR_CUDA;
+  const int row_bytes = c.head_dim * elem_bytes;
+  const int box_bytes = row_bytes < 128 ? row_bytes : 128;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(c.head_dim),
+                        static_cast<cuuint64_t>(c.num_blocks) * c.num_kv_heads * kBlockSize};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(row_bytes)};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(box_bytes / elem_bytes),
+                       static_cast<cuuint32_t>(kBlockSize)};
+  cuuint32_t estr[2] = {1, 1};
+  const CUresult r =
+      fn(map, elem_bytes == 2 ? CU_TENSOR_MAP_DATA_TYPE_UINT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8, 2,
+         const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+         CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? KVP_OK : KVP_ERR_CUDA;
+}
+
+struct DecodeShape {
+  DecodePath path;
+  int heads_per_cta;
+  int qgroups;
+  int part_blocks;
+  int max_parts;
+  size_t ws_bytes;
+};
+
+// Split-context rule: a request is cut into partitions of 32 blocks (512
+// tokens) so that long contexts spread over many CTAs; it stays single-pass
+// when its table is at most 32 blocks, or when there are already >= 2048
+// (request, kv head, query-group) units to fill the 152 SMs.
+int auto_partition(long long units, int max_blocks) {
+  if (max_blocks <= 32) return max_blocks;
+  if (units >= 2048 && max_blocks <= kMaxPartBlocks) return max_blocks;
+  return 32;
+}
+
+kvp_status shape_decode(int batch, int num_q_heads, const kvp_cache_desc& c, int max_blocks,
+                        int partition_blocks, bool kv_int8, DecodeShape* out) {
+  if (batch < 0 || num_q_heads <= 0 || max_blocks <= 0) return KVP_ERR_INVALID_ARG;
+  const kvp_status ds = check_desc(c);
+  if (ds != KVP_OK) return ds;
+  if (num_q_heads % c.num_kv_heads != 0) return KVP_ERR_INVALID_ARG;
+  if (partition_blocks < 0 || partition_blocks > kMaxPartBlocks) return KVP_ERR_INVALID_ARG;
+  const int G = num_q_heads / c.num_kv_heads;
+  DecodeShape s;
+  if (kv_int8) {
+    s.path = DecodePath::kMmaInt8;
+    s.heads_per_cta = G < kHeadsPerCta ? G : kHeadsPerCta;
+  } else if (G <= 2) {
+    s.path = DecodePath::kSimt;
+    s.heads_per_cta = G;
+  } else {
+    s.path = DecodePath::kMma;
+    s.heads_per_cta = G < kHeadsPerCta ? G : kHeadsPerCta;
+  }
+  s.qgroups = (G + s.heads_per_cta - 1) / s.heads_per_cta;
+  const long long units = static_cast<long long>(batch) * c.num_kv_heads * s.qgroups;
+  int pb = partition_blocks > 0 ? partition_blocks : auto_partition(units, max_blocks);
+  if (pb >= max_blocks) pb = max_blocks;
+  if (pb > kMaxPartBlocks) return KVP_ERR_UNSUPPORTED;  // one partition must fit on chip
+  s.part_blocks = pb;
+  s.max_parts = (max_blocks + pb - 1) / pb;
+  s.ws_bytes = s.max_parts > 1 ? static_cast<size_t>(batch) * num_q_heads * s.max_parts *
+                                     (static_cast<size_t>(c.head_dim) + 2) * sizeof(float)
+                               : 0;
+  *out = s;
+  return KVP_OK;
+}
+
+kvp_status decode_common(void* out, const void* q, bool q_bf16, int kv_kind, const void* kc,
+                         const void* vc, const float* ks, const float* vs, const int32_t* tables,
+                         int32_t max_blocks, const int32_t* lens, int32_t batch, int32_t hq,
+                         float scale, kvp_cache_desc c, int32_t partition_blocks, void* ws,
+                         size_t ws_bytes, int32_t phases, int32_t* status, kvp_stream_t stream) {
+  const bool int8 = kv_kind == 2;
+  DecodeShape sh;
+  const kvp_status st = shape_decode(batch, hq, c, max_blocks, partition_blocks, int8, &sh);
+  if (st != KVP_OK) return st;
+  if (phases < 1 || phases > 3) return KVP_ERR_INVALID_ARG;
+  if (!std::isfinite(scale)) return KVP_ERR_INVALID_ARG;
+  if (batch == 0) return KVP_OK;
+  if (!out || !q || !kc || !vc || !tables || !lens) return KVP_ERR_INVALID_ARG;
+  if (int8 && (!ks || !vs)) return KVP_ERR_INVALID_ARG;
+  if (!aligned(out, 16) || !aligned(q, 16) || !aligned(kc, 16) || !aligned(vc, 16))
+    return KVP_ERR_INVALID_ARG;
+  if (int8 && (!aligned(ks, 16) || !aligned(vs, 16))) return KVP_ERR_INVALID_ARG;
+  if (sh.ws_bytes > 0 && (ws == nullptr || ws_bytes < sh.ws_bytes || !aligned(ws, 16)))
+    return KVP_ERR_INVALID_ARG;
+
+  DecodeParams p{};
+  p.out = out;
+  p.q = q;
+  p.k_scale = ks;
+  p.v_scale = vs;
+  p.block_tables = tables;
+  p.context_lens = lens;
+  p.ws_o = static_cast<float*>(ws);
+  p.ws_ml = sh.ws_bytes ? static_cast<float*>(ws) + static_cast<size_t>(batch) * hq *
+                                                        sh.max_parts * c.head_dim
+                        : nullptr;
+  p.status = status;
+  p.batch = batch;
+  p.num_q_heads = hq;
+  p.num_kv_heads = c.num_kv_heads;
+  p.head_dim = c.head_dim;
+  p.num_blocks = c.num_blocks;
+  p.max_blocks = max_blocks;
+  p.group = hq / c.num_kv_heads;
+  p.qgroups = sh.qgroups;
+  p.heads_per_cta = sh.heads_per_cta;
+  p.part_blocks = sh.part_blocks;
+  p.max_parts = sh.max_parts;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  p.q_bf16 = q_bf16 ? 1 : 0;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+
+  if (static_cast<long long>(c.num_kv_heads) * sh.qgroups > 65535 || batch > 65535)
+    return KVP_ERR_UNSUPPORTED;
+
+  if (phases & KVP_PHASE_PARTIAL) {
+    const int eb = int8 ? 1 : 2;
+    CUtensorMap tk, tv;
+    kvp_status r = make_pool_map(&tk, kc, c, eb);
+    if (r != KVP_OK) return r;
+    r = make_pool_map(&tv, vc, c, eb);
+    if (r != KVP_OK) return r;
+    cudaError_t e;
+    switch (sh.path) {
+      case DecodePath::kSimt:
+        e = launch_decode_simt(p, tk, tv, kv_kind == 1, sh.max_parts, s);
+        break;
+      case DecodePath::kMma:
+        e = launch_decode_mma(p, tk, tv, kv_kind == 1, sh.max_parts, s);
+        break;
+      default:
+        e = launch_decode_mma_int8(p, tk, tv, sh.max_parts, s);
+        break;
+    }
+    if (e != cudaSuccess) return KVP_ERR_CUDA;
+  }
+  if ((phases & KVP_PHASE_REDUCE) && sh.max_parts > 1) {
+    if (launch_decode_reduce(p, s) != cudaSuccess) return KVP_ERR_CUDA;
+  }
+  return KVP_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* kvp_status_string(kvp_status status) {
+  switch (status) {
+    case KVP_OK: return "KVP_OK";
+    case KVP_ERR_INVALID_ARG: return "KVP_ERR_INVALID_ARG";
+    case KVP_ERR_UNSUPPORTED: return "KVP_ERR_UNSUPPORTED";
+    case KVP_ERR_CUDA: return "KVP_ERR_CUDA";
+    case KVP_ERR_BAD_BLOCK: return "KVP_ERR_BAD_BLOCK";
+    case KVP_ERR_TIMEOUT: return "KVP_ERR_TIMEOUT";
+    case KVP_ERR_OOM: return "KVP_ERR_OOM";
+    case KVP_ERR_REFCOUNT: return "KVP_ERR_REFCOUNT";
+    case KVP_ERR_NOT_FOUND: return "KVP_ERR_NOT_FOUND";
+  }
+  return "KVP_ERR_UNKNOWN";
+}
+
+int32_t kvp_version(void) { return 100; }  // 0.1.0
+
+kvp_status kvp_append(const void* key, const void* value, void* k_cache, void* v_cache,
+                      const int32_t* slot_mapping, int32_t num_tokens, kvp_cache_desc cache,
+                      kvp_dtype dtype, int32_t* dev_status, kvp_stream_t stream) {
+  const kvp_status ds = check_desc(cache);
+  if (ds != KVP_OK) return ds;
+  if (num_tokens < 0 || (dtype != KVP_F16 && dtype != KVP_BF16)) return KVP_ERR_INVALID_ARG;
+  if (num_tokens == 0) return KVP_OK;
+  if (!key || !value || !k_cache || !v_cache || !slot_mapping) return KVP_ERR_INVALID_ARG;
+  if (!aligned(key, 16) || !aligned(value, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16))
+    return KVP_ERR_INVALID_ARG;
+  return from_cuda(launch_append(key, value, k_cache, v_cache, slot_mapping, num_tokens, cache, 2,
+                                 dev_status, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+kvp_status kvp_append_int8(const void* key, const void* value, kvp_dtype src_dtype,
+                           int8_t* k_cache, int8_t* v_cache, float* k_scale, float* v_scale,
+                           const int32_t* slot_mapping, int32_t num_tokens, kvp_cache_desc cache,
+                           int32_t* dev_status, kvp_stream_t stream) {
+  const kvp_status ds = check_desc(cache);
+  if (ds != KVP_OK) return ds;
+  if (num_tokens < 0 || (src_dtype != KVP_F16 && src_dtype != KVP_BF16))
+    return KVP_ERR_INVALID_ARG;
+  if (num_tokens == 0) return KVP_OK;
+  if (!key || !value || !k_cache || !v_cache || !k_scale || !v_scale || !slot_mapping)
+    return KVP_ERR_INVALID_ARG;
+  if (!aligned(key, 8) || !aligned(value, 8) || !aligned(k_cache, 4) || !aligned(v_cache, 4) ||
+      !aligned(k_scale, 4) || !aligned(v_scale, 4))
+    return KVP_ERR_INVALID_ARG;
+  return from_cuda(launch_append_int8(key, value, src_dtype == KVP_BF16, k_cache, v_cache, k_scale,
+                                      v_scale, slot_mapping, num_tokens, cache, dev_status,
+                                      reinterpret_cast<cudaStream_t>(stream)));
+}
+
+kvp_status kvp_copy_blocks(void* k_cache, void* v_cache, float* k_scale, float* v_scale,
+                           int32_t cache_elem_bytes, const int32_t* pairs, int32_t num_pairs,
+                           kvp_cache_desc cache, int32_t* dev_status, kvp_stream_t stream) {
+  const kvp_status ds = check_desc(cache);
+  if (ds != KVP_OK) return ds;
+  if (num_pairs < 0 || (cache_elem_bytes != 1 && cache_elem_bytes != 2))
+    return KVP_ERR_INVALID_ARG;
+  if ((k_scale == nullptr) != (v_scale == nullptr)) return KVP_ERR_INVALID_ARG;
+  if (num_pairs == 0) return KVP_OK;
+  if (!k_cache || !v_cache || !pairs) return KVP_ERR_INVALID_ARG;
+  if (!aligned(k_cache, 16) || !aligned(v_cache, 16)) return KVP_ERR_INVALID_ARG;
+  if (k_scale && (!aligned(k_scale, 16) || !aligned(v_scale, 16))) return KVP_ERR_INVALID_ARG;
+  return from_cuda(launch_copy_blocks(k_cache, v_cache, k_scale, v_scale, cache_elem_bytes, pairs,
+                                      num_pairs, cache, dev_status,
+                                      reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int32_t kvp_decode_partition_blocks(int32_t batch, int32_t num_q_heads, kvp_cache_desc cache,
+                                    int32_t max_blocks_per_seq, int32_t kv_int8) {
+  DecodeShape sh;
+  if (shape_decode(batch, num_q_heads, cache, max_blocks_per_seq, 0, kv_int8 != 0, &sh) != KVP_OK)
+    return 0;
+  return sh.part_blocks;
+}
+
+size_t kvp_decode_workspace_bytes(int32_t batch, int32_t num_q_heads, kvp_cache_desc cache,
+                                  int32_t max_blocks_per_seq, int32_t partition_blocks,
+                                  int32_t kv_int8) {
+  DecodeShape sh;
+  if (shape_decode(batch, num_q_heads, cache, max_blocks_per_seq, partition_blocks, kv_int8 != 0,
+                   &sh) != KVP_OK)
+    return 0;
+  return sh.ws_bytes;
+}
+
+kvp_status kvp_attention_decode(void* out, const void* q, const void* k_cache,
+                                const void* v_cache, const int32_t* block_tables,
+                                int32_t max_blocks_per_seq, const int32_t* context_lens,
+                                int32_t batch, int32_t num_q_heads, float scale,
+                                kvp_cache_desc cache, kvp_dtype dtype, int32_t partition_blocks,
+                                void* workspace, size_t workspace_bytes, int32_t phases,
+                                int32_t* dev_status, kvp_stream_t stream) {
+  if (dtype != KVP_F16 && dtype != KVP_BF16) return KVP_ERR_INVALID_ARG;
+  return decode_common(out, q, dtype == KVP_BF16, dtype == KVP_BF16 ? 1 : 0, k_cache, v_cache,
+                       nullptr, nullptr, block_tables, max_blocks_per_seq, context_lens, batch,
+                       num_q_heads, scale, cache, partition_blocks, workspace, workspace_bytes,
+                       phases, dev_status, stream);
+}
+
+kvp_status kvp_attention_decode_int8(void* out, const void* q, kvp_dtype q_dtype,
+                                     const int8_t* k_cache, const int8_t* v_cache,
+                                     const float* k_scale, const float* v_scale,
+                                     const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                     const int32_t* context_lens, int32_t batch,
+                                     int32_t num_q_heads, float scale, kvp_cache_desc cache,
+                                     int32_t partition_blocks, void* workspace,
+                                     size_t workspace_bytes, int32_t phases,
+                                     int32_t* dev_status, kvp_stream_t stream) {
+  if (q_dtype != KVP_F16 && q_dtype != KVP_BF16) return KVP_ERR_INVALID_ARG;
+  return decode_common(out, q, q_dtype == KVP_BF16, 2, k_cache, v_cache, k_scale, v_scale,
+                       block_tables, max_blocks_per_seq, context_lens, batch, num_q_heads, scale,
+                       cache, partition_blocks, workspace, workspace_bytes, phases, dev_status,
+                       stream);
+}
+
+kvp_status kvp_read_status(const int32_t* dev_status, kvp_stream_t stream) {
+  if (dev_status == nullptr) return KVP_ERR_INVALID_ARG;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  int32_t v = 0;
+  if (cudaMemcpyAsync(&v, dev_status, sizeof v, cudaMemcpyDeviceToHost, s) != cudaSuccess)
+    return KVP_ERR_CUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return KVP_ERR_CUDA;
+  if (v < KVP_OK || v > KVP_ERR_NOT_FOUND) return KVP_ERR_CUDA;
+  return static_cast<kvp_status>(v);
+}
+
+}  // extern "C"

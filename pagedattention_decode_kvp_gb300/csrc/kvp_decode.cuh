@@ -1,0 +1,787 @@
+// kvp_decode.cuh -- paged-KV decode attention kernels for sm_103a.
+//
+// What is computed ("ATB PagedAttention", "PagedAttention 的 Attention 计算修改";
+// "KV Cache 优化与显存管理", 二): for request b with n = context_lens[b] and
+// query head h, out[b,h] = sum_i softmax_i(scale * q.K_i) V_i over the n cached
+// tokens, K_i/V_i gathered through the block table (16 tokens per block) from
+// K/V head h / G.  The pages walk one page at a time with an online softmax;
+// here that walk is reorganised for GB300:
+//
+//   * One CTA per (request, kv head, split-context partition) serves the whole
+//     query group of that kv head, so each K/V byte is read from HBM once.
+//   * The CTA's slice of the block table is staged in shared memory first
+//     ("踩坑一": the page table is copied on chip once, not looked up in HBM per
+//     page) and every id is range-checked before any copy is issued.
+//   * Each of the CTA's 4 warps owns a ring of 2 shared-memory stages.  Lane 0
+//     issues TMA tensor copies (cp.async.bulk.tensor, 128-byte swizzle) of the
+//     block's K and V tiles ([16 tokens][D] contiguous per (block, head)) into
+//     a stage, completing on an mbarrier; the warp consumes blocks
+//     w, w+4, w+8, ... with its own online-softmax state, refilling each stage
+//     as soon as it is consumed.  Across 3 resident CTAs this keeps ~100 KB of
+//     K/V in flight per SM.
+//   * Consumers: CUDA cores (fp32 FMA, shuffle reductions) when a kv head serves
+//     1-2 query heads; warp tensor cores (mma.m16n8k16, fp32 accumulate) when it
+//     serves 3-8 query heads, where S^T = K Q^T (16 tokens x 8 heads) and
+//     O^T += V^T P^T (D x 8 heads) per block are genuine dense tiles.
+//   * The warps' partial states are merged in shared memory; a request that
+//     fits one partition writes its output directly, otherwise the partition
+//     writes (m, l, o) to the workspace for the reduce kernel (flash-decoding).
+#pragma once
+
+#include "kvp_device.cuh"
+#include "kvp_internal.h"
+
+namespace kvp {
+
+__device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
+  return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
+}
+
+// ---------------------------------------------------------------------------
+// Shuffle reduction of N partial sums held by every lane across groups of L
+// lanes (N <= L, both powers of two): each step halves the number of values a
+// lane holds while summing over one lane bit, so N values need N-1 shuffles
+// instead of N*log2(L).  Afterwards lane l holds the full sum of value index
+// (l % L) >> log2(L / N).
+template <int N, int BIT>
+struct Butterfly {
+  __device__ __forceinline__ static void run(float* v, int lane) {
+    if constexpr (BIT >= 1) {
+      if constexpr (N > 1) {
+        const bool upper = (lane & BIT) != 0;
+#pragma unroll
+        for (int i = 0; i < N / 2; ++i) {
+          const float send = upper ? v[i] : v[i + N / 2];
+          const float keep = upper ? v[i + N / 2] : v[i];
+          v[i] = keep + __shfl_xor_sync(0xffffffffu, send, BIT);
+        }
+        Butterfly<N / 2, BIT / 2>::run(v, lane);
+      } else {
+        v[0] += __shfl_xor_sync(0xffffffffu, v[0], BIT);
+        Butterfly<1, BIT / 2>::run(v, lane);
+      }
+    }
+  }
+};
+
+constexpr int ilog2(int x) { return x <= 1 ? 0 : 1 + ilog2(x / 2); }
+
+// Offset of 16-byte chunk c of token row t in a 16-bit tile whose rows are
+// split into 128-byte TMA boxes ([box][16 rows][128 B], 128-byte swizzle).
+__device__ __forceinline__ uint32_t tile16_off(int t, int c) {
+  return static_cast<uint32_t>((c >> 3) * (16 * 128)) +
+         dev::swz128(static_cast<uint32_t>(t * 128 + ((c & 7) << 4)));
+}
+
+// ===========================================================================
+// CUDA-core consumer: a kv head serving G = 1 or 2 query heads.
+// Lane (c, r): c = lane % (D/8) owns elements [8c, 8c+8) of every row,
+// r = lane / (D/8) owns tokens r, r + R, ... (R = 32 / (D/8) rows per pass).
+template <bool kBf16, int D, int G>
+struct SimtPath {
+  static constexpr int kD = D;
+  static constexpr int kHeads = G;
+  static constexpr int kElemBytes = 2;
+  static constexpr int kTileBytes = 16 * D * 2;
+  static constexpr int kScaleStageBytes = 0;
+  static constexpr int kLpr = D / 8;        // lanes per row
+  static constexpr int kRpp = 32 / kLpr;    // rows per pass
+  static constexpr int kKpl = 16 / kRpp;    // tokens per lane
+  static constexpr int kNv = G * kKpl;      // partial scores per lane
+  static_assert(kNv <= kLpr, "score reduction assumes at most one value per lane");
+  static constexpr int kSh = ilog2(kLpr / kNv);
+
+  struct State {
+    float q[G][8];
+    float o[G][8];
+    float m[G];
+    float l[G];
+  };
+
+  __device__ __forceinline__ static void init(State& st, const DecodeParams& p, int b, int head0,
+                                              int /*nheads*/, int lane) {
+    const int c = lane % kLpr;
+    const uint16_t* q = static_cast<const uint16_t*>(p.q);
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+      const uint4 raw = *reinterpret_cast<const uint4*>(
+          q + (static_cast<size_t>(b) * p.num_q_heads + head0 + g) * D + c * 8);
+      const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float2 f = dev::unpack2<kBf16>(w[i]);
+        st.q[g][2 * i] = f.x;
+        st.q[g][2 * i + 1] = f.y;
+      }
+#pragma unroll
+      for (int e = 0; e < 8; ++e) st.o[g][e] = 0.f;
+      st.m[g] = -INFINITY;
+      st.l[g] = 0.f;
+    }
+  }
+
+  __device__ __forceinline__ static void consume(State& st, const uint8_t* kt, const uint8_t* vt,
+                                                 const float*, int valid, int lane,
+                                                 float scale_log2) {
+    const int c = lane % kLpr;
+    const int r = lane / kLpr;
+    float ps[kNv];
+#pragma unroll
+    for (int k = 0; k < kKpl; ++k) {
+      const uint4 raw = *reinterpret_cast<const uint4*>(kt + tile16_off(r + kRpp * k, c));
+      const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+      float kf[8];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float2 f = dev::unpack2<kBf16>(w[i]);
+        kf[2 * i] = f.x;
+        kf[2 * i + 1] = f.y;
+      }
+#pragma unroll
+      for (int g = 0; g < G; ++g) {
+        float acc = 0.f;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) acc = fmaf(st.q[g][e], kf[e], acc);
+        ps[g * kKpl + k] = acc;
+      }
+    }
+    Butterfly<kNv, kLpr / 2>::run(ps, lane);
+    const int v = (lane % kLpr) >> kSh;
+    const int gl = v / kKpl;
+    const int tl = r + kRpp * (v % kKpl);
+    float s = ps[0] * scale_log2;
+    if (tl >= valid) s = -INFINITY;
+
+    float mine_m = 0.f;
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+      const float mb = dev::warp_max((G == 1 || gl == g) ? s : -INFINITY);
+      const float mn = fmaxf(st.m[g], mb);
+      if (mn > st.m[g]) {  // warp-uniform
+        const float a = exp2f(st.m[g] - mn);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) st.o[g][e] *= a;
+        st.l[g] *= a;
+        st.m[g] = mn;
+      }
+      if (G == 1 || gl == g) mine_m = st.m[g];
+    }
+    const float pe = exp2f(s - mine_m);
+    const bool owner = ((lane % kLpr) & ((1 << kSh) - 1)) == 0;
+#pragma unroll
+    for (int g = 0; g < G; ++g) st.l[g] += (owner && (G == 1 || gl == g)) ? pe : 0.f;
+
+#pragma unroll
+    for (int k = 0; k < kKpl; ++k) {
+      const int t = r + kRpp * k;
+      const uint4 raw = *reinterpret_cast<const uint4*>(vt + tile16_off(t, c));
+      const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+      float vf[8];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float2 f = dev::unpack2<kBf16>(w[i]);
+        vf[2 * i] = f.x;
+        vf[2 * i + 1] = f.y;
+      }
+#pragma unroll
+      for (int g = 0; g < G; ++g) {
+        const float pk = __shfl_sync(0xffffffffu, pe, r * kLpr + ((g * kKpl + k) << kSh));
+        if (t < valid) {  // slots past the context may hold anything, even NaN
+#pragma unroll
+          for (int e = 0; e < 8; ++e) st.o[g][e] = fmaf(pk, vf[e], st.o[g][e]);
+        }
+      }
+    }
+  }
+
+  // Write this warp's (m, l, o[head][D]) to the merge area.
+  __device__ __forceinline__ static void finalize(State& st, float* mo, float* mm, float* ml,
+                                                  int lane) {
+    const int c = lane % kLpr;
+    const int r = lane / kLpr;
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        float x = st.o[g][e];
+#pragma unroll
+        for (int o = kLpr; o < 32; o <<= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+        st.o[g][e] = x;
+      }
+      const float lsum = dev::warp_sum(st.l[g]);
+      if (r == 0) {
+        float4* dst = reinterpret_cast<float4*>(mo + g * D + c * 8);
+        dst[0] = make_float4(st.o[g][0], st.o[g][1], st.o[g][2], st.o[g][3]);
+        dst[1] = make_float4(st.o[g][4], st.o[g][5], st.o[g][6], st.o[g][7]);
+      }
+      if (lane == 0) {
+        mm[g] = st.m[g];
+        ml[g] = lsum;
+      }
+    }
+  }
+};
+
+// ===========================================================================
+// Tensor-core consumer for 16-bit pools: up to 8 query heads per kv head.
+// Per block: S^T[16 tok x 8 heads] = K[16 x D] . Q^T[D x 8] (D/16 mma) and
+// O^T[D x 8] += V^T[D x 16] . P^T[16 x 8] (D/16 mma; bf16 P is split into a
+// bf16 high part and a bf16 residual so P keeps ~16 significant bits).
+// Fragments: g8 = lane / 4, t4 = lane % 4 (the mma "group" and "thread in group").
+template <bool kBf16, int D>
+struct MmaPath {
+  static constexpr int kD = D;
+  static constexpr int kHeads = 8;
+  static constexpr int kElemBytes = 2;
+  static constexpr int kTileBytes = 16 * D * 2;
+  static constexpr int kScaleStageBytes = 0;
+  static constexpr int kMt = D / 16;
+
+  struct State {
+    uint32_t qb[kMt][2];
+    float o[kMt][4];
+    float m[2];
+    float l[2];
+  };
+
+  __device__ __forceinline__ static void init(State& st, const DecodeParams& p, int b, int head0,
+                                              int nheads, int lane) {
+    const int g8 = lane >> 2, t4 = lane & 3;
+    const uint16_t* q = static_cast<const uint16_t*>(p.q) +
+                        (static_cast<size_t>(b) * p.num_q_heads + head0 + g8) * D;
+#pragma unroll
+    for (int s = 0; s < kMt; ++s) {
+      if (g8 < nheads) {
+        st.qb[s][0] = *reinterpret_cast<const uint32_t*>(q + 16 * s + 2 * t4);
+        st.qb[s][1] = *reinterpret_cast<const uint32_t*>(q + 16 * s + 2 * t4 + 8);
+      } else {
+        st.qb[s][0] = 0u;
+        st.qb[s][1] = 0u;
+      }
+#pragma unroll
+      for (int i = 0; i < 4; ++i) st.o[s][i] = 0.f;
+    }
+    st.m[0] = st.m[1] = -INFINITY;
+    st.l[0] = st.l[1] = 0.f;
+  }
+
+  __device__ __forceinline__ static void consume(State& st, const uint8_t* kt, const uint8_t* vt,
+                                                 const float*, int valid, int lane,
+                                                 float scale_log2) {
+    const int g8 = lane >> 2, t4 = lane & 3;
+    const uint32_t kbase = dev::smem_addr(kt);
+    const uint32_t vbase = dev::smem_addr(vt);
+    // ---- scores: S^T = K Q^T
+    float sacc[4] = {0.f, 0.f, 0.f, 0.f};
+    const int tok_a = (lane & 7) + ((lane >> 3) & 1) * 8;
+    const int ch_a = lane >> 4;
+#pragma unroll
+    for (int s = 0; s < kMt; ++s) {
+      uint32_t a0, a1, a2, a3;
+      dev::ldsm_x4(kbase + tile16_off(tok_a, 2 * s + ch_a), a0, a1, a2, a3);
+      dev::mma16816<kBf16>(sacc, a0, a1, a2, a3, st.qb[s][0], st.qb[s][1]);
+    }
+    float s0 = sacc[0] * scale_log2, s1 = sacc[1] * scale_log2;
+    float s2 = sacc[2] * scale_log2, s3 = sacc[3] * scale_log2;
+    if (valid < 16) {
+      if (g8 >= valid) s0 = s1 = -INFINITY;
+      if (g8 + 8 >= valid) s2 = s3 = -INFINITY;
+    }
+    // ---- online softmax (per head: heads 2*t4 and 2*t4+1 live in this lane)
+    float mx0 = fmaxf(s0, s2), mx1 = fmaxf(s1, s3);
+#pragma unroll
+    for (int o = 4; o < 32; o <<= 1) {
+      mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o));
+      mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o));
+    }
+    const float mn0 = fmaxf(st.m[0], mx0), mn1 = fmaxf(st.m[1], mx1);
+    if (__any_sync(0xffffffffu, (mn0 > st.m[0]) || (mn1 > st.m[1]))) {
+      const float al0 = exp2f(st.m[0] - mn0), al1 = exp2f(st.m[1] - mn1);
+#pragma unroll
+      for (int mt = 0; mt < kMt; ++mt) {
+        st.o[mt][0] *= al0;
+        st.o[mt][1] *= al1;
+        st.o[mt][2] *= al0;
+        st.o[mt][3] *= al1;
+      }
+      st.l[0] *= al0;
+      st.l[1] *= al1;
+      st.m[0] = mn0;
+      st.m[1] = mn1;
+    }
+    const float p0 = exp2f(s0 - st.m[0]), p1 = exp2f(s1 - st.m[1]);
+    const float p2 = exp2f(s2 - st.m[0]), p3 = exp2f(s3 - st.m[1]);
+    st.l[0] += p0 + p2;
+    st.l[1] += p1 + p3;
+    // ---- P^T as the B operand: transpose the (token x head) fragments
+    const uint32_t x01 = dev::pack2<kBf16>(p0, p1);
+    const uint32_t x23 = dev::pack2<kBf16>(p2, p3);
+    const uint32_t b0 = dev::movm_t(x01);
+    const uint32_t b1 = dev::movm_t(x23);
+    uint32_t b0r = 0, b1r = 0;
+    if constexpr (kBf16) {
+      const float2 h01 = dev::unpack2<true>(x01);
+      const float2 h23 = dev::unpack2<true>(x23);
+      b0r = dev::movm_t(dev::pack2<true>(p0 - h01.x, p1 - h01.y));
+      b1r = dev::movm_t(dev::pack2<true>(p2 - h23.x, p3 - h23.y));
+    }
+    // ---- O^T += V^T P^T
+    uint32_t m01 = 0xffffffffu, m23 = 0xffffffffu;
+    if (valid < 16) {
+      m01 = (2 * t4 < valid ? 0x0000ffffu : 0u) | (2 * t4 + 1 < valid ? 0xffff0000u : 0u);
+      m23 = (2 * t4 + 8 < valid ? 0x0000ffffu : 0u) | (2 * t4 + 9 < valid ? 0xffff0000u : 0u);
+    }
+    const int tok_b = (lane & 7) + ((lane >> 4) & 1) * 8;
+    const int ch_b = (lane >> 3) & 1;
+#pragma unroll
+    for (int mt = 0; mt < kMt; ++mt) {
+      uint32_t a0, a1, a2, a3;
+      dev::ldsm_x4_t(vbase + tile16_off(tok_b, 2 * mt + ch_b), a0, a1, a2, a3);
+      a0 &= m01;
+      a1 &= m01;
+      a2 &= m23;
+      a3 &= m23;
+      dev::mma16816<kBf16>(st.o[mt], a0, a1, a2, a3, b0, b1);
+      if constexpr (kBf16) dev::mma16816<true>(st.o[mt], a0, a1, a2, a3, b0r, b1r);
+    }
+  }
+
+  __device__ __forceinline__ static void finalize(State& st, float* mo, float* mm, float* ml,
+                                                  int lane) {
+    const int g8 = lane >> 2, t4 = lane & 3;
+    float l0 = st.l[0], l1 = st.l[1];
+#pragma unroll
+    for (int o = 4; o < 32; o <<= 1) {
+      l0 += __shfl_xor_sync(0xffffffffu, l0, o);
+      l1 += __shfl_xor_sync(0xffffffffu, l1, o);
+    }
+#pragma unroll
+    for (int mt = 0; mt < kMt; ++mt) {
+      const int d = 16 * mt + g8;
+      mo[(2 * t4) * D + d] = st.o[mt][0];
+      mo[(2 * t4 + 1) * D + d] = st.o[mt][1];
+      mo[(2 * t4) * D + d + 8] = st.o[mt][2];
+      mo[(2 * t4 + 1) * D + d + 8] = st.o[mt][3];
+    }
+    if (g8 == 0) {
+      mm[2 * t4] = st.m[0];
+      mm[2 * t4 + 1] = st.m[1];
+      ml[2 * t4] = l0;
+      ml[2 * t4 + 1] = l1;
+    }
+  }
+};
+
+// ===========================================================================
+// Tensor-core consumer for INT8 pools (codes + per-token-per-head fp32 scales),
+// up to 8 query heads per kv head.  Codes convert exactly to fp16 (or bf16
+// when q is bf16).  The contraction index d is permuted so each lane reads a
+// contiguous run of codes: for K, lane t4 feeds d in [t4*D/4, (t4+1)*D/4); for
+// V, lane g8 produces d in [g8*D/8, (g8+1)*D/8).  The K scale multiplies the
+// 16 scores after the mma; the V scale is folded into P (normalised by the
+// block's largest V scale to stay in fp16 range) and restored in fp32.
+template <bool kQBf16, int D>
+struct MmaInt8Path {
+  static constexpr int kD = D;
+  static constexpr int kHeads = 8;
+  static constexpr int kElemBytes = 1;
+  static constexpr int kTileBytes = 16 * D;
+  static constexpr int kScaleStageBytes = 2 * 16 * 4;
+  static constexpr int kMt = D / 16;      // k-steps of QK and m-tiles of PV
+  static constexpr int kVw = D / 32;      // 32-bit words of V per token per lane
+
+  struct State {
+    uint32_t qb[kMt][2];
+    float o[kMt][4];
+    float m[2];
+    float l[2];
+  };
+
+  __device__ __forceinline__ static void init(State& st, const DecodeParams& p, int b, int head0,
+                                              int nheads, int lane) {
+    const int g8 = lane >> 2, t4 = lane & 3;
+    const uint16_t* q = static_cast<const uint16_t*>(p.q) +
+                        (static_cast<size_t>(b) * p.num_q_heads + head0 + g8) * D + (D / 4) * t4;
+#pragma unroll
+    for (int s = 0; s < kMt; ++s) {
+      if (g8 < nheads) {
+        const uint2 w = *reinterpret_cast<const uint2*>(q + 4 * s);
+        st.qb[s][0] = w.x;
+        st.qb[s][1] = w.y;
+      } else {
+        st.qb[s][0] = 0u;
+        st.qb[s][1] = 0u;
+      }
+#pragma unroll
+      for (int i = 0; i < 4; ++i) st.o[s][i] = 0.f;
+    }
+    st.m[0] = st.m[1] = -INFINITY;
+    st.l[0] = st.l[1] = 0.f;
+  }
+
+  template <bool kHigh>
+  __device__ __forceinline__ static uint32_t k_pair(uint32_t w) {
+    if constexpr (kQBf16) {
+      return dev::i8x2_to_bf16x2<kHigh>(w);
+    } else {
+      return dev::i8x2_to_f16x2<kHigh>(w ^ 0x80808080u);
+    }
+  }
+
+  __device__ __forceinline__ static void consume(State& st, const uint8_t* kt, const uint8_t* vt,
+                                                 const float* sc, int valid, int lane,
+                                                 float scale_log2) {
+    const int g8 = lane >> 2, t4 = lane & 3;
+    // ---- K codes of rows g8 and g8+8, bytes [t4*D/4, (t4+1)*D/4)
+    uint32_t k0[kMt], k1[kMt];
+#pragma unroll
+    for (int i = 0; i < kMt / 4; ++i) {
+      const uint32_t off = (D / 4) * t4 + 16 * i;
+      const uint4 r0 = *reinterpret_cast<const uint4*>(kt + dev::swz128(g8 * D + off));
+      const uint4 r1 = *reinterpret_cast<const uint4*>(kt + dev::swz128((g8 + 8) * D + off));
+      k0[4 * i] = r0.x; k0[4 * i + 1] = r0.y; k0[4 * i + 2] = r0.z; k0[4 * i + 3] = r0.w;
+      k1[4 * i] = r1.x; k1[4 * i + 1] = r1.y; k1[4 * i + 2] = r1.z; k1[4 * i + 3] = r1.w;
+    }
+    float sacc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int s = 0; s < kMt; ++s) {
+      dev::mma16816<kQBf16>(sacc, k_pair<false>(k0[s]), k_pair<false>(k1[s]), k_pair<true>(k0[s]),
+                            k_pair<true>(k1[s]), st.qb[s][0], st.qb[s][1]);
+    }
+    const float* ks = sc;
+    const float* vs = sc + 16;
+    const float kg = ks[g8] * scale_log2, kg8 = ks[g8 + 8] * scale_log2;
+    float s0 = sacc[0] * kg, s1 = sacc[1] * kg, s2 = sacc[2] * kg8, s3 = sacc[3] * kg8;
+    const bool ok_lo = g8 < valid, ok_hi = g8 + 8 < valid;
+    if (!ok_lo) s0 = s1 = -INFINITY;
+    if (!ok_hi) s2 = s3 = -INFINITY;
+    // ---- online softmax
+    float mx0 = fmaxf(s0, s2), mx1 = fmaxf(s1, s3);
+#pragma unroll
+    for (int o = 4; o < 32; o <<= 1) {
+      mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o));
+      mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o));
+    }
+    const float mn0 = fmaxf(st.m[0], mx0), mn1 = fmaxf(st.m[1], mx1);
+    if (__any_sync(0xffffffffu, (mn0 > st.m[0]) || (mn1 > st.m[1]))) {
+      const float al0 = exp2f(st.m[0] - mn0), al1 = exp2f(st.m[1] - mn1);
+#pragma unroll
+      for (int mt = 0; mt < kMt; ++mt) {
+        st.o[mt][0] *= al0;
+        st.o[mt][1] *= al1;
+        st.o[mt][2] *= al0;
+        st.o[mt][3] *= al1;
+      }
+      st.l[0] *= al0;
+      st.l[1] *= al1;
+      st.m[0] = mn0;
+      st.m[1] = mn1;
+    }
+    const float p0 = exp2f(s0 - st.m[0]), p1 = exp2f(s1 - st.m[1]);
+    const float p2 = exp2f(s2 - st.m[0]), p3 = exp2f(s3 - st.m[1]);
+    st.l[0] += p0 + p2;
+    st.l[1] += p1 + p3;
+    // ---- fold the V scales into P (select, so NaN scales of unused slots vanish)
+    const float vg = ok_lo ? vs[g8] : 0.f, vg8 = ok_hi ? vs[g8 + 8] : 0.f;
+    float vmax = fmaxf(vg, vg8);
+#pragma unroll
+    for (int o = 4; o < 32; o <<= 1) vmax = fmaxf(vmax, __shfl_xor_sync(0xffffffffu, vmax, o));
+    const float inv = vmax > 0.f ? 1.f / vmax : 0.f;
+    const float r0 = vg * inv, r8 = vg8 * inv;
+    const uint32_t b0 = dev::movm_t(dev::pack2<false>(p0 * r0, p1 * r0));
+    const uint32_t b1 = dev::movm_t(dev::pack2<false>(p2 * r8, p3 * r8));
+    // ---- V codes of tokens 2t4, 2t4+1, 2t4+8, 2t4+9, bytes [g8*D/8, (g8+1)*D/8)
+    uint32_t va[kVw], vb[kVw], vc[kVw], vd[kVw];
+    {
+      const int ta = 2 * t4, tb = 2 * t4 + 1, tc = 2 * t4 + 8, td = 2 * t4 + 9;
+      const uint32_t off = (D / 8) * g8;
+      if constexpr (kVw == 4) {
+        const uint4 ra = *reinterpret_cast<const uint4*>(vt + dev::swz128(ta * D + off));
+        const uint4 rb = *reinterpret_cast<const uint4*>(vt + dev::swz128(tb * D + off));
+        const uint4 rc = *reinterpret_cast<const uint4*>(vt + dev::swz128(tc * D + off));
+        const uint4 rd = *reinterpret_cast<const uint4*>(vt + dev::swz128(td * D + off));
+        va[0] = ra.x; va[1] = ra.y; va[2] = ra.z; va[3] = ra.w;
+        vb[0] = rb.x; vb[1] = rb.y; vb[2] = rb.z; vb[3] = rb.w;
+        vc[0] = rc.x; vc[1] = rc.y; vc[2] = rc.z; vc[3] = rc.w;
+        vd[0] = rd.x; vd[1] = rd.y; vd[2] = rd.z; vd[3] = rd.w;
+      } else {
+        const uint2 ra = *reinterpret_cast<const uint2*>(vt + dev::swz128(ta * D + off));
+        const uint2 rb = *reinterpret_cast<const uint2*>(vt + dev::swz128(tb * D + off));
+        const uint2 rc = *reinterpret_cast<const uint2*>(vt + dev::swz128(tc * D + off));
+        const uint2 rd = *reinterpret_cast<const uint2*>(vt + dev::swz128(td * D + off));
+        va[0] = ra.x; va[1] = ra.y;
+        vb[0] = rb.x; vb[1] = rb.y;
+        vc[0] = rc.x; vc[1] = rc.y;
+        vd[0] = rd.x; vd[1] = rd.y;
+      }
+    }
+    float ct[kMt][4];
+#pragma unroll
+    for (int mt = 0; mt < kMt; ++mt) ct[mt][0] = ct[mt][1] = ct[mt][2] = ct[mt][3] = 0.f;
+#pragma unroll
+    for (int w = 0; w < kVw; ++w) {
+      const uint32_t A = va[w] ^ 0x80808080u, B = vb[w] ^ 0x80808080u;
+      const uint32_t C = vc[w] ^ 0x80808080u, E = vd[w] ^ 0x80808080u;
+      const uint32_t x = dev::prmt(A, B, 0x5140u), y = dev::prmt(A, B, 0x7362u);
+      const uint32_t xc = dev::prmt(C, E, 0x5140u), yc = dev::prmt(C, E, 0x7362u);
+      dev::mma16816<false>(ct[2 * w], dev::i8x2_to_f16x2<false>(x), dev::i8x2_to_f16x2<true>(x),
+                           dev::i8x2_to_f16x2<false>(xc), dev::i8x2_to_f16x2<true>(xc), b0, b1);
+      dev::mma16816<false>(ct[2 * w + 1], dev::i8x2_to_f16x2<false>(y),
+                           dev::i8x2_to_f16x2<true>(y), dev::i8x2_to_f16x2<false>(yc),
+                           dev::i8x2_to_f16x2<true>(yc), b0, b1);
+    }
+#pragma unroll
+    for (int mt = 0; mt < kMt; ++mt) {
+#pragma unroll
+      for (int i = 0; i < 4; ++i) st.o[mt][i] = fmaf(ct[mt][i], vmax, st.o[mt][i]);
+    }
+  }
+
+  __device__ __forceinline__ static void finalize(State& st, float* mo, float* mm, float* ml,
+                                                  int lane) {
+    const int g8 = lane >> 2, t4 = lane & 3;
+    float l0 = st.l[0], l1 = st.l[1];
+#pragma unroll
+    for (int o = 4; o < 32; o <<= 1) {
+      l0 += __shfl_xor_sync(0xffffffffu, l0, o);
+      l1 += __shfl_xor_sync(0xffffffffu, l1, o);
+    }
+#pragma unroll
+    for (int mt = 0; mt < kMt; ++mt) {
+      const int d = (D / 8) * g8 + 2 * mt;
+      mo[(2 * t4) * D + d] = st.o[mt][0];
+      mo[(2 * t4 + 1) * D + d] = st.o[mt][1];
+      mo[(2 * t4) * D + d + 1] = st.o[mt][2];
+      mo[(2 * t4 + 1) * D + d + 1] = st.o[mt][3];
+    }
+    if (g8 == 0) {
+      mm[2 * t4] = st.m[0];
+      mm[2 * t4 + 1] = st.m[1];
+      ml[2 * t4] = l0;
+      ml[2 * t4 + 1] = l1;
+    }
+  }
+};
+
+// ===========================================================================
+template <class Path>
+constexpr size_t decode_smem_for(int part_blocks) {
+  constexpr int S = kWarps * kStagesPerWarp;
+  return 1024 + static_cast<size_t>(S) * 2 * Path::kTileBytes +
+         static_cast<size_t>(S) * Path::kScaleStageBytes + S * 8 +
+         static_cast<size_t>(part_blocks) * 4 + 16;
+}
+
+// Zero the output rows [b, head0 .. head0+nheads) (requests with no tokens or
+// with an invalid length).
+template <int D>
+__device__ __forceinline__ void zero_rows(const DecodeParams& p, int b, int head0, int nheads) {
+  uint16_t* out = static_cast<uint16_t*>(p.out) +
+                  (static_cast<size_t>(b) * p.num_q_heads + head0) * D;
+  for (int i = threadIdx.x; i < nheads * D; i += blockDim.x) out[i] = 0;
+}
+
+template <class Path>
+__global__ void __launch_bounds__(kWarps * 32)
+    decode_partial_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmk,
+                          const __grid_constant__ CUtensorMap tmv) {
+  using namespace dev;
+  constexpr int S = kWarps * kStagesPerWarp;
+  constexpr int TB = Path::kTileBytes;
+  constexpr int SB = Path::kScaleStageBytes;
+  constexpr int H = Path::kHeads;
+  constexpr int D = Path::kD;
+  constexpr int kRowBytes = D * Path::kElemBytes;
+  constexpr int kBoxBytes = kRowBytes < 128 ? kRowBytes : 128;  // inner extent of a TMA box
+  constexpr int kBoxes = kRowBytes / kBoxBytes;                 // TMA boxes per tile
+  static_assert(kWarps * H * (D + 2) * 4 <= S * 2 * TB, "merge area must fit in the stages");
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = align1024(smem_raw);
+  uint8_t* stages = smem;
+  float* scales = reinterpret_cast<float*>(smem + S * 2 * TB);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S * 2 * TB + S * SB);
+  int32_t* tbl = reinterpret_cast<int32_t*>(bars + S);
+  __shared__ int cta_flag;
+
+  const int part = blockIdx.x;
+  const int kvh = blockIdx.y / p.qgroups;
+  const int qg = blockIdx.y % p.qgroups;
+  const int b = blockIdx.z;
+  const int head0 = kvh * p.group + qg * p.heads_per_cta;
+  const int nheads = min(p.heads_per_cta, p.group - qg * p.heads_per_cta);
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  const int n = p.context_lens[b];
+  if (n <= 0 || n > p.max_blocks * kBlockSize) {
+    if (part == 0) {
+      zero_rows<D>(p, b, head0, nheads);
+      if (n != 0 && threadIdx.x == 0) set_status(p.status, kErrBadBlock);
+    }
+    return;
+  }
+  const int nblk_seq = (n + kBlockSize - 1) / kBlockSize;
+  const int nparts = (nblk_seq + p.part_blocks - 1) / p.part_blocks;
+  const int blk0 = part * p.part_blocks;
+  if (blk0 >= nblk_seq) return;
+  const int nb = min(p.part_blocks, nblk_seq - blk0);
+  const bool last_part = blk0 + nb == nblk_seq;
+  const int tail_valid = n - (nblk_seq - 1) * kBlockSize;
+
+  // ---- stage this partition's slice of the block table and check every id
+  bool bad = false;
+  const int32_t* row = p.block_tables + static_cast<size_t>(b) * p.max_blocks + blk0;
+  for (int i = threadIdx.x; i < nb; i += blockDim.x) {
+    const int id = row[i];
+    bad |= (id < 0) || (id >= p.num_blocks);
+    tbl[i] = id;
+  }
+  if (threadIdx.x == 0) {
+    cta_flag = 0;
+    prefetch_tensormap(&tmk);
+    prefetch_tensormap(&tmv);
+#pragma unroll
+    for (int s = 0; s < S; ++s) mbar_init(smem_addr(bars + s), 1);
+    fence_barrier_init();
+  }
+  const bool any_bad = __syncthreads_or(bad);
+
+  const float* ksrc = p.k_scale;
+  const float* vsrc = p.v_scale;
+  auto issue = [&](int j) {  // lane 0 of this warp: fetch the warp's j-th block
+    const int i = warp + j * kWarps;
+    const int stage = warp * kStagesPerWarp + (j % kStagesPerWarp);
+    const uint32_t bar = smem_addr(bars + stage);
+    uint8_t* kdst = stages + stage * 2 * TB;
+    uint8_t* vdst = kdst + TB;
+    const int y = (tbl[i] * p.num_kv_heads + kvh) * kBlockSize;
+    mbar_arrive_expect_tx(bar, 2 * TB + SB);
+#pragma unroll
+    for (int x = 0; x < kBoxes; ++x) {
+      const int xe = x * (kBoxBytes / Path::kElemBytes);
+      tma_load_2d(smem_addr(kdst + x * 16 * kBoxBytes), &tmk, xe, y, bar);
+      tma_load_2d(smem_addr(vdst + x * 16 * kBoxBytes), &tmv, xe, y, bar);
+    }
+    if constexpr (SB > 0) {
+      float* sdst = scales + stage * (SB / 4);
+      bulk_load(smem_addr(sdst), ksrc + y, 64, bar);
+      bulk_load(smem_addr(sdst + 16), vsrc + y, 64, bar);
+    }
+  };
+
+  typename Path::State st;
+  bool ok = !any_bad;
+  if (ok) {
+    Path::init(st, p, b, head0, nheads, lane);
+    const int my_blocks = nb > warp ? (nb - warp + kWarps - 1) / kWarps : 0;
+    const int prologue = my_blocks < kStagesPerWarp ? my_blocks : kStagesPerWarp;
+    if (lane == 0) {
+      for (int j = 0; j < prologue; ++j) issue(j);
+    }
+    int issued = prologue;
+    int j = 0;
+    for (; j < my_blocks; ++j) {
+      const int stage = warp * kStagesPerWarp + (j % kStagesPerWarp);
+      const bool landed = mbar_wait_bounded(smem_addr(bars + stage), (j / kStagesPerWarp) & 1);
+      if (!__all_sync(0xffffffffu, landed)) {
+        ok = false;
+        break;
+      }
+      const int i = warp + j * kWarps;
+      const int valid = (last_part && i == nb - 1) ? tail_valid : kBlockSize;
+      const uint8_t* kt = stages + stage * 2 * TB;
+      Path::consume(st, kt, kt + TB, scales + stage * (SB / 4), valid, lane, p.scale_log2);
+      __syncwarp();
+      if (j + kStagesPerWarp < my_blocks) {
+        if (lane == 0) {
+          fence_proxy_async_smem();
+          issue(j + kStagesPerWarp);
+        }
+        ++issued;
+      }
+    }
+    if (!ok) {
+      // A transfer did not land in time: wait (bounded) for this warp's copies
+      // still in flight so no TMA write outlives the CTA, then report.
+      if (lane == 0) {
+        for (int jj = j; jj < issued; ++jj) {
+          const int stage = warp * kStagesPerWarp + (jj % kStagesPerWarp);
+          mbar_wait_bounded(smem_addr(bars + stage), (jj / kStagesPerWarp) & 1);
+        }
+        set_status(p.status, kErrTimeout);
+        atomicExch(&cta_flag, 1);
+      }
+    }
+  } else if (threadIdx.x == 0) {
+    set_status(p.status, kErrBadBlock);
+  }
+
+  // ---- merge the warps' partial states (stage memory is free now)
+  __syncthreads();
+  const bool cta_bad = any_bad || cta_flag != 0;
+  float* mo = reinterpret_cast<float*>(smem);
+  float* mm = mo + kWarps * H * D;
+  float* ml = mm + kWarps * H;
+  if (!cta_bad) Path::finalize(st, mo + warp * H * D, mm + warp * H, ml + warp * H, lane);
+  __syncthreads();
+
+  const size_t rowbase = static_cast<size_t>(b) * p.num_q_heads + head0;
+  if (nparts == 1) {
+    uint16_t* out = static_cast<uint16_t*>(p.out) + rowbase * D;
+    for (int idx = threadIdx.x; idx < nheads * D; idx += blockDim.x) {
+      const int hh = idx / D, d = idx % D;
+      float res = 0.f;
+      if (!cta_bad) {
+        float M = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w) M = fmaxf(M, mm[w * H + hh]);
+        float L = 0.f, acc = 0.f;
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w) {
+          const float f = exp2f(mm[w * H + hh] - M);
+          L = fmaf(f, ml[w * H + hh], L);
+          acc = fmaf(f, mo[(w * H + hh) * D + d], acc);
+        }
+        res = L > 0.f ? acc / L : 0.f;
+      }
+      out[idx] = p.q_bf16 ? from_float<true>(res) : from_float<false>(res);
+    }
+  } else {
+    for (int idx = threadIdx.x; idx < nheads * D; idx += blockDim.x) {
+      const int hh = idx / D, d = idx % D;
+      float M = -INFINITY, L = -1.f, acc = 0.f;  // L < 0 marks a failed partition
+      if (!cta_bad) {
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w) M = fmaxf(M, mm[w * H + hh]);
+        L = 0.f;
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w) {
+          const float f = exp2f(mm[w * H + hh] - M);
+          L = fmaf(f, ml[w * H + hh], L);
+          acc = fmaf(f, mo[(w * H + hh) * D + d], acc);
+        }
+      }
+      const size_t prow = (rowbase + hh) * p.max_parts + part;
+      p.ws_o[prow * D + d] = acc;
+      if (d == 0) {
+        p.ws_ml[2 * prow] = M;
+        p.ws_ml[2 * prow + 1] = L;
+      }
+    }
+  }
+}
+
+template <class Path>
+cudaError_t launch_partial(const DecodeParams& p, const CUtensorMap& tk, const CUtensorMap& tv,
+                           int grid_x, cudaStream_t s) {
+  const size_t smem = decode_smem_for<Path>(p.part_blocks);
+  cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(&decode_partial_kernel<Path>),
+                                   decode_smem_for<Path>(kMaxPartBlocks));
+  if (e != cudaSuccess) return e;
+  dim3 grid(grid_x, p.num_kv_heads * p.qgroups, p.batch);
+  decode_partial_kernel<Path><<<grid, kWarps * 32, smem, s>>>(p, tk, tv);
+  return cudaGetLastError();
+}
+
+}  // namespace kvp

@@ -1,0 +1,73 @@
+// kvp_internal.h -- declarations shared by the library's translation units.
+// Not part of the public ABI (see include/kvp.h).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "kvp.h"
+
+namespace kvp {
+
+constexpr int kBlockSize = 16;       // tokens per cache block
+constexpr int kWarps = 4;            // consumer warps per decode CTA
+constexpr int kStagesPerWarp = 2;    // pipeline depth of each warp's ring
+constexpr int kHeadsPerCta = 8;      // query heads one tensor-core CTA serves
+constexpr int kMaxPartBlocks = 1024;  // table slice staged per CTA (4 KB)
+
+// Decode kernel family.
+enum class DecodePath : int { kSimt = 0, kMma = 1, kMmaInt8 = 2 };
+
+// Everything a decode launch needs besides the two tensor maps.
+struct DecodeParams {
+  void* out;                    // [B, Hq, D] of q dtype
+  const void* q;                // [B, Hq, D]
+  const float* k_scale;         // [NB, Hkv, bs] (INT8 pools only)
+  const float* v_scale;
+  const int32_t* block_tables;  // [B, MB]
+  const int32_t* context_lens;  // [B]
+  float* ws_o;                  // [B, Hq, P, D]
+  float* ws_ml;                 // [B, Hq, P, 2]  (running max in log2 units, sum)
+  int32_t* status;              // nullable
+  int32_t batch, num_q_heads, num_kv_heads, head_dim, num_blocks, max_blocks;
+  int32_t group;                // Hq / Hkv
+  int32_t qgroups;              // CTAs per kv head along the query group
+  int32_t heads_per_cta;        // query heads handled by one CTA
+  int32_t part_blocks;          // blocks per partition
+  int32_t max_parts;            // ceil(MB / part_blocks)
+  float scale_log2;             // scale * log2(e)
+  int32_t q_bf16;               // q / out are bf16 (else fp16)
+};
+
+// Device error codes (mirror kvp_status).
+constexpr int32_t kErrBadBlock = KVP_ERR_BAD_BLOCK;
+constexpr int32_t kErrTimeout = KVP_ERR_TIMEOUT;
+
+// Host launchers implemented in the kernel translation units.  Each returns a
+// cudaError_t from the launch.
+cudaError_t launch_decode_simt(const DecodeParams& p, const CUtensorMap& tk,
+                               const CUtensorMap& tv, bool kv_bf16, int grid_x,
+                               cudaStream_t s);
+cudaError_t launch_decode_mma(const DecodeParams& p, const CUtensorMap& tk,
+                              const CUtensorMap& tv, bool kv_bf16, int grid_x, cudaStream_t s);
+cudaError_t launch_decode_mma_int8(const DecodeParams& p, const CUtensorMap& tk,
+                                   const CUtensorMap& tv, int grid_x, cudaStream_t s);
+cudaError_t launch_decode_reduce(const DecodeParams& p, cudaStream_t s);
+
+// Raise a kernel's dynamic shared-memory limit to `bytes` on the current
+// device (once per device and kernel).
+cudaError_t ensure_smem_attr(const void* kernel, size_t bytes);
+
+cudaError_t launch_append(const void* key, const void* value, void* k_cache, void* v_cache,
+                          const int32_t* slots, int num_tokens, const kvp_cache_desc& c,
+                          int elem_bytes, int32_t* status, cudaStream_t s);
+cudaError_t launch_append_int8(const void* key, const void* value, bool src_bf16,
+                               int8_t* k_cache, int8_t* v_cache, float* k_scale,
+                               float* v_scale, const int32_t* slots, int num_tokens,
+                               const kvp_cache_desc& c, int32_t* status, cudaStream_t s);
+cudaError_t launch_copy_blocks(void* k_cache, void* v_cache, float* k_scale, float* v_scale,
+                               int elem_bytes, const int32_t* pairs, int num_pairs,
+                               const kvp_cache_desc& c, int32_t* status, cudaStream_t s);
+
+}  // namespace kvp

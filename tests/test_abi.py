@@ -1,0 +1,99 @@
+"""The C-ABI library builds, loads and exports every symbol include/kvp.h
+declares; host-side argument checks answer without touching a GPU."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import pagedattention_decode_kvp_gb300 as kvp
+from pagedattention_decode_kvp_gb300 import _build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    _build.build()
+    return kvp.load_library()
+
+
+def _declared():
+    names = set()
+    for fn in os.listdir(os.path.join(ROOT, "include")):
+        if fn.endswith(".h"):
+            text = open(os.path.join(ROOT, "include", fn)).read()
+            text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+            names |= set(re.findall(r"\b(kvp_\w+)\s*\(", text))
+    return names
+
+
+def test_header_declares_the_boundary():
+    names = _declared()
+    for must in ("kvp_append", "kvp_append_int8", "kvp_copy_blocks", "kvp_attention_decode",
+                 "kvp_attention_decode_int8", "kvp_decode_workspace_bytes", "kvp_read_status",
+                 "kvp_bm_create", "kvp_bm_allocate", "kvp_bm_append_slot", "kvp_bm_free"):
+        assert must in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in _declared():
+        assert hasattr(lib, name), name
+    # the binding types every declared symbol
+    assert _declared() <= set(kvp.SIGNATURES)
+
+
+def test_version_and_status_strings(lib):
+    assert kvp.kvp_version() >= 100
+    assert kvp.kvp_status_string(0) == "KVP_OK"
+    assert kvp.kvp_status_string(kvp.KVP_ERR_REFCOUNT) == "KVP_ERR_REFCOUNT"
+
+
+def _desc(nb=64, hkv=2, bs=16, d=64):
+    return kvp.kvp_cache_desc(nb, hkv, bs, d)
+
+
+def test_workspace_sizing_rules(lib):
+    # single pass when the table fits one partition: no workspace
+    assert kvp.kvp_decode_workspace_bytes(4, 8, _desc(), 16) == 0
+    # 4096-token contexts, 32 x 32 heads: 32-block partitions, 8 of them
+    d = _desc(10000, 32, 16, 128)
+    assert kvp.kvp_decode_partition_blocks(32, 32, d, 256) == 32
+    assert kvp.kvp_decode_workspace_bytes(32, 32, d, 256) == 32 * 32 * 8 * (128 + 2) * 4
+    # explicit partition size
+    assert kvp.kvp_decode_workspace_bytes(32, 32, d, 256, 64) == 32 * 32 * 4 * (128 + 2) * 4
+    # invalid sizes answer 0
+    assert kvp.kvp_decode_workspace_bytes(4, 6, _desc(hkv=4), 16) == 0      # 6 % 4 != 0
+    assert kvp.kvp_decode_workspace_bytes(4, 8, _desc(d=96), 16) == 0       # head_dim 96
+
+
+def test_invalid_arguments_fail_before_any_launch(lib):
+    P = None
+    # unsupported block size / head_dim
+    assert lib.kvp_append(P, P, P, P, P, 1, _desc(bs=32), 0, P, P) == kvp.KVP_ERR_UNSUPPORTED
+    assert lib.kvp_append(P, P, P, P, P, 1, _desc(d=80), 0, P, P) == kvp.KVP_ERR_UNSUPPORTED
+    # null pointers with work to do
+    assert lib.kvp_append(P, P, P, P, P, 1, _desc(), 0, P, P) == kvp.KVP_ERR_INVALID_ARG
+    # zero tokens is a no-op even with null pointers
+    assert lib.kvp_append(P, P, P, P, P, 0, _desc(), 0, P, P) == kvp.KVP_OK
+    assert lib.kvp_copy_blocks(P, P, P, P, 2, P, 0, _desc(), P, P) == kvp.KVP_OK
+    assert lib.kvp_copy_blocks(P, P, P, P, 3, P, 1, _desc(), P, P) == kvp.KVP_ERR_INVALID_ARG
+    # decode: Hq not a multiple of Hkv, null buffers, bad phases, missing workspace
+    args = lambda hq, phases, ws_bytes: (P, P, P, P, P, 16, P, 4, hq, 0.125, _desc(), 0, 0, P,
+                                         ws_bytes, phases, P, P)
+    assert lib.kvp_attention_decode(*args(7, 3, 0)) == kvp.KVP_ERR_INVALID_ARG
+    assert lib.kvp_attention_decode(*args(8, 3, 0)) == kvp.KVP_ERR_INVALID_ARG
+    assert lib.kvp_attention_decode(*args(8, 4, 0)) == kvp.KVP_ERR_INVALID_ARG
+    big = (P, P, P, P, P, 256, P, 4, 8, 0.125, _desc(), 0, 0, P, 0, 3, P, P)
+    assert lib.kvp_attention_decode(*big) == kvp.KVP_ERR_INVALID_ARG  # needs workspace
+    # batch 0 is a no-op
+    zero = (P, P, P, P, P, 16, P, 0, 8, 0.125, _desc(), 0, 0, P, 0, 3, P, P)
+    assert lib.kvp_attention_decode(*zero) == kvp.KVP_OK
+    assert lib.kvp_read_status(P, P) == kvp.KVP_ERR_INVALID_ARG
+
+
+def test_product_fails_loudly_without_library(monkeypatch, tmp_path):
+    monkeypatch.setattr(kvp, "_lib", None)
+    monkeypatch.setattr(kvp, "LIB_PATH", str(tmp_path / "missing.so"))
+    with pytest.raises(RuntimeError, match="not built"):
+        kvp.load_library()

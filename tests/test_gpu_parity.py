@@ -1,0 +1,313 @@
+"""GPU parity: the CUDA library, called through its C ABI, against the CPU oracle
+on the same seeded inputs.
+
+Bars: append, copy_blocks and INT8 quantisation bit-exact; attention outputs
+(fp32 accumulation, fp16/bf16 out) within 3e-3 absolute OR 1e-2 relative of the
+fp64 oracle, element by element.  Inputs given to the oracle never come from
+the GPU: the oracle applies its own copy/append/quantise to the host pools.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads
+import pagedattention_decode_kvp_gb300 as kvp
+
+pytestmark = pytest.mark.gpu
+
+ATOL, RTOL = 3e-3, 1e-2
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    from pagedattention_decode_kvp_gb300 import _build
+    _build.build()
+    kvp.load_library()
+
+
+def assert_attn_close(gpu_out, ref, what=""):
+    g = gpu_out.detach().double().cpu().numpy().reshape(ref.shape)
+    assert np.isfinite(g).all(), f"{what}: non-finite output"
+    err = np.abs(g - ref)
+    ok = (err <= ATOL) | (err <= RTOL * np.abs(ref))
+    if not ok.all():
+        i = np.unravel_index(np.argmax(np.where(ok, 0, err)), err.shape)
+        raise AssertionError(f"{what}: {int((~ok).sum())} elements out of tolerance; worst at "
+                             f"{i}: gpu {g[i]} ref {ref[i]} (max abs err {err.max():.3e})")
+
+
+def workspace_for(w, partition_blocks=0):
+    d = kvp.kvp_cache_desc(w.num_blocks, w.Hkv, 16, w.D)
+    nbytes = kvp.kvp_decode_workspace_bytes(w.B, w.Hq, d, w.max_blocks, partition_blocks,
+                                            w.kv_int8)
+    if nbytes == 0:
+        return None
+    return torch.empty(nbytes // 4 + 4, dtype=torch.float32, device="cuda")
+
+
+def gpu_decode_16(w, partition_blocks=0, status=None):
+    """copy-on-write pairs, append, decode: the whole 16-bit step on the GPU."""
+    kp = w.k_pool.cuda()
+    vp = w.v_pool.cuda()
+    if w.cow_pairs is not None:
+        kvp.kvp_copy_blocks(kp, vp, w.cow_pairs.cuda(), status=status)
+    kvp.kvp_append(w.new_k.cuda(), w.new_v.cuda(), kp, vp, w.slot_mapping.cuda(), status=status)
+    out = torch.full_like(w.q, float("nan"), device="cuda")
+    kvp.kvp_attention_decode(out, w.q.cuda(), kp, vp, w.block_tables.cuda(),
+                             w.context_lens.cuda(), w.scale,
+                             workspace=workspace_for(w, partition_blocks),
+                             partition_blocks=partition_blocks, status=status)
+    torch.cuda.synchronize()
+    return out, kp, vp
+
+
+def oracle_pools_16(w):
+    kp, vp = w.k_pool, w.v_pool
+    if w.cow_pairs is not None:
+        kp = oracle.copy_blocks(kp, w.cow_pairs)
+        vp = oracle.copy_blocks(vp, w.cow_pairs)
+    kp = oracle.append(kp, w.new_k, w.slot_mapping)
+    vp = oracle.append(vp, w.new_v, w.slot_mapping)
+    return kp, vp
+
+
+def same_bits(a, b):
+    a = a.detach().cpu().contiguous()
+    b = b.detach().cpu().contiguous()
+    if a.dtype in (torch.float16, torch.bfloat16):
+        a, b = a.view(torch.int16), b.view(torch.int16)
+    elif a.dtype == torch.float32:
+        a, b = a.view(torch.int32), b.view(torch.int32)
+    return torch.equal(a, b)
+
+
+# --------------------------------------------------------------- tiny workload
+def test_tiny_workload_full_parity():
+    w = workloads.make("tiny")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out, kp, vp = gpu_decode_16(w, status=status)
+    assert kvp.kvp_read_status(status) == kvp.KVP_OK
+    okp, ovp = oracle_pools_16(w)
+    assert same_bits(kp, okp) and same_bits(vp, ovp)  # append is a byte scatter
+    ref = oracle.attention_decode(w.q, okp, ovp, w.block_tables, w.context_lens, w.scale)
+    assert_attn_close(out, ref, "tiny")
+    # context_len 1 returns V_0 exactly
+    assert same_bits(out[0], okp.new_empty(0)) or True
+    blk = int(w.block_tables[0, 0])
+    v0 = ovp[blk, :, 0, :]  # [Hkv, D]
+    G = w.Hq // w.Hkv
+    for h in range(w.Hq):
+        assert same_bits(out[0, h].cpu(), v0[h // G])
+
+
+# --------------------------------------------------------------- shape sweep
+SWEEP = []
+for dtype in (torch.float16, torch.bfloat16):
+    for D in (64, 128):
+        for Hq, Hkv in ((4, 4), (8, 4), (12, 4), (16, 2), (8, 1), (24, 2)):
+            SWEEP.append((dtype, D, Hq, Hkv))
+
+
+@pytest.mark.parametrize("dtype,D,Hq,Hkv", SWEEP)
+@pytest.mark.parametrize("partition_blocks", [0, 8, 3])
+def test_decode_shape_sweep(dtype, D, Hq, Hkv, partition_blocks):
+    lens = [1, 15, 16, 17, 100, 257, 530, 0, 48]
+    w = workloads.make_custom(B=len(lens), Hq=Hq, Hkv=Hkv, D=D, lens=lens, num_blocks=160,
+                              dtype=dtype, seed=hash((D, Hq, Hkv)) % 1000, max_blocks=40)
+    out, kp, vp = gpu_decode_16(w, partition_blocks)
+    okp, ovp = oracle_pools_16(w)
+    assert same_bits(kp, okp) and same_bits(vp, ovp)
+    ref = oracle.attention_decode(w.q, okp, ovp, w.block_tables, w.context_lens, w.scale)
+    assert_attn_close(out, ref, f"{dtype} D{D} {Hq}/{Hkv} pb{partition_blocks}")
+    assert torch.count_nonzero(out[7]) == 0  # context 0 -> zero row
+
+
+def test_scattered_vs_contiguous_tables_agree_with_oracle():
+    lens = [700, 1500, 64]
+    for p in (0.0, 0.85, 1.0):
+        w = workloads.make_custom(B=3, Hq=8, Hkv=1, D=128, lens=lens, num_blocks=200,
+                                  dtype=torch.bfloat16, contiguous_p=p, seed=3)
+        out, _, _ = gpu_decode_16(w)
+        okp, ovp = oracle_pools_16(w)
+        ref = oracle.attention_decode(w.q, okp, ovp, w.block_tables, w.context_lens, w.scale)
+        assert_attn_close(out, ref, f"contiguity {p}")
+
+
+def test_split_phases_equal_single_call():
+    w = workloads.make_custom(B=3, Hq=16, Hkv=2, D=128, lens=[900, 33, 2000], num_blocks=300,
+                              dtype=torch.float16, seed=4)
+    out_all, kp, vp = gpu_decode_16(w, 16)
+    out = torch.zeros_like(out_all)
+    ws = workspace_for(w, 16)
+    args = (out, w.q.cuda(), kp, vp, w.block_tables.cuda(), w.context_lens.cuda(), w.scale)
+    kvp.kvp_attention_decode(*args, workspace=ws, partition_blocks=16,
+                             phases=kvp.KVP_PHASE_PARTIAL)
+    kvp.kvp_attention_decode(*args, workspace=ws, partition_blocks=16,
+                             phases=kvp.KVP_PHASE_REDUCE)
+    torch.cuda.synchronize()
+    assert same_bits(out, out_all)
+
+
+def test_decode_is_deterministic():
+    w = workloads.make_custom(B=4, Hq=8, Hkv=8, D=128, lens=[4000, 10, 2500, 1234],
+                              num_blocks=700, dtype=torch.float16, seed=8)
+    a, _, _ = gpu_decode_16(w)
+    b, _, _ = gpu_decode_16(w)
+    assert same_bits(a, b)
+
+
+# --------------------------------------------------------------- copy_blocks
+@pytest.mark.parametrize("dtype", [torch.float16, torch.bfloat16, torch.int8])
+def test_copy_blocks_bit_exact(dtype):
+    g = torch.Generator().manual_seed(2)
+    NB, Hkv, D = 40, 4, 128
+    if dtype == torch.int8:
+        kp = torch.randint(-128, 128, (NB, Hkv, 16, D), generator=g, dtype=torch.int8)
+        vp = torch.randint(-128, 128, (NB, Hkv, 16, D), generator=g, dtype=torch.int8)
+        ks = torch.rand(NB, Hkv, 16, generator=g)
+        vs = torch.rand(NB, Hkv, 16, generator=g)
+    else:
+        kp = torch.randn(NB, Hkv, 16, D, generator=g).to(dtype)
+        vp = torch.randn(NB, Hkv, 16, D, generator=g).to(dtype)
+        ks = vs = None
+    pairs = torch.tensor([[3, 10], [3, 11], [7, 0], [5, 5], [39, 20]], dtype=torch.int32)
+    gk, gv = kp.cuda(), vp.cuda()
+    gks = ks.cuda() if ks is not None else None
+    gvs = vs.cuda() if vs is not None else None
+    kvp.kvp_copy_blocks(gk, gv, pairs.cuda(), k_scale=gks, v_scale=gvs)
+    torch.cuda.synchronize()
+    assert same_bits(gk, oracle.copy_blocks(kp, pairs))
+    assert same_bits(gv, oracle.copy_blocks(vp, pairs))
+    if ks is not None:
+        assert same_bits(gks, oracle.copy_blocks(ks, pairs))
+        assert same_bits(gvs, oracle.copy_blocks(vs, pairs))
+
+
+# --------------------------------------------------------------- INT8
+@pytest.mark.parametrize("src_dtype", [torch.float16, torch.bfloat16])
+@pytest.mark.parametrize("D", [64, 128])
+def test_append_int8_bit_exact(src_dtype, D):
+    g = torch.Generator().manual_seed(31)
+    NB, Hkv, T = 64, 4, 300
+    key = (torch.randn(T, Hkv, D, generator=g) * torch.rand(T, Hkv, 1, generator=g) * 4)
+    value = torch.randn(T, Hkv, D, generator=g)
+    key[5] = 0.0                           # all-zero rows keep scale 1
+    key[6, :, :3] = 2.5                    # ties after division
+    key, value = key.to(src_dtype), value.to(src_dtype)
+    slots = torch.randperm(NB * 16, generator=g)[:T].to(torch.int32)
+    slots[7] = -1                          # padding token
+    kc = torch.zeros(NB, Hkv, 16, D, dtype=torch.int8)
+    vc = torch.zeros_like(kc)
+    ks = torch.full((NB, Hkv, 16), -7.0)
+    vs = torch.full((NB, Hkv, 16), -7.0)
+    gkc, gvc, gks, gvs = kc.cuda(), vc.cuda(), ks.cuda(), vs.cuda()
+    kvp.kvp_append_int8(key.cuda(), value.cuda(), gkc, gvc, gks, gvs, slots.cuda())
+    torch.cuda.synchronize()
+    okc, oks = oracle.append_int8(kc, ks, key, slots)
+    ovc, ovs = oracle.append_int8(vc, vs, value, slots)
+    assert same_bits(gkc, okc) and same_bits(gks, oks)
+    assert same_bits(gvc, ovc) and same_bits(gvs, ovs)
+
+
+def int8_workload(B, Hq, Hkv, D, lens, NB, q_dtype, seed, max_blocks=None):
+    w = workloads.make_custom(B=B, Hq=Hq, Hkv=Hkv, D=D, lens=lens, num_blocks=NB,
+                              dtype=q_dtype, kv_int8=True, seed=seed, max_blocks=max_blocks)
+    # the oracle quantises the fp16 source pools; unused scale slots hold NaN
+    kc, ks = oracle.quantize_int8(w.k_pool)
+    vc, vs = oracle.quantize_int8(w.v_pool)
+    ks = torch.from_numpy(ks)
+    vs = torch.from_numpy(vs)
+    used = torch.zeros(NB, 16, dtype=torch.bool)
+    for b, n in enumerate(lens):
+        for i in range(n):
+            used[int(w.block_tables[b, i // 16]), i % 16] = True
+    ks[~used[:, None, :].expand_as(ks)] = float("nan")
+    vs[~used[:, None, :].expand_as(vs)] = float("nan")
+    return w, torch.from_numpy(kc), torch.from_numpy(vc), ks, vs
+
+
+def gpu_decode_int8(w, kc, vc, ks, vs, partition_blocks=0):
+    gkc, gvc, gks, gvs = kc.cuda(), vc.cuda(), ks.cuda(), vs.cuda()
+    kvp.kvp_append_int8(w.new_k.cuda(), w.new_v.cuda(), gkc, gvc, gks, gvs, w.slot_mapping.cuda())
+    out = torch.full_like(w.q, float("nan"), device="cuda")
+    kvp.kvp_attention_decode_int8(out, w.q.cuda(), gkc, gvc, gks, gvs, w.block_tables.cuda(),
+                                  w.context_lens.cuda(), w.scale,
+                                  workspace=workspace_for(w, partition_blocks),
+                                  partition_blocks=partition_blocks)
+    torch.cuda.synchronize()
+    return out, gkc, gvc, gks, gvs
+
+
+@pytest.mark.parametrize("q_dtype", [torch.float16, torch.bfloat16])
+@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("Hq,Hkv", [(8, 1), (16, 2), (4, 4), (6, 2)])
+@pytest.mark.parametrize("partition_blocks", [0, 8])
+def test_decode_int8_parity(q_dtype, D, Hq, Hkv, partition_blocks):
+    lens = [1, 17, 300, 16, 640, 0]
+    w, kc, vc, ks, vs = int8_workload(len(lens), Hq, Hkv, D, lens, 120, q_dtype,
+                                      seed=D + Hq, max_blocks=40)
+    out, gkc, gvc, gks, gvs = gpu_decode_int8(w, kc, vc, ks, vs, partition_blocks)
+    okc, oks = oracle.append_int8(kc, ks, w.new_k, w.slot_mapping)
+    ovc, ovs = oracle.append_int8(vc, vs, w.new_v, w.slot_mapping)
+    assert same_bits(gkc, okc) and same_bits(gvc, ovc)
+    assert same_bits(gks, oks) and same_bits(gvs, ovs)
+    ref = oracle.attention_decode(w.q, okc, ovc, w.block_tables, w.context_lens, w.scale,
+                                  k_scale=oks, v_scale=ovs)
+    assert_attn_close(out, ref, f"int8 {q_dtype} D{D} {Hq}/{Hkv} pb{partition_blocks}")
+
+
+# --------------------------------------------------------------- device errors
+def test_bad_block_id_sets_status_and_zeroes_rows():
+    w = workloads.make_custom(B=3, Hq=8, Hkv=2, D=64, lens=[40, 300, 20], num_blocks=64,
+                              dtype=torch.float16, seed=9)
+    w.block_tables[1, 5] = 64        # out of range
+    w.block_tables[2, 0] = -3
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out, _, _ = gpu_decode_16(w, 8, status=status)
+    assert kvp.kvp_read_status(status) == kvp.KVP_ERR_BAD_BLOCK
+    assert torch.count_nonzero(out[1]) == 0 and torch.count_nonzero(out[2]) == 0
+    okp, ovp = oracle_pools_16(w)
+    ref = oracle.attention_decode(w.q[:1], okp, ovp, w.block_tables[:1], w.context_lens[:1],
+                                  w.scale)
+    assert_attn_close(out[:1], ref, "healthy request next to bad ones")
+
+
+def test_context_longer_than_table_sets_status():
+    w = workloads.make_custom(B=2, Hq=4, Hkv=4, D=128, lens=[20, 30], num_blocks=16,
+                              dtype=torch.float16, seed=10)
+    lens = w.context_lens.clone()
+    lens[1] = w.max_blocks * 16 + 1
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    kp, vp = w.k_pool.cuda(), w.v_pool.cuda()
+    out = torch.full_like(w.q, 1.0, device="cuda")
+    kvp.kvp_attention_decode(out, w.q.cuda(), kp, vp, w.block_tables.cuda(), lens.cuda(),
+                             w.scale, workspace=workspace_for(w), status=status)
+    assert kvp.kvp_read_status(status) == kvp.KVP_ERR_BAD_BLOCK
+    assert torch.count_nonzero(out[1]) == 0
+
+
+def test_append_slot_out_of_range_sets_status_and_skips():
+    kp = torch.zeros(4, 2, 16, 64, dtype=torch.float16, device="cuda")
+    vp = torch.zeros_like(kp)
+    key = torch.ones(3, 2, 64, dtype=torch.float16, device="cuda")
+    slots = torch.tensor([3, 64, -1], dtype=torch.int32, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    kvp.kvp_append(key, key, kp, vp, slots, status=status)
+    assert kvp.kvp_read_status(status) == kvp.KVP_ERR_BAD_BLOCK
+    assert torch.count_nonzero(kp) == 2 * 64 and bool((kp[0, :, 3] == 1).all())
+
+
+def test_empty_inputs_are_no_ops():
+    kp = torch.zeros(4, 2, 16, 64, dtype=torch.float16, device="cuda")
+    key = torch.zeros(0, 2, 64, dtype=torch.float16, device="cuda")
+    kvp.kvp_append(key, key, kp, kp.clone(), torch.zeros(0, dtype=torch.int32, device="cuda"))
+    pairs = torch.zeros(0, 2, dtype=torch.int32, device="cuda")
+    kvp.kvp_copy_blocks(kp, kp.clone(), pairs)
+    q = torch.zeros(0, 8, 64, dtype=torch.float16, device="cuda")
+    kvp.kvp_attention_decode(q.clone(), q, kp, kp, torch.zeros(0, 4, dtype=torch.int32,
+                                                               device="cuda"),
+                             torch.zeros(0, dtype=torch.int32, device="cuda"), 0.1)
+    torch.cuda.synchronize()
