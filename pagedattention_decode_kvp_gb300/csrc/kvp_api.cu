@@ -46,7 +46,8 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 
 // TMA descriptor over a whole pool viewed as [NB * Hkv * 16 rows][D elements]:
 // a box is 16 token rows by at most 128 bytes, written to shared memory with
-// the 128-byte swizzle (a 256-byte row takes two boxes).
+// the 128-byte swizzle (a 256-byte row takes two boxes); 64-byte rows (INT8,
+// D = 64) are copied unswizzled.
 kvp_status make_pool_map(CUtensorMap* map, const void* base, const kvp_cache_desc& c,
                          int elem_bytes) {
   auto fn = encode_fn();
@@ -62,7 +63,8 @@ kvp_status make_pool_map(CUtensorMap* map, const void* base, const kvp_cache_des
   const CUresult r =
       fn(map, elem_bytes == 2 ? CU_TENSOR_MAP_DATA_TYPE_UINT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8, 2,
          const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-         CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+         box_bytes == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+         CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? KVP_OK : KVP_ERR_CUDA;
 }

@@ -419,6 +419,16 @@ struct MmaInt8Path {
     st.l[0] = st.l[1] = 0.f;
   }
 
+  // Tiles with 128-byte rows arrive 128B-swizzled; 64-byte rows (D = 64)
+  // arrive unswizzled (a 64-byte box does not take the 128-byte pattern).
+  __device__ __forceinline__ static uint32_t off(uint32_t o) {
+    if constexpr (D >= 128) {
+      return dev::swz128(o);
+    } else {
+      return o;
+    }
+  }
+
   template <bool kHigh>
   __device__ __forceinline__ static uint32_t k_pair(uint32_t w) {
     if constexpr (kQBf16) {
@@ -436,9 +446,9 @@ struct MmaInt8Path {
     uint32_t k0[kMt], k1[kMt];
 #pragma unroll
     for (int i = 0; i < kMt / 4; ++i) {
-      const uint32_t off = (D / 4) * t4 + 16 * i;
-      const uint4 r0 = *reinterpret_cast<const uint4*>(kt + dev::swz128(g8 * D + off));
-      const uint4 r1 = *reinterpret_cast<const uint4*>(kt + dev::swz128((g8 + 8) * D + off));
+      const uint32_t o = (D / 4) * t4 + 16 * i;
+      const uint4 r0 = *reinterpret_cast<const uint4*>(kt + off(g8 * D + o));
+      const uint4 r1 = *reinterpret_cast<const uint4*>(kt + off((g8 + 8) * D + o));
       k0[4 * i] = r0.x; k0[4 * i + 1] = r0.y; k0[4 * i + 2] = r0.z; k0[4 * i + 3] = r0.w;
       k1[4 * i] = r1.x; k1[4 * i + 1] = r1.y; k1[4 * i + 2] = r1.z; k1[4 * i + 3] = r1.w;
     }
@@ -494,21 +504,21 @@ struct MmaInt8Path {
     uint32_t va[kVw], vb[kVw], vc[kVw], vd[kVw];
     {
       const int ta = 2 * t4, tb = 2 * t4 + 1, tc = 2 * t4 + 8, td = 2 * t4 + 9;
-      const uint32_t off = (D / 8) * g8;
+      const uint32_t o = (D / 8) * g8;
       if constexpr (kVw == 4) {
-        const uint4 ra = *reinterpret_cast<const uint4*>(vt + dev::swz128(ta * D + off));
-        const uint4 rb = *reinterpret_cast<const uint4*>(vt + dev::swz128(tb * D + off));
-        const uint4 rc = *reinterpret_cast<const uint4*>(vt + dev::swz128(tc * D + off));
-        const uint4 rd = *reinterpret_cast<const uint4*>(vt + dev::swz128(td * D + off));
+        const uint4 ra = *reinterpret_cast<const uint4*>(vt + off(ta * D + o));
+        const uint4 rb = *reinterpret_cast<const uint4*>(vt + off(tb * D + o));
+        const uint4 rc = *reinterpret_cast<const uint4*>(vt + off(tc * D + o));
+        const uint4 rd = *reinterpret_cast<const uint4*>(vt + off(td * D + o));
         va[0] = ra.x; va[1] = ra.y; va[2] = ra.z; va[3] = ra.w;
         vb[0] = rb.x; vb[1] = rb.y; vb[2] = rb.z; vb[3] = rb.w;
         vc[0] = rc.x; vc[1] = rc.y; vc[2] = rc.z; vc[3] = rc.w;
         vd[0] = rd.x; vd[1] = rd.y; vd[2] = rd.z; vd[3] = rd.w;
       } else {
-        const uint2 ra = *reinterpret_cast<const uint2*>(vt + dev::swz128(ta * D + off));
-        const uint2 rb = *reinterpret_cast<const uint2*>(vt + dev::swz128(tb * D + off));
-        const uint2 rc = *reinterpret_cast<const uint2*>(vt + dev::swz128(tc * D + off));
-        const uint2 rd = *reinterpret_cast<const uint2*>(vt + dev::swz128(td * D + off));
+        const uint2 ra = *reinterpret_cast<const uint2*>(vt + off(ta * D + o));
+        const uint2 rb = *reinterpret_cast<const uint2*>(vt + off(tb * D + o));
+        const uint2 rc = *reinterpret_cast<const uint2*>(vt + off(tc * D + o));
+        const uint2 rd = *reinterpret_cast<const uint2*>(vt + off(td * D + o));
         va[0] = ra.x; va[1] = ra.y;
         vb[0] = rb.x; vb[1] = rb.y;
         vc[0] = rc.x; vc[1] = rc.y;
