@@ -320,7 +320,7 @@ def run_ours(args):
     barrier(world)
     kvp.load_library()
 
-    w = workloads.make(args.workload, device=dev, nan_sentinel=False)
+    w = workloads.make(args.workload, device=dev, nan_sentinel=False, batch=args.batch)
     step = Step(w, kvp, dev)
     lens = [int(x) for x in w.context_lens]
     dbytes = decode_bytes(w, lens)
@@ -409,7 +409,7 @@ def run_ours(args):
         "dtype": {torch.float16: "f16", torch.bfloat16: "bf16"}[w.dtype] + (
             " (int8 KV)" if w.kv_int8 else ""),
         "data": "synthetic (seeded N(0,1), shapes of the pages' workloads)",
-        "config": {"workload": w.name, "batch": w.B, "q_heads": w.Hq, "kv_heads": w.Hkv,
+        "config": {"workload": w.name + (f" (batch {w.B})" if args.batch else ""), "batch": w.B, "q_heads": w.Hq, "kv_heads": w.Hkv,
                    "head_dim": w.D, "block_size": 16, "num_blocks": w.num_blocks,
                    "context_tokens": kv_total, "max_context": max(lens),
                    "new_tokens": int(w.slot_mapping.numel()),
@@ -473,7 +473,7 @@ def run_reference(args):
     import oracle
     oracle.build()
     dev = "cuda" if torch.cuda.is_available() else "cpu"
-    w = workloads.make(args.workload, device=dev, nan_sentinel=False)
+    w = workloads.make(args.workload, device=dev, nan_sentinel=False, batch=args.batch)
     w = workloads.Workload(**{k: (v.cpu() if isinstance(v, torch.Tensor) else v)
                               for k, v in w.__dict__.items()})
     kp, vp, ks, vs = w.k_pool, w.v_pool, None, None
@@ -518,6 +518,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-rows", type=int, default=0,
                     help="(request, head) rows the CPU oracle times (0 = default sample)")
+    ap.add_argument("--batch", type=int, default=None,
+                    help="fewer requests (pool scaled in proportion), for profiler captures")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()

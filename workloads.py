@@ -215,11 +215,15 @@ def _assemble(name, B, Hq, Hkv, D, NB, dtype, kv_int8, scale, lens, tables, seed
                     info=dict(info or {}))
 
 
-def make(name: str, device="cpu", nan_sentinel=True) -> Workload:
-    """Build one of the named workloads (see module docstring)."""
+def make(name: str, device="cpu", nan_sentinel=True, batch=None) -> Workload:
+    """Build one of the named workloads (see module docstring).  ``batch``
+    shrinks llama7b / gqa70b / int8long to fewer requests with the pool scaled
+    in proportion (same per-request shapes), e.g. for profiler captures."""
     idx = WORKLOAD_NAMES.index(name)
     seed = 1000 + idx
     base = seed * 100
+    if batch is not None and name in ("llama7b", "gqa70b", "int8long"):
+        return _make_scaled(name, int(batch), device, nan_sentinel, seed)
     if name == "tiny":
         lens = [1, 17, 100, 255]
         g = _gen(base + 5, "cpu")
@@ -259,6 +263,30 @@ def make(name: str, device="cpu", nan_sentinel=True) -> Workload:
                          1.0 / math.sqrt(128), [n] * B, perm.contiguous(), seed, device,
                          nan_sentinel)
     raise KeyError(name)
+
+
+def _make_scaled(name, B, device, nan_sentinel, seed) -> Workload:
+    base = seed * 100
+    if name == "llama7b":
+        NB = -(-10000 * B // 32)
+        g = _gen(base + 5, "cpu")
+        perm = torch.randperm(NB, generator=g)[:B * 256].view(B, 256).to(torch.int32)
+        return _assemble(name, B, 32, 32, 128, NB, torch.float16, False, 1.0 / math.sqrt(128),
+                         [4096] * B, perm.contiguous(), seed, device, nan_sentinel)
+    if name == "gqa70b":
+        NB = -(-40000 * B // 64)
+        lens = np.random.default_rng(base + 6).integers(512, 8192, size=B, endpoint=True).tolist()
+        lists = _draw_tables(np.random.default_rng(base + 5), [-(-n // BLOCK_SIZE) for n in lens],
+                             NB, 0.85)
+        tables = _tables_from_lists(lists, 512)
+        info = {"contiguous_share": contiguous_share(tables, lens)}
+        return _assemble(name, B, 64, 8, 128, NB, torch.bfloat16, False, 1.0 / math.sqrt(128),
+                         lens, tables, seed, device, nan_sentinel, info)
+    NB = -(-40000 * B // 4)
+    g = _gen(base + 5, "cpu")
+    perm = torch.randperm(NB, generator=g)[:B * 8192].view(B, 8192).to(torch.int32)
+    return _assemble(name, B, 64, 8, 128, NB, torch.float16, True, 1.0 / math.sqrt(128),
+                     [131072] * B, perm.contiguous(), seed, device, nan_sentinel)
 
 
 def _make_prefix(seed, device, nan_sentinel) -> Workload:
