@@ -67,7 +67,8 @@ typedef enum {
   KVP_ERR_TIMEOUT = 5,     /* device: a bounded pipeline wait gave up          */
   KVP_ERR_OOM = 6,         /* block manager: not enough free blocks            */
   KVP_ERR_REFCOUNT = 7,    /* block manager: release by a non-holder           */
-  KVP_ERR_NOT_FOUND = 8    /* block manager: unknown request id                */
+  KVP_ERR_NOT_FOUND = 8,   /* block manager: unknown request id                */
+  KVP_ERR_SCRATCH_LIMIT = 9 /* decode_noalloc: sizes need more than its scratch */
 } kvp_status;
 
 typedef enum { KVP_F16 = 0, KVP_BF16 = 1 } kvp_dtype;
@@ -208,6 +209,42 @@ kvp_status kvp_attention_decode_int8(void* out, const void* q, kvp_dtype q_dtype
                                      int32_t partition_blocks, void* workspace,
                                      size_t workspace_bytes, int32_t phases,
                                      int32_t* dev_status, kvp_stream_t stream);
+
+/*
+ * kvp_attention_decode_noalloc -- kvp_attention_decode for callers that cannot
+ * allocate device memory.  (The pages have no counterpart: this entry point
+ * exists for integration, not for the method.)
+ *
+ * Long contexts need a workspace for their split-context partial results, and
+ * kvp_attention_decode takes it from the caller.  Callers that cannot allocate
+ * -- a plugin whose host framework owns all device memory and hands it only
+ * input and output buffers, or a serving loop that gave nearly all free HBM to
+ * the KV pool and must not risk a failing or synchronising cudaMalloc in the
+ * middle of a step -- call this instead: it uses a scratch array built into
+ * the library (KVP_NOALLOC_SCRATCH_BYTES of device memory that every GPU which
+ * loads the library holds until the process exits) and calls no cudaMalloc,
+ * cudaFree or other allocating routine.
+ *   - Arguments and results are those of kvp_attention_decode (fp16/bf16 pools,
+ *     all phases) without the workspace arguments.
+ *   - Returns KVP_ERR_SCRATCH_LIMIT, before launching anything, when these sizes
+ *     need more than KVP_NOALLOC_SCRATCH_BYTES of workspace
+ *     (kvp_decode_workspace_bytes tells how much they need).
+ *   - The first call on each device looks up the scratch array's device address
+ *     (cudaGetSymbolAddress, with that device current); make that first call
+ *     before any stream capture.
+ *   - Every call, on any stream, shares the one array: calls that overlap on the
+ *     GPU race and corrupt each other's results.  Serialise them (one stream, or
+ *     events).  The array keeps the last call's contents; nothing in it needs to
+ *     start at zero, each call rewrites what it reads.
+ */
+#define KVP_NOALLOC_SCRATCH_BYTES (64u * 1024u * 1024u)
+kvp_status kvp_attention_decode_noalloc(void* out, const void* q, const void* k_cache,
+                                        const void* v_cache, const int32_t* block_tables,
+                                        int32_t max_blocks_per_seq, const int32_t* context_lens,
+                                        int32_t batch, int32_t num_q_heads, float scale,
+                                        kvp_cache_desc cache, kvp_dtype dtype,
+                                        int32_t partition_blocks, int32_t* dev_status,
+                                        kvp_stream_t stream);
 
 /*
  * kvp_read_status -- synchronise `stream`, read the device status word and

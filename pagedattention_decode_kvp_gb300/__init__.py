@@ -29,6 +29,8 @@ KVP_ERR_TIMEOUT = 5
 KVP_ERR_OOM = 6
 KVP_ERR_REFCOUNT = 7
 KVP_ERR_NOT_FOUND = 8
+KVP_ERR_SCRATCH_LIMIT = 9
+NOALLOC_SCRATCH_BYTES = 64 * 1024 * 1024
 KVP_F16 = 0
 KVP_BF16 = 1
 KVP_PHASE_PARTIAL = 1
@@ -71,6 +73,8 @@ SIGNATURES = {
                                     _P, _SZ, _I32, _P, _P]),
     "kvp_attention_decode_int8": (_I32, [_P, _P, _I32, _P, _P, _P, _P, _P, _I32, _P, _I32, _I32,
                                          _F, _D, _I32, _P, _SZ, _I32, _P, _P]),
+    "kvp_attention_decode_noalloc": (_I32, [_P, _P, _P, _P, _P, _I32, _P, _I32, _I32, _F, _D,
+                                            _I32, _I32, _P, _P]),
     "kvp_read_status": (_I32, [_P, _P]),
     "kvp_bm_create": (_P, [_I32, _I32, _I64]),
     "kvp_bm_destroy": (None, [_P]),
@@ -250,6 +254,24 @@ def kvp_attention_decode_int8(out, q, k_cache, v_cache, k_scale, v_scale, block_
         _ptr(v_scale), _ptr(block_tables), int(block_tables.shape[1]), _ptr(context_lens), B, Hq,
         float(scale), cache_desc(k_cache), int(partition_blocks), _ptr(workspace), ws_bytes,
         int(phases), _ptr(status), _stream_ptr(stream)), "kvp_attention_decode_int8")
+
+
+def kvp_attention_decode_noalloc(out, q, k_cache, v_cache, block_tables, context_lens, scale, *,
+                                 partition_blocks=0, status=None, stream=None) -> None:
+    """kvp_attention_decode without a workspace argument, for callers that cannot
+    allocate device memory: the library's built-in scratch array
+    (NOALLOC_SCRATCH_BYTES per GPU) holds the split-context partials.  Calls that
+    overlap on the GPU share that array and race; serialise them."""
+    lib = load_library()
+    _need_cuda(out, q, k_cache, v_cache, block_tables, context_lens, status)
+    if q.dtype != k_cache.dtype or out.dtype != q.dtype:
+        raise TypeError("q, out and the pools must share one dtype")
+    B, Hq, _ = (int(x) for x in q.shape)
+    _check(lib.kvp_attention_decode_noalloc(
+        _ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
+        int(block_tables.shape[1]), _ptr(context_lens), B, Hq, float(scale), cache_desc(k_cache),
+        _dtype_code(q), int(partition_blocks), _ptr(status), _stream_ptr(stream)),
+        "kvp_attention_decode_noalloc")
 
 
 def kvp_read_status(status, stream=None) -> int:

@@ -27,6 +27,7 @@ SOURCES = [
     "kvp_decode_int8.cu",
     "kvp_reduce.cu",
     "kvp_block_manager.cpp",
+    "kvp_noalloc.cu",
 ]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC,-O3",

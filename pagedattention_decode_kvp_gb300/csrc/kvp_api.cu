@@ -213,6 +213,7 @@ const char* kvp_status_string(kvp_status status) {
     case KVP_ERR_OOM: return "KVP_ERR_OOM";
     case KVP_ERR_REFCOUNT: return "KVP_ERR_REFCOUNT";
     case KVP_ERR_NOT_FOUND: return "KVP_ERR_NOT_FOUND";
+    case KVP_ERR_SCRATCH_LIMIT: return "KVP_ERR_SCRATCH_LIMIT";
   }
   return "KVP_ERR_UNKNOWN";
 }
