@@ -174,7 +174,7 @@ class ClockSampler:
 class Step:
     """Device buffers of one workload and the step through the public API."""
 
-    def __init__(self, w, kvp, dev):
+    def __init__(self, w, kvp, dev, partition_blocks=0):
         self.w, self.kvp, self.dev = w, kvp, dev
         self.q = w.q.to(dev)
         self.tables = w.block_tables.to(dev)
@@ -191,11 +191,14 @@ class Step:
             self.kp = w.k_pool.to(dev)
             self.vp = w.v_pool.to(dev)
         desc = kvp.cache_desc(self.kp)
-        nb = kvp.kvp_decode_workspace_bytes(w.B, w.Hq, desc, w.max_blocks, 0, w.kv_int8)
+        self.pb_arg = partition_blocks
+        nb = kvp.kvp_decode_workspace_bytes(w.B, w.Hq, desc, w.max_blocks, partition_blocks,
+                                            w.kv_int8)
         self.ws = torch.empty(max(nb // 4, 1), dtype=torch.float32, device=dev) if nb else None
         self.split = nb > 0
-        self.part_blocks = kvp.kvp_decode_partition_blocks(w.B, w.Hq, desc, w.max_blocks,
-                                                           w.kv_int8)
+        self.part_blocks = (min(partition_blocks, w.max_blocks) if partition_blocks else
+                            kvp.kvp_decode_partition_blocks(w.B, w.Hq, desc, w.max_blocks,
+                                                            w.kv_int8))
 
     def _init_int8(self):
         """Quantise the fp16 source pools into the INT8 pools on the GPU: each
@@ -243,11 +246,12 @@ class Step:
             if w.kv_int8:
                 kvp.kvp_attention_decode_int8(self.out, self.q, self.kp, self.vp, self.ks,
                                               self.vs, self.tables, self.lens, w.scale,
-                                              workspace=self.ws, phases=ph, status=self.status)
+                                              workspace=self.ws, phases=ph, status=self.status,
+                                              partition_blocks=self.pb_arg)
             else:
                 kvp.kvp_attention_decode(self.out, self.q, self.kp, self.vp, self.tables,
                                          self.lens, w.scale, workspace=self.ws, phases=ph,
-                                         status=self.status)
+                                         status=self.status, partition_blocks=self.pb_arg)
             if ev is not None and i == 0:
                 ev[1].record()
 
@@ -321,7 +325,7 @@ def run_ours(args):
     kvp.load_library()
 
     w = workloads.make(args.workload, device=dev, nan_sentinel=False, batch=args.batch)
-    step = Step(w, kvp, dev)
+    step = Step(w, kvp, dev, args.partition_blocks)
     lens = [int(x) for x in w.context_lens]
     dbytes = decode_bytes(w, lens)
     sbytes = dbytes["call"] + append_bytes(w) + copy_bytes(w)
@@ -520,6 +524,8 @@ def main():
                     help="(request, head) rows the CPU oracle times (0 = default sample)")
     ap.add_argument("--batch", type=int, default=None,
                     help="fewer requests (pool scaled in proportion), for profiler captures")
+    ap.add_argument("--partition-blocks", type=int, default=0,
+                    help="split-context partition size in blocks (0 = the library's choice)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()

@@ -178,8 +178,8 @@ size_t kvp_decode_workspace_bytes(int32_t batch, int32_t num_q_heads, kvp_cache_
  * zero row.  Only the first ceil(n / 16) table entries of a request are read,
  * and only its first n slots; other slots may hold anything (even NaN).
  * q, out: [batch, Hq, D] of `dtype`; pools of `dtype`; Hq % Hkv == 0.
- * partition_blocks: blocks per split-context partition, a multiple of 8, or 0
- * for the automatic choice.  workspace: >= kvp_decode_workspace_bytes(...)
+ * partition_blocks: blocks per split-context partition (1 to 1024; values at or
+ * above max_blocks_per_seq mean single pass), or 0 for the automatic choice.  workspace: >= kvp_decode_workspace_bytes(...)
  * bytes, 16-byte aligned (may be NULL when that is 0).  phases: KVP_PHASE_ALL,
  * or one of KVP_PHASE_PARTIAL / KVP_PHASE_REDUCE to run the halves as separate
  * calls (same arguments) -- e.g. to time them or to merge partials elsewhere.

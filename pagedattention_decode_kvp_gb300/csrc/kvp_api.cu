@@ -78,14 +78,41 @@ struct DecodeShape {
   size_t ws_bytes;
 };
 
-// Split-context rule: a request is cut into partitions of 32 blocks (512
-// tokens) so that long contexts spread over many CTAs; it stays single-pass
-// when its table is at most 32 blocks, or when there are already >= 2048
-// (request, kv head, query-group) units to fill the 152 SMs.
-int auto_partition(long long units, int max_blocks) {
-  if (max_blocks <= 32) return max_blocks;
-  if (units >= 2048 && max_blocks <= kMaxPartBlocks) return max_blocks;
-  return 32;
+// Split-context rule.  Each (request, kv head, query group) unit is cut into
+// `parts` partitions of ceil(MB / parts) blocks, run as independent CTAs on
+// GB300's 152 SMs (3 resident decode CTAs per SM for 16-bit tiles, 4 for INT8
+// tiles, from their shared-memory and register use).  The count of parts
+// minimises a simple makespan model: waves * (blocks per CTA + a fixed
+// per-CTA cost of about 4 blocks of streaming), plus a small cost for the
+// reduce pass when parts > 1.  Partitions stay >= 16 blocks (256 tokens) and
+// <= kMaxPartBlocks (the table slice staged on chip).  The model sees only the
+// table width MB, not the actual lengths, so it is exact for uniform contexts
+// and conservative for ragged ones.
+constexpr int kSms = 152;
+constexpr double kCtaOverheadBlocks = 4.0;
+constexpr double kReduceCostBlocks = 2.0;
+
+int resident_ctas(DecodePath path) { return path == DecodePath::kMmaInt8 ? 4 : 3; }
+
+int auto_partition(DecodePath path, long long units, int max_blocks) {
+  const long long slots = static_cast<long long>(kSms) * resident_ctas(path);
+  int best_pb = max_blocks <= kMaxPartBlocks ? max_blocks : kMaxPartBlocks;
+  double best = 1e300;
+  for (int parts = 1; parts <= max_blocks; ++parts) {
+    const int pb = (max_blocks + parts - 1) / parts;
+    if (parts > 1 && pb < 16) break;
+    if (pb > kMaxPartBlocks) continue;
+    if ((max_blocks + pb - 1) / pb != parts) continue;  // same split as a smaller count
+    const long long ctas = units * parts;
+    const long long waves = (ctas + slots - 1) / slots;
+    const double cost = static_cast<double>(waves) * (pb + kCtaOverheadBlocks) +
+                        (parts > 1 ? kReduceCostBlocks : 0.0);
+    if (cost < best * 0.999) {
+      best = cost;
+      best_pb = pb;
+    }
+  }
+  return best_pb;
 }
 
 kvp_status shape_decode(int batch, int num_q_heads, const kvp_cache_desc& c, int max_blocks,
@@ -109,7 +136,7 @@ kvp_status shape_decode(int batch, int num_q_heads, const kvp_cache_desc& c, int
   }
   s.qgroups = (G + s.heads_per_cta - 1) / s.heads_per_cta;
   const long long units = static_cast<long long>(batch) * c.num_kv_heads * s.qgroups;
-  int pb = partition_blocks > 0 ? partition_blocks : auto_partition(units, max_blocks);
+  int pb = partition_blocks > 0 ? partition_blocks : auto_partition(s.path, units, max_blocks);
   if (pb >= max_blocks) pb = max_blocks;
   if (pb > kMaxPartBlocks) return KVP_ERR_UNSUPPORTED;  // one partition must fit on chip
   s.part_blocks = pb;

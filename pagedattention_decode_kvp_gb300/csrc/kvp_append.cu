@@ -18,6 +18,8 @@ __global__ void __launch_bounds__(256)
                   uint4* __restrict__ kc, uint4* __restrict__ vc, const int32_t* __restrict__ slots,
                   long long total_chunks, int num_kv_heads, int chunks_per_row,
                   long long num_slots, int32_t* status) {
+  dev::grid_dependency_wait();
+  dev::launch_dependents();
   const long long idx = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
   if (idx >= total_chunks) return;
   const int ch = static_cast<int>(idx % chunks_per_row);
@@ -36,6 +38,24 @@ __global__ void __launch_bounds__(256)
   vc[dst] = value[row * chunks_per_row + ch];
 }
 
+// rint(x / s) clipped to [-128, 127], with x / s the IEEE float32 quotient.
+// r = x * (1/s) is within 2e-5 of x / s for |x / s| <= 127.0001 (two roundings
+// of relative size 2^-24 each), and RN(x / s) within 8e-6 of it, so whenever r
+// lies more than 1e-4 from a half-integer both round to the same integer; only
+// inside that band is the exact quotient computed.
+__device__ __forceinline__ int quantise_code(float x, float s, float inv) {
+  const float r = x * inv;
+  const float fl = floorf(r);
+  const float frac = r - fl;
+  int q;
+  if (fabsf(frac - 0.5f) > 1.0e-4f) {
+    q = static_cast<int>(frac > 0.5f ? fl + 1.0f : fl);
+  } else {
+    q = __float2int_rn(__fdiv_rn(x, s));
+  }
+  return min(127, max(-128, q));
+}
+
 // One group of D/4 lanes per (token, head) row; each lane owns 4 elements.
 template <bool kBf16, int D>
 __global__ void __launch_bounds__(256)
@@ -44,6 +64,8 @@ __global__ void __launch_bounds__(256)
                        float* __restrict__ vs, const int32_t* __restrict__ slots, long long rows,
                        int num_kv_heads, long long num_slots, int32_t* status) {
   constexpr int L = D / 4;
+  dev::grid_dependency_wait();
+  dev::launch_dependents();
   const long long gt = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
   const long long row = gt / L;
   const int sub = static_cast<int>(gt % L);
@@ -81,11 +103,12 @@ __global__ void __launch_bounds__(256)
   float sv = __fdiv_rn(av, 127.0f);
   sk = sk > 0.f ? sk : 1.0f;
   sv = sv > 0.f ? sv : 1.0f;
+  const float ik = __frcp_rn(sk), iv = __frcp_rn(sv);
   uint32_t pk = 0u, pv = 0u;
 #pragma unroll
   for (int e = 0; e < 4; ++e) {
-    const int qk = min(127, max(-128, __float2int_rn(__fdiv_rn(xk[e], sk))));
-    const int qv = min(127, max(-128, __float2int_rn(__fdiv_rn(xv[e], sv))));
+    const int qk = quantise_code(xk[e], sk, ik);
+    const int qv = quantise_code(xv[e], sv, iv);
     pk |= (static_cast<uint32_t>(qk) & 0xffu) << (8 * e);
     pv |= (static_cast<uint32_t>(qv) & 0xffu) << (8 * e);
   }
@@ -104,6 +127,8 @@ __global__ void __launch_bounds__(256)
     copy_blocks_kernel(uint4* kc, uint4* vc, uint4* ks, uint4* vs, const int32_t* __restrict__ pairs,
                        int num_pairs, long long chunks_kv, long long chunks_scale, int num_blocks,
                        int32_t* status) {
+  dev::grid_dependency_wait();
+  dev::launch_dependents();
   const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
   const long long first = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
   for (int pr = blockIdx.y; pr < num_pairs; pr += gridDim.y) {
@@ -141,11 +166,11 @@ cudaError_t launch_append(const void* key, const void* value, void* k_cache, voi
   const long long total = static_cast<long long>(num_tokens) * c.num_kv_heads * cpr;
   if (total == 0) return cudaSuccess;
   const long long grid = (total + 255) / 256;
-  append_kernel<<<static_cast<unsigned>(grid), 256, 0, s>>>(
-      static_cast<const uint4*>(key), static_cast<const uint4*>(value),
-      static_cast<uint4*>(k_cache), static_cast<uint4*>(v_cache), slots, total, c.num_kv_heads,
-      cpr, static_cast<long long>(c.num_blocks) * kBlockSize, status);
-  return cudaGetLastError();
+  return launch_pdl(append_kernel, dim3(static_cast<unsigned>(grid)), dim3(256), 0, s,
+                    static_cast<const uint4*>(key), static_cast<const uint4*>(value),
+                    static_cast<uint4*>(k_cache), static_cast<uint4*>(v_cache), slots, total,
+                    c.num_kv_heads, cpr, static_cast<long long>(c.num_blocks) * kBlockSize,
+                    status);
 }
 
 cudaError_t launch_append_int8(const void* key, const void* value, bool src_bf16,
@@ -161,10 +186,9 @@ cudaError_t launch_append_int8(const void* key, const void* value, bool src_bf16
   const uint16_t* v = static_cast<const uint16_t*>(value);
 #define KVP_I8_CASE(BF, DD)                                                                   \
   if (src_bf16 == BF && c.head_dim == DD) {                                                   \
-    append_int8_kernel<BF, DD><<<grid, 256, 0, s>>>(k, v, k_cache, v_cache, k_scale, v_scale, \
-                                                    slots, rows, c.num_kv_heads, nslots,      \
-                                                    status);                                  \
-    return cudaGetLastError();                                                                \
+    return launch_pdl(append_int8_kernel<BF, DD>, dim3(grid), dim3(256), 0, s, k, v,         \
+                      k_cache, v_cache, k_scale, v_scale, slots, rows, c.num_kv_heads,        \
+                      nslots, status);                                                        \
   }
   KVP_I8_CASE(false, 64)
   KVP_I8_CASE(false, 128)
@@ -187,12 +211,10 @@ cudaError_t launch_copy_blocks(void* k_cache, void* v_cache, float* k_scale, flo
   if (gx > 1024) gx = 1024;
   const dim3 grid(static_cast<unsigned>(gx),
                   static_cast<unsigned>(num_pairs < 65535 ? num_pairs : 65535));
-  copy_blocks_kernel<<<grid, 256, 0, s>>>(
-      static_cast<uint4*>(k_cache), static_cast<uint4*>(v_cache),
-      reinterpret_cast<uint4*>(k_scale), reinterpret_cast<uint4*>(v_scale), pairs, num_pairs,
-      chunks_kv,
-      chunks_scale, c.num_blocks, status);
-  return cudaGetLastError();
+  return launch_pdl(copy_blocks_kernel, grid, dim3(256), 0, s, static_cast<uint4*>(k_cache),
+                    static_cast<uint4*>(v_cache), reinterpret_cast<uint4*>(k_scale),
+                    reinterpret_cast<uint4*>(v_scale), pairs, num_pairs, chunks_kv,
+                    chunks_scale, c.num_blocks, status);
 }
 
 }  // namespace kvp

@@ -623,6 +623,7 @@ __global__ void __launch_bounds__(kWarps * 32)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
+  grid_dependency_wait();  // the previous kernel (e.g. the append) has landed
   const int n = p.context_lens[b];
   if (n <= 0 || n > p.max_blocks * kBlockSize) {
     if (part == 0) {
@@ -728,6 +729,7 @@ __global__ void __launch_bounds__(kWarps * 32)
   }
 
   // ---- merge the warps' partial states (stage memory is free now)
+  launch_dependents();
   __syncthreads();
   const bool cta_bad = any_bad || cta_flag != 0;
   float* mo = reinterpret_cast<float*>(smem);
@@ -789,9 +791,8 @@ cudaError_t launch_partial(const DecodeParams& p, const CUtensorMap& tk, const C
   cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(&decode_partial_kernel<Path>),
                                    decode_smem_for<Path>(kMaxPartBlocks));
   if (e != cudaSuccess) return e;
-  dim3 grid(grid_x, p.num_kv_heads * p.qgroups, p.batch);
-  decode_partial_kernel<Path><<<grid, kWarps * 32, smem, s>>>(p, tk, tv);
-  return cudaGetLastError();
+  const dim3 grid(grid_x, p.num_kv_heads * p.qgroups, p.batch);
+  return launch_pdl(decode_partial_kernel<Path>, grid, dim3(kWarps * 32), smem, s, p, tk, tv);
 }
 
 }  // namespace kvp

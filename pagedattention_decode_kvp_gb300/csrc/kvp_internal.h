@@ -6,6 +6,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <utility>
+
 #include "kvp.h"
 
 namespace kvp {
@@ -54,6 +56,26 @@ cudaError_t launch_decode_mma(const DecodeParams& p, const CUtensorMap& tk,
 cudaError_t launch_decode_mma_int8(const DecodeParams& p, const CUtensorMap& tk,
                                    const CUtensorMap& tv, int grid_x, cudaStream_t s);
 cudaError_t launch_decode_reduce(const DecodeParams& p, cudaStream_t s);
+
+// Launch `kernel` on stream `s` with programmatic stream serialisation, so its
+// CTAs can be scheduled while the previous kernel drains (every kernel of this
+// library starts with a grid-dependency wait, so this never lets it read data
+// a predecessor is still writing).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t s, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 // Raise a kernel's dynamic shared-memory limit to `bytes` on the current
 // device (once per device and kernel).

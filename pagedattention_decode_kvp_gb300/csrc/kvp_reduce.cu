@@ -2,7 +2,8 @@
 // query head) into the final output row (flash-decoding's second pass).
 //   M = max_p m_p;  w_p = 2^(m_p - M);  out = sum_p w_p o_p / sum_p w_p l_p
 // (m_p is kept in log2 units, o_p unnormalised).  A partition that failed its
-// checks is marked with l_p < 0 and turns the whole row into zeros.
+// checks is marked with l_p < 0 and turns the whole row into zeros.  The
+// partials were written moments before, so they are read mostly from L2.
 #include <mutex>
 #include <set>
 #include <utility>
@@ -12,12 +13,20 @@
 
 namespace kvp {
 
+// One CTA of 8 warps per (request, query head) row: all threads find the
+// largest partition max, warp w accumulates partitions w, w+8, ... (one lane
+// per D/32 output elements, independent loads), shared memory sums the warps.
 template <int D, bool kBf16Out>
-__global__ void __launch_bounds__(128) decode_reduce_kernel(const DecodeParams p) {
+__global__ void __launch_bounds__(256) decode_reduce_kernel(const DecodeParams p) {
   constexpr int E = D / 32;  // output elements per lane
+  constexpr int W = 8;
+  __shared__ __align__(16) float s_acc[W][D];
+  __shared__ float s_m[W];
+  __shared__ float s_l[W];
+  dev::grid_dependency_wait();  // the partition pass has written the workspace
+  dev::launch_dependents();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int row = blockIdx.x * 4 + warp;  // (b, h) flattened
-  if (row >= p.batch * p.num_q_heads) return;
+  const int row = blockIdx.x;  // (b, h) flattened
   const int b = row / p.num_q_heads;
   const int n = p.context_lens[b];
   if (n <= 0 || n > p.max_blocks * kBlockSize) return;  // written by the partition pass
@@ -29,13 +38,17 @@ __global__ void __launch_bounds__(128) decode_reduce_kernel(const DecodeParams p
   const float* wo = p.ws_o + static_cast<size_t>(row) * p.max_parts * D + lane * E;
   float M = -INFINITY;
   bool bad = false;
-  for (int i = lane; i < nparts; i += 32) {
+  for (int i = threadIdx.x; i < nparts; i += blockDim.x) {
     const float2 v = *reinterpret_cast<const float2*>(ml + 2 * i);
     M = fmaxf(M, v.x);
     bad |= v.y < 0.f;
   }
   M = dev::warp_max(M);
-  bad = __any_sync(0xffffffffu, bad);
+  if (lane == 0) s_m[warp] = M;
+  bad = __syncthreads_or(bad);
+  M = s_m[0];
+#pragma unroll
+  for (int w = 1; w < W; ++w) M = fmaxf(M, s_m[w]);
 
   float acc[E];
 #pragma unroll
@@ -43,7 +56,7 @@ __global__ void __launch_bounds__(128) decode_reduce_kernel(const DecodeParams p
   float L = 0.f;
   if (!bad) {
 #pragma unroll 4
-    for (int i = 0; i < nparts; ++i) {
+    for (int i = warp; i < nparts; i += W) {
       const float2 v = *reinterpret_cast<const float2*>(ml + 2 * i);
       const float f = exp2f(v.x - M);
       L = fmaf(f, v.y, L);
@@ -60,27 +73,38 @@ __global__ void __launch_bounds__(128) decode_reduce_kernel(const DecodeParams p
       }
     }
   }
-  uint16_t* out = static_cast<uint16_t*>(p.out) + static_cast<size_t>(row) * D + lane * E;
+  if constexpr (E == 4) {
+    *reinterpret_cast<float4*>(&s_acc[warp][lane * 4]) = make_float4(acc[0], acc[1], acc[2], acc[3]);
+  } else {
+    *reinterpret_cast<float2*>(&s_acc[warp][lane * 2]) = make_float2(acc[0], acc[1]);
+  }
+  if (lane == 0) s_l[warp] = L;
+  __syncthreads();
+  if (threadIdx.x < D) {
+    float a = 0.f, lt = 0.f;
 #pragma unroll
-  for (int e = 0; e < E; ++e) {
-    const float r = (!bad && L > 0.f) ? acc[e] / L : 0.f;
-    out[e] = dev::from_float<kBf16Out>(r);
+    for (int w = 0; w < W; ++w) {
+      a += s_acc[w][threadIdx.x];
+      lt += s_l[w];
+    }
+    const float r = (!bad && lt > 0.f) ? a / lt : 0.f;
+    static_cast<uint16_t*>(p.out)[static_cast<size_t>(row) * D + threadIdx.x] =
+        dev::from_float<kBf16Out>(r);
   }
 }
 
 cudaError_t launch_decode_reduce(const DecodeParams& p, cudaStream_t s) {
-  const int rows = p.batch * p.num_q_heads;
-  const dim3 grid((rows + 3) / 4);
+  const dim3 grid(p.batch * p.num_q_heads);
+  const dim3 block(256);
   if (p.head_dim == 64) {
-    if (p.q_bf16) decode_reduce_kernel<64, true><<<grid, 128, 0, s>>>(p);
-    else decode_reduce_kernel<64, false><<<grid, 128, 0, s>>>(p);
-  } else if (p.head_dim == 128) {
-    if (p.q_bf16) decode_reduce_kernel<128, true><<<grid, 128, 0, s>>>(p);
-    else decode_reduce_kernel<128, false><<<grid, 128, 0, s>>>(p);
-  } else {
-    return cudaErrorInvalidValue;
+    return p.q_bf16 ? launch_pdl(decode_reduce_kernel<64, true>, grid, block, 0, s, p)
+                    : launch_pdl(decode_reduce_kernel<64, false>, grid, block, 0, s, p);
   }
-  return cudaGetLastError();
+  if (p.head_dim == 128) {
+    return p.q_bf16 ? launch_pdl(decode_reduce_kernel<128, true>, grid, block, 0, s, p)
+                    : launch_pdl(decode_reduce_kernel<128, false>, grid, block, 0, s, p);
+  }
+  return cudaErrorInvalidValue;
 }
 
 cudaError_t ensure_smem_attr(const void* kernel, size_t bytes) {

@@ -56,12 +56,18 @@ def _desc(nb=64, hkv=2, bs=16, d=64):
 def test_workspace_sizing_rules(lib):
     # single pass when the table fits one partition: no workspace
     assert kvp.kvp_decode_workspace_bytes(4, 8, _desc(), 16) == 0
-    # 4096-token contexts, 32 x 32 heads: 32-block partitions, 8 of them
+    # 4096-token contexts, 32 x 32 heads: the automatic split, and its workspace
     d = _desc(10000, 32, 16, 128)
-    assert kvp.kvp_decode_partition_blocks(32, 32, d, 256) == 32
-    assert kvp.kvp_decode_workspace_bytes(32, 32, d, 256) == 32 * 32 * 8 * (128 + 2) * 4
+    pb = kvp.kvp_decode_partition_blocks(32, 32, d, 256)
+    assert 16 <= pb < 256
+    parts = -(-256 // pb)
+    assert kvp.kvp_decode_workspace_bytes(32, 32, d, 256) == 32 * 32 * parts * (128 + 2) * 4
     # explicit partition size
     assert kvp.kvp_decode_workspace_bytes(32, 32, d, 256, 64) == 32 * 32 * 4 * (128 + 2) * 4
+    assert kvp.kvp_decode_workspace_bytes(32, 32, d, 256, 256) == 0   # single pass
+    # many short requests stay single pass; one very long one is split
+    assert kvp.kvp_decode_workspace_bytes(128, 32, _desc(8192, 32, 16, 128), 97) == 0
+    assert kvp.kvp_decode_partition_blocks(4, 64, _desc(40000, 8, 16, 128), 8192, 1) <= 1024
     # invalid sizes answer 0
     assert kvp.kvp_decode_workspace_bytes(4, 6, _desc(hkv=4), 16) == 0      # 6 % 4 != 0
     assert kvp.kvp_decode_workspace_bytes(4, 8, _desc(d=96), 16) == 0       # head_dim 96

@@ -195,7 +195,12 @@ def test_append_int8_bit_exact(src_dtype, D):
     key = (torch.randn(T, Hkv, D, generator=g) * torch.rand(T, Hkv, 1, generator=g) * 4)
     value = torch.randn(T, Hkv, D, generator=g)
     key[5] = 0.0                           # all-zero rows keep scale 1
-    key[6, :, :3] = 2.5                    # ties after division
+    key[6, :, :3] = 2.5
+    # abs-max 127 gives scale exactly 1, so x.5 entries are exact ties (-> even)
+    ties = (torch.arange(D, dtype=torch.float32) - D / 2) + 0.5
+    ties[0] = 127.0
+    key[8] = ties
+    value[9] = -ties
     key, value = key.to(src_dtype), value.to(src_dtype)
     slots = torch.randperm(NB * 16, generator=g)[:T].to(torch.int32)
     slots[7] = -1                          # padding token

@@ -57,11 +57,12 @@ def test_noalloc_matches_workspace_decode_on_two_calls_in_a_row(lib):
 
 
 def test_noalloc_rejects_sizes_beyond_its_scratch(lib):
-    # 64 requests x 64 heads x 8192-block tables: far more partials than 64 MiB
+    # 64 requests x 64 heads x 8192-block tables cut into 16-block partitions:
+    # far more partials than the scratch array holds
     desc = kvp.kvp_cache_desc(40000, 8, 16, 128)
-    assert kvp.kvp_decode_workspace_bytes(64, 64, desc, 8192) > kvp.NOALLOC_SCRATCH_BYTES
+    assert kvp.kvp_decode_workspace_bytes(64, 64, desc, 8192, 16) > kvp.NOALLOC_SCRATCH_BYTES
     st = lib.kvp_attention_decode_noalloc(None, None, None, None, None, 8192, None, 64, 64,
-                                          ctypes.c_float(0.1), desc, kvp.KVP_BF16, 0, None,
+                                          ctypes.c_float(0.1), desc, kvp.KVP_BF16, 16, None,
                                           None)
     assert st == kvp.KVP_ERR_SCRATCH_LIMIT
     assert kvp.kvp_status_string(st) == "KVP_ERR_SCRATCH_LIMIT"
