@@ -207,7 +207,8 @@ class Step:
         w, kvp = self.w, self.kvp
         NB, Hkv, D = w.num_blocks, w.Hkv, w.D
         ks, vs = w.k_pool.to(self.dev), w.v_pool.to(self.dev)
-        self.kp = torch.empty(NB, Hkv, 16, D, dtype=torch.int8, device=self.dev)
+        code_dtype = torch.uint8 if w.kv_fp8 else torch.int8
+        self.kp = torch.empty(NB, Hkv, 16, D, dtype=code_dtype, device=self.dev)
         self.vp = torch.empty_like(self.kp)
         self.ks = torch.empty(NB, Hkv, 16, dtype=torch.float32, device=self.dev)
         self.vs = torch.empty_like(self.ks)
@@ -216,8 +217,9 @@ class Step:
         flat = lambda t: t.view(NB * Hkv, 1, 16, *t.shape[3:])  # noqa: E731
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record()
-        kvp.kvp_append_int8(ks.view(rows, 1, D), vs.view(rows, 1, D), flat(self.kp),
-                            flat(self.vp), flat(self.ks), flat(self.vs), slots)
+        append = kvp.kvp_append_fp8 if w.kv_fp8 else kvp.kvp_append_int8
+        append(ks.view(rows, 1, D), vs.view(rows, 1, D), flat(self.kp), flat(self.vp),
+               flat(self.ks), flat(self.vs), slots)
         e1.record()
         torch.cuda.synchronize()
         ms = e0.elapsed_time(e1)
@@ -234,8 +236,9 @@ class Step:
         if self.pairs is not None:
             kvp.kvp_copy_blocks(self.kp, self.vp, self.pairs, status=self.status)
         if w.kv_int8:
-            kvp.kvp_append_int8(self.new_k, self.new_v, self.kp, self.vp, self.ks, self.vs,
-                                self.slots, status=self.status)
+            append = kvp.kvp_append_fp8 if w.kv_fp8 else kvp.kvp_append_int8
+            append(self.new_k, self.new_v, self.kp, self.vp, self.ks, self.vs, self.slots,
+                   status=self.status)
         else:
             kvp.kvp_append(self.new_k, self.new_v, self.kp, self.vp, self.slots,
                            status=self.status)
@@ -244,10 +247,11 @@ class Step:
         phases = [kvp.KVP_PHASE_PARTIAL, kvp.KVP_PHASE_REDUCE] if self.split else [kvp.KVP_PHASE_ALL]
         for i, ph in enumerate(phases):
             if w.kv_int8:
-                kvp.kvp_attention_decode_int8(self.out, self.q, self.kp, self.vp, self.ks,
-                                              self.vs, self.tables, self.lens, w.scale,
-                                              workspace=self.ws, phases=ph, status=self.status,
-                                              partition_blocks=self.pb_arg)
+                decode = kvp.kvp_attention_decode_fp8 if w.kv_fp8 else \
+                    kvp.kvp_attention_decode_int8
+                decode(self.out, self.q, self.kp, self.vp, self.ks,
+                       self.vs, self.tables, self.lens, w.scale, workspace=self.ws, phases=ph,
+                       status=self.status, partition_blocks=self.pb_arg)
             else:
                 kvp.kvp_attention_decode(self.out, self.q, self.kp, self.vp, self.tables,
                                          self.lens, w.scale, workspace=self.ws, phases=ph,
@@ -411,7 +415,7 @@ def run_ours(args):
         "scaling": "weak",
         "vs_baseline": None,
         "dtype": {torch.float16: "f16", torch.bfloat16: "bf16"}[w.dtype] + (
-            " (int8 KV)" if w.kv_int8 else ""),
+            (" (fp8 e4m3 KV)" if w.kv_fp8 else " (int8 KV)") if w.kv_int8 else ""),
         "data": "synthetic (seeded N(0,1), shapes of the pages' workloads)",
         "config": {"workload": w.name + (f" (batch {w.B})" if args.batch else ""), "batch": w.B, "q_heads": w.Hq, "kv_heads": w.Hkv,
                    "head_dim": w.D, "block_size": 16, "num_blocks": w.num_blocks,
@@ -446,6 +450,8 @@ def run_ours(args):
         w_host = workloads.Workload(**{k: (v.cpu() if isinstance(v, torch.Tensor) else v)
                                        for k, v in w.__dict__.items()})
         hk, hv = step.kp.cpu(), step.vp.cpu()
+        if w.kv_fp8:
+            hk, hv = hk.view(torch.float8_e4m3fn), hv.view(torch.float8_e4m3fn)
         hks = step.ks.cpu() if w.kv_int8 else None
         hvs = step.vs.cpu() if w.kv_int8 else None
         rows = sample_rows(w, args.cpu_rows)
@@ -482,9 +488,12 @@ def run_reference(args):
                               for k, v in w.__dict__.items()})
     kp, vp, ks, vs = w.k_pool, w.v_pool, None, None
     if w.kv_int8:
-        kc, ksn = oracle.quantize_int8(kp)
-        vc, vsn = oracle.quantize_int8(vp)
+        quant = oracle.quantize_fp8 if w.kv_fp8 else oracle.quantize_int8
+        kc, ksn = quant(kp)
+        vc, vsn = quant(vp)
         kp, vp = torch.from_numpy(kc), torch.from_numpy(vc)
+        if w.kv_fp8:
+            kp, vp = kp.view(torch.float8_e4m3fn), vp.view(torch.float8_e4m3fn)
         ks, vs = torch.from_numpy(ksn), torch.from_numpy(vsn)
     rows = sample_rows(w, args.cpu_rows)
     for _ in range(args.warmup):

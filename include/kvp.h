@@ -121,12 +121,45 @@ kvp_status kvp_append(const void* key, const void* value, void* k_cache, void* v
  *   k_cache[blk, h, off, :] = clip(rint(x / s), -128, 127);  k_scale[blk, h, off] = s
  * and the same for V.  Results are bit-exact with that float32 definition.
  * key, value: [num_tokens, Hkv, D] of `src_dtype`; k_cache, v_cache: int8 pools;
- * k_scale, v_scale: float32 [NB, Hkv, bs].  Errors as kvp_append.
+ * k_scale, v_scale: float32 [NB, Hkv, bs].  Sources 16-byte aligned, int8 pools
+ * 8-byte aligned.  Errors as kvp_append.
  */
 kvp_status kvp_append_int8(const void* key, const void* value, kvp_dtype src_dtype,
                            int8_t* k_cache, int8_t* v_cache, float* k_scale,
                            float* v_scale, const int32_t* slot_mapping, int32_t num_tokens,
                            kvp_cache_desc cache, int32_t* dev_status, kvp_stream_t stream);
+
+/*
+ * kvp_append_int8_fixed -- per-tensor INT8: quantise with a given scale, scatter.
+ * Source: "KV Cache 优化与显存管理", 三, KVCacheQuantizer, per_tensor branch (one
+ * scale for the whole tensor, abs-max / 127).  A cache filled token by token
+ * cannot see the whole tensor, so the scale is fixed ahead by the caller:
+ *   k_cache[blk, h, off, :] = clip(rint(float32(key[t, h, :]) / k_scale), -128, 127)
+ * (IEEE float32 division, round half to even) and k_scale is also written to
+ * k_scale_pool[blk, h, off], so kvp_attention_decode_int8 reads these pools as
+ * it reads per-token ones.  Same for V.  k_scale, v_scale: finite and > 0.
+ * Other arguments and errors as kvp_append_int8.
+ */
+kvp_status kvp_append_int8_fixed(const void* key, const void* value, kvp_dtype src_dtype,
+                                 int8_t* k_cache, int8_t* v_cache, float* k_scale_pool,
+                                 float* v_scale_pool, float k_scale, float v_scale,
+                                 const int32_t* slot_mapping, int32_t num_tokens,
+                                 kvp_cache_desc cache, int32_t* dev_status, kvp_stream_t stream);
+
+/*
+ * kvp_append_fp8 -- FP8 (E4M3) per token and head quantisation, then scatter.
+ * Source: "KV Cache 优化与显存管理", 二 (K and V quantised from FP16 to INT8 or
+ * FP8).  The pages give the rule for INT8 only; this is the same rule with the
+ * E4M3 format's largest magnitude, 448, in place of 127:
+ *   s = amax|x| / 448 (IEEE float32 division); s = 1 if s is not > 0;
+ *   code = E4M3 round-to-nearest-even of the float32 quotient x / s (saturating
+ *          at +-448; OCP "e4m3fn" encoding: bias 7, no infinities).
+ * Codes are bytes in uint8_t pools; otherwise as kvp_append_int8.
+ */
+kvp_status kvp_append_fp8(const void* key, const void* value, kvp_dtype src_dtype,
+                          uint8_t* k_cache, uint8_t* v_cache, float* k_scale, float* v_scale,
+                          const int32_t* slot_mapping, int32_t num_tokens, kvp_cache_desc cache,
+                          int32_t* dev_status, kvp_stream_t stream);
 
 /*
  * kvp_copy_blocks -- copy whole blocks (copy-on-write of a shared last block).
@@ -152,7 +185,7 @@ kvp_status kvp_copy_blocks(void* k_cache, void* v_cache, float* k_scale, float* 
  * means single-pass (no workspace needed).  Returns 0 on invalid sizes.
  */
 int32_t kvp_decode_partition_blocks(int32_t batch, int32_t num_q_heads, kvp_cache_desc cache,
-                                    int32_t max_blocks_per_seq, int32_t kv_int8);
+                                    int32_t max_blocks_per_seq, int32_t kv_8bit);
 
 /*
  * kvp_decode_workspace_bytes -- bytes of workspace the decode needs for these
@@ -160,10 +193,11 @@ int32_t kvp_decode_partition_blocks(int32_t batch, int32_t num_q_heads, kvp_cach
  * decode (0 = automatic).  The workspace holds, per (request, query head,
  * partition), the partition's running max, sum and unnormalised output in
  * float32; it needs no initialisation and is fully rewritten by each call.
+ * kv_8bit: nonzero for the INT8 / FP8 decodes (their CTAs are shaped alike).
  */
 size_t kvp_decode_workspace_bytes(int32_t batch, int32_t num_q_heads, kvp_cache_desc cache,
                                   int32_t max_blocks_per_seq, int32_t partition_blocks,
-                                  int32_t kv_int8);
+                                  int32_t kv_8bit);
 
 /*
  * kvp_attention_decode -- single-query paged attention over fp16/bf16 pools.
@@ -209,6 +243,22 @@ kvp_status kvp_attention_decode_int8(void* out, const void* q, kvp_dtype q_dtype
                                      int32_t partition_blocks, void* workspace,
                                      size_t workspace_bytes, int32_t phases,
                                      int32_t* dev_status, kvp_stream_t stream);
+
+/*
+ * kvp_attention_decode_fp8 -- as kvp_attention_decode_int8 over FP8 (E4M3)
+ * pools: K_i = e4m3(k_cache[...]) * k_scale[blk, g, off] (V likewise), exact
+ * widening of the codes, float32 accumulation.  Source: "KV Cache 优化与显存管理",
+ * 二 (FP8 KV) and 三 (dequantize: code * scale).
+ */
+kvp_status kvp_attention_decode_fp8(void* out, const void* q, kvp_dtype q_dtype,
+                                    const uint8_t* k_cache, const uint8_t* v_cache,
+                                    const float* k_scale, const float* v_scale,
+                                    const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                    const int32_t* context_lens, int32_t batch,
+                                    int32_t num_q_heads, float scale, kvp_cache_desc cache,
+                                    int32_t partition_blocks, void* workspace,
+                                    size_t workspace_bytes, int32_t phases, int32_t* dev_status,
+                                    kvp_stream_t stream);
 
 /*
  * kvp_attention_decode_noalloc -- kvp_attention_decode for callers that cannot

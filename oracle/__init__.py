@@ -32,7 +32,7 @@ _SRC = os.path.join(_HERE, "kvp_oracle.c")
 _BUILD_DIR = os.path.join(_HERE, "_build")
 _LIB_PATH = os.path.join(_BUILD_DIR, "libkvp_oracle.so")
 
-F16, BF16, I8 = 0, 1, 2
+F16, BF16, I8, E4M3 = 0, 1, 2, 3
 _lock = threading.Lock()
 _lib = None
 
@@ -78,6 +78,14 @@ def _load():
         lib.orc_copy_blocks.restype = I
         lib.orc_quantize_int8.argtypes = [P, I, ctypes.c_longlong, I, P, P]
         lib.orc_quantize_int8.restype = None
+        lib.orc_quantize_int8_fixed.argtypes = [P, I, ctypes.c_longlong, ctypes.c_float, P]
+        lib.orc_quantize_int8_fixed.restype = None
+        lib.orc_quantize_fp8.argtypes = [P, I, ctypes.c_longlong, I, P, P]
+        lib.orc_quantize_fp8.restype = None
+        lib.orc_e4m3_to_f64.argtypes = [ctypes.c_uint8]
+        lib.orc_e4m3_to_f64.restype = ctypes.c_double
+        lib.orc_f32_to_e4m3.argtypes = [ctypes.c_float]
+        lib.orc_f32_to_e4m3.restype = ctypes.c_uint8
         _lib = lib
         return lib
 
@@ -95,6 +103,10 @@ def _raw(x):
                 return x.view(torch.int16).numpy().view(np.uint16), BF16
             if x.dtype == torch.int8:
                 return x.numpy(), I8
+            if x.dtype == torch.float8_e4m3fn:
+                return x.view(torch.uint8).numpy(), E4M3
+            if x.dtype == torch.uint8:          # E4M3 bit patterns
+                return x.numpy(), E4M3
             x = x.numpy()
     except ImportError:  # pragma: no cover
         pass
@@ -103,6 +115,8 @@ def _raw(x):
         return x.view(np.uint16), F16
     if x.dtype == np.int8:
         return x, I8
+    if x.dtype == np.uint8:                     # E4M3 bit patterns
+        return x, E4M3
     raise TypeError(f"unsupported element type {x.dtype}")
 
 
@@ -147,6 +161,14 @@ def bf16_to_f64(bits: int) -> float:
     return _load().orc_bf16_to_f64(int(bits))
 
 
+def e4m3_to_f64(code: int) -> float:
+    return _load().orc_e4m3_to_f64(int(code))
+
+
+def f32_to_e4m3(x: float) -> int:
+    return int(_load().orc_f32_to_e4m3(float(x)))
+
+
 def attention_decode(q, k_cache, v_cache, block_tables, context_lens, scale,
                      *, k_scale=None, v_scale=None, rows=None):
     """softmax(q K^T * scale) V through block tables, in float64.
@@ -170,10 +192,11 @@ def attention_decode(q, k_cache, v_cache, block_tables, context_lens, scale,
     cl = _i32(context_lens).reshape(-1)
     if bt.ndim != 2 or bt.shape[0] != B or cl.shape[0] != B:
         raise ValueError("block_tables must be [B, MB] and context_lens [B]")
-    ks = _f32(k_scale) if kk == I8 else None
-    vs = _f32(v_scale) if kk == I8 else None
-    if kk == I8 and (ks is None or vs is None):
-        raise ValueError("int8 pools need k_scale and v_scale")
+    quant = kk in (I8, E4M3)
+    ks = _f32(k_scale) if quant else None
+    vs = _f32(v_scale) if quant else None
+    if quant and (ks is None or vs is None):
+        raise ValueError("int8 / fp8 pools need k_scale and v_scale")
     if rows is None:
         ra, n_rows = None, B * Hq
         out = np.zeros((B, Hq, D), dtype=np.float64)
@@ -270,6 +293,49 @@ def quantize_int8(src):
     s = np.empty(a.shape[:-1], dtype=np.float32)
     _load().orc_quantize_int8(_ptr(a), kind, rows, D, _ptr(q), _ptr(s))
     return q, s
+
+
+def quantize_int8_fixed(src, scale):
+    """Per-tensor INT8 quantisation of f16/bf16 ``src`` with a given scale."""
+    a, kind = _raw(src)
+    if kind not in (F16, BF16):
+        raise TypeError("quantize_int8_fixed takes f16 or bf16 input")
+    q = np.empty(a.shape, dtype=np.int8)
+    _load().orc_quantize_int8_fixed(_ptr(a), kind, a.size, float(scale), _ptr(q))
+    return q
+
+
+def quantize_fp8(src):
+    """Per-row (last axis) E4M3 quantisation of f16/bf16 ``src`` [..., D].
+    Returns (codes as uint8 bit patterns [..., D], scales float32 [...])."""
+    a, kind = _raw(src)
+    if kind not in (F16, BF16):
+        raise TypeError("quantize_fp8 takes f16 or bf16 input")
+    D = a.shape[-1]
+    rows = a.size // D if D else 0
+    q = np.empty(a.shape, dtype=np.uint8)
+    s = np.empty(a.shape[:-1], dtype=np.float32)
+    _load().orc_quantize_fp8(_ptr(a), kind, rows, D, _ptr(q), _ptr(s))
+    return q, s
+
+
+def append_fp8(k_codes, k_scales, src, slot_mapping):
+    """As append_int8 with the FP8 (E4M3) quantiser; codes are uint8 bit patterns
+    (or torch float8_e4m3fn tensors, returned as such)."""
+    q, s = quantize_fp8(src)
+    codes = append(k_codes, q.view(np.uint8), slot_mapping)
+    scales = _like(append_rows(_f32(k_scales), s, slot_mapping), k_scales)
+    return codes, scales
+
+
+def append_int8_fixed(k_codes, k_scales, src, slot_mapping, scale):
+    """Per-tensor INT8 append: codes with the given scale, which is also written
+    to the scale pool at each slot."""
+    q = quantize_int8_fixed(src, scale)
+    codes = append(k_codes, q, slot_mapping)
+    rows = np.full(q.shape[:-1], scale, dtype=np.float32)
+    scales = _like(append_rows(_f32(k_scales), rows, slot_mapping), k_scales)
+    return codes, scales
 
 
 def append_int8(k_codes, k_scales, src, slot_mapping):

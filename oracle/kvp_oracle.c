@@ -31,7 +31,7 @@
 #endif
 
 /* element kinds of a cache pool or of q */
-enum { ORC_F16 = 0, ORC_BF16 = 1, ORC_I8 = 2 };
+enum { ORC_F16 = 0, ORC_BF16 = 1, ORC_I8 = 2, ORC_E4M3 = 3 };
 
 /* ---------------------------------------------------------------------------
  * Exact widening of the two 16-bit float formats to double.
@@ -60,10 +60,47 @@ double orc_bf16_to_f64(uint16_t h) {
   return (double)f;
 }
 
+/* OCP FP8 E4M3 ("fn" variant): 1 sign, 4 exponent (bias 7), 3 fraction bits;
+ * exponent 0 is subnormal (m * 2^-9); S.1111.111 is NaN; there is no infinity;
+ * the largest finite magnitude is 1.75 * 2^8 = 448. */
+double orc_e4m3_to_f64(uint8_t c) {
+  int sign = (c >> 7) & 1;
+  int e = (c >> 3) & 0xf;
+  int m = c & 7;
+  double v;
+  if (e == 15 && m == 7) return NAN;
+  if (e == 0) v = ldexp((double)m, -9);
+  else v = ldexp((double)(8 + m), e - 10);
+  return sign ? -v : v;
+}
+
+/* Round a float to the nearest E4M3 value, ties to the even code (even
+ * fraction), magnitudes beyond 448 saturating to 448 ("satfinite"); NaN stays
+ * NaN.  The 127 non-negative finite codes are increasing in value, so the two
+ * neighbours of |x| are found by bisection over the codes. */
+uint8_t orc_f32_to_e4m3(float x) {
+  if (isnan(x)) return 0x7f;
+  uint8_t sign = signbit(x) ? 0x80 : 0x00;
+  double a = fabs((double)x);
+  if (a >= 448.0) return sign | 0x7e;
+  int lo = 0, hi = 0x7e; /* value(lo) <= a < value(hi) */
+  while (hi - lo > 1) {
+    int mid = (lo + hi) / 2;
+    if (orc_e4m3_to_f64((uint8_t)mid) <= a) lo = mid; else hi = mid;
+  }
+  double vl = orc_e4m3_to_f64((uint8_t)lo), vh = orc_e4m3_to_f64((uint8_t)hi);
+  int code;
+  if (a - vl < vh - a) code = lo;
+  else if (a - vl > vh - a) code = hi;
+  else code = (lo % 2 == 0) ? lo : hi;
+  return sign | (uint8_t)code;
+}
+
 static double load_elem(const void* base, size_t idx, int kind) {
   switch (kind) {
     case ORC_F16: return orc_f16_to_f64(((const uint16_t*)base)[idx]);
     case ORC_BF16: return orc_bf16_to_f64(((const uint16_t*)base)[idx]);
+    case ORC_E4M3: return orc_e4m3_to_f64(((const uint8_t*)base)[idx]);
     default: return (double)((const int8_t*)base)[idx];
   }
 }
@@ -100,8 +137,9 @@ void orc_set_num_threads(int n) {
  *   s_i = scale * sum_d q[b,h,d] * K_i[d]
  *   p   = softmax(s)           (subtract max, exp, divide by the sum)
  *   out = sum_i p_i * V_i
- * INT8 pools hold codes; the value is code * scale_pool[blk, g, off] ([OPT] 三,
- * dequantize multiplies the code by its scale).  n == 0 gives a zero row.
+ * INT8 and FP8 pools hold codes; the value is code * scale_pool[blk, g, off]
+ * ([OPT] 三, dequantize multiplies the code by its scale; FP8 codes are first
+ * widened exactly).  n == 0 gives a zero row.
  *
  * rows: [n_rows, 2] (b, h) pairs, or NULL for every (b, h) in order.
  * out:  [n_rows, D] doubles.
@@ -142,7 +180,7 @@ int orc_attention_decode(double* out, const int32_t* rows, int n_rows,
       int off = i % bs;
       if (blk < 0 || blk >= num_blocks) { bad = 1; break; }
       size_t row = (((size_t)blk * Hkv + g) * bs + off);
-      double kscale = (cache_kind == ORC_I8) ? (double)k_scale[row] : 1.0;
+      double kscale = (cache_kind >= ORC_I8) ? (double)k_scale[row] : 1.0;
       double acc = 0.0;
       for (int d = 0; d < D; ++d)
         acc += qv[d] * (load_elem(k_cache, row * D + d, cache_kind) * kscale);
@@ -160,7 +198,7 @@ int orc_attention_decode(double* out, const int32_t* rows, int n_rows,
       int blk = block_tables[(size_t)b * max_blocks + i / bs];
       int off = i % bs;
       size_t row = (((size_t)blk * Hkv + g) * bs + off);
-      double vscale = (cache_kind == ORC_I8) ? (double)v_scale[row] : 1.0;
+      double vscale = (cache_kind >= ORC_I8) ? (double)v_scale[row] : 1.0;
       for (int d = 0; d < D; ++d)
         o[d] += s[i] * (load_elem(v_cache, row * D + d, cache_kind) * vscale);
     }
@@ -258,5 +296,58 @@ void orc_quantize_int8(const uint16_t* src, int src_kind, long long rows, int D,
       }
       scale_out[r] = sc;
     }
+  }
+}
+
+/* ---------------------------------------------------------------------------
+ * Per-tensor INT8 quantisation with a given scale ([OPT] 三, the per_tensor
+ * branch: one scale for the whole tensor; a paged cache that appends token by
+ * token fixes that scale ahead, so it is an input here):
+ *   q_j = clip(round_half_even(x_j / scale), -128, 127) in float32.
+ * ------------------------------------------------------------------------- */
+void orc_quantize_int8_fixed(const uint16_t* src, int src_kind, long long n, float scale,
+                             int8_t* q) {
+#pragma omp parallel
+  {
+    fesetround(FE_TONEAREST);
+#pragma omp for schedule(static)
+    for (long long i = 0; i < n; ++i) {
+      float x = (float)(src_kind == ORC_BF16 ? orc_bf16_to_f64(src[i]) : orc_f16_to_f64(src[i]));
+      volatile float ratio = x / scale;
+      float rq = nearbyintf(ratio);
+      if (rq > 127.0f) rq = 127.0f;
+      if (rq < -128.0f) rq = -128.0f;
+      q[i] = (int8_t)rq;
+    }
+  }
+}
+
+/* ---------------------------------------------------------------------------
+ * FP8 (E4M3) quantiser, per token and per head ([OPT] 二: K/V quantised from
+ * FP16 to INT8 or FP8).  The pages give the INT8 rule only; the FP8 rule here
+ * is the same with the format's largest magnitude in place of 127:
+ *   scale = amax / 448 (float32 division; 1 if not > 0),
+ *   code  = E4M3 round-to-nearest-even of the float32 quotient x / scale,
+ *           saturating at 448.
+ * ------------------------------------------------------------------------- */
+void orc_quantize_fp8(const uint16_t* src, int src_kind, long long rows, int D, uint8_t* q,
+                      float* scale_out) {
+#pragma omp parallel for schedule(static)
+  for (long long r = 0; r < rows; ++r) {
+    const uint16_t* x16 = src + (size_t)r * D;
+    float amax = 0.0f;
+    for (int j = 0; j < D; ++j) {
+      float x = (float)(src_kind == ORC_BF16 ? orc_bf16_to_f64(x16[j]) : orc_f16_to_f64(x16[j]));
+      float a = fabsf(x);
+      if (a > amax) amax = a;
+    }
+    volatile float s = amax / 448.0f;
+    float sc = (s > 0.0f) ? s : 1.0f;
+    for (int j = 0; j < D; ++j) {
+      float x = (float)(src_kind == ORC_BF16 ? orc_bf16_to_f64(x16[j]) : orc_f16_to_f64(x16[j]));
+      volatile float ratio = x / sc;
+      q[(size_t)r * D + j] = orc_f32_to_e4m3(ratio);
+    }
+    scale_out[r] = sc;
   }
 }

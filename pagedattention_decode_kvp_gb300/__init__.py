@@ -66,6 +66,9 @@ SIGNATURES = {
     "kvp_version": (_I32, []),
     "kvp_append": (_I32, [_P, _P, _P, _P, _P, _I32, _D, _I32, _P, _P]),
     "kvp_append_int8": (_I32, [_P, _P, _I32, _P, _P, _P, _P, _P, _I32, _D, _P, _P]),
+    "kvp_append_int8_fixed": (_I32, [_P, _P, _I32, _P, _P, _P, _P, _F, _F, _P, _I32, _D, _P,
+                                     _P]),
+    "kvp_append_fp8": (_I32, [_P, _P, _I32, _P, _P, _P, _P, _P, _I32, _D, _P, _P]),
     "kvp_copy_blocks": (_I32, [_P, _P, _P, _P, _I32, _P, _I32, _D, _P, _P]),
     "kvp_decode_partition_blocks": (_I32, [_I32, _I32, _D, _I32, _I32]),
     "kvp_decode_workspace_bytes": (_SZ, [_I32, _I32, _D, _I32, _I32, _I32]),
@@ -73,6 +76,8 @@ SIGNATURES = {
                                     _P, _SZ, _I32, _P, _P]),
     "kvp_attention_decode_int8": (_I32, [_P, _P, _I32, _P, _P, _P, _P, _P, _I32, _P, _I32, _I32,
                                          _F, _D, _I32, _P, _SZ, _I32, _P, _P]),
+    "kvp_attention_decode_fp8": (_I32, [_P, _P, _I32, _P, _P, _P, _P, _P, _I32, _P, _I32, _I32,
+                                        _F, _D, _I32, _P, _SZ, _I32, _P, _P]),
     "kvp_attention_decode_noalloc": (_I32, [_P, _P, _P, _P, _P, _I32, _P, _I32, _I32, _F, _D,
                                             _I32, _I32, _P, _P]),
     "kvp_read_status": (_I32, [_P, _P]),
@@ -197,6 +202,33 @@ def kvp_append_int8(key, value, k_cache, v_cache, k_scale, v_scale, slot_mapping
            "kvp_append_int8")
 
 
+def kvp_append_int8_fixed(key, value, k_cache, v_cache, k_scale_pool, v_scale_pool, k_scale,
+                          v_scale, slot_mapping, *, status=None, stream=None) -> None:
+    """Per-tensor INT8: quantise key/value with the given scales (also written to
+    the scale pools at each slot) and scatter the codes."""
+    lib = load_library()
+    _need_cuda(key, value, k_cache, v_cache, k_scale_pool, v_scale_pool, slot_mapping, status)
+    T = int(slot_mapping.numel())
+    _check(lib.kvp_append_int8_fixed(_ptr(key), _ptr(value), _dtype_code(key), _ptr(k_cache),
+                                     _ptr(v_cache), _ptr(k_scale_pool), _ptr(v_scale_pool),
+                                     float(k_scale), float(v_scale), _ptr(slot_mapping), T,
+                                     cache_desc(k_cache), _ptr(status), _stream_ptr(stream)),
+           "kvp_append_int8_fixed")
+
+
+def kvp_append_fp8(key, value, k_cache, v_cache, k_scale, v_scale, slot_mapping, *,
+                   status=None, stream=None) -> None:
+    """Quantise key/value [T, Hkv, D] to FP8 E4M3 per token and head (uint8 or
+    float8_e4m3fn pools) with float32 scales [NB, Hkv, bs], then scatter."""
+    lib = load_library()
+    _need_cuda(key, value, k_cache, v_cache, k_scale, v_scale, slot_mapping, status)
+    T = int(slot_mapping.numel())
+    _check(lib.kvp_append_fp8(_ptr(key), _ptr(value), _dtype_code(key), _ptr(k_cache),
+                              _ptr(v_cache), _ptr(k_scale), _ptr(v_scale), _ptr(slot_mapping),
+                              T, cache_desc(k_cache), _ptr(status), _stream_ptr(stream)),
+           "kvp_append_fp8")
+
+
 def kvp_copy_blocks(k_cache, v_cache, pairs, *, k_scale=None, v_scale=None, status=None,
                     stream=None) -> None:
     """Copy block pairs[i, 0] onto pairs[i, 1] in both pools (and scale pools)."""
@@ -254,6 +286,24 @@ def kvp_attention_decode_int8(out, q, k_cache, v_cache, k_scale, v_scale, block_
         _ptr(v_scale), _ptr(block_tables), int(block_tables.shape[1]), _ptr(context_lens), B, Hq,
         float(scale), cache_desc(k_cache), int(partition_blocks), _ptr(workspace), ws_bytes,
         int(phases), _ptr(status), _stream_ptr(stream)), "kvp_attention_decode_int8")
+
+
+def kvp_attention_decode_fp8(out, q, k_cache, v_cache, k_scale, v_scale, block_tables,
+                             context_lens, scale, *, workspace=None, partition_blocks=0,
+                             phases=KVP_PHASE_ALL, status=None, stream=None) -> None:
+    """As kvp_attention_decode over FP8 (E4M3) pools with float32 scales."""
+    lib = load_library()
+    _need_cuda(out, q, k_cache, v_cache, k_scale, v_scale, block_tables, context_lens, workspace,
+               status)
+    if out.dtype != q.dtype:
+        raise TypeError("out must have q's dtype")
+    B, Hq, _ = (int(x) for x in q.shape)
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    _check(lib.kvp_attention_decode_fp8(
+        _ptr(out), _ptr(q), _dtype_code(q), _ptr(k_cache), _ptr(v_cache), _ptr(k_scale),
+        _ptr(v_scale), _ptr(block_tables), int(block_tables.shape[1]), _ptr(context_lens), B, Hq,
+        float(scale), cache_desc(k_cache), int(partition_blocks), _ptr(workspace), ws_bytes,
+        int(phases), _ptr(status), _stream_ptr(stream)), "kvp_attention_decode_fp8")
 
 
 def kvp_attention_decode_noalloc(out, q, k_cache, v_cache, block_tables, context_lens, scale, *,

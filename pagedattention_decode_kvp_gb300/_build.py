@@ -25,6 +25,7 @@ SOURCES = [
     "kvp_decode_simt.cu",
     "kvp_decode_mma.cu",
     "kvp_decode_int8.cu",
+    "kvp_decode_fp8.cu",
     "kvp_reduce.cu",
     "kvp_block_manager.cpp",
     "kvp_noalloc.cu",

@@ -116,7 +116,7 @@ int auto_partition(DecodePath path, long long units, int max_blocks) {
 }
 
 kvp_status shape_decode(int batch, int num_q_heads, const kvp_cache_desc& c, int max_blocks,
-                        int partition_blocks, bool kv_int8, DecodeShape* out) {
+                        int partition_blocks, bool kv_8bit, DecodeShape* out) {
   if (batch < 0 || num_q_heads <= 0 || max_blocks <= 0) return KVP_ERR_INVALID_ARG;
   const kvp_status ds = check_desc(c);
   if (ds != KVP_OK) return ds;
@@ -124,8 +124,8 @@ kvp_status shape_decode(int batch, int num_q_heads, const kvp_cache_desc& c, int
   if (partition_blocks < 0 || partition_blocks > kMaxPartBlocks) return KVP_ERR_INVALID_ARG;
   const int G = num_q_heads / c.num_kv_heads;
   DecodeShape s;
-  if (kv_int8) {
-    s.path = DecodePath::kMmaInt8;
+  if (kv_8bit) {
+    s.path = DecodePath::kMmaInt8;  // INT8 and FP8 share the shape (8-bit tiles)
     s.heads_per_cta = G < kHeadsPerCta ? G : kHeadsPerCta;
   } else if (G <= 2) {
     s.path = DecodePath::kSimt;
@@ -153,7 +153,7 @@ kvp_status decode_common(void* out, const void* q, bool q_bf16, int kv_kind, con
                          int32_t max_blocks, const int32_t* lens, int32_t batch, int32_t hq,
                          float scale, kvp_cache_desc c, int32_t partition_blocks, void* ws,
                          size_t ws_bytes, int32_t phases, int32_t* status, kvp_stream_t stream) {
-  const bool int8 = kv_kind == 2;
+  const bool int8 = kv_kind >= 2;  // 8-bit codes with scales: INT8 (2) or FP8 E4M3 (3)
   DecodeShape sh;
   const kvp_status st = shape_decode(batch, hq, c, max_blocks, partition_blocks, int8, &sh);
   if (st != KVP_OK) return st;
@@ -214,7 +214,8 @@ kvp_status decode_common(void* out, const void* q, bool q_bf16, int kv_kind, con
         e = launch_decode_mma(p, tk, tv, kv_kind == 1, sh.max_parts, s);
         break;
       default:
-        e = launch_decode_mma_int8(p, tk, tv, sh.max_parts, s);
+        e = kv_kind == 3 ? launch_decode_mma_fp8(p, tk, tv, sh.max_parts, s)
+                         : launch_decode_mma_int8(p, tk, tv, sh.max_parts, s);
         break;
     }
     if (e != cudaSuccess) return KVP_ERR_CUDA;
@@ -272,12 +273,54 @@ kvp_status kvp_append_int8(const void* key, const void* value, kvp_dtype src_dty
   if (num_tokens == 0) return KVP_OK;
   if (!key || !value || !k_cache || !v_cache || !k_scale || !v_scale || !slot_mapping)
     return KVP_ERR_INVALID_ARG;
-  if (!aligned(key, 8) || !aligned(value, 8) || !aligned(k_cache, 4) || !aligned(v_cache, 4) ||
+  if (!aligned(key, 16) || !aligned(value, 16) || !aligned(k_cache, 8) || !aligned(v_cache, 8) ||
       !aligned(k_scale, 4) || !aligned(v_scale, 4))
     return KVP_ERR_INVALID_ARG;
   return from_cuda(launch_append_int8(key, value, src_dtype == KVP_BF16, k_cache, v_cache, k_scale,
                                       v_scale, slot_mapping, num_tokens, cache, dev_status,
                                       reinterpret_cast<cudaStream_t>(stream)));
+}
+
+kvp_status kvp_append_int8_fixed(const void* key, const void* value, kvp_dtype src_dtype,
+                                 int8_t* k_cache, int8_t* v_cache, float* k_scale_pool,
+                                 float* v_scale_pool, float k_scale, float v_scale,
+                                 const int32_t* slot_mapping, int32_t num_tokens,
+                                 kvp_cache_desc cache, int32_t* dev_status, kvp_stream_t stream) {
+  const kvp_status ds = check_desc(cache);
+  if (ds != KVP_OK) return ds;
+  if (num_tokens < 0 || (src_dtype != KVP_F16 && src_dtype != KVP_BF16))
+    return KVP_ERR_INVALID_ARG;
+  if (!(k_scale > 0.f) || !(v_scale > 0.f) || !std::isfinite(k_scale) || !std::isfinite(v_scale))
+    return KVP_ERR_INVALID_ARG;
+  if (num_tokens == 0) return KVP_OK;
+  if (!key || !value || !k_cache || !v_cache || !k_scale_pool || !v_scale_pool || !slot_mapping)
+    return KVP_ERR_INVALID_ARG;
+  if (!aligned(key, 16) || !aligned(value, 16) || !aligned(k_cache, 8) || !aligned(v_cache, 8) ||
+      !aligned(k_scale_pool, 4) || !aligned(v_scale_pool, 4))
+    return KVP_ERR_INVALID_ARG;
+  return from_cuda(launch_append_int8_fixed(key, value, src_dtype == KVP_BF16, k_cache, v_cache,
+                                            k_scale_pool, v_scale_pool, k_scale, v_scale,
+                                            slot_mapping, num_tokens, cache, dev_status,
+                                            reinterpret_cast<cudaStream_t>(stream)));
+}
+
+kvp_status kvp_append_fp8(const void* key, const void* value, kvp_dtype src_dtype,
+                          uint8_t* k_cache, uint8_t* v_cache, float* k_scale, float* v_scale,
+                          const int32_t* slot_mapping, int32_t num_tokens, kvp_cache_desc cache,
+                          int32_t* dev_status, kvp_stream_t stream) {
+  const kvp_status ds = check_desc(cache);
+  if (ds != KVP_OK) return ds;
+  if (num_tokens < 0 || (src_dtype != KVP_F16 && src_dtype != KVP_BF16))
+    return KVP_ERR_INVALID_ARG;
+  if (num_tokens == 0) return KVP_OK;
+  if (!key || !value || !k_cache || !v_cache || !k_scale || !v_scale || !slot_mapping)
+    return KVP_ERR_INVALID_ARG;
+  if (!aligned(key, 16) || !aligned(value, 16) || !aligned(k_cache, 8) || !aligned(v_cache, 8) ||
+      !aligned(k_scale, 4) || !aligned(v_scale, 4))
+    return KVP_ERR_INVALID_ARG;
+  return from_cuda(launch_append_fp8(key, value, src_dtype == KVP_BF16, k_cache, v_cache, k_scale,
+                                     v_scale, slot_mapping, num_tokens, cache, dev_status,
+                                     reinterpret_cast<cudaStream_t>(stream)));
 }
 
 kvp_status kvp_copy_blocks(void* k_cache, void* v_cache, float* k_scale, float* v_scale,
@@ -340,6 +383,22 @@ kvp_status kvp_attention_decode_int8(void* out, const void* q, kvp_dtype q_dtype
                                      int32_t* dev_status, kvp_stream_t stream) {
   if (q_dtype != KVP_F16 && q_dtype != KVP_BF16) return KVP_ERR_INVALID_ARG;
   return decode_common(out, q, q_dtype == KVP_BF16, 2, k_cache, v_cache, k_scale, v_scale,
+                       block_tables, max_blocks_per_seq, context_lens, batch, num_q_heads, scale,
+                       cache, partition_blocks, workspace, workspace_bytes, phases, dev_status,
+                       stream);
+}
+
+kvp_status kvp_attention_decode_fp8(void* out, const void* q, kvp_dtype q_dtype,
+                                    const uint8_t* k_cache, const uint8_t* v_cache,
+                                    const float* k_scale, const float* v_scale,
+                                    const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                    const int32_t* context_lens, int32_t batch,
+                                    int32_t num_q_heads, float scale, kvp_cache_desc cache,
+                                    int32_t partition_blocks, void* workspace,
+                                    size_t workspace_bytes, int32_t phases, int32_t* dev_status,
+                                    kvp_stream_t stream) {
+  if (q_dtype != KVP_F16 && q_dtype != KVP_BF16) return KVP_ERR_INVALID_ARG;
+  return decode_common(out, q, q_dtype == KVP_BF16, 3, k_cache, v_cache, k_scale, v_scale,
                        block_tables, max_blocks_per_seq, context_lens, batch, num_q_heads, scale,
                        cache, partition_blocks, workspace, workspace_bytes, phases, dev_status,
                        stream);

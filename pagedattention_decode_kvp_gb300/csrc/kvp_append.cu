@@ -3,7 +3,9 @@
 //     三, write_page; "ATB PagedAttention", "踩坑三", WriteKV), slot = block * 16 +
 //     offset ("ATB 的 PagedAttention 实现": page = pos / size, offset = pos % size);
 //   * append_int8: per token and head abs-max / 127 quantisation, then scatter
-//     ("KV Cache 优化与显存管理", 三, KVCacheQuantizer per-channel branch);
+//     ("KV Cache 优化与显存管理", 三, KVCacheQuantizer per-channel branch); the
+//     fixed-scale variant (per-tensor branch) and the FP8 (E4M3) variant
+//     ("KV Cache 优化与显存管理", 二: INT8 or FP8) share the kernel;
 //   * copy_blocks: whole-block copies for copy-on-write ("踩坑三", ExtendKVPage).
 // All three are pure HBM streams: 16-byte vector loads and stores, one thread
 // per 16-byte chunk, rows of a block contiguous so every warp access coalesces.
@@ -13,109 +15,166 @@
 namespace kvp {
 namespace {
 
+// grid = (ceil(T / tokens per CTA), Hkv); CPR 16-byte chunks per row, one per
+// thread, so a row's chunks are adjacent lanes (coalesced source and slot).
+template <int CPR>
 __global__ void __launch_bounds__(256)
     append_kernel(const uint4* __restrict__ key, const uint4* __restrict__ value,
                   uint4* __restrict__ kc, uint4* __restrict__ vc, const int32_t* __restrict__ slots,
-                  long long total_chunks, int num_kv_heads, int chunks_per_row,
-                  long long num_slots, int32_t* status) {
+                  int num_tokens, int num_kv_heads, int num_slots, int32_t* status) {
+  constexpr int kTokens = 256 / CPR;
   dev::grid_dependency_wait();
   dev::launch_dependents();
-  const long long idx = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
-  if (idx >= total_chunks) return;
-  const int ch = static_cast<int>(idx % chunks_per_row);
-  const long long row = idx / chunks_per_row;  // t * Hkv + h
-  const long long t = row / num_kv_heads;
-  const int h = static_cast<int>(row % num_kv_heads);
+  const int t = blockIdx.x * kTokens + static_cast<int>(threadIdx.x) / CPR;
+  const int ch = threadIdx.x % CPR;
+  const int h = blockIdx.y;
+  if (t >= num_tokens) return;
   const int slot = slots[t];
   if (slot < 0) return;  // padding token
   if (slot >= num_slots) {
     if (h == 0 && ch == 0) dev::set_status(status, kErrBadBlock);
     return;
   }
-  const long long blk = slot / kBlockSize, off = slot % kBlockSize;
-  const long long dst = ((blk * num_kv_heads + h) * kBlockSize + off) * chunks_per_row + ch;
-  kc[dst] = key[row * chunks_per_row + ch];
-  vc[dst] = value[row * chunks_per_row + ch];
+  const size_t src = (static_cast<size_t>(t) * num_kv_heads + h) * CPR + ch;
+  const size_t dst =
+      ((static_cast<size_t>(slot / kBlockSize) * num_kv_heads + h) * kBlockSize +
+       slot % kBlockSize) * CPR + ch;
+  kc[dst] = key[src];
+  vc[dst] = value[src];
 }
 
-// rint(x / s) clipped to [-128, 127], with x / s the IEEE float32 quotient.
-// r = x * (1/s) is within 2e-5 of x / s for |x / s| <= 127.0001 (two roundings
-// of relative size 2^-24 each), and RN(x / s) within 8e-6 of it, so whenever r
-// lies more than 1e-4 from a half-integer both round to the same integer; only
-// inside that band is the exact quotient computed.
-__device__ __forceinline__ int quantise_code(float x, float s, float inv) {
-  const float r = x * inv;
-  const float fl = floorf(r);
-  const float frac = r - fl;
-  int q;
-  if (fabsf(frac - 0.5f) > 1.0e-4f) {
-    q = static_cast<int>(frac > 0.5f ? fl + 1.0f : fl);
-  } else {
-    q = __float2int_rn(__fdiv_rn(x, s));
+// Codes rint(x_e / s) for 8 elements, x / s being the IEEE float32 quotient,
+// packed 4 per word.  r = x * (1/s) is within 2e-5 of x / s for |x / s| <=
+// 127.0001 (two roundings of relative size 2^-24), and RN(x / s) within 8e-6
+// of it, so whenever r lies more than 1e-4 from a half-integer both round to
+// the same integer; only elements inside that band take the exact quotient.
+// The clip to [-128, 127] of the definition never binds: s = RN(amax / 127)
+// keeps |x / s| <= 127 * (1 + 2^-23), which rounds to at most 127.
+template <bool kClip>
+__device__ __forceinline__ void quantise8(const float (&x)[8], float s, float inv,
+                                          uint32_t (&packed)[2]) {
+  int q[8];
+  bool near_tie = false;
+#pragma unroll
+  for (int e = 0; e < 8; ++e) {
+    const float r = x[e] * inv;
+    const float rr = rintf(r);
+    q[e] = static_cast<int>(rr);
+    near_tie |= fabsf(r - rr) > 0.5f - 1.0e-4f;
   }
-  return min(127, max(-128, q));
+  if (near_tie) {
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      const float r = x[e] * inv;
+      if (fabsf(r - rintf(r)) > 0.5f - 1.0e-4f) q[e] = __float2int_rn(__fdiv_rn(x[e], s));
+    }
+  }
+  if constexpr (kClip) {  // a fixed scale can put x / s outside [-128, 127]
+#pragma unroll
+    for (int e = 0; e < 8; ++e) q[e] = min(127, max(-128, q[e]));
+  }
+#pragma unroll
+  for (int w = 0; w < 2; ++w) {
+    const uint32_t lo = __byte_perm(q[4 * w], q[4 * w + 1], 0x0040);
+    const uint32_t hi = __byte_perm(q[4 * w + 2], q[4 * w + 3], 0x0040);
+    packed[w] = __byte_perm(lo, hi, 0x5410);
+  }
 }
 
-// One group of D/4 lanes per (token, head) row; each lane owns 4 elements.
-template <bool kBf16, int D>
+// E4M3 codes of x_e / s (IEEE float32 quotient), round-to-nearest-even,
+// saturating at 448, packed 4 per word (low byte first).
+__device__ __forceinline__ void quantise8_fp8(const float (&x)[8], float s, uint32_t (&packed)[2]) {
+#pragma unroll
+  for (int w = 0; w < 2; ++w) {
+    const uint32_t lo = dev::f32x2_to_e4m3x2(__fdiv_rn(x[4 * w], s), __fdiv_rn(x[4 * w + 1], s));
+    const uint32_t hi =
+        dev::f32x2_to_e4m3x2(__fdiv_rn(x[4 * w + 2], s), __fdiv_rn(x[4 * w + 3], s));
+    packed[w] = lo | (hi << 16);
+  }
+}
+
+enum class QuantMode { kInt8, kInt8Fixed, kFp8 };
+
+// Quantise-and-scatter.  One group of D/8 lanes per (token, head) row, each
+// lane owning 8 elements (one 16-byte load of K and of V); grid =
+// (ceil(T / tokens per CTA), Hkv).
+//   kInt8:      scale = amax / 127 (1 if not > 0), code = rint(x / scale)
+//   kInt8Fixed: the given scale, code = clip(rint(x / scale), -128, 127)
+//   kFp8:       scale = amax / 448 (1 if not > 0), code = E4M3(x / scale)
+// and the scale is stored beside the codes.
+template <bool kBf16, int D, QuantMode kMode>
 __global__ void __launch_bounds__(256)
-    append_int8_kernel(const uint16_t* __restrict__ key, const uint16_t* __restrict__ value,
-                       int8_t* __restrict__ kc, int8_t* __restrict__ vc, float* __restrict__ ks,
-                       float* __restrict__ vs, const int32_t* __restrict__ slots, long long rows,
-                       int num_kv_heads, long long num_slots, int32_t* status) {
-  constexpr int L = D / 4;
+    append_quant_kernel(const uint4* __restrict__ key, const uint4* __restrict__ value,
+                        uint8_t* __restrict__ kc, uint8_t* __restrict__ vc,
+                        float* __restrict__ ks, float* __restrict__ vs, float fixed_ks,
+                        float fixed_vs, const int32_t* __restrict__ slots, int num_tokens,
+                        int num_kv_heads, int num_slots, int32_t* status) {
+  constexpr int L = D / 8;
+  constexpr int kTokens = 256 / L;
   dev::grid_dependency_wait();
   dev::launch_dependents();
-  const long long gt = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
-  const long long row = gt / L;
-  const int sub = static_cast<int>(gt % L);
-  const bool in = row < rows;
+  const int t = blockIdx.x * kTokens + static_cast<int>(threadIdx.x) / L;
+  const int sub = threadIdx.x % L;
+  const int h = blockIdx.y;
+  const bool in = t < num_tokens;
   int slot = -1;
-  float xk[4] = {0.f, 0.f, 0.f, 0.f}, xv[4] = {0.f, 0.f, 0.f, 0.f};
+  float xk[8], xv[8];
+#pragma unroll
+  for (int e = 0; e < 8; ++e) xk[e] = xv[e] = 0.f;
   if (in) {
-    slot = slots[row / num_kv_heads];
-    const uint2 rk = *reinterpret_cast<const uint2*>(key + row * D + sub * 4);
-    const uint2 rv = *reinterpret_cast<const uint2*>(value + row * D + sub * 4);
-    const float2 k0 = dev::unpack2<kBf16>(rk.x), k1 = dev::unpack2<kBf16>(rk.y);
-    const float2 v0 = dev::unpack2<kBf16>(rv.x), v1 = dev::unpack2<kBf16>(rv.y);
-    xk[0] = k0.x; xk[1] = k0.y; xk[2] = k1.x; xk[3] = k1.y;
-    xv[0] = v0.x; xv[1] = v0.y; xv[2] = v1.x; xv[3] = v1.y;
-  }
-  float ak = 0.f, av = 0.f;
+    slot = slots[t];
+    const size_t src = (static_cast<size_t>(t) * num_kv_heads + h) * L + sub;
+    const uint4 rk = key[src];
+    const uint4 rv = value[src];
+    const uint32_t wk[4] = {rk.x, rk.y, rk.z, rk.w};
+    const uint32_t wv[4] = {rv.x, rv.y, rv.z, rv.w};
 #pragma unroll
-  for (int e = 0; e < 4; ++e) {
-    ak = fmaxf(ak, fabsf(xk[e]));
-    av = fmaxf(av, fabsf(xv[e]));
+    for (int i = 0; i < 4; ++i) {
+      const float2 a = dev::unpack2<kBf16>(wk[i]);
+      const float2 c = dev::unpack2<kBf16>(wv[i]);
+      xk[2 * i] = a.x;
+      xk[2 * i + 1] = a.y;
+      xv[2 * i] = c.x;
+      xv[2 * i + 1] = c.y;
+    }
   }
+  float sk = fixed_ks, sv = fixed_vs;
+  if constexpr (kMode != QuantMode::kInt8Fixed) {
+    float ak = 0.f, av = 0.f;
 #pragma unroll
-  for (int o = L / 2; o >= 1; o >>= 1) {
-    ak = fmaxf(ak, __shfl_xor_sync(0xffffffffu, ak, o));
-    av = fmaxf(av, __shfl_xor_sync(0xffffffffu, av, o));
+    for (int e = 0; e < 8; ++e) {
+      ak = fmaxf(ak, fabsf(xk[e]));
+      av = fmaxf(av, fabsf(xv[e]));
+    }
+#pragma unroll
+    for (int o = L / 2; o >= 1; o >>= 1) {
+      ak = fmaxf(ak, __shfl_xor_sync(0xffffffffu, ak, o));
+      av = fmaxf(av, __shfl_xor_sync(0xffffffffu, av, o));
+    }
+    // float32 IEEE division for the scale, as the quantiser is defined
+    const float qmax = kMode == QuantMode::kFp8 ? 448.0f : 127.0f;
+    sk = __fdiv_rn(ak, qmax);
+    sv = __fdiv_rn(av, qmax);
+    sk = sk > 0.f ? sk : 1.0f;
+    sv = sv > 0.f ? sv : 1.0f;
   }
   if (!in || slot < 0) return;
-  const int h = static_cast<int>(row % num_kv_heads);
   if (slot >= num_slots) {
     if (sub == 0 && h == 0) dev::set_status(status, kErrBadBlock);
     return;
   }
-  // float32 IEEE division and round-half-even, as the quantiser is defined
-  float sk = __fdiv_rn(ak, 127.0f);
-  float sv = __fdiv_rn(av, 127.0f);
-  sk = sk > 0.f ? sk : 1.0f;
-  sv = sv > 0.f ? sv : 1.0f;
-  const float ik = __frcp_rn(sk), iv = __frcp_rn(sv);
-  uint32_t pk = 0u, pv = 0u;
-#pragma unroll
-  for (int e = 0; e < 4; ++e) {
-    const int qk = quantise_code(xk[e], sk, ik);
-    const int qv = quantise_code(xv[e], sv, iv);
-    pk |= (static_cast<uint32_t>(qk) & 0xffu) << (8 * e);
-    pv |= (static_cast<uint32_t>(qv) & 0xffu) << (8 * e);
+  uint32_t pk[2], pv[2];
+  if constexpr (kMode == QuantMode::kFp8) {
+    quantise8_fp8(xk, sk, pk);
+    quantise8_fp8(xv, sv, pv);
+  } else {
+    quantise8<kMode == QuantMode::kInt8Fixed>(xk, sk, __frcp_rn(sk), pk);
+    quantise8<kMode == QuantMode::kInt8Fixed>(xv, sv, __frcp_rn(sv), pv);
   }
-  const long long blk = slot / kBlockSize, off = slot % kBlockSize;
-  const long long srow = (blk * num_kv_heads + h) * kBlockSize + off;
-  *reinterpret_cast<uint32_t*>(kc + srow * D + sub * 4) = pk;
-  *reinterpret_cast<uint32_t*>(vc + srow * D + sub * 4) = pv;
+  const size_t srow = (static_cast<size_t>(slot / kBlockSize) * num_kv_heads + h) * kBlockSize +
+                      slot % kBlockSize;
+  *reinterpret_cast<uint2*>(kc + srow * D + sub * 8) = make_uint2(pk[0], pk[1]);
+  *reinterpret_cast<uint2*>(vc + srow * D + sub * 8) = make_uint2(pv[0], pv[1]);
   if (sub == 0) {
     ks[srow] = sk;
     vs[srow] = sv;
@@ -162,40 +221,76 @@ __global__ void __launch_bounds__(256)
 cudaError_t launch_append(const void* key, const void* value, void* k_cache, void* v_cache,
                           const int32_t* slots, int num_tokens, const kvp_cache_desc& c,
                           int elem_bytes, int32_t* status, cudaStream_t s) {
+  if (num_tokens == 0) return cudaSuccess;
   const int cpr = c.head_dim * elem_bytes / 16;
-  const long long total = static_cast<long long>(num_tokens) * c.num_kv_heads * cpr;
-  if (total == 0) return cudaSuccess;
-  const long long grid = (total + 255) / 256;
-  return launch_pdl(append_kernel, dim3(static_cast<unsigned>(grid)), dim3(256), 0, s,
-                    static_cast<const uint4*>(key), static_cast<const uint4*>(value),
-                    static_cast<uint4*>(k_cache), static_cast<uint4*>(v_cache), slots, total,
-                    c.num_kv_heads, cpr, static_cast<long long>(c.num_blocks) * kBlockSize,
-                    status);
+  const int nslots = c.num_blocks * kBlockSize;
+  const auto* k = static_cast<const uint4*>(key);
+  const auto* v = static_cast<const uint4*>(value);
+  auto* kd = static_cast<uint4*>(k_cache);
+  auto* vd = static_cast<uint4*>(v_cache);
+  if (cpr == 16) {
+    const dim3 grid((num_tokens + 15) / 16, c.num_kv_heads);
+    return launch_pdl(append_kernel<16>, grid, dim3(256), 0, s, k, v, kd, vd, slots, num_tokens,
+                      c.num_kv_heads, nslots, status);
+  }
+  if (cpr == 8) {
+    const dim3 grid((num_tokens + 31) / 32, c.num_kv_heads);
+    return launch_pdl(append_kernel<8>, grid, dim3(256), 0, s, k, v, kd, vd, slots, num_tokens,
+                      c.num_kv_heads, nslots, status);
+  }
+  return cudaErrorInvalidValue;
+}
+
+template <QuantMode kMode>
+cudaError_t launch_quant(const void* key, const void* value, bool src_bf16, void* k_cache,
+                         void* v_cache, float* k_scale, float* v_scale, float fixed_ks,
+                         float fixed_vs, const int32_t* slots, int num_tokens,
+                         const kvp_cache_desc& c, int32_t* status, cudaStream_t s) {
+  if (num_tokens == 0) return cudaSuccess;
+  const int nslots = c.num_blocks * kBlockSize;
+  const auto* k = static_cast<const uint4*>(key);
+  const auto* v = static_cast<const uint4*>(value);
+  auto* kd = static_cast<uint8_t*>(k_cache);
+  auto* vd = static_cast<uint8_t*>(v_cache);
+  const int tokens_per_cta = 256 / (c.head_dim / 8);
+  const dim3 grid((num_tokens + tokens_per_cta - 1) / tokens_per_cta, c.num_kv_heads);
+#define KVP_Q_CASE(BF, DD)                                                                     \
+  if (src_bf16 == BF && c.head_dim == DD)                                                      \
+    return launch_pdl(append_quant_kernel<BF, DD, kMode>, grid, dim3(256), 0, s, k, v, kd, vd, \
+                      k_scale, v_scale, fixed_ks, fixed_vs, slots, num_tokens, c.num_kv_heads, \
+                      nslots, status);
+  KVP_Q_CASE(false, 64)
+  KVP_Q_CASE(false, 128)
+  KVP_Q_CASE(true, 64)
+  KVP_Q_CASE(true, 128)
+#undef KVP_Q_CASE
+  return cudaErrorInvalidValue;
 }
 
 cudaError_t launch_append_int8(const void* key, const void* value, bool src_bf16,
                                int8_t* k_cache, int8_t* v_cache, float* k_scale,
                                float* v_scale, const int32_t* slots, int num_tokens,
                                const kvp_cache_desc& c, int32_t* status, cudaStream_t s) {
-  const long long rows = static_cast<long long>(num_tokens) * c.num_kv_heads;
-  if (rows == 0) return cudaSuccess;
-  const long long threads = rows * (c.head_dim / 4);
-  const unsigned grid = static_cast<unsigned>((threads + 255) / 256);
-  const long long nslots = static_cast<long long>(c.num_blocks) * kBlockSize;
-  const uint16_t* k = static_cast<const uint16_t*>(key);
-  const uint16_t* v = static_cast<const uint16_t*>(value);
-#define KVP_I8_CASE(BF, DD)                                                                   \
-  if (src_bf16 == BF && c.head_dim == DD) {                                                   \
-    return launch_pdl(append_int8_kernel<BF, DD>, dim3(grid), dim3(256), 0, s, k, v,         \
-                      k_cache, v_cache, k_scale, v_scale, slots, rows, c.num_kv_heads,        \
-                      nslots, status);                                                        \
-  }
-  KVP_I8_CASE(false, 64)
-  KVP_I8_CASE(false, 128)
-  KVP_I8_CASE(true, 64)
-  KVP_I8_CASE(true, 128)
-#undef KVP_I8_CASE
-  return cudaErrorInvalidValue;
+  return launch_quant<QuantMode::kInt8>(key, value, src_bf16, k_cache, v_cache, k_scale, v_scale,
+                                        0.f, 0.f, slots, num_tokens, c, status, s);
+}
+
+cudaError_t launch_append_int8_fixed(const void* key, const void* value, bool src_bf16,
+                                     int8_t* k_cache, int8_t* v_cache, float* k_scale_pool,
+                                     float* v_scale_pool, float k_scale, float v_scale,
+                                     const int32_t* slots, int num_tokens,
+                                     const kvp_cache_desc& c, int32_t* status, cudaStream_t s) {
+  return launch_quant<QuantMode::kInt8Fixed>(key, value, src_bf16, k_cache, v_cache,
+                                             k_scale_pool, v_scale_pool, k_scale, v_scale, slots,
+                                             num_tokens, c, status, s);
+}
+
+cudaError_t launch_append_fp8(const void* key, const void* value, bool src_bf16,
+                              uint8_t* k_cache, uint8_t* v_cache, float* k_scale, float* v_scale,
+                              const int32_t* slots, int num_tokens, const kvp_cache_desc& c,
+                              int32_t* status, cudaStream_t s) {
+  return launch_quant<QuantMode::kFp8>(key, value, src_bf16, k_cache, v_cache, k_scale, v_scale,
+                                       0.f, 0.f, slots, num_tokens, c, status, s);
 }
 
 cudaError_t launch_copy_blocks(void* k_cache, void* v_cache, float* k_scale, float* v_scale,

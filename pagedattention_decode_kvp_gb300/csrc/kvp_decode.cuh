@@ -373,14 +373,15 @@ struct MmaPath {
 };
 
 // ===========================================================================
-// Tensor-core consumer for INT8 pools (codes + per-token-per-head fp32 scales),
-// up to 8 query heads per kv head.  Codes convert exactly to fp16 (or bf16
-// when q is bf16).  The contraction index d is permuted so each lane reads a
-// contiguous run of codes: for K, lane t4 feeds d in [t4*D/4, (t4+1)*D/4); for
-// V, lane g8 produces d in [g8*D/8, (g8+1)*D/8).  The K scale multiplies the
-// 16 scores after the mma; the V scale is folded into P (normalised by the
-// block's largest V scale to stay in fp16 range) and restored in fp32.
-template <bool kQBf16, int D>
+// Tensor-core consumer for 8-bit code pools (INT8, or FP8 E4M3 when kFp8) with
+// per-token-per-head fp32 scales, up to 8 query heads per kv head.  Codes
+// convert exactly to fp16 (or bf16 when q is bf16).  The contraction index d
+// is permuted so each lane reads a contiguous run of codes: for K, lane t4
+// feeds d in [t4*D/4, (t4+1)*D/4); for V, lane g8 produces d in
+// [g8*D/8, (g8+1)*D/8).  The K scale multiplies the 16 scores after the mma;
+// the V scale is folded into P (normalised by the block's largest V scale to
+// stay in fp16 range) and restored in fp32.
+template <bool kQBf16, int D, bool kFp8 = false>
 struct MmaInt8Path {
   static constexpr int kD = D;
   static constexpr int kHeads = 8;
@@ -429,12 +430,43 @@ struct MmaInt8Path {
     }
   }
 
+  // FP8 codes are widened by the hardware E4M3 -> fp16 convert.  (Measured
+  // alternatives: an exact bit move into fp16 at value * 2^-8 for K and V, or
+  // for V only, both ran slower because the move is all integer-pipe work.)
+  static constexpr float kCodeUnscale = 1.0f;
+  static constexpr float kVUnscale = 1.0f;
+
+  // Codes (bytes 0,1 or 2,3 of w) as the QK operand type.
   template <bool kHigh>
   __device__ __forceinline__ static uint32_t k_pair(uint32_t w) {
-    if constexpr (kQBf16) {
+    if constexpr (kFp8) {
+      const uint32_t h = dev::e4m3x2_to_f16x2(static_cast<uint16_t>(kHigh ? (w >> 16) : w));
+      if constexpr (kQBf16) {
+        const float2 f = dev::unpack2<false>(h);
+        return dev::pack2<true>(f.x, f.y);
+      } else {
+        return h;
+      }
+    } else if constexpr (kQBf16) {
       return dev::i8x2_to_bf16x2<kHigh>(w);
     } else {
       return dev::i8x2_to_f16x2<kHigh>(w ^ 0x80808080u);
+    }
+  }
+
+  // V codes of tokens A and B (byte j of each word, j = 0..3) as the fp16
+  // pair (A_j, B_j) for the PV mma (FP8: times 2^-8).
+  template <int J>
+  __device__ __forceinline__ static uint32_t v_pair(uint32_t a, uint32_t b) {
+    if constexpr (kFp8) {
+      // interleave (A_j, B_j) as the two bytes of a 16-bit pair, then convert
+      const uint32_t x = dev::prmt(a, b, (J < 2) ? 0x5140u : 0x7362u);
+      return dev::e4m3x2_to_f16x2(static_cast<uint16_t>((J & 1) ? (x >> 16) : x));
+    } else {
+      // interleave (A_j, B_j) as bytes, then the biased-byte conversion
+      const uint32_t x = dev::prmt(a ^ 0x80808080u, b ^ 0x80808080u,
+                                   (J < 2) ? 0x5140u : 0x7362u);
+      return dev::i8x2_to_f16x2<(J & 1) != 0>(x);
     }
   }
 
@@ -460,7 +492,8 @@ struct MmaInt8Path {
     }
     const float* ks = sc;
     const float* vs = sc + 16;
-    const float kg = ks[g8] * scale_log2, kg8 = ks[g8 + 8] * scale_log2;
+    const float kg = ks[g8] * (scale_log2 * kCodeUnscale);
+    const float kg8 = ks[g8 + 8] * (scale_log2 * kCodeUnscale);
     float s0 = sacc[0] * kg, s1 = sacc[1] * kg, s2 = sacc[2] * kg8, s3 = sacc[3] * kg8;
     const bool ok_lo = g8 < valid, ok_hi = g8 + 8 < valid;
     if (!ok_lo) s0 = s1 = -INFINITY;
@@ -530,20 +563,18 @@ struct MmaInt8Path {
     for (int mt = 0; mt < kMt; ++mt) ct[mt][0] = ct[mt][1] = ct[mt][2] = ct[mt][3] = 0.f;
 #pragma unroll
     for (int w = 0; w < kVw; ++w) {
-      const uint32_t A = va[w] ^ 0x80808080u, B = vb[w] ^ 0x80808080u;
-      const uint32_t C = vc[w] ^ 0x80808080u, E = vd[w] ^ 0x80808080u;
-      const uint32_t x = dev::prmt(A, B, 0x5140u), y = dev::prmt(A, B, 0x7362u);
-      const uint32_t xc = dev::prmt(C, E, 0x5140u), yc = dev::prmt(C, E, 0x7362u);
-      dev::mma16816<false>(ct[2 * w], dev::i8x2_to_f16x2<false>(x), dev::i8x2_to_f16x2<true>(x),
-                           dev::i8x2_to_f16x2<false>(xc), dev::i8x2_to_f16x2<true>(xc), b0, b1);
-      dev::mma16816<false>(ct[2 * w + 1], dev::i8x2_to_f16x2<false>(y),
-                           dev::i8x2_to_f16x2<true>(y), dev::i8x2_to_f16x2<false>(yc),
-                           dev::i8x2_to_f16x2<true>(yc), b0, b1);
+      // m-tile 2w takes bytes 0 (rows g8) and 1 (rows g8+8) of word w; m-tile
+      // 2w+1 takes bytes 2 and 3
+      dev::mma16816<false>(ct[2 * w], v_pair<0>(va[w], vb[w]), v_pair<1>(va[w], vb[w]),
+                           v_pair<0>(vc[w], vd[w]), v_pair<1>(vc[w], vd[w]), b0, b1);
+      dev::mma16816<false>(ct[2 * w + 1], v_pair<2>(va[w], vb[w]), v_pair<3>(va[w], vb[w]),
+                           v_pair<2>(vc[w], vd[w]), v_pair<3>(vc[w], vd[w]), b0, b1);
     }
+    const float vrestore = vmax * kVUnscale;
 #pragma unroll
     for (int mt = 0; mt < kMt; ++mt) {
 #pragma unroll
-      for (int i = 0; i < 4; ++i) st.o[mt][i] = fmaf(ct[mt][i], vmax, st.o[mt][i]);
+      for (int i = 0; i < 4; ++i) st.o[mt][i] = fmaf(ct[mt][i], vrestore, st.o[mt][i]);
     }
   }
 

@@ -6,6 +6,7 @@
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
+#include <cuda_fp8.h>
 #include <stdint.h>
 
 namespace kvp {
@@ -229,6 +230,18 @@ __device__ __forceinline__ uint32_t i8x2_to_bf16x2(uint32_t x) {
   const int lo = static_cast<int8_t>((x >> (kHigh ? 16 : 0)) & 0xff);
   const int hi = static_cast<int8_t>((x >> (kHigh ? 24 : 8)) & 0xff);
   return pack2<true>(static_cast<float>(lo), static_cast<float>(hi));
+}
+
+// Two E4M3 codes (low byte first) as an exact fp16x2 (low half first).
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint16_t x) {
+  const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(x), __NV_E4M3);
+  return static_cast<uint32_t>(h.x) | (static_cast<uint32_t>(h.y) << 16);
+}
+
+// Two floats (lo first) rounded to nearest-even E4M3 codes, saturating at 448.
+__device__ __forceinline__ uint16_t f32x2_to_e4m3x2(float lo, float hi) {
+  return static_cast<uint16_t>(
+      __nv_cvt_float2_to_fp8x2(make_float2(lo, hi), __NV_SATFINITE, __NV_E4M3));
 }
 
 __device__ __forceinline__ float warp_max(float v) {

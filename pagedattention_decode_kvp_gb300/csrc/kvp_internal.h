@@ -19,7 +19,7 @@ constexpr int kHeadsPerCta = 8;      // query heads one tensor-core CTA serves
 constexpr int kMaxPartBlocks = 1024;  // table slice staged per CTA (4 KB)
 
 // Decode kernel family.
-enum class DecodePath : int { kSimt = 0, kMma = 1, kMmaInt8 = 2 };
+enum class DecodePath : int { kSimt = 0, kMma = 1, kMmaInt8 = 2, kMmaFp8 = 3 };
 
 // Everything a decode launch needs besides the two tensor maps.
 struct DecodeParams {
@@ -55,6 +55,8 @@ cudaError_t launch_decode_mma(const DecodeParams& p, const CUtensorMap& tk,
                               const CUtensorMap& tv, bool kv_bf16, int grid_x, cudaStream_t s);
 cudaError_t launch_decode_mma_int8(const DecodeParams& p, const CUtensorMap& tk,
                                    const CUtensorMap& tv, int grid_x, cudaStream_t s);
+cudaError_t launch_decode_mma_fp8(const DecodeParams& p, const CUtensorMap& tk,
+                                  const CUtensorMap& tv, int grid_x, cudaStream_t s);
 cudaError_t launch_decode_reduce(const DecodeParams& p, cudaStream_t s);
 
 // Launch `kernel` on stream `s` with programmatic stream serialisation, so its
@@ -88,6 +90,15 @@ cudaError_t launch_append_int8(const void* key, const void* value, bool src_bf16
                                int8_t* k_cache, int8_t* v_cache, float* k_scale,
                                float* v_scale, const int32_t* slots, int num_tokens,
                                const kvp_cache_desc& c, int32_t* status, cudaStream_t s);
+cudaError_t launch_append_fp8(const void* key, const void* value, bool src_bf16,
+                              uint8_t* k_cache, uint8_t* v_cache, float* k_scale, float* v_scale,
+                              const int32_t* slots, int num_tokens, const kvp_cache_desc& c,
+                              int32_t* status, cudaStream_t s);
+cudaError_t launch_append_int8_fixed(const void* key, const void* value, bool src_bf16,
+                                     int8_t* k_cache, int8_t* v_cache, float* k_scale_pool,
+                                     float* v_scale_pool, float k_scale, float v_scale,
+                                     const int32_t* slots, int num_tokens,
+                                     const kvp_cache_desc& c, int32_t* status, cudaStream_t s);
 cudaError_t launch_copy_blocks(void* k_cache, void* v_cache, float* k_scale, float* v_scale,
                                int elem_bytes, const int32_t* pairs, int num_pairs,
                                const kvp_cache_desc& c, int32_t* status, cudaStream_t s);

@@ -32,6 +32,7 @@ def test_header_declares_the_boundary():
     names = _declared()
     for must in ("kvp_append", "kvp_append_int8", "kvp_copy_blocks", "kvp_attention_decode",
                  "kvp_attention_decode_int8", "kvp_decode_workspace_bytes", "kvp_read_status",
+                 "kvp_append_fp8", "kvp_attention_decode_fp8", "kvp_append_int8_fixed",
                  "kvp_bm_create", "kvp_bm_allocate", "kvp_bm_append_slot", "kvp_bm_free"):
         assert must in names
 
@@ -96,6 +97,10 @@ def test_invalid_arguments_fail_before_any_launch(lib):
     zero = (P, P, P, P, P, 16, P, 0, 8, 0.125, _desc(), 0, 0, P, 0, 3, P, P)
     assert lib.kvp_attention_decode(*zero) == kvp.KVP_OK
     assert lib.kvp_read_status(P, P) == kvp.KVP_ERR_INVALID_ARG
+    # the per-tensor INT8 scale must be finite and positive
+    assert lib.kvp_append_int8_fixed(P, P, 0, P, P, P, P, 0.0, 1.0, P, 1, _desc(), P, P) == \
+        kvp.KVP_ERR_INVALID_ARG
+    assert lib.kvp_append_fp8(P, P, 0, P, P, P, P, P, 1, _desc(), P, P) == kvp.KVP_ERR_INVALID_ARG
 
 
 def test_product_fails_loudly_without_library(monkeypatch, tmp_path):

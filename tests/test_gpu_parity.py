@@ -316,3 +316,91 @@ def test_empty_inputs_are_no_ops():
                                                                device="cuda"),
                              torch.zeros(0, dtype=torch.int32, device="cuda"), 0.1)
     torch.cuda.synchronize()
+
+
+# --------------------------------------------------------------- FP8 (E4M3) and per-tensor INT8
+@pytest.mark.parametrize("src_dtype", [torch.float16, torch.bfloat16])
+@pytest.mark.parametrize("D", [64, 128])
+def test_append_fp8_bit_exact(src_dtype, D):
+    g = torch.Generator().manual_seed(51)
+    NB, Hkv, T = 64, 4, 300
+    key = (torch.randn(T, Hkv, D, generator=g) * torch.rand(T, Hkv, 1, generator=g) * 4)
+    value = torch.randn(T, Hkv, D, generator=g) * 0.01
+    key[5] = 0.0
+    key, value = key.to(src_dtype), value.to(src_dtype)
+    slots = torch.randperm(NB * 16, generator=g)[:T].to(torch.int32)
+    slots[7] = -1
+    kc = torch.zeros(NB, Hkv, 16, D, dtype=torch.uint8)
+    vc = torch.zeros_like(kc)
+    ks = torch.full((NB, Hkv, 16), -7.0)
+    vs = torch.full((NB, Hkv, 16), -7.0)
+    gkc, gvc, gks, gvs = kc.cuda(), vc.cuda(), ks.cuda(), vs.cuda()
+    kvp.kvp_append_fp8(key.cuda(), value.cuda(), gkc, gvc, gks, gvs, slots.cuda())
+    torch.cuda.synchronize()
+    okc, oks = oracle.append_fp8(kc.view(torch.float8_e4m3fn), ks, key, slots)
+    ovc, ovs = oracle.append_fp8(vc.view(torch.float8_e4m3fn), vs, value, slots)
+    assert torch.equal(gkc.cpu(), okc.view(torch.uint8)) and same_bits(gks, oks)
+    assert torch.equal(gvc.cpu(), ovc.view(torch.uint8)) and same_bits(gvs, ovs)
+
+
+@pytest.mark.parametrize("src_dtype", [torch.float16, torch.bfloat16])
+def test_append_int8_fixed_scale_bit_exact(src_dtype):
+    g = torch.Generator().manual_seed(52)
+    NB, Hkv, D, T = 32, 2, 128, 200
+    key = (torch.randn(T, Hkv, D, generator=g) * 3).to(src_dtype)
+    key[0, 0, :4] = torch.tensor([1e4, -1e4, 6.0, -6.1])   # clip both ways
+    value = (torch.randn(T, Hkv, D, generator=g)).to(src_dtype)
+    slots = torch.randperm(NB * 16, generator=g)[:T].to(torch.int32)
+    kc = torch.zeros(NB, Hkv, 16, D, dtype=torch.int8)
+    vc = torch.zeros_like(kc)
+    ks = torch.zeros(NB, Hkv, 16)
+    vs = torch.zeros(NB, Hkv, 16)
+    gkc, gvc, gks, gvs = kc.cuda(), vc.cuda(), ks.cuda(), vs.cuda()
+    kvp.kvp_append_int8_fixed(key.cuda(), value.cuda(), gkc, gvc, gks, gvs, 0.05, 0.0125,
+                              slots.cuda())
+    torch.cuda.synchronize()
+    okc, oks = oracle.append_int8_fixed(kc, ks, key, slots, 0.05)
+    ovc, ovs = oracle.append_int8_fixed(vc, vs, value, slots, 0.0125)
+    assert same_bits(gkc, okc) and same_bits(gks, oks)
+    assert same_bits(gvc, ovc) and same_bits(gvs, ovs)
+    assert int(gkc.cpu().view(-1).max()) == 127 and int(gkc.cpu().view(-1).min()) == -128
+
+
+def fp8_workload(B, Hq, Hkv, D, lens, NB, q_dtype, seed, max_blocks=None):
+    w = workloads.make_custom(B=B, Hq=Hq, Hkv=Hkv, D=D, lens=lens, num_blocks=NB,
+                              dtype=q_dtype, kv_int8=True, seed=seed, max_blocks=max_blocks)
+    kc, ks = oracle.quantize_fp8(w.k_pool)
+    vc, vs = oracle.quantize_fp8(w.v_pool)
+    ks, vs = torch.from_numpy(ks), torch.from_numpy(vs)
+    used = torch.zeros(NB, 16, dtype=torch.bool)
+    for b, n in enumerate(lens):
+        for i in range(n):
+            used[int(w.block_tables[b, i // 16]), i % 16] = True
+    ks[~used[:, None, :].expand_as(ks)] = float("nan")
+    vs[~used[:, None, :].expand_as(vs)] = float("nan")
+    return w, torch.from_numpy(kc), torch.from_numpy(vc), ks, vs
+
+
+@pytest.mark.parametrize("q_dtype", [torch.float16, torch.bfloat16])
+@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("Hq,Hkv", [(8, 1), (16, 2), (4, 4), (6, 2)])
+@pytest.mark.parametrize("partition_blocks", [0, 8])
+def test_decode_fp8_parity(q_dtype, D, Hq, Hkv, partition_blocks):
+    lens = [1, 17, 300, 16, 640, 0]
+    w, kc, vc, ks, vs = fp8_workload(len(lens), Hq, Hkv, D, lens, 120, q_dtype,
+                                     seed=D + Hq + 5, max_blocks=40)
+    gkc, gvc, gks, gvs = kc.cuda(), vc.cuda(), ks.cuda(), vs.cuda()
+    kvp.kvp_append_fp8(w.new_k.cuda(), w.new_v.cuda(), gkc, gvc, gks, gvs, w.slot_mapping.cuda())
+    out = torch.full_like(w.q, float("nan"), device="cuda")
+    kvp.kvp_attention_decode_fp8(out, w.q.cuda(), gkc, gvc, gks, gvs, w.block_tables.cuda(),
+                                 w.context_lens.cuda(), w.scale,
+                                 workspace=workspace_for(w, partition_blocks),
+                                 partition_blocks=partition_blocks)
+    torch.cuda.synchronize()
+    okc, oks = oracle.append_fp8(kc.view(torch.float8_e4m3fn), ks, w.new_k, w.slot_mapping)
+    ovc, ovs = oracle.append_fp8(vc.view(torch.float8_e4m3fn), vs, w.new_v, w.slot_mapping)
+    assert torch.equal(gkc.cpu(), okc.view(torch.uint8))
+    assert torch.equal(gvc.cpu(), ovc.view(torch.uint8))
+    ref = oracle.attention_decode(w.q, okc, ovc, w.block_tables, w.context_lens, w.scale,
+                                  k_scale=oks, v_scale=ovs)
+    assert_attn_close(out, ref, f"fp8 {q_dtype} D{D} {Hq}/{Hkv} pb{partition_blocks}")

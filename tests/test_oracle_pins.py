@@ -336,3 +336,93 @@ def test_append_int8_matches_quantise_then_scatter():
     assert np.array_equal(c[0, :, 5], qc[0]) and np.array_equal(c[3, :, 15], qc[2])
     assert np.array_equal(s[0, :, 5], qs[0]) and np.array_equal(s[3, :, 15], qs[2])
     assert int(np.count_nonzero(s)) == 2 * Hkv
+
+
+# ------------------------------------------------------------ FP8 (E4M3) and per-tensor INT8
+def test_e4m3_widening_exhaustive():
+    codes = torch.arange(256, dtype=torch.int32).to(torch.uint8)
+    ref = codes.view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    got = np.array([oracle.e4m3_to_f64(int(c)) for c in codes.tolist()])
+    both_nan = np.isnan(ref) & np.isnan(got)
+    assert np.all(both_nan | (ref == got))
+
+
+def test_e4m3_rounding_matches_library_and_ties_go_even():
+    g = torch.Generator().manual_seed(40)
+    x = torch.cat([torch.randn(20000, generator=g) * 30,
+                   torch.rand(5000, generator=g) * 896 - 448,
+                   torch.randn(5000, generator=g) * 0.01])
+    ref = x.to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    got = np.array([oracle.f32_to_e4m3(float(v)) for v in x.tolist()], dtype=np.uint8)
+    assert np.array_equal(got, ref)
+    # exact midpoints between neighbouring codes round to the even code
+    vals = [oracle.e4m3_to_f64(c) for c in range(0x7f)]
+    for c in range(0x7e):
+        mid = (vals[c] + vals[c + 1]) / 2
+        want = c if c % 2 == 0 else c + 1
+        assert oracle.f32_to_e4m3(mid) == want
+        assert oracle.f32_to_e4m3(-mid) == 0x80 | want
+    assert oracle.f32_to_e4m3(1e6) == 0x7e and oracle.f32_to_e4m3(-500.0) == 0xfe  # saturate
+
+
+def test_fp8_quantiser_matches_library_restatement():
+    g = torch.Generator().manual_seed(41)
+    x = (torch.randn(300, 128, generator=g) * torch.rand(300, 1, generator=g) * 5).half()
+    x[3] = 0
+    codes, scales = oracle.quantize_fp8(x)
+    xf = x.float()
+    amax = xf.abs().amax(dim=-1, keepdim=True)
+    sc = amax / 448.0
+    sc = torch.where(sc > 0, sc, torch.ones_like(sc))
+    ref = (xf / sc).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert np.array_equal(codes, ref)
+    assert np.array_equal(scales.view(np.uint32), sc[:, 0].numpy().view(np.uint32))
+    assert codes[3].tolist() == [0] * 128 and scales[3] == 1.0
+
+
+def test_fixed_scale_int8_matches_numpy_restatement():
+    g = torch.Generator().manual_seed(42)
+    x = (torch.randn(64, 128, generator=g) * 3).half()
+    s = 0.0375
+    got = oracle.quantize_int8_fixed(x, s)
+    ref = np.clip(np.round(x.float().numpy() / np.float32(s)), -128, 127).astype(np.int8)
+    assert np.array_equal(got, ref)
+    big = torch.full((1, 8), 60000.0, dtype=torch.float16)
+    assert oracle.quantize_int8_fixed(big, 1.0).tolist() == [[127] * 8]   # clip
+
+
+def test_fp8_decode_equals_dense_on_dequantised_values():
+    g = torch.Generator().manual_seed(43)
+    lens = [21, 77]
+    q = torch.randn(2, 8, 64, generator=g).half()
+    src_k = torch.randn(2, 2, 77, 64, generator=g).half()
+    src_v = torch.randn(2, 2, 77, 64, generator=g).half()
+    ck, sk = oracle.quantize_fp8(src_k)
+    cv, sv = oracle.quantize_fp8(src_v)
+    Kc = torch.from_numpy(ck).view(torch.float8_e4m3fn)
+    Vc = torch.from_numpy(cv).view(torch.float8_e4m3fn)
+    kp, vp, tables = _paged_from_dense(Kc.view(torch.uint8), Vc.view(torch.uint8), lens, 16,
+                                       seed=4, fill=0)
+    ksp, vsp, _ = _paged_from_dense(torch.from_numpy(sk)[..., None],
+                                    torch.from_numpy(sv)[..., None], lens, 16, seed=4, fill=0)
+    got = oracle.attention_decode(q, kp.view(torch.float8_e4m3fn), vp.view(torch.float8_e4m3fn),
+                                  tables, lens, 0.125, k_scale=ksp[..., 0], v_scale=vsp[..., 0])
+    Kd = Kc.to(torch.float64) * torch.from_numpy(sk).double()[..., None]
+    Vd = Vc.to(torch.float64) * torch.from_numpy(sv).double()[..., None]
+    ref = _dense_reference(q, Kd, Vd, lens, 0.125).numpy()
+    np.testing.assert_allclose(got, ref, rtol=1e-12, atol=1e-13)
+
+
+def test_append_fp8_matches_quantise_then_scatter():
+    g = torch.Generator().manual_seed(44)
+    NB, Hkv, D = 4, 2, 64
+    codes = torch.zeros(NB, Hkv, BS, D, dtype=torch.uint8).view(torch.float8_e4m3fn)
+    scales = torch.zeros(NB, Hkv, BS)
+    src = torch.randn(3, Hkv, D, generator=g).half()
+    slots = torch.tensor([5, -1, 63], dtype=torch.int32)
+    c, s = oracle.append_fp8(codes, scales, src, slots)
+    assert c.dtype == torch.float8_e4m3fn
+    qc, qs = oracle.quantize_fp8(src)
+    assert np.array_equal(c.view(torch.uint8)[0, :, 5].numpy(), qc[0])
+    assert np.array_equal(c.view(torch.uint8)[3, :, 15].numpy(), qc[2])
+    assert np.array_equal(s[0, :, 5].numpy(), qs[0]) and np.array_equal(s[3, :, 15].numpy(), qs[2])

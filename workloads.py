@@ -25,6 +25,8 @@ Workloads (shapes follow the pages' examples; values are N(0, 1)):
   int8long  long-context INT8: B=4, context 131072, Hq=64, Hkv=8, D=128, fp16
             source pools to be quantised per token and head, 40000-block pool,
             fully scattered tables, 1 appended token/request.
+  fp8long   the same shapes with FP8 (E4M3) codes ("KV Cache 优化与显存管理", 二:
+            INT8 or FP8).
 
 Seeds: workload i (in the order above) uses base seed 1000 + i; each draw has
 its own generator seeded base * 100 + k with k = 0 q, 1 K pool, 2 V pool,
@@ -42,7 +44,7 @@ import numpy as np
 import torch
 
 BLOCK_SIZE = 16
-WORKLOAD_NAMES = ("tiny", "llama7b", "gqa70b", "prefix", "int8long")
+WORKLOAD_NAMES = ("tiny", "llama7b", "gqa70b", "prefix", "int8long", "fp8long")
 
 
 @dataclass
@@ -54,7 +56,7 @@ class Workload:
     D: int
     num_blocks: int
     dtype: torch.dtype          # q, new K/V and 16-bit pools
-    kv_int8: bool               # pools hold INT8 codes + float32 scales
+    kv_int8: bool               # pools hold 8-bit codes + float32 scales
     scale: float
     q: torch.Tensor             # [B, Hq, D]
     k_pool: torch.Tensor        # [NB, Hkv, bs, D] (int8 workloads: fp16 source values)
@@ -66,6 +68,7 @@ class Workload:
     slot_mapping: torch.Tensor  # [T] int32
     cow_pairs: Optional[torch.Tensor] = None  # [P, 2] int32 (src, dst)
     info: dict = field(default_factory=dict)
+    kv_fp8: bool = False        # the 8-bit codes are FP8 E4M3 (else INT8)
 
     @property
     def block_size(self) -> int:
@@ -222,6 +225,10 @@ def make(name: str, device="cpu", nan_sentinel=True, batch=None) -> Workload:
     idx = WORKLOAD_NAMES.index(name)
     seed = 1000 + idx
     base = seed * 100
+    if name == "fp8long":
+        w = make("int8long", device=device, nan_sentinel=nan_sentinel, batch=batch)
+        w.name, w.kv_fp8 = "fp8long", True
+        return w
     if batch is not None and name in ("llama7b", "gqa70b", "int8long"):
         return _make_scaled(name, int(batch), device, nan_sentinel, seed)
     if name == "tiny":
