@@ -328,7 +328,8 @@ def run_ours(args):
     barrier(world)
     kvp.load_library()
 
-    w = workloads.make(args.workload, device=dev, nan_sentinel=False, batch=args.batch)
+    w = workloads.make(args.workload, device=dev, nan_sentinel=False, batch=args.batch,
+                       contiguity=args.contiguity)
     step = Step(w, kvp, dev, args.partition_blocks)
     lens = [int(x) for x in w.context_lens]
     dbytes = decode_bytes(w, lens)
@@ -441,8 +442,8 @@ def run_ours(args):
     }
     if w.kv_int8:
         res["prefill_int8"] = step.prefill
-    if w.name == "gqa70b":
-        res["config"]["contiguous_share"] = round(w.info.get("contiguous_share", 0.0), 4)
+    if "contiguous_share" in w.info:
+        res["config"]["contiguous_share"] = round(w.info["contiguous_share"], 4)
 
     if world == 1 and not args.no_cpu_baseline:
         import oracle
@@ -535,6 +536,8 @@ def main():
                     help="fewer requests (pool scaled in proportion), for profiler captures")
     ap.add_argument("--partition-blocks", type=int, default=0,
                     help="split-context partition size in blocks (0 = the library's choice)")
+    ap.add_argument("--contiguity", type=float, default=None,
+                    help="redraw llama7b/gqa70b block tables as runs with this probability")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()

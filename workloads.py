@@ -218,10 +218,15 @@ def _assemble(name, B, Hq, Hkv, D, NB, dtype, kv_int8, scale, lens, tables, seed
                     info=dict(info or {}))
 
 
-def make(name: str, device="cpu", nan_sentinel=True, batch=None) -> Workload:
+def make(name: str, device="cpu", nan_sentinel=True, batch=None, contiguity=None) -> Workload:
     """Build one of the named workloads (see module docstring).  ``batch``
     shrinks llama7b / gqa70b / int8long to fewer requests with the pool scaled
-    in proportion (same per-request shapes), e.g. for profiler captures."""
+    in proportion (same per-request shapes), e.g. for profiler captures.
+    ``contiguity`` (llama7b, gqa70b) redraws the block tables so each block
+    follows its predecessor with that probability (0 = fully scattered, 1 = one
+    contiguous run per request)."""
+    if contiguity is not None and name in ("llama7b", "gqa70b"):
+        return _make_with_contiguity(name, float(contiguity), device, nan_sentinel, batch)
     idx = WORKLOAD_NAMES.index(name)
     seed = 1000 + idx
     base = seed * 100
@@ -270,6 +275,18 @@ def make(name: str, device="cpu", nan_sentinel=True, batch=None) -> Workload:
                          1.0 / math.sqrt(128), [n] * B, perm.contiguous(), seed, device,
                          nan_sentinel)
     raise KeyError(name)
+
+
+def _make_with_contiguity(name, p, device, nan_sentinel, batch) -> Workload:
+    w = make(name, device="cpu", nan_sentinel=False, batch=batch)
+    lens = [int(x) for x in w.context_lens]
+    seed = 1000 + WORKLOAD_NAMES.index(name)
+    lists = _draw_tables(np.random.default_rng(seed * 100 + 5), [-(-n // BLOCK_SIZE) for n in lens],
+                         w.num_blocks, p)
+    tables = _tables_from_lists(lists, w.max_blocks)
+    info = {"contiguous_share": contiguous_share(tables, lens), "contiguity_p": p}
+    return _assemble(name, w.B, w.Hq, w.Hkv, w.D, w.num_blocks, w.dtype, False, w.scale, lens,
+                     tables, seed, device, nan_sentinel, info)
 
 
 def _make_scaled(name, B, device, nan_sentinel, seed) -> Workload:
