@@ -174,8 +174,11 @@ class ClockSampler:
 class Step:
     """Device buffers of one workload and the step through the public API."""
 
-    def __init__(self, w, kvp, dev, partition_blocks=0):
+    def __init__(self, w, kvp, dev, partition_blocks=0, fused=False):
         self.w, self.kvp, self.dev = w, kvp, dev
+        # the fused step needs one new token per request at position n - 1
+        self.fused = fused and not w.kv_int8 and w.cow_pairs is None and \
+            int(w.slot_mapping.numel()) == w.B
         self.q = w.q.to(dev)
         self.tables = w.block_tables.to(dev)
         self.lens = w.context_lens.to(dev)
@@ -228,11 +231,25 @@ class Step:
         del ks, vs
 
     def launches_per_step(self) -> int:
-        return (1 if self.pairs is not None else 0) + 1 + 1 + (1 if self.split else 0)
+        append = 0 if self.fused else 1
+        return (1 if self.pairs is not None else 0) + append + 1 + (1 if self.split else 0)
 
     def run(self, ev=None):
         """One step; ev = (e_decode_start, e_partial_end) events to record."""
         kvp, w = self.kvp, self.w
+        if self.fused:
+            if ev is not None:
+                ev[0].record()
+            phases = [kvp.KVP_PHASE_PARTIAL, kvp.KVP_PHASE_REDUCE] if self.split else \
+                [kvp.KVP_PHASE_ALL]
+            for i, ph in enumerate(phases):
+                kvp.kvp_append_attention_decode(self.new_k, self.new_v, self.out, self.q, self.kp,
+                                                self.vp, self.tables, self.lens, w.scale,
+                                                workspace=self.ws, phases=ph, status=self.status,
+                                                partition_blocks=self.pb_arg)
+                if ev is not None and i == 0:
+                    ev[1].record()
+            return
         if self.pairs is not None:
             kvp.kvp_copy_blocks(self.kp, self.vp, self.pairs, status=self.status)
         if w.kv_int8:
@@ -330,7 +347,7 @@ def run_ours(args):
 
     w = workloads.make(args.workload, device=dev, nan_sentinel=False, batch=args.batch,
                        contiguity=args.contiguity)
-    step = Step(w, kvp, dev, args.partition_blocks)
+    step = Step(w, kvp, dev, args.partition_blocks, fused=not args.unfused)
     lens = [int(x) for x in w.context_lens]
     dbytes = decode_bytes(w, lens)
     sbytes = dbytes["call"] + append_bytes(w) + copy_bytes(w)
@@ -402,7 +419,9 @@ def run_ours(args):
         return
 
     peak, peak_src = measured_peak()
-    achieved = dbytes["partial_pass"] / (partial_ms / 1e3) / 1e9
+    # the fused partition pass also moves the appended rows (read source, write slot)
+    partial_bytes = dbytes["partial_pass"] + (append_bytes(w) if step.fused else 0)
+    achieved = partial_bytes / (partial_ms / 1e3) / 1e9
     traffic = profiled_traffic(args.workload)
     res = {
         "metric": METRIC,
@@ -424,6 +443,7 @@ def run_ours(args):
                    "new_tokens": int(w.slot_mapping.numel()),
                    "cow_pairs": int(w.cow_pairs.shape[0]) if w.cow_pairs is not None else 0,
                    "partition_blocks": step.part_blocks,
+                   "append": "fused into the decode" if step.fused else "separate kernel",
                    "l2": ("inputs larger than L2: {:.2f} GB of K/V per step vs 129 MB L2"
                           .format(dbytes["kv"] / 1e9)) if dbytes["kv"] > 4 * L2_BYTES else
                          "inputs partly L2-resident (L2 reuse is part of this workload)",
@@ -434,7 +454,7 @@ def run_ours(args):
         "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak,
                      "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": traffic,
                      "kernel": "decode_partial_kernel", "peak_source": peak_src,
-                     "algorithmic_bytes_per_launch": dbytes["partial_pass"],
+                     "algorithmic_bytes_per_launch": partial_bytes,
                      "launch_ms": round(partial_ms, 5)},
         "e2e": e2e,
         "gpu_launches": step.launches_per_step() * args.steps,
@@ -538,6 +558,9 @@ def main():
                     help="split-context partition size in blocks (0 = the library's choice)")
     ap.add_argument("--contiguity", type=float, default=None,
                     help="redraw llama7b/gqa70b block tables as runs with this probability")
+    ap.add_argument("--unfused", action="store_true",
+                    help="append with kvp_append, then decode (default: the fused entry point "
+                         "where every request appends one token at its last position)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()

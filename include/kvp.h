@@ -229,6 +229,28 @@ kvp_status kvp_attention_decode(void* out, const void* q, const void* k_cache,
                                 kvp_stream_t stream);
 
 /*
+ * kvp_append_attention_decode -- one decode step in one pass: append each
+ * request's new token, then decode (fp16/bf16 pools).
+ * Sources: as kvp_append and kvp_attention_decode.  key, value: [batch, Hkv, D]
+ * of `dtype`, the K/V of request b's new token, which is written at position
+ * context_lens[b] - 1 (slot = block_tables[b][(n-1)/16] * 16 + (n-1) % 16);
+ * requests with context_lens[b] == 0 append nothing.  The result equals
+ * kvp_append with those slots followed by kvp_attention_decode (KVP_PHASE_ALL),
+ * but the append is done by the decode CTAs that read the request's last block,
+ * saving a kernel launch and a pass over the new rows.  key/value 16-byte
+ * aligned.  The append happens in the KVP_PHASE_PARTIAL pass.  Other arguments
+ * and errors as kvp_attention_decode.
+ */
+kvp_status kvp_append_attention_decode(const void* key, const void* value, void* out,
+                                       const void* q, void* k_cache, void* v_cache,
+                                       const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                       const int32_t* context_lens, int32_t batch,
+                                       int32_t num_q_heads, float scale, kvp_cache_desc cache,
+                                       kvp_dtype dtype, int32_t partition_blocks,
+                                       void* workspace, size_t workspace_bytes, int32_t phases,
+                                       int32_t* dev_status, kvp_stream_t stream);
+
+/*
  * kvp_attention_decode_int8 -- as kvp_attention_decode over INT8 pools.
  * Source: "KV Cache 优化与显存管理", 三 (dequantize: code * scale), 二.
  * K_i = k_cache[...] * k_scale[blk, g, off] (V likewise); q and out are of

@@ -74,6 +74,8 @@ SIGNATURES = {
     "kvp_decode_workspace_bytes": (_SZ, [_I32, _I32, _D, _I32, _I32, _I32]),
     "kvp_attention_decode": (_I32, [_P, _P, _P, _P, _P, _I32, _P, _I32, _I32, _F, _D, _I32, _I32,
                                     _P, _SZ, _I32, _P, _P]),
+    "kvp_append_attention_decode": (_I32, [_P, _P, _P, _P, _P, _P, _P, _I32, _P, _I32, _I32, _F,
+                                           _D, _I32, _I32, _P, _SZ, _I32, _P, _P]),
     "kvp_attention_decode_int8": (_I32, [_P, _P, _I32, _P, _P, _P, _P, _P, _I32, _P, _I32, _I32,
                                          _F, _D, _I32, _P, _SZ, _I32, _P, _P]),
     "kvp_attention_decode_fp8": (_I32, [_P, _P, _I32, _P, _P, _P, _P, _P, _I32, _P, _I32, _I32,
@@ -268,6 +270,26 @@ def kvp_attention_decode(out, q, k_cache, v_cache, block_tables, context_lens, s
         int(block_tables.shape[1]), _ptr(context_lens), B, Hq, float(scale), cache_desc(k_cache),
         _dtype_code(q), int(partition_blocks), _ptr(workspace), ws_bytes, int(phases),
         _ptr(status), _stream_ptr(stream)), "kvp_attention_decode")
+
+
+def kvp_append_attention_decode(key, value, out, q, k_cache, v_cache, block_tables, context_lens,
+                                scale, *, workspace=None, partition_blocks=0,
+                                phases=KVP_PHASE_ALL, status=None, stream=None) -> None:
+    """One fused decode step over fp16/bf16 pools: request b's new token
+    key/value[b] ([B, Hkv, D]) is written at position context_lens[b] - 1, then
+    out = paged decode attention of q."""
+    lib = load_library()
+    _need_cuda(key, value, out, q, k_cache, v_cache, block_tables, context_lens, workspace,
+               status)
+    if q.dtype != k_cache.dtype or out.dtype != q.dtype or key.dtype != k_cache.dtype:
+        raise TypeError("key, value, q, out and the pools must share one dtype")
+    B, Hq, _ = (int(x) for x in q.shape)
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    _check(lib.kvp_append_attention_decode(
+        _ptr(key), _ptr(value), _ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache),
+        _ptr(block_tables), int(block_tables.shape[1]), _ptr(context_lens), B, Hq, float(scale),
+        cache_desc(k_cache), _dtype_code(q), int(partition_blocks), _ptr(workspace), ws_bytes,
+        int(phases), _ptr(status), _stream_ptr(stream)), "kvp_append_attention_decode")
 
 
 def kvp_attention_decode_int8(out, q, k_cache, v_cache, k_scale, v_scale, block_tables,

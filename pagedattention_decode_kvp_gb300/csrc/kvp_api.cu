@@ -152,7 +152,8 @@ kvp_status decode_common(void* out, const void* q, bool q_bf16, int kv_kind, con
                          const void* vc, const float* ks, const float* vs, const int32_t* tables,
                          int32_t max_blocks, const int32_t* lens, int32_t batch, int32_t hq,
                          float scale, kvp_cache_desc c, int32_t partition_blocks, void* ws,
-                         size_t ws_bytes, int32_t phases, int32_t* status, kvp_stream_t stream) {
+                         size_t ws_bytes, int32_t phases, int32_t* status, kvp_stream_t stream,
+                         const void* new_k = nullptr, const void* new_v = nullptr) {
   const bool int8 = kv_kind >= 2;  // 8-bit codes with scales: INT8 (2) or FP8 E4M3 (3)
   DecodeShape sh;
   const kvp_status st = shape_decode(batch, hq, c, max_blocks, partition_blocks, int8, &sh);
@@ -193,6 +194,10 @@ kvp_status decode_common(void* out, const void* q, bool q_bf16, int kv_kind, con
   p.max_parts = sh.max_parts;
   p.scale_log2 = scale * 1.4426950408889634f;
   p.q_bf16 = q_bf16 ? 1 : 0;
+  p.new_k = new_k;
+  p.new_v = new_v;
+  p.k_pool = kc;
+  p.v_pool = vc;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
 
   if (static_cast<long long>(c.num_kv_heads) * sh.qgroups > 65535 || batch > 65535)
@@ -370,6 +375,24 @@ kvp_status kvp_attention_decode(void* out, const void* q, const void* k_cache,
                        nullptr, nullptr, block_tables, max_blocks_per_seq, context_lens, batch,
                        num_q_heads, scale, cache, partition_blocks, workspace, workspace_bytes,
                        phases, dev_status, stream);
+}
+
+kvp_status kvp_append_attention_decode(const void* key, const void* value, void* out,
+                                       const void* q, void* k_cache, void* v_cache,
+                                       const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                       const int32_t* context_lens, int32_t batch,
+                                       int32_t num_q_heads, float scale, kvp_cache_desc cache,
+                                       kvp_dtype dtype, int32_t partition_blocks,
+                                       void* workspace, size_t workspace_bytes,
+                                       int32_t phases, int32_t* dev_status,
+                                       kvp_stream_t stream) {
+  if (dtype != KVP_F16 && dtype != KVP_BF16) return KVP_ERR_INVALID_ARG;
+  if (batch > 0 && (!key || !value || !aligned(key, 16) || !aligned(value, 16)))
+    return KVP_ERR_INVALID_ARG;
+  return decode_common(out, q, dtype == KVP_BF16, dtype == KVP_BF16 ? 1 : 0, k_cache, v_cache,
+                       nullptr, nullptr, block_tables, max_blocks_per_seq, context_lens, batch,
+                       num_q_heads, scale, cache, partition_blocks, workspace, workspace_bytes,
+                       phases, dev_status, stream, key, value);
 }
 
 kvp_status kvp_attention_decode_int8(void* out, const void* q, kvp_dtype q_dtype,

@@ -689,6 +689,31 @@ __global__ void __launch_bounds__(kWarps * 32)
   }
   const bool any_bad = __syncthreads_or(bad);
 
+  // ---- fused append: the new token of this request (position n-1) lies in
+  // the sequence's last block, which only last-partition CTAs read; they write
+  // its K/V row for this kv head into the slot, then make the write visible to
+  // the TMA (async proxy) before any copy is issued.  CTAs of other query
+  // groups of the same kv head write the same bytes.
+  if constexpr (Path::kElemBytes == 2) {
+    if (p.new_k != nullptr && last_part && !any_bad) {
+      constexpr int kChunks = D * 2 / 16;  // 16-byte chunks per row
+      const size_t srow =
+          (static_cast<size_t>(tbl[nb - 1]) * p.num_kv_heads + kvh) * kBlockSize +
+          (n - 1) % kBlockSize;
+      const size_t nrow = static_cast<size_t>(b) * p.num_kv_heads + kvh;
+      if (threadIdx.x < 2 * kChunks) {
+        const int c = threadIdx.x % kChunks;
+        const bool is_v = threadIdx.x >= kChunks;
+        const uint4* src = static_cast<const uint4*>(is_v ? p.new_v : p.new_k) + nrow * kChunks;
+        uint4* dst = reinterpret_cast<uint4*>(const_cast<void*>(is_v ? p.v_pool : p.k_pool)) +
+                     srow * kChunks;
+        dst[c] = src[c];
+        fence_proxy_async_global();
+      }
+      __syncthreads();
+    }
+  }
+
   const float* ksrc = p.k_scale;
   const float* vsrc = p.v_scale;
   auto issue = [&](int j) {  // lane 0 of this warp: fetch the warp's j-th block

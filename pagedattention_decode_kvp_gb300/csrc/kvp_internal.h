@@ -40,6 +40,10 @@ struct DecodeParams {
   int32_t max_parts;            // ceil(MB / part_blocks)
   float scale_log2;             // scale * log2(e)
   int32_t q_bf16;               // q / out are bf16 (else fp16)
+  const void* new_k;            // fused append: [B, Hkv, D] token at position n-1, or null
+  const void* new_v;
+  const void* k_pool;           // pool base pointers (the fused append writes through them)
+  const void* v_pool;
 };
 
 // Device error codes (mirror kvp_status).

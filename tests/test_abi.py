@@ -33,6 +33,7 @@ def test_header_declares_the_boundary():
     for must in ("kvp_append", "kvp_append_int8", "kvp_copy_blocks", "kvp_attention_decode",
                  "kvp_attention_decode_int8", "kvp_decode_workspace_bytes", "kvp_read_status",
                  "kvp_append_fp8", "kvp_attention_decode_fp8", "kvp_append_int8_fixed",
+                 "kvp_append_attention_decode",
                  "kvp_bm_create", "kvp_bm_allocate", "kvp_bm_append_slot", "kvp_bm_free"):
         assert must in names
 

@@ -404,3 +404,32 @@ def test_decode_fp8_parity(q_dtype, D, Hq, Hkv, partition_blocks):
     ref = oracle.attention_decode(w.q, okc, ovc, w.block_tables, w.context_lens, w.scale,
                                   k_scale=oks, v_scale=ovs)
     assert_attn_close(out, ref, f"fp8 {q_dtype} D{D} {Hq}/{Hkv} pb{partition_blocks}")
+
+
+# --------------------------------------------------------------- fused append + decode
+@pytest.mark.parametrize("dtype", [torch.float16, torch.bfloat16])
+@pytest.mark.parametrize("Hq,Hkv,D", [(8, 8, 128), (16, 2, 64), (24, 2, 128), (8, 1, 128)])
+@pytest.mark.parametrize("partition_blocks", [0, 8])
+def test_fused_append_decode_equals_separate_calls(dtype, Hq, Hkv, D, partition_blocks):
+    lens = [1, 16, 17, 300, 0, 530]
+    w = workloads.make_custom(B=len(lens), Hq=Hq, Hkv=Hkv, D=D, lens=lens, num_blocks=120,
+                              dtype=dtype, seed=Hq * 7 + D, max_blocks=40)
+    out_sep, kp_sep, vp_sep = gpu_decode_16(w, partition_blocks)
+    # one new row per request (rows of requests with no context are ignored)
+    key = torch.zeros(w.B, w.Hkv, w.D, dtype=dtype)
+    val = torch.zeros_like(key)
+    active = [b for b in range(w.B) if lens[b] > 0]
+    key[active] = w.new_k
+    val[active] = w.new_v
+    kp, vp = w.k_pool.cuda(), w.v_pool.cuda()
+    out = torch.full_like(w.q, float("nan"), device="cuda")
+    kvp.kvp_append_attention_decode(key.cuda(), val.cuda(), out, w.q.cuda(), kp, vp,
+                                    w.block_tables.cuda(), w.context_lens.cuda(), w.scale,
+                                    workspace=workspace_for(w, partition_blocks),
+                                    partition_blocks=partition_blocks)
+    torch.cuda.synchronize()
+    assert same_bits(kp, kp_sep) and same_bits(vp, vp_sep)
+    assert same_bits(out, out_sep)
+    okp, ovp = oracle_pools_16(w)
+    ref = oracle.attention_decode(w.q, okp, ovp, w.block_tables, w.context_lens, w.scale)
+    assert_attn_close(out, ref, f"fused {dtype} {Hq}/{Hkv} D{D} pb{partition_blocks}")
