@@ -78,6 +78,9 @@ def _load():
         lib.orc_copy_blocks.restype = I
         lib.orc_quantize_int8.argtypes = [P, I, ctypes.c_longlong, I, P, P]
         lib.orc_quantize_int8.restype = None
+        lib.orc_attention_prefill.argtypes = [P, P, I, P, I, P, P, I, P, I, P, P, I, I, I, I, I,
+                                              I, ctypes.c_double]
+        lib.orc_attention_prefill.restype = I
         lib.orc_quantize_int8_fixed.argtypes = [P, I, ctypes.c_longlong, ctypes.c_float, P]
         lib.orc_quantize_int8_fixed.restype = None
         lib.orc_quantize_fp8.argtypes = [P, I, ctypes.c_longlong, I, P, P]
@@ -211,6 +214,39 @@ def attention_decode(q, k_cache, v_cache, block_tables, context_lens, scale,
     if err != 0:
         raise ValueError(f"oracle attention_decode: bad block table or length ({err})")
     return out
+
+
+def attention_prefill(q, k_cache, v_cache, block_tables, context_lens, query_start, scale,
+                      *, rows=None):
+    """Causal multi-query paged attention in float64.  q [T, Hq, D] holds each
+    request's chunk of queries (rows query_start[b] .. query_start[b+1]-1), the
+    chunk being the last tokens of the request's context_lens[b]; query i of a
+    chunk of length L attends to positions 0 .. n - L + i.  Returns float64
+    [T, Hq, D] (or [len(rows), D] for the given (row, head) pairs)."""
+    lib = _load()
+    qa, qk = _raw(q)
+    ka, kk = _raw(k_cache)
+    va, _ = _raw(v_cache)
+    T, Hq, D = qa.shape
+    NB, Hkv, bs, _ = ka.shape
+    bt = _i32(block_tables)
+    cl = _i32(context_lens).reshape(-1)
+    qs = _i32(query_start).reshape(-1)
+    B = cl.shape[0]
+    if qs.shape[0] != B + 1 or bt.shape[0] != B:
+        raise ValueError("query_start must be [B+1], block_tables [B, MB]")
+    if rows is None:
+        ra = np.array([(t, h) for t in range(T) for h in range(Hq)], dtype=np.int32)
+        out = np.zeros((T * Hq, D), dtype=np.float64)
+    else:
+        ra = _i32(rows).reshape(-1, 2)
+        out = np.zeros((ra.shape[0], D), dtype=np.float64)
+    err = lib.orc_attention_prefill(_ptr(out), _ptr(ra), ra.shape[0], _ptr(qa), qk, _ptr(ka),
+                                    _ptr(va), kk, _ptr(bt), bt.shape[1], _ptr(cl), _ptr(qs), B, Hq,
+                                    Hkv, D, NB, bs, float(scale))
+    if err != 0:
+        raise ValueError(f"oracle attention_prefill: bad table or lengths ({err})")
+    return out.reshape(T, Hq, D) if rows is None else out
 
 
 def _like(result, template):

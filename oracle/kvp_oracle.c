@@ -351,3 +351,65 @@ void orc_quantize_fp8(const uint16_t* src, int src_kind, long long rows, int D, 
     scale_out[r] = sc;
   }
 }
+
+/* ---------------------------------------------------------------------------
+ * Multi-query paged attention (prefill / chunked prefill).  ([ATB-KV]
+ * "Prefix Caching": requests sharing a system prompt reuse its cached K/V;
+ * the new part of each request is computed against it.)  Request b holds
+ * n = context_lens[b] tokens, the last L = query_start[b+1] - query_start[b]
+ * of which are this chunk's queries (their K/V already appended).  Query i of
+ * the chunk (global row query_start[b] + i) sits at position n - L + i and
+ * attends causally to positions 0 .. n - L + i: the decode definition above
+ * with the context cut at that position.
+ * rows: [n_rows, 2] (global query row, query head) pairs to compute.
+ * Returns 0, -1 on a bad block id / length (L > n, n > max_blocks * bs).
+ * ------------------------------------------------------------------------- */
+int orc_attention_prefill(double* out, const int32_t* rows, int n_rows, const void* q, int q_kind,
+                          const void* k_cache, const void* v_cache, int cache_kind,
+                          const int32_t* block_tables, int max_blocks,
+                          const int32_t* context_lens, const int32_t* query_start, int B,
+                          int Hq, int Hkv, int D, int num_blocks, int bs, double scale) {
+  int group = Hq / Hkv;
+  int err = 0;
+#pragma omp parallel for schedule(dynamic, 1) reduction(min : err)
+  for (int r = 0; r < n_rows; ++r) {
+    int t = rows[2 * r], h = rows[2 * r + 1];
+    double* o = out + (size_t)r * D;
+    for (int d = 0; d < D; ++d) o[d] = 0.0;
+    int b = 0;
+    while (b < B && !(t >= query_start[b] && t < query_start[b + 1])) ++b;
+    if (b == B) { err = -1; continue; }
+    int L = query_start[b + 1] - query_start[b];
+    int n = context_lens[b];
+    if (L > n || n > max_blocks * bs) { err = -1; continue; }
+    int npos = n - L + (t - query_start[b]) + 1; /* keys 0 .. npos-1 */
+    int g = h / group;
+    double* qv = (double*)malloc(sizeof(double) * (size_t)D);
+    double* s = (double*)malloc(sizeof(double) * (size_t)npos);
+    if (!qv || !s) { free(qv); free(s); err = -2; continue; }
+    for (int d = 0; d < D; ++d) qv[d] = load_elem(q, ((size_t)t * Hq + h) * D + d, q_kind);
+    int bad = 0;
+    for (int i = 0; i < npos; ++i) {
+      int blk = block_tables[(size_t)b * max_blocks + i / bs];
+      if (blk < 0 || blk >= num_blocks) { bad = 1; break; }
+      size_t row = (((size_t)blk * Hkv + g) * bs + i % bs);
+      double acc = 0.0;
+      for (int d = 0; d < D; ++d) acc += qv[d] * load_elem(k_cache, row * D + d, cache_kind);
+      s[i] = scale * acc;
+    }
+    if (bad) { err = -1; free(qv); free(s); continue; }
+    double m = s[0];
+    for (int i = 1; i < npos; ++i) if (s[i] > m) m = s[i];
+    double sum = 0.0;
+    for (int i = 0; i < npos; ++i) { s[i] = exp(s[i] - m); sum += s[i]; }
+    for (int i = 0; i < npos; ++i) s[i] /= sum;
+    for (int i = 0; i < npos; ++i) {
+      int blk = block_tables[(size_t)b * max_blocks + i / bs];
+      size_t row = (((size_t)blk * Hkv + g) * bs + i % bs);
+      for (int d = 0; d < D; ++d) o[d] += s[i] * load_elem(v_cache, row * D + d, cache_kind);
+    }
+    free(qv);
+    free(s);
+  }
+  return err;
+}

@@ -426,3 +426,52 @@ def test_append_fp8_matches_quantise_then_scatter():
     assert np.array_equal(c.view(torch.uint8)[0, :, 5].numpy(), qc[0])
     assert np.array_equal(c.view(torch.uint8)[3, :, 15].numpy(), qc[2])
     assert np.array_equal(s[0, :, 5].numpy(), qs[0]) and np.array_equal(s[3, :, 15].numpy(), qs[2])
+
+
+# ------------------------------------------------------------ multi-query (prefill) attention
+def _causal_reference(q, K, V, starts, lens, scale):
+    """torch float64 scaled_dot_product_attention with an explicit causal mask
+    for queries that are the last L of n cached tokens."""
+    import torch.nn.functional as F
+    T, Hq, D = q.shape
+    Hkv = K.shape[1]
+    out = torch.zeros(T, Hq, D, dtype=torch.float64)
+    for b in range(len(lens)):
+        n, L = lens[b], starts[b + 1] - starts[b]
+        k = K[b, :, :n].double().repeat_interleave(Hq // Hkv, dim=0)   # [Hq, n, D]
+        v = V[b, :, :n].double().repeat_interleave(Hq // Hkv, dim=0)
+        qq = q[starts[b]:starts[b + 1]].double().transpose(0, 1)        # [Hq, L, D]
+        pos = torch.arange(n - L, n)
+        mask = torch.arange(n)[None, :] <= pos[:, None]                 # [L, n]
+        o = F.scaled_dot_product_attention(qq, k, v, attn_mask=mask, scale=scale)
+        out[starts[b]:starts[b + 1]] = o.transpose(0, 1)
+    return out
+
+
+@pytest.mark.parametrize("Hq,Hkv,D", [(4, 4, 64), (8, 2, 64), (8, 1, 128)])
+def test_prefill_equals_causal_sdpa(Hq, Hkv, D):
+    g = torch.Generator().manual_seed(60)
+    lens = [40, 100, 17]
+    qlens = [40, 7, 1]          # full prefill, a chunk, a single token
+    starts = [0]
+    for L in qlens:
+        starts.append(starts[-1] + L)
+    q = torch.randn(starts[-1], Hq, D, generator=g).half()
+    K = torch.randn(3, Hkv, 100, D, generator=g).half()
+    V = torch.randn(3, Hkv, 100, D, generator=g).half()
+    kp, vp, tables = _paged_from_dense(K, V, lens, 32, seed=5)
+    got = oracle.attention_prefill(q, kp, vp, tables, lens, starts, 1 / math.sqrt(D))
+    ref = _causal_reference(q, K, V, starts, lens, 1 / math.sqrt(D)).numpy()
+    np.testing.assert_allclose(got, ref, rtol=1e-12, atol=1e-13)
+
+
+def test_prefill_single_token_chunks_equal_decode():
+    g = torch.Generator().manual_seed(61)
+    lens = [33, 80]
+    q = torch.randn(2, 8, 64, generator=g).half()
+    K = torch.randn(2, 2, 80, 64, generator=g).half()
+    V = torch.randn(2, 2, 80, 64, generator=g).half()
+    kp, vp, tables = _paged_from_dense(K, V, lens, 16, seed=6)
+    pre = oracle.attention_prefill(q, kp, vp, tables, lens, [0, 1, 2], 0.2)
+    dec = oracle.attention_decode(q, kp, vp, tables, lens, 0.2)
+    np.testing.assert_allclose(pre, dec, rtol=1e-13, atol=1e-14)
