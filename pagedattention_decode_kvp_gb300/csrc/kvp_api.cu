@@ -427,6 +427,54 @@ kvp_status kvp_attention_decode_fp8(void* out, const void* q, kvp_dtype q_dtype,
                        stream);
 }
 
+kvp_status kvp_attention_prefill(void* out, const void* q, const void* k_cache,
+                                 const void* v_cache, const int32_t* block_tables,
+                                 int32_t max_blocks_per_seq, const int32_t* context_lens,
+                                 const int32_t* query_start, int32_t batch, int32_t num_q_heads,
+                                 int32_t max_query_len, float scale, kvp_cache_desc cache,
+                                 kvp_dtype dtype, int32_t* dev_status, kvp_stream_t stream) {
+  const kvp_status st = check_desc(cache);
+  if (st != KVP_OK) return st;
+  if (dtype != KVP_F16 && dtype != KVP_BF16) return KVP_ERR_INVALID_ARG;
+  if (batch < 0 || num_q_heads <= 0 || max_blocks_per_seq <= 0 || max_query_len < 0)
+    return KVP_ERR_INVALID_ARG;
+  if (num_q_heads % cache.num_kv_heads != 0) return KVP_ERR_INVALID_ARG;
+  if (!std::isfinite(scale)) return KVP_ERR_INVALID_ARG;
+  const int group = num_q_heads / cache.num_kv_heads;
+  if (128 % group != 0) return KVP_ERR_UNSUPPORTED;  // a 128-row tile holds whole groups
+  if (batch == 0 || max_query_len == 0) return KVP_OK;
+  if (!out || !q || !k_cache || !v_cache || !block_tables || !context_lens || !query_start)
+    return KVP_ERR_INVALID_ARG;
+  if (!aligned(out, 16) || !aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16))
+    return KVP_ERR_INVALID_ARG;
+  const long long tiles = (static_cast<long long>(max_query_len) * group + 127) / 128;
+  if (tiles > 0x7fffffffll || cache.num_kv_heads > 65535 || batch > 65535)
+    return KVP_ERR_UNSUPPORTED;
+
+  CUtensorMap tk, tv;
+  kvp_status r = make_pool_map(&tk, k_cache, cache, 2);
+  if (r != KVP_OK) return r;
+  r = make_pool_map(&tv, v_cache, cache, 2);
+  if (r != KVP_OK) return r;
+  PrefillParams p{};
+  p.out = out;
+  p.q = q;
+  p.block_tables = block_tables;
+  p.context_lens = context_lens;
+  p.query_start = query_start;
+  p.status = dev_status;
+  p.batch = batch;
+  p.num_q_heads = num_q_heads;
+  p.num_kv_heads = cache.num_kv_heads;
+  p.head_dim = cache.head_dim;
+  p.num_blocks = cache.num_blocks;
+  p.max_blocks = max_blocks_per_seq;
+  p.group = group;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  return from_cuda(launch_prefill(p, tk, tv, dtype == KVP_BF16, static_cast<int>(tiles),
+                                  reinterpret_cast<cudaStream_t>(stream)));
+}
+
 kvp_status kvp_read_status(const int32_t* dev_status, kvp_stream_t stream) {
   if (dev_status == nullptr) return KVP_ERR_INVALID_ARG;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);

@@ -33,10 +33,6 @@
 
 namespace kvp {
 
-__device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
-  return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
-}
-
 // ---------------------------------------------------------------------------
 // Shuffle reduction of N partial sums held by every lane across groups of L
 // lanes (N <= L, both powers of two): each step halves the number of values a

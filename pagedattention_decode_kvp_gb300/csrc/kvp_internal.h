@@ -46,6 +46,21 @@ struct DecodeParams {
   const void* v_pool;
 };
 
+// Everything a multi-query (prefill / chunked-prefill) launch needs besides the
+// two tensor maps.  Query rows of request b are q[query_start[b] ..
+// query_start[b+1]) and sit at the last positions of its context_lens[b].
+struct PrefillParams {
+  void* out;                     // [T, Hq, D] of the pool dtype
+  const void* q;                 // [T, Hq, D]
+  const int32_t* block_tables;   // [B, MB]
+  const int32_t* context_lens;   // [B]
+  const int32_t* query_start;    // [B + 1]
+  int32_t* status;               // nullable
+  int32_t batch, num_q_heads, num_kv_heads, head_dim, num_blocks, max_blocks;
+  int32_t group;                 // Hq / Hkv (divides 128)
+  float scale_log2;              // scale * log2(e)
+};
+
 // Device error codes (mirror kvp_status).
 constexpr int32_t kErrBadBlock = KVP_ERR_BAD_BLOCK;
 constexpr int32_t kErrTimeout = KVP_ERR_TIMEOUT;
@@ -62,6 +77,8 @@ cudaError_t launch_decode_mma_int8(const DecodeParams& p, const CUtensorMap& tk,
 cudaError_t launch_decode_mma_fp8(const DecodeParams& p, const CUtensorMap& tk,
                                   const CUtensorMap& tv, int grid_x, cudaStream_t s);
 cudaError_t launch_decode_reduce(const DecodeParams& p, cudaStream_t s);
+cudaError_t launch_prefill(const PrefillParams& p, const CUtensorMap& tk, const CUtensorMap& tv,
+                           bool bf16, int grid_x, cudaStream_t s);
 
 // Launch `kernel` on stream `s` with programmatic stream serialisation, so its
 // CTAs can be scheduled while the previous kernel drains (every kernel of this

@@ -1,0 +1,175 @@
+"""GPU parity of the causal multi-query (prefill / chunked-prefill) kernel,
+called through the C ABI, against the fp64 CPU oracle on the same seeded inputs.
+
+Bar: within 3e-3 absolute OR 1e-2 relative of the oracle, element by element
+(the same bar as the decode: fp16/bf16 inputs, fp32 accumulation, P rounded to
+the input type -- bf16 P carried as a high part plus a bf16 residual).
+Cases span several 128-row query tiles and 64-key chunks with ragged tails, a
+whole-prompt prefill, chunks that start mid-context, single-token chunks, empty
+chunks, NaN in every pool slot no request owns, and the data errors the header
+documents."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads
+import pagedattention_decode_kvp_gb300 as kvp
+
+pytestmark = pytest.mark.gpu
+
+ATOL, RTOL = 3e-3, 1e-2
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    from pagedattention_decode_kvp_gb300 import _build
+    _build.build()
+    kvp.load_library()
+
+
+def assert_close(gpu_out, ref, what=""):
+    g = gpu_out.detach().double().cpu().numpy().reshape(ref.shape)
+    assert np.isfinite(g).all(), f"{what}: non-finite output"
+    err = np.abs(g - ref)
+    ok = (err <= ATOL) | (err <= RTOL * np.abs(ref))
+    if not ok.all():
+        i = np.unravel_index(np.argmax(np.where(ok, 0, err)), err.shape)
+        raise AssertionError(f"{what}: {int((~ok).sum())} elements out of tolerance; worst at "
+                             f"{i}: gpu {g[i]} ref {ref[i]} (max abs err {err.max():.3e})")
+
+
+def run_gpu(w, status=None, max_query_len=None, out=None, q=None):
+    if out is None:
+        out = torch.full((w.T, w.Hq, w.D), float("nan"), dtype=w.dtype, device="cuda")
+    kvp.kvp_attention_prefill(out, (w.q if q is None else q).cuda(), w.k_pool.cuda(),
+                              w.v_pool.cuda(),
+                              w.block_tables.cuda(), w.context_lens.cuda(),
+                              w.query_start.cuda(),
+                              w.max_query_len if max_query_len is None else max_query_len,
+                              w.scale, status=status)
+    torch.cuda.synchronize()
+    return out
+
+
+# (context length, chunk length) per request: a whole prompt spanning several
+# tiles, chunks starting mid-context and crossing tile / chunk boundaries, one
+# token, an empty chunk, exact multiples of 64 and 128.
+CASES = [(300, 300), (1030, 200), (17, 1), (50, 0), (64, 64), (129, 129), (200, 37),
+         (16, 16), (1, 1), (520, 130)]
+SHAPES = [(4, 4, 128), (8, 2, 64), (16, 2, 128), (8, 1, 128), (32, 4, 64)]
+
+
+@pytest.mark.parametrize("dtype", [torch.float16, torch.bfloat16])
+@pytest.mark.parametrize("Hq,Hkv,D", SHAPES)
+def test_prefill_parity(dtype, Hq, Hkv, D):
+    lens = [c[0] for c in CASES]
+    qlens = [c[1] for c in CASES]
+    w = workloads.make_prefill(B=len(CASES), Hq=Hq, Hkv=Hkv, D=D, lens=lens, qlens=qlens,
+                               num_blocks=200, dtype=dtype, seed=Hq * 13 + D + Hkv)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out = run_gpu(w, status)
+    assert kvp.kvp_read_status(status) == kvp.KVP_OK
+    ref = oracle.attention_prefill(w.q, w.k_pool, w.v_pool, w.block_tables, w.context_lens,
+                                   w.query_start, w.scale)
+    assert_close(out, ref, f"prefill {dtype} {Hq}/{Hkv} D{D}")
+
+
+def test_prefill_scattered_and_contiguous_tables():
+    for p in (0.0, 1.0):
+        w = workloads.make_prefill(B=4, Hq=8, Hkv=2, D=128, lens=[700, 333, 129, 64],
+                                   qlens=[700, 100, 129, 3], num_blocks=120,
+                                   dtype=torch.bfloat16, seed=5, contiguous_p=p)
+        out = run_gpu(w)
+        ref = oracle.attention_prefill(w.q, w.k_pool, w.v_pool, w.block_tables,
+                                       w.context_lens, w.query_start, w.scale)
+        assert_close(out, ref, f"contiguity {p}")
+
+
+def test_one_token_chunks_match_the_decode_definition():
+    """A chunk of one query per request is a decode step: compare with the
+    oracle's decode on the same pools."""
+    lens = [1, 16, 17, 300, 1000]
+    w = workloads.make_prefill(B=5, Hq=16, Hkv=2, D=128, lens=lens, qlens=[1] * 5,
+                               num_blocks=120, dtype=torch.float16, seed=9)
+    out = run_gpu(w)
+    ref = oracle.attention_decode(w.q, w.k_pool, w.v_pool, w.block_tables, w.context_lens,
+                                  w.scale)
+    assert_close(out, ref, "one-token chunks")
+
+
+def test_long_prompt_sampled_rows():
+    """A 4096-token prompt (32 query tiles for G = 1; 64 key chunks for the last
+    tile), checked on sampled rows the oracle computes one by one."""
+    w = workloads.make_prefill(B=2, Hq=8, Hkv=8, D=128, lens=[4096, 2500], qlens=[4096, 900],
+                               num_blocks=450, dtype=torch.bfloat16, seed=21)
+    out = run_gpu(w)
+    rng = np.random.default_rng(3)
+    t = rng.integers(0, w.T, size=96)
+    t[:4] = [0, 4095, 4096, w.T - 1]
+    h = rng.integers(0, w.Hq, size=96)
+    rows = np.stack([t, h], axis=1).astype(np.int32)
+    ref = oracle.attention_prefill(w.q, w.k_pool, w.v_pool, w.block_tables, w.context_lens,
+                                   w.query_start, w.scale, rows=rows)
+    got = out.cpu()[torch.from_numpy(t).long(), torch.from_numpy(h).long()]
+    assert_close(got, ref, "long prompt sampled")
+
+
+def test_prefill_is_deterministic():
+    w = workloads.make_prefill(B=3, Hq=8, Hkv=2, D=64, lens=[400, 90, 33], qlens=[400, 90, 5],
+                               num_blocks=60, dtype=torch.float16, seed=2)
+    a = run_gpu(w)
+    b = run_gpu(w)
+    assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+
+
+def test_chunk_longer_than_context_sets_status_and_zeroes_rows():
+    w = workloads.make_prefill(B=2, Hq=8, Hkv=2, D=64, lens=[40, 100], qlens=[40, 60],
+                               num_blocks=20, dtype=torch.float16, seed=4)
+    w.context_lens = torch.tensor([40, 50], dtype=torch.int32)  # request 1: L = 60 > n = 50
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out = run_gpu(w, status)
+    assert kvp.kvp_read_status(status) == kvp.KVP_ERR_BAD_BLOCK
+    assert torch.count_nonzero(out[40:].float()) == 0
+    ref = oracle.attention_prefill(w.q[:40], w.k_pool, w.v_pool, w.block_tables[:1],
+                                   w.context_lens[:1], w.query_start[:2], w.scale)
+    assert_close(out[:40], ref, "healthy request beside a bad one")
+
+
+def test_bad_block_id_sets_status_and_zeroes_rows():
+    w = workloads.make_prefill(B=2, Hq=4, Hkv=4, D=128, lens=[70, 90], qlens=[70, 20],
+                               num_blocks=20, dtype=torch.bfloat16, seed=6)
+    w.block_tables[1, 2] = 20  # == num_blocks: out of range
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out = run_gpu(w, status)
+    assert kvp.kvp_read_status(status) == kvp.KVP_ERR_BAD_BLOCK
+    assert torch.count_nonzero(out[70:].float()) == 0
+    assert torch.isfinite(out[:70].float()).all()
+
+
+def test_max_query_len_too_small_sets_status():
+    w = workloads.make_prefill(B=1, Hq=8, Hkv=1, D=128, lens=[300], qlens=[300],
+                               num_blocks=20, dtype=torch.float16, seed=8)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    run_gpu(w, status, max_query_len=100)  # grid covers 112 tokens of 300
+    assert kvp.kvp_read_status(status) == kvp.KVP_ERR_BAD_BLOCK
+
+
+def test_empty_prefill_calls_are_no_ops():
+    w = workloads.make_prefill(B=2, Hq=8, Hkv=2, D=64, lens=[30, 20], qlens=[0, 0],
+                               num_blocks=8, dtype=torch.float16, seed=1)
+    out = torch.full((1, 8, 64), 7.0, dtype=torch.float16, device="cuda")
+    q = torch.zeros((1, 8, 64), dtype=torch.float16)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    run_gpu(w, status, out=out, q=q)  # max_query_len 0: nothing launched
+    run_gpu(w, status, max_query_len=16, out=out, q=q)  # launched, every chunk empty
+    assert kvp.kvp_read_status(status) == kvp.KVP_OK
+    assert bool((out == 7.0).all())  # nothing written
+
+
+def test_prefill_rejects_unsupported_groups():
+    w = workloads.make_prefill(B=1, Hq=12, Hkv=4, D=64, lens=[20], qlens=[20],
+                               num_blocks=4, dtype=torch.float16, seed=1)  # G = 3
+    with pytest.raises(kvp.KvpError) as e:
+        run_gpu(w)
+    assert e.value.status == kvp.KVP_ERR_UNSUPPORTED

@@ -362,3 +362,70 @@ def _make_prefix(seed, device, nan_sentinel) -> Workload:
                     info={"prefix_tokens": prefix, "shared_blocks": shared,
                           "suffix_tokens": T})
 
+
+
+# ------------------------------------------------------------------ multi-query
+@dataclass
+class PrefillWorkload:
+    """Inputs of one causal multi-query (prefill / chunked-prefill) call: the
+    pools already hold every request's context_lens[b] tokens, the last
+    qlens[b] of which are this call's query rows."""
+    name: str
+    B: int
+    Hq: int
+    Hkv: int
+    D: int
+    num_blocks: int
+    dtype: torch.dtype
+    scale: float
+    q: torch.Tensor             # [T, Hq, D], T = sum(qlens)
+    k_pool: torch.Tensor        # [NB, Hkv, bs, D]
+    v_pool: torch.Tensor
+    block_tables: torch.Tensor  # [B, MB] int32, -1 past each request's blocks
+    context_lens: torch.Tensor  # [B] int32
+    query_start: torch.Tensor   # [B + 1] int32
+    max_query_len: int
+    info: dict = field(default_factory=dict)
+
+    @property
+    def max_blocks(self) -> int:
+        return int(self.block_tables.shape[1])
+
+    @property
+    def T(self) -> int:
+        return int(self.q.shape[0])
+
+
+def make_prefill(*, B, Hq, Hkv, D, lens, qlens, num_blocks, dtype=torch.float16, seed=11,
+                 contiguous_p=0.0, max_blocks=None, device="cpu", name="prefill_custom",
+                 nan_sentinel=True) -> PrefillWorkload:
+    """Request b: lens[b] cached tokens, its last qlens[b] are queries
+    (qlens[b] <= lens[b]).  Seeds base = seed * 100: k = 0 q, 1 K pool, 2 V
+    pool, 5 tables.  Slots past every request's tokens hold NaN (16-bit)."""
+    lens = [int(x) for x in lens]
+    qlens = [int(x) for x in qlens]
+    if len(lens) != B or len(qlens) != B:
+        raise ValueError("lens and qlens need one entry per request")
+    nblk = [-(-n // BLOCK_SIZE) for n in lens]
+    mb = max_blocks if max_blocks is not None else max(1, max(nblk) if nblk else 1)
+    if sum(nblk) > num_blocks:
+        raise ValueError("pool too small for the requested lengths")
+    base = seed * 100
+    lists = _draw_tables(np.random.default_rng(base + 5), nblk, num_blocks, contiguous_p)
+    tables = _tables_from_lists(lists, mb)
+    T = sum(qlens)
+    q = _randn((max(T, 1), Hq, D), dtype, base + 0, device)[:T]
+    k_pool = _randn((num_blocks, Hkv, BLOCK_SIZE, D), dtype, base + 1, device)
+    v_pool = _randn((num_blocks, Hkv, BLOCK_SIZE, D), dtype, base + 2, device)
+    if nan_sentinel:
+        _nan_unfilled(k_pool, tables, lens)
+        _nan_unfilled(v_pool, tables, lens)
+    qs = [0]
+    for L in qlens:
+        qs.append(qs[-1] + L)
+    return PrefillWorkload(name=name, B=B, Hq=Hq, Hkv=Hkv, D=D, num_blocks=num_blocks,
+                           dtype=dtype, scale=1.0 / math.sqrt(D), q=q, k_pool=k_pool,
+                           v_pool=v_pool, block_tables=tables.to(device),
+                           context_lens=torch.tensor(lens, dtype=torch.int32).to(device),
+                           query_start=torch.tensor(qs, dtype=torch.int32).to(device),
+                           max_query_len=max(qlens) if qlens else 0)
