@@ -38,9 +38,12 @@ import torch  # noqa: E402
 import workloads  # noqa: E402
 
 METRIC = ("paged-attention decode achieved HBM GB/s (% of peak) and attended KV tokens/s")
+PREFILL_METRIC = ("paged-attention prefill of prefix-cached prompts: achieved tensor TFLOP/s "
+                  "(causal attention FLOPs) and query tokens/s")
 L2_BYTES = 129 * 1024 * 1024
 KERNEL_SOURCES = ["kvp_decode.cuh", "kvp_device.cuh", "kvp_decode_simt.cu", "kvp_decode_mma.cu",
                   "kvp_decode_int8.cu", "kvp_internal.h"]
+PREFILL_SOURCES = ["kvp_prefill.cu", "kvp_umma.cuh", "kvp_device.cuh", "kvp_internal.h"]
 
 
 # ------------------------------------------------------------------ byte model
@@ -90,18 +93,30 @@ def measured_peak():
         return 6800.0, "fallback (6.8 TB/s)"
 
 
-def kernel_source_hash() -> str:
+def measured_tensor_peak():
+    """Dense 16-bit tensor peak in TFLOP/s (fp16 and bf16 run at one rate): the
+    burst figure, for a kernel timed in steps of a few milliseconds."""
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["bf16_tflops"]), "measured (MEASURED_PEAKS.json bf16_tflops, burst)"
+    except Exception:
+        return 1900.0, "fallback (1.9 PFLOP/s bf16 burst)"
+
+
+def kernel_source_hash(sources=None) -> str:
     h = hashlib.sha256()
-    for f in KERNEL_SOURCES:
+    for f in (sources or KERNEL_SOURCES):
         with open(os.path.join(ROOT, "pagedattention_decode_kvp_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
 
 
-def profiled_traffic(workload: str):
-    """Per-launch DRAM bytes of the decode partition kernel from a committed ncu
-    summary, valid only while the kernel sources are unchanged."""
-    want = kernel_source_hash()
+def profiled_traffic(workload: str, sources=None):
+    """Per-launch DRAM bytes of the workload's dominant kernel from a committed
+    ncu summary, valid only while the kernel sources are unchanged."""
+    want = kernel_source_hash(sources)
     pdir = os.path.join(ROOT, "profiles")
     if not os.path.isdir(pdir):
         return None
@@ -487,6 +502,256 @@ def run_ours(args):
         dist.destroy_process_group()
 
 
+# ------------------------------------------------------------------ prefill workloads
+def prefill_work(w):
+    """(FLOPs, attended (query row, key) pairs per head) of one causal
+    multi-query call: row i of a chunk of L rows at context n attends to
+    n - L + i + 1 keys; q.K and p.V cost 2 * D FLOPs per key each."""
+    lens = [int(x) for x in w.context_lens.cpu()]
+    qs = [int(x) for x in w.query_start.cpu()]
+    pairs = 0
+    for b, n in enumerate(lens):
+        L = qs[b + 1] - qs[b]
+        pairs += L * (n - L) + L * (L + 1) // 2
+    return 4 * w.D * w.Hq * pairs, pairs
+
+
+class PrefillStep:
+    """One prompt pass through the public API: append the chunk's K/V into its
+    slots (kvp_append), then causal multi-query attention
+    (kvp_attention_prefill)."""
+
+    def __init__(self, w, kvp, dev):
+        self.w, self.kvp = w, kvp
+        self.q = w.q.to(dev)
+        self.kp, self.vp = w.k_pool.to(dev), w.v_pool.to(dev)
+        self.tables = w.block_tables.to(dev)
+        self.lens = w.context_lens.to(dev)
+        self.qs = w.query_start.to(dev)
+        lens = [int(x) for x in w.context_lens.cpu()]
+        qs = [int(x) for x in w.query_start.cpu()]
+        tab = w.block_tables.cpu()
+        slots = [int(tab[b, p // 16]) * 16 + p % 16 for b, n in enumerate(lens)
+                 for p in range(n - (qs[b + 1] - qs[b]), n)]
+        self.slots = torch.tensor(slots, dtype=torch.int32, device=dev)
+        blk, off = (self.slots // 16).long(), (self.slots % 16).long()
+        # the chunk's K/V rows are the ones the pool already holds at those slots,
+        # so every step's append rewrites them unchanged
+        self.new_k = self.kp[blk, :, off, :].contiguous()
+        self.new_v = self.vp[blk, :, off, :].contiguous()
+        self.out = torch.empty_like(self.q)
+        self.status = torch.zeros(1, dtype=torch.int32, device=dev)
+
+    def append_bytes(self) -> int:
+        T = int(self.slots.numel())
+        return 2 * 2 * T * self.w.Hkv * self.w.D * 2 + 4 * T
+
+    def run(self, ev=None):
+        kvp, w = self.kvp, self.w
+        kvp.kvp_append(self.new_k, self.new_v, self.kp, self.vp, self.slots, status=self.status)
+        if ev is not None:
+            ev[0].record()
+        kvp.kvp_attention_prefill(self.out, self.q, self.kp, self.vp, self.tables, self.lens,
+                                  self.qs, w.max_query_len, w.scale, status=self.status)
+        if ev is not None:
+            ev[1].record()
+
+
+def prefill_sample_rows(w, n):
+    total = w.T * w.Hq
+    n = min(n, total)
+    stride = total / n
+    return [(int(i * stride) // w.Hq, int(i * stride) % w.Hq) for i in range(n)]
+
+
+def cpu_oracle_prefill(w, host_k, host_v, rows):
+    """Time the CPU oracle (as it stands) on sampled (query row, head) pairs of
+    one prefill call; FLOPs counted as the GPU's (4 * D per attended key)."""
+    import oracle
+    import numpy as np
+    lens = [int(x) for x in w.context_lens.cpu()]
+    qs = [int(x) for x in w.query_start.cpu()]
+    starts = np.array(qs[:-1])
+    keys = 0
+    for t, _ in rows:
+        b = int(np.searchsorted(starts, t, side="right")) - 1
+        while qs[b + 1] == qs[b]:
+            b += 1
+        keys += lens[b] - (qs[b + 1] - qs[b]) + (t - qs[b]) + 1
+    t0 = time.perf_counter()
+    oracle.attention_prefill(w.q, host_k, host_v, w.block_tables, w.context_lens,
+                             w.query_start, w.scale, rows=np.array(rows, dtype=np.int32))
+    dt = time.perf_counter() - t0
+    return {"seconds": dt, "flops": 4.0 * w.D * keys, "rows": len(rows), "keys": keys,
+            "cores": oracle.num_threads()}
+
+
+def run_prefill(args):
+    import pagedattention_decode_kvp_gb300 as kvp
+    from pagedattention_decode_kvp_gb300 import _build
+
+    world, rank, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    if rank == 0 or world == 1:
+        _build.build()
+    barrier(world)
+    kvp.load_library()
+
+    w = workloads.make_prefill_named(args.workload, device=dev, nan_sentinel=False,
+                                     batch=args.batch)
+    step = PrefillStep(w, kvp, dev)
+    flops, pairs = prefill_work(w)
+    stream = torch.cuda.current_stream()
+    for _ in range(args.warmup):
+        step.run()
+    torch.cuda.synchronize()
+    st = kvp.kvp_read_status(step.status)
+    if st != kvp.KVP_OK:
+        raise RuntimeError(f"device status after warm-up: {kvp.kvp_status_string(st)}")
+
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.steps)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        start.record(stream)
+        for i in range(args.steps):
+            step.run(evs[i])
+        end.record(stream)
+        torch.cuda.synchronize()
+    barrier(world)
+    elapsed_ms = max_over_ranks(start.elapsed_time(end), world, dev)
+    kernel_ms = statistics.mean(e0.elapsed_time(e1) for e0, e1 in evs)
+    ms_per_step = elapsed_ms / args.steps
+    total_flops = sum_over_ranks(flops * args.steps, world, dev)
+    value = total_flops / (elapsed_ms / 1e3) / 1e12
+    q_tokens_per_s = sum_over_ranks(w.T * args.steps, world, dev) / (elapsed_ms / 1e3)
+
+    e2e = None
+    if not args.no_e2e:
+        host = {k: getattr(step, k).cpu().pin_memory() for k in
+                ("q", "tables", "lens", "qs", "slots", "new_k", "new_v")}
+        out_host = torch.empty(step.out.shape, dtype=step.out.dtype).pin_memory()
+        h2d = sum(t.numel() * t.element_size() for t in host.values())
+        d2h = out_host.numel() * out_host.element_size()
+
+        def e2e_step():
+            for k, t in host.items():
+                getattr(step, k).copy_(t, non_blocking=True)
+            step.run()
+            out_host.copy_(step.out, non_blocking=True)
+            torch.cuda.current_stream().synchronize()
+
+        for _ in range(args.warmup):
+            e2e_step()
+        barrier(world)
+        t0 = time.perf_counter()
+        for _ in range(args.steps):
+            e2e_step()
+        e2e_s = max_over_ranks(time.perf_counter() - t0, world, dev)
+        barrier(world)
+        e2e = {"value": round(total_flops / e2e_s / 1e12, 3), "unit": "TFLOP/s",
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+               "ms_per_step": round(e2e_s * 1e3 / args.steps, 4)}
+
+    if rank != 0:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+        return
+
+    peak, peak_src = measured_tensor_peak()
+    achieved = flops / (kernel_ms / 1e3) / 1e12
+    res = {
+        "metric": PREFILL_METRIC,
+        "value": round(value, 3),
+        "unit": "TFLOP/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_per_step, 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f16",
+        "data": "synthetic (seeded N(0,1), shapes of the pages' prefix-sharing workload)",
+        "config": {"workload": w.name + (f" (batch {w.B})" if args.batch else ""), "batch": w.B,
+                   "q_heads": w.Hq, "kv_heads": w.Hkv, "head_dim": w.D, "block_size": 16,
+                   "num_blocks": w.num_blocks, "query_tokens": w.T,
+                   "prefix_tokens": w.info.get("prefix_tokens"),
+                   "context_tokens": int(w.context_lens.sum()),
+                   "attended_pairs_per_head": pairs,
+                   "l2": "K/V of the shared prefix is L2-resident across requests (prefix "
+                         "reuse is part of this workload); the chunk's append writes "
+                         "{:.2f} GB per step".format(step.append_bytes() / 1e9),
+                   "parallelism": "replicas" if world > 1 else "single GPU"},
+        "query_tokens_per_s": round(q_tokens_per_s, 1),
+        "roofline": {"bound": "tensor", "achieved": round(achieved, 3), "peak": peak,
+                     "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
+                     "traffic": profiled_traffic(args.workload, PREFILL_SOURCES),
+                     "kernel": "prefill_kernel", "peak_source": peak_src,
+                     "algorithmic_flops_per_launch": flops,
+                     "launch_ms": round(kernel_ms, 5)},
+        "e2e": e2e,
+        "gpu_launches": 2 * args.steps,
+        "clocks": clk.summary(),
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        import oracle
+        oracle.build()
+        wh = workloads.PrefillWorkload(**{k: (v.cpu() if isinstance(v, torch.Tensor) else v)
+                                          for k, v in w.__dict__.items()})
+        cb = cpu_oracle_prefill(wh, step.kp.cpu(), step.vp.cpu(),
+                                prefill_sample_rows(wh, args.cpu_rows))
+        res["cpu_baseline"] = {"value": round(cb["flops"] / cb["seconds"] / 1e12, 6),
+                               "unit": "TFLOP/s", "cores": cb["cores"], "kind": "oracle",
+                               "sample": f"{cb['rows']} of {w.T * w.Hq} (query row, head) "
+                                         f"pairs of one prefill call, {cb['seconds']:.2f} s"}
+    print(json.dumps(res))
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def run_reference_prefill(args):
+    """The CPU oracle as the reference arm of a prefill workload (rank 0 only)."""
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return
+    import oracle
+    oracle.build()
+    w = workloads.make_prefill_named(args.workload, device="cpu", nan_sentinel=False,
+                                     batch=args.batch)
+    rows = prefill_sample_rows(w, args.cpu_rows)
+    for _ in range(args.warmup):
+        cpu_oracle_prefill(w, w.k_pool, w.v_pool, rows)
+    secs = flops = 0.0
+    for _ in range(args.steps):
+        cb = cpu_oracle_prefill(w, w.k_pool, w.v_pool, rows)
+        secs += cb["seconds"]
+        flops += cb["flops"]
+    value = flops / secs / 1e12
+    sample = f"{cb['rows']} of {w.T * w.Hq} (query row, head) pairs of one prefill call per step"
+    res = {"impl": "reference", "metric": PREFILL_METRIC, "value": round(value, 6),
+           "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+           "ms_per_step": round(secs * 1e3 / args.steps, 3), "higher_is_better": True,
+           "scaling": "weak", "vs_baseline": None, "dtype": "f64 (oracle)",
+           "data": "synthetic (seeded N(0,1))",
+           "config": {"workload": w.name, "batch": w.B, "q_heads": w.Hq, "kv_heads": w.Hkv,
+                      "head_dim": w.D, "query_tokens": w.T},
+           "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": cb["cores"],
+                            "kind": "oracle", "sample": sample},
+           "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                   "d2h_bytes_per_step": 0}}
+    print(json.dumps(res))
+
+
 def sample_rows(w, n):
     total = w.B * w.Hq
     if n <= 0 or n >= total:
@@ -548,7 +813,8 @@ def main():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=30)
     ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--workload", default="llama7b", choices=workloads.WORKLOAD_NAMES)
+    ap.add_argument("--workload", default="llama7b",
+                    choices=workloads.WORKLOAD_NAMES + workloads.PREFILL_NAMES)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-rows", type=int, default=0,
                     help="(request, head) rows the CPU oracle times (0 = default sample)")
@@ -566,12 +832,16 @@ def main():
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
+    prefill = args.workload in workloads.PREFILL_NAMES
     if args.cpu_rows == 0:
-        args.cpu_rows = 256 if args.impl == "ours" else 64
+        if prefill:
+            args.cpu_rows = 8192 if args.impl == "ours" else 2048
+        else:
+            args.cpu_rows = 256 if args.impl == "ours" else 64
     if args.impl == "reference":
-        run_reference(args)
+        (run_reference_prefill if prefill else run_reference)(args)
     else:
-        run_ours(args)
+        (run_prefill if prefill else run_ours)(args)
 
 
 if __name__ == "__main__":

@@ -173,3 +173,44 @@ def test_prefill_rejects_unsupported_groups():
     with pytest.raises(kvp.KvpError) as e:
         run_gpu(w)
     assert e.value.status == kvp.KVP_ERR_UNSUPPORTED
+
+
+def test_prefix_prefill_workload_full_size_sampled():
+    """The benchmarked prefix-cached prompt pass at full size (128 requests,
+    33K query tokens, 1030-token shared prefix), through the same call the
+    bench times, on sampled (row, head) outputs."""
+    w = workloads.make_prefill_named("prefix_prefill", device="cuda", nan_sentinel=True)
+    out = torch.empty((w.T, w.Hq, w.D), dtype=w.dtype, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    kvp.kvp_attention_prefill(out, w.q, w.k_pool, w.v_pool, w.block_tables, w.context_lens,
+                              w.query_start, w.max_query_len, w.scale, status=status)
+    assert kvp.kvp_read_status(status) == kvp.KVP_OK
+    rng = np.random.default_rng(17)
+    t = rng.integers(0, w.T, size=256)
+    h = rng.integers(0, w.Hq, size=256)
+    qs = w.query_start.cpu().numpy()
+    t[:3] = [0, int(qs[1]) - 1, w.T - 1]  # first row, end of the first chunk, last row
+    rows = np.stack([t, h], axis=1).astype(np.int32)
+    ref = oracle.attention_prefill(w.q.cpu(), w.k_pool.cpu(), w.v_pool.cpu(),
+                                   w.block_tables.cpu(), w.context_lens.cpu(),
+                                   w.query_start.cpu(), w.scale, rows=rows)
+    got = out.cpu()[torch.from_numpy(t).long(), torch.from_numpy(h).long()]
+    assert_close(got, ref, "prefix_prefill sampled")
+
+
+def test_context_beyond_the_staged_table():
+    """A 17000-token context (1063 blocks) reaches past the block ids a tile
+    keeps on chip; the chunk's last rows read those blocks from the table in
+    global memory.  Sampled rows against the oracle."""
+    w = workloads.make_prefill(B=2, Hq=8, Hkv=2, D=128, lens=[17000, 300], qlens=[150, 300],
+                               num_blocks=1100, dtype=torch.float16, seed=31)
+    out = run_gpu(w)
+    rng = np.random.default_rng(5)
+    t = rng.integers(0, w.T, size=64)
+    t[:3] = [0, 149, 150]
+    h = rng.integers(0, w.Hq, size=64)
+    rows = np.stack([t, h], axis=1).astype(np.int32)
+    ref = oracle.attention_prefill(w.q, w.k_pool, w.v_pool, w.block_tables, w.context_lens,
+                                   w.query_start, w.scale, rows=rows)
+    got = out.cpu()[torch.from_numpy(t).long(), torch.from_numpy(h).long()]
+    assert_close(got, ref, "context beyond the staged table")

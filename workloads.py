@@ -429,3 +429,44 @@ def make_prefill(*, B, Hq, Hkv, D, lens, qlens, num_blocks, dtype=torch.float16,
                            context_lens=torch.tensor(lens, dtype=torch.int32).to(device),
                            query_start=torch.tensor(qs, dtype=torch.int32).to(device),
                            max_query_len=max(qlens) if qlens else 0)
+
+
+PREFILL_NAMES = ("prefix_prefill",)
+
+
+def make_prefill_named(name: str, device="cpu", nan_sentinel=True,
+                       batch=None) -> PrefillWorkload:
+    """prefix_prefill: the prefix-sharing workload's prompt pass with the prefix
+    cached ("ATB KV Cache management", "Prefix Caching"): 128 requests (32/32
+    heads, D 128, fp16, 8192-block pool) whose tables share the 1030-token
+    prefix blocks; each request's private suffix (U[16, 512] tokens, already
+    appended) is its chunk of queries, attending causally to prefix + suffix.
+    Same tables and lengths as the `prefix` decode workload; q drawn with seed
+    base + 0 as [T, Hq, D].  ``batch`` keeps the first requests only."""
+    if name != "prefix_prefill":
+        raise KeyError(name)
+    seed = 1000 + WORKLOAD_NAMES.index("prefix")
+    src = _make_prefix(seed, device, False)
+    prefix = src.info["prefix_tokens"]
+    lens = [int(x) for x in src.context_lens.cpu()]
+    B = len(lens) if batch is None else min(int(batch), len(lens))
+    lens = lens[:B]
+    tables = src.block_tables[:B].cpu().clone()
+    qlens = [n - prefix for n in lens]
+    T = sum(qlens)
+    base = seed * 100
+    q = _randn((T, src.Hq, src.D), torch.float16, base + 0, device)
+    k_pool, v_pool = src.k_pool.to(device), src.v_pool.to(device)
+    if nan_sentinel:
+        _nan_unfilled(k_pool, tables, lens)
+        _nan_unfilled(v_pool, tables, lens)
+    qs = [0]
+    for L in qlens:
+        qs.append(qs[-1] + L)
+    return PrefillWorkload(name=name, B=B, Hq=src.Hq, Hkv=src.Hkv, D=src.D,
+                           num_blocks=src.num_blocks, dtype=torch.float16, scale=src.scale,
+                           q=q, k_pool=k_pool, v_pool=v_pool, block_tables=tables.to(device),
+                           context_lens=torch.tensor(lens, dtype=torch.int32).to(device),
+                           query_start=torch.tensor(qs, dtype=torch.int32).to(device),
+                           max_query_len=max(qlens),
+                           info={"prefix_tokens": prefix, "query_tokens": T})
