@@ -9,25 +9,29 @@
 // the block table.  Unlike the decode, this is a dense contraction: a 128-row
 // query tile against 64-key tiles.
 //
-// Design (one CTA of 4 warps per (request, kv head, 128-row query tile)):
+// Design (one CTA of 11 warps per (request, kv head, 128-row query tile)):
 //   * Tile rows are (query token, query head of the kv head's group) pairs, so
 //     every K/V byte a tile reads serves the whole GQA group.
 //   * K/V arrive in 64-key chunks (4 blocks) through separate K and V rings
 //     in shared memory: TMA copies (128-byte swizzle, the layout the tensor
-//     core reads directly) issued by four producer warps, one per block slot
-//     of a chunk, so copy issue is spread over several threads.
+//     core reads directly) issued by two producer warps, one per tensor.
 //   * One thread issues the tensor-core work: S = Q K^T (tcgen05.mma, M=128,
-//     N=64, K=D) into TMEM score buffers two chunks ahead of the softmax, and
-//     O += P V (M=128, N=D, K=64) into a TMEM accumulator, so the tensor core
-//     works while the CUDA cores exponentiate.
-//   * Thread r owns TMEM lane r, i.e. query row r: it loads its 64 scores,
-//     applies the causal mask and the scale, and keeps the row's running max
-//     and sum in registers -- no shuffles.  The running max is updated lazily:
-//     only when a row's max grows by more than 2^8 are its O columns rescaled
-//     in TMEM (exact, since numerator and denominator share the stale max).
-//   * P goes to shared memory (fp16; bf16 as a high part plus a bf16 residual
-//     so P keeps ~16 bits).
-//   * At the end each thread divides its O row by its sum and writes it out.
+//     N=64, K=D) into TMEM score buffers three chunks ahead of the softmax,
+//     and O += P V (M=128, N=D, K=64) into TMEM accumulators, so the tensor
+//     core works while the CUDA cores exponentiate.
+//   * Two threads own each query row (TMEM lane): each takes 32 of every
+//     chunk's 64 keys, applies the causal mask and the scale, and keeps its own
+//     running max and sum in registers, with its own O accumulator in TMEM
+//     (P V is split by key half) -- no exchange between them until the end,
+//     where the two (max, sum, O) are merged.  The running max is updated
+//     lazily: only when it grows by more than 2^8 is the O accumulator
+//     rescaled in TMEM (exact: numerator and denominator share the stale max).
+//   * P stays in tensor memory: each thread writes its 32 probabilities,
+//     packed as 16-bit pairs, over the scores it has read (fp16; bf16 as a
+//     high part plus a bf16 residual so P keeps ~16 bits), and P V takes its
+//     A operand from TMEM -- no shared-memory round trip, no proxy fence.
+//   * At the end the two threads of a row merge their (max, sum, O) and each
+//     writes half of the output row.
 #include "kvp_device.cuh"
 #include "kvp_internal.h"
 #include "kvp_umma.cuh"
@@ -36,11 +40,14 @@ namespace kvp {
 namespace {
 
 constexpr int kRows = 128;                            // M: query rows per CTA
-constexpr int kKeys = 64;                             // key tokens per chunk
-constexpr int kSoftmaxWarps = 8;                      // two per TMEM lane quarter
+constexpr int kKeys = 64;                             // key tokens per chunk (4 blocks)
+constexpr int kSplit = 2;                             // softmax threads per query row
+constexpr int kKeysPerThread = kKeys / kSplit;        // 32 keys of each chunk
+constexpr int kSoftmaxWarps = 4 * kSplit;             // kSplit per TMEM lane quarter
 constexpr int kSoftmaxThreads = kSoftmaxWarps * 32;
 constexpr int kMmaWarp = kSoftmaxWarps;               // issues the tensor-core work
-constexpr int kProducerWarps = 4;                     // TMA issue, one per block of a chunk
+// TMA issue: one warp streams K tiles, one V tiles
+constexpr int kProducerWarps = 2;
 constexpr int kThreads = kSoftmaxThreads + 32 + kProducerWarps * 32;
 constexpr int kSmemPerSm = 233472;                    // shared memory of one SM (bytes)
 constexpr int kTableCap = 1024;                       // block ids staged on chip per tile
@@ -50,30 +57,31 @@ struct PrefillLayout {
   static constexpr int kHalves = D / 64;                  // 64-element K-major halves
   static constexpr uint32_t kQ = kRows * D * 2;           // Q tile
   static constexpr uint32_t kKV = kKeys * D * 2;          // one K or V tile
-  static constexpr uint32_t kP = kRows * kKeys * 2;       // one P tile
-  static constexpr uint32_t kPBuf = kBf16 ? 2 * kP : kP;  // P (and its bf16 residual)
   // Separate K and V rings: a K stage is free once its S is computed, a V
   // stage once its P V is; depths fill the shared memory left by Q and P.
-  static constexpr int kKStages = D == 64 ? 6 : (kBf16 ? 4 : 5);
-  static constexpr int kVStages = D == 64 ? 5 : (kBf16 ? 3 : 4);
-  static constexpr int kAhead = 2;                        // S computed 2 chunks ahead
-  static constexpr int kSBufs = kAhead + 1;               // TMEM score buffers
+  static constexpr int kKStages = D == 64 ? 8 : 5;
+  static constexpr int kVStages = D == 64 ? 8 : 5;
+  static constexpr int kAhead = 3;                        // S computed 3 chunks ahead
+  static constexpr int kSBufs = kAhead + 1;               // TMEM score (then P) buffers
   static constexpr uint32_t kQOff = 0;
   static constexpr uint32_t kKOff = kQ;
   static constexpr uint32_t kVOff = kKOff + kKStages * kKV;
-  static constexpr uint32_t kPOff = kVOff + kVStages * kKV;  // 2 P buffers
-  static constexpr uint32_t kRedOff = kPOff + 2 * kPBuf;  // [2][2][kRows] float
-  static constexpr uint32_t kTblOff = kRedOff + 2 * 2 * kRows * 4;  // [kTableCap] int32
+  static constexpr uint32_t kRedOff = kVOff + kVStages * kKV;  // [2][kSplit][kRows] float
+  static constexpr uint32_t kTblOff = kRedOff + 2 * kSplit * kRows * 4;  // [kTableCap] int32
   static constexpr uint32_t kBarOff = kTblOff + kTableCap * 4;
-  // kfull[], vfull[], kempty[], vempty[], s[], pv[2], p[2]
-  static constexpr int kBars = 2 * (kKStages + kVStages) + kSBufs + 4;
+  // kfull[], vfull[], kempty[], vempty[], s[], p[], pv[2]
+  static constexpr int kBars = 2 * (kKStages + kVStages) + 2 * kSBufs + 2;
   // + 1024 bytes of alignment slack, the barriers and the TMEM address slot
   static constexpr size_t kSmem = 1024 + kBarOff + kBars * 8 + 16;
-  // TMEM columns: score buffer i at [64 i, 64 i + 64), O at [256, 256 + D).
-  // The shared memory keeps a second CTA off the SM, so all 512 columns are free.
+  // TMEM columns: score buffer i at [64 i, 64 i + 64) (key half h's P is
+  // written over its scores at [64 i + 32 h, +16), its bf16 residual at
+  // [64 i + 32 h + 16, +16)); the O accumulator of
+  // key half h at [256 + h D, 256 + (h+1) D).  The shared memory keeps a
+  // second CTA off the SM, so all 512 columns are free.
   static constexpr uint32_t kOCol = 256;
   static constexpr uint32_t kTmemCols = 512;
   static_assert(kSBufs * kKeys <= static_cast<int>(kOCol), "score buffers overlap O");
+  static_assert(kOCol + kSplit * D <= kTmemCols, "O accumulators exceed TMEM");
   static_assert(2 * (kSmem + 1024) > kSmemPerSm, "TMEM budget assumes one CTA per SM");
   static_assert(kSmem <= 232448, "exceeds the per-block shared-memory limit");
 };
@@ -96,21 +104,23 @@ __device__ __forceinline__ void zero_tile_rows(const PrefillParams& p, int kvh, 
 
 // Warp roles: warps 0-7 run the softmax -- warp w serves query rows
 // 32*(w%4) .. +31 (the TMEM lanes it may access) for keys [32*(w/4), +32) of
-// each chunk and O columns [D/2*(w/4), +D/2); warp 8 (one thread) issues the
-// tensor-core instructions; warps 9-12 are producers -- producer i copies
-// block i of every chunk (its lane 0 the K tile, lane 1 the V tile).
+// each chunk, accumulated into O accumulator w/4; warp 8 issues the
+// tensor-core instructions; warps 9 and 10 are producers of the K and the V
+// tiles.  The MMA and producer warps run their loops converged (waits and
+// address arithmetic warp-uniform) and issue from one elected lane.
 // Hand-offs (mbarriers; every wait is at most one phase behind its barrier):
-//   kfull[c % kKStages]   producers -> MMA    chunk c's K landed (4 arrivals + bytes)
+//   kfull[c % kKStages]   producer -> MMA     chunk c's K landed (1 arrival + bytes)
 //   vfull[c % kVStages]   producers -> MMA    chunk c's V landed
 //   kempty[c % kKStages]  MMA -> producers    S(c) done: K stage free
 //   vempty[c % kVStages]  MMA -> producers    P V(c) done: V stage free
-//   s[c % kSBufs]         MMA -> softmax      S of chunk c in score buffer c % kSBufs
-//   p[c % 2]              softmax -> MMA      P of chunk c in P buffer c % 2 (8 arrivals)
-//   pv[c % 2]             MMA -> softmax      O += P V of chunk c complete
-// Per chunk j the MMA thread waits p(j) and V(j), issues P V(j), then S(j +
-// kAhead).  The softmax of chunk j needs only S(j) -- P buffer j%2 was freed
-// by P V(j-2), and O is touched (lazy rescale, after P V(j-1)) only when a
-// row's max jumps.
+//   s[c % kSBufs]         MMA -> softmax      S of chunk c in TMEM buffer c % kSBufs
+//   p[c % kSBufs]         softmax -> MMA      P of chunk c written over it (8 arrivals)
+//   pv[c % 2]             MMA -> softmax, MMA O += P V of chunk c complete
+// Per chunk j the MMA thread waits p(j) and V(j), issues P V(j), then -- once
+// P V(j-1) has read its P -- S(j + kAhead) into chunk j-1's buffer.  The
+// softmax of chunk j needs only S(j); O is touched (lazy rescale, after
+// P V(j-1)) only when a row's max jumps.  The producers start as soon as the
+// block table is on chip, while the softmax warps load Q.
 template <bool kBf16, int D>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmk,
@@ -131,15 +141,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* ke_bar = vf_bar + kVStages;                              // [kKStages]
   uint64_t* ve_bar = ke_bar + kKStages;                              // [kVStages]
   uint64_t* s_bar = ve_bar + kVStages;                               // [kSBufs]
-  uint64_t* pv_bar = s_bar + kSBufs;                                 // [2]
-  uint64_t* p_bar = pv_bar + 2;                                      // [2]
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(p_bar + 2);
+  uint64_t* p_bar = s_bar + kSBufs;                                  // [kSBufs]
+  uint64_t* pv_bar = p_bar + kSBufs;                                 // [2]
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(pv_bar + 2);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const bool mma_warp = warp == kMmaWarp;
   const bool producer = warp > kMmaWarp;
   const int quarter = warp & 3;
-  const int half = (warp >> 2) & 1;
+  const int part = (warp >> 2) & (kSplit - 1);  // which key half / O accumulator
   const int row = quarter * 32 + lane;
   const int b = blockIdx.z, kvh = blockIdx.y, tile = blockIdx.x;
   const int G = p.group;
@@ -165,8 +175,18 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int nblk = (nkeys + kBlockSize - 1) / kBlockSize;
   const int nchunks = (nkeys + kKeys - 1) / kKeys;
   const int32_t* tbl = p.block_tables + static_cast<size_t>(b) * p.max_blocks;
+  if (mma_warp && lane == 0) {
+    prefetch_tensormap(&tmk);
+    prefetch_tensormap(&tmv);
+    for (int i = 0; i < 2 * (kKStages + kVStages) + kSBufs; ++i)
+      mbar_init(smem_addr(kf_bar + i), 1);
+    for (int i = 0; i < kSBufs; ++i) mbar_init(smem_addr(p_bar + i), kSoftmaxWarps);
+    mbar_init(smem_addr(pv_bar), 1);
+    mbar_init(smem_addr(pv_bar + 1), 1);
+    fence_barrier_init();
+  }
   // range-check every block id the tile reads; the first kTableCap are kept on
-  // chip so the copy issuer never waits on a global load
+  // chip so the copy issuers never wait on a global load
   bool bad = false;
   for (int i = tid; i < nblk; i += kThreads) {
     const int id = tbl[i];
@@ -179,8 +199,46 @@ __global__ void __launch_bounds__(kThreads, 1)
     return;
   }
 
+  // ---- producers: warp 9 streams the K tiles, warp 10 the V tiles
+  const bool is_k = warp == kMmaWarp + 1;
+  const CUtensorMap* map = is_k ? &tmk : &tmv;
+  const int nst = is_k ? kKStages : kVStages;
+  uint64_t* full = is_k ? kf_bar : vf_bar;
+  uint64_t* empty = is_k ? ke_bar : ve_bar;
+  const uint32_t ring = smem_addr(sm + (is_k ? L::kKOff : L::kVOff));
+  auto produce = [&](int c) {  // the whole warp; one lane issues the copies
+    const int st = c % nst;
+    bool fine = true;
+    if (c >= nst) fine = mbar_wait_bounded(smem_addr(empty + st), ((c / nst) - 1) & 1);
+    const int blk0 = c * (kKeys / kBlockSize);
+    const int nb = min(kKeys / kBlockSize, nblk - blk0);
+    int my_id = 0;
+    if (lane < nb) my_id = blk0 + lane < kTableCap ? stbl[blk0 + lane] : tbl[blk0 + lane];
+    int ids[kKeys / kBlockSize];
+#pragma unroll
+    for (int i = 0; i < kKeys / kBlockSize; ++i) ids[i] = __shfl_sync(0xffffffffu, my_id, i);
+    if (elect_one()) {
+      const uint32_t bar = smem_addr(full + st);
+      mbar_arrive_expect_tx(bar, static_cast<uint32_t>(nb * L::kHalves * 2048));
+#pragma unroll
+      for (int i = 0; i < kKeys / kBlockSize; ++i) {
+        if (i < nb) {
+          const int y = (ids[i] * p.num_kv_heads + kvh) * kBlockSize;
+#pragma unroll
+          for (int hf = 0; hf < L::kHalves; ++hf)
+            tma_load_2d(ring + st * L::kKV + i * 2048 + hf * (kKeys * 128), map, hf * 64, y, bar);
+        }
+      }
+    }
+    __syncwarp();
+    return fine;
+  };
+  // chunk 0 goes out at once; the rest waits until Q is staged, so the first
+  // copies do not queue ahead of the Q loads
+  if (producer) produce(0);
+
   // ---- Q tile: row r = (query token r / G, query head r % G), K-major
-  // swizzled; softmax thread (row, half) stores half of its row
+  // swizzled; softmax thread (row, part) stores half of its row
   const int my_t = row / G;
   const int my_g = row % G;
   const bool row_valid = warp < kSoftmaxWarps && my_t < ntok;
@@ -192,25 +250,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                                         kvh * G + my_g) *
                                            D);
 #pragma unroll
-    for (int i = 0; i < D / 16; ++i) {
-      const int c = half * (D / 16) + i;
+    for (int i = 0; i < D / (8 * kSplit); ++i) {
+      const int c = part * (D / (8 * kSplit)) + i;
       const uint4 v = row_valid ? src[c] : make_uint4(0u, 0u, 0u, 0u);
       *reinterpret_cast<uint4*>(sQ + (c >> 3) * (kRows * 128) + sw_chunk(row, c)) = v;
     }
     fence_proxy_async_smem();  // Q is read by the tensor core (async proxy)
   } else if (mma_warp) {
-    if (lane == 0) {
-      prefetch_tensormap(&tmk);
-      prefetch_tensormap(&tmv);
-      for (int i = 0; i < kKStages + kVStages; ++i)
-        mbar_init(smem_addr(kf_bar + i), kProducerWarps);
-      for (int i = kKStages + kVStages; i < 2 * (kKStages + kVStages) + kSBufs + 2; ++i)
-        mbar_init(smem_addr(kf_bar + i), 1);
-      mbar_init(smem_addr(p_bar), kSoftmaxWarps);
-      mbar_init(smem_addr(p_bar + 1), kSoftmaxWarps);
-      fence_barrier_init();
-    }
-    __syncwarp();
     umma::alloc(smem_addr(tmem_slot), L::kTmemCols);
   }
   umma::fence_before_sync();
@@ -220,78 +266,68 @@ __global__ void __launch_bounds__(kThreads, 1)
   bool ok = true;
 
   if (producer) {
-    if (lane < 2) {
-      // lane 0 streams K tiles, lane 1 V tiles: block `slot` of every chunk
-      const int slot = warp - kMmaWarp - 1;
-      const bool is_k = lane == 0;
-      const CUtensorMap* map = is_k ? &tmk : &tmv;
-      const int nst = is_k ? kKStages : kVStages;
-      uint64_t* full = is_k ? kf_bar : vf_bar;
-      uint64_t* empty = is_k ? ke_bar : ve_bar;
-      uint8_t* ring = sm + (is_k ? L::kKOff : L::kVOff);
-      for (int c = 0; c < nchunks; ++c) {
-        const int st = c % nst;
-        if (c >= nst) ok &= mbar_wait_bounded(smem_addr(empty + st), ((c / nst) - 1) & 1);
-        const int blk = c * (kKeys / kBlockSize) + slot;
-        const bool has = blk < nblk;
-        const uint32_t bar = smem_addr(full + st);
-        mbar_arrive_expect_tx(bar, has ? static_cast<uint32_t>(L::kHalves * 2048) : 0u);
-        if (has) {
-          const int id = blk < kTableCap ? stbl[blk] : tbl[blk];
-          const int y = (id * p.num_kv_heads + kvh) * kBlockSize;
-          uint8_t* dst = ring + st * L::kKV + slot * 2048;
-#pragma unroll
-          for (int hf = 0; hf < L::kHalves; ++hf)
-            tma_load_2d(smem_addr(dst + hf * (kKeys * 128)), map, hf * 64, y, bar);
-        }
-      }
-    }
-    __syncwarp();
+    for (int c = 1; c < nchunks; ++c) ok &= produce(c);
   } else if (mma_warp) {
-    if (lane == 0) {
-      auto k_tile = [&](int c) { return sm + L::kKOff + (c % kKStages) * L::kKV; };
-      auto v_tile = [&](int c) { return sm + L::kVOff + (c % kVStages) * L::kKV; };
+    // the whole warp runs this loop (waits and descriptor arithmetic stay
+    // warp-uniform); one elected lane issues each group of tensor instructions
+    {
       constexpr uint32_t kIdS = umma::instr_desc_f16(kRows, kKeys, kBf16, false, false);
       constexpr uint32_t kIdO = umma::instr_desc_f16(kRows, D, kBf16, false, true);
-      const uint32_t qa = smem_addr(sQ);
+      // shared-memory descriptors are built once; an operand at byte offset o
+      // from a base is the base descriptor plus o >> 4 (the start-address
+      // field, which never carries: every address is below 256 KB)
+      const uint64_t q_desc = umma::smem_desc_sw128(smem_addr(sQ), 16, 1024);
+      const uint64_t k_desc = umma::smem_desc_sw128(smem_addr(sm + L::kKOff), 16, 1024);
+      const uint64_t v_desc = umma::smem_desc_sw128(smem_addr(sm + L::kVOff), kKeys * 128, 1024);
       auto issue_s = [&](int c) {  // wait for chunk c's K, S(c) = Q K(c)^T, free the K stage
         ok &= mbar_wait_bounded(smem_addr(kf_bar + c % kKStages), (c / kKStages) & 1);
         umma::fence_after_sync();
-        const uint32_t ka = smem_addr(k_tile(c));
+        const uint64_t kd = k_desc + (((c % kKStages) * L::kKV) >> 4);
         const uint32_t d = tmem + (c % kSBufs) * kKeys;
+        if (elect_one()) {
 #pragma unroll
-        for (int s = 0; s < D / 16; ++s) {
-          const uint32_t qoff = (s >> 2) * (kRows * 128) + (s & 3) * 32;
-          const uint32_t koff = (s >> 2) * (kKeys * 128) + (s & 3) * 32;
-          umma::mma_f16(d, umma::smem_desc_sw128(qa + qoff, 16, 1024),
-                        umma::smem_desc_sw128(ka + koff, 16, 1024), kIdS, s > 0 ? 1u : 0u);
+          for (int s = 0; s < D / 16; ++s) {
+            const uint32_t qoff = (s >> 2) * (kRows * 128) + (s & 3) * 32;
+            const uint32_t koff = (s >> 2) * (kKeys * 128) + (s & 3) * 32;
+            umma::mma_f16(d, q_desc + (qoff >> 4), kd + (koff >> 4), kIdS, s > 0 ? 1u : 0u);
+          }
+          umma::commit(smem_addr(s_bar + c % kSBufs));
+          umma::commit(smem_addr(ke_bar + c % kKStages));
         }
-        umma::commit(smem_addr(s_bar + c % kSBufs));
-        umma::commit(smem_addr(ke_bar + c % kKStages));
+        __syncwarp();
       };
 
       for (int c = 0; c < min(kAhead, nchunks); ++c) issue_s(c);
       for (int j = 0; j < nchunks; ++j) {
-        ok &= mbar_wait_bounded(smem_addr(p_bar + (j & 1)), (j >> 1) & 1);
+        ok &= mbar_wait_bounded(smem_addr(p_bar + j % kSBufs), (j / kSBufs) & 1);
         ok &= mbar_wait_bounded(smem_addr(vf_bar + j % kVStages), (j / kVStages) & 1);
         umma::fence_after_sync();
-        const uint32_t pa = smem_addr(sm + L::kPOff + (j & 1) * L::kPBuf);
-        const uint32_t va = smem_addr(v_tile(j));
+        const uint32_t pa = tmem + (j % kSBufs) * kKeys;  // P of chunk j (TMEM)
+        const uint64_t vd = v_desc + (((j % kVStages) * L::kKV) >> 4);
+        if (elect_one()) {
+          // key half h (16-key steps t = 0, 1) into O accumulator h
 #pragma unroll
-        for (int t = 0; t < kKeys / 16; ++t) {
-          const uint64_t vd = umma::smem_desc_sw128(va + t * 2048, kKeys * 128, 1024);
-          umma::mma_f16(tmem + L::kOCol, umma::smem_desc_sw128(pa + t * 32, 16, 1024), vd, kIdO,
-                        (j > 0 || t > 0) ? 1u : 0u);
-          if constexpr (kBf16) {
-            umma::mma_f16(tmem + L::kOCol, umma::smem_desc_sw128(pa + L::kP + t * 32, 16, 1024),
-                          vd, kIdO, 1u);
+          for (int h = 0; h < kSplit; ++h) {
+#pragma unroll
+            for (int t = 0; t < kKeysPerThread / 16; ++t) {
+              const uint32_t o_acc = tmem + L::kOCol + h * D;
+              const uint32_t a = pa + h * kKeysPerThread + t * 8;
+              const uint64_t b = vd + (((h * kKeysPerThread + t * 16) * 128) >> 4);
+              umma::mma_f16_tmem_a(o_acc, a, b, kIdO, (j > 0 || t > 0) ? 1u : 0u);
+              if constexpr (kBf16)
+                umma::mma_f16_tmem_a(o_acc, a + kKeysPerThread / 2, b, kIdO, 1u);
+            }
           }
+          umma::commit(smem_addr(pv_bar + (j & 1)));
+          umma::commit(smem_addr(ve_bar + j % kVStages));
         }
-        umma::commit(smem_addr(pv_bar + (j & 1)));
-        umma::commit(smem_addr(ve_bar + j % kVStages));
-        // S(j+kAhead): its score buffer was last read by the softmax of chunk
-        // j-1, which handed off before P V(j-1) was issued
-        if (j + kAhead < nchunks) issue_s(j + kAhead);
+        __syncwarp();
+        // S(j+kAhead) goes over chunk j-1's P: wait until P V(j-1) has read it
+        if (j + kAhead < nchunks) {
+          if (j >= 1)
+            ok &= mbar_wait_bounded(smem_addr(pv_bar + ((j - 1) & 1)), ((j - 1) >> 1) & 1);
+          issue_s(j + kAhead);
+        }
       }
     }
     __syncwarp();
@@ -303,39 +339,51 @@ __global__ void __launch_bounds__(kThreads, 1)
     // (max and mask commute with it); otherwise they are scaled first
     const bool pos_scale = sl2 > 0.f;
     const float mul = pos_scale ? sl2 : 1.0f;
-    float m = -INFINITY, l = 0.f;  // running max (log2 units) and this half's sum
+    float m = -INFINITY, l = 0.f;  // this key half's running max (log2 units) and sum
     const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
-    const uint32_t tOh = tmem + L::kOCol + half * (D / 2) + lane_base;
+    const uint32_t tOp = tmem + L::kOCol + part * D + lane_base;  // this half's O row
+    auto o_scale = [&](float alpha) {  // this half's O row *= alpha
+#pragma unroll
+      for (int c = 0; c < D / 32; ++c) {
+        float o[32];
+        umma::ld32(tOp + c * 32, o);
+        umma::wait_ld();
+#pragma unroll
+        for (int i = 0; i < 32; ++i) o[i] *= alpha;
+        umma::st32(tOp + c * 32, o);
+      }
+      umma::wait_st();
+    };
     for (int j = 0; j < nchunks; ++j) {
       ok &= mbar_wait_bounded(smem_addr(s_bar + j % kSBufs), (j / kSBufs) & 1);
       umma::fence_after_sync();
-      float s[32];
-      umma::ld32(tmem + (j % kSBufs) * kKeys + half * 32 + lane_base, s);
+      float s[kKeysPerThread];
+      const uint32_t tS = tmem + (j % kSBufs) * kKeys + part * kKeysPerThread + lane_base;
+#pragma unroll
+      for (int c = 0; c < kKeysPerThread / 32; ++c)
+        umma::ld32(tS + c * 32, *reinterpret_cast<float(*)[32]>(s + c * 32));
       umma::wait_ld();
-      const int kbase = j * kKeys + half * 32;
+      const int kbase = j * kKeys + part * kKeysPerThread;
       if (j * kKeys + kKeys - 1 > pos0) {  // chunk reaches past some row's position
 #pragma unroll
-        for (int k = 0; k < 32; ++k) s[k] = (row_valid && kbase + k <= qpos) ? s[k] : -INFINITY;
+        for (int k = 0; k < kKeysPerThread; ++k)
+          s[k] = (row_valid && kbase + k <= qpos) ? s[k] : -INFINITY;
       }
       if (!pos_scale) {
 #pragma unroll
-        for (int k = 0; k < 32; ++k) s[k] = s[k] == -INFINITY ? -INFINITY : s[k] * sl2;
+        for (int k = 0; k < kKeysPerThread; ++k)
+          s[k] = s[k] == -INFINITY ? -INFINITY : s[k] * sl2;
       }
       float mx0 = fmaxf(s[0], s[1]), mx1 = fmaxf(s[2], s[3]);
       float mx2 = fmaxf(s[4], s[5]), mx3 = fmaxf(s[6], s[7]);
 #pragma unroll
-      for (int k = 8; k < 32; k += 8) {
+      for (int k = 8; k < kKeysPerThread; k += 8) {
         mx0 = fmaxf(mx0, fmaxf(s[k], s[k + 1]));
         mx1 = fmaxf(mx1, fmaxf(s[k + 2], s[k + 3]));
         mx2 = fmaxf(mx2, fmaxf(s[k + 4], s[k + 5]));
         mx3 = fmaxf(mx3, fmaxf(s[k + 6], s[k + 7]));
       }
-      float rowmax = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * mul;
-      // the partner warp holds the row's other 32 keys
-      float* rb = red + (j & 1) * (2 * kRows);
-      rb[half * kRows + row] = rowmax;
-      named_bar_sync(1 + quarter, 64);
-      rowmax = fmaxf(rowmax, rb[(1 - half) * kRows + row]);
+      const float rowmax = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * mul;
       const float mnew = fmaxf(m, rowmax);
       const bool grow = mnew > m + 8.0f;  // lazy: rescale only when the max grows by > 2^8
       const float alpha = grow ? ex2_approx(m - mnew) : 1.0f;
@@ -343,57 +391,44 @@ __global__ void __launch_bounds__(kThreads, 1)
         l *= alpha;
         m = mnew;
       }
-      // ---- this half of the P row (32 keys), into registers
-      const float negm = -m;
+      // ---- P over this thread's scores in TMEM (it has read them all); a
+      // half whose keys are all masked so far (m = -inf) gets P = 0
+      const float negm = m == -INFINITY ? 0.f : -m;
       float ps0 = 0.f, ps1 = 0.f, ps2 = 0.f, ps3 = 0.f;
-      uint32_t hi[16], lo[16];
 #pragma unroll
-      for (int k = 0; k < 32; k += 4) {
-        const float p0 = ex2_approx(fmaf(s[k], mul, negm));
-        const float p1 = ex2_approx(fmaf(s[k + 1], mul, negm));
-        const float p2 = ex2_approx(fmaf(s[k + 2], mul, negm));
-        const float p3 = ex2_approx(fmaf(s[k + 3], mul, negm));
-        ps0 += p0;
-        ps1 += p1;
-        ps2 += p2;
-        ps3 += p3;
-        hi[k / 2] = pack2<kBf16>(p0, p1);
-        hi[k / 2 + 1] = pack2<kBf16>(p2, p3);
-        if constexpr (kBf16) {
-          const float2 h01 = unpack2<true>(hi[k / 2]);
-          const float2 h23 = unpack2<true>(hi[k / 2 + 1]);
-          lo[k / 2] = pack2<true>(p0 - h01.x, p1 - h01.y);
-          lo[k / 2 + 1] = pack2<true>(p2 - h23.x, p3 - h23.y);
+      for (int sub = 0; sub < kKeysPerThread / 32; ++sub) {
+        uint32_t hi[16], lo[16];
+#pragma unroll
+        for (int k = 0; k < 32; k += 4) {
+          const float* sk = s + sub * 32 + k;
+          const float p0 = ex2_approx(fmaf(sk[0], mul, negm));
+          const float p1 = ex2_approx(fmaf(sk[1], mul, negm));
+          const float p2 = ex2_approx(fmaf(sk[2], mul, negm));
+          const float p3 = ex2_approx(fmaf(sk[3], mul, negm));
+          ps0 += p0;
+          ps1 += p1;
+          ps2 += p2;
+          ps3 += p3;
+          hi[k / 2] = pack2<kBf16>(p0, p1);
+          hi[k / 2 + 1] = pack2<kBf16>(p2, p3);
+          if constexpr (kBf16) {
+            const float2 h01 = unpack2<true>(hi[k / 2]);
+            const float2 h23 = unpack2<true>(hi[k / 2 + 1]);
+            lo[k / 2] = pack2<true>(p0 - h01.x, p1 - h01.y);
+            lo[k / 2 + 1] = pack2<true>(p2 - h23.x, p3 - h23.y);
+          }
         }
+        umma::st16_bits(tS + sub * 16, hi);
+        if constexpr (kBf16) umma::st16_bits(tS + kKeysPerThread / 2 + sub * 16, lo);
       }
       l += (ps0 + ps1) + (ps2 + ps3);
       // ---- O: rescale the rows whose max jumped, once P V(j-1) is in it
       if (__any_sync(0xffffffffu, grow && j > 0)) {
         ok &= mbar_wait_bounded(smem_addr(pv_bar + ((j - 1) & 1)), ((j - 1) >> 1) & 1);
         umma::fence_after_sync();
-#pragma unroll
-        for (int c = 0; c < D / 64; ++c) {
-          float o[32];
-          umma::ld32(tOh + c * 32, o);
-          umma::wait_ld();
-#pragma unroll
-          for (int i = 0; i < 32; ++i) o[i] *= alpha;
-          umma::st32(tOh + c * 32, o);
-        }
-        umma::wait_st();
+        o_scale(alpha);
       }
-      // ---- P buffer j%2 is free once P V(j-2) is done
-      if (j >= 2) ok &= mbar_wait_bounded(smem_addr(pv_bar + (j & 1)), ((j - 2) >> 1) & 1);
-      uint8_t* sP = sm + L::kPOff + (j & 1) * L::kPBuf;
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        *reinterpret_cast<uint4*>(sP + sw_chunk(row, 4 * half + c)) =
-            make_uint4(hi[4 * c], hi[4 * c + 1], hi[4 * c + 2], hi[4 * c + 3]);
-        if constexpr (kBf16) {
-          *reinterpret_cast<uint4*>(sP + L::kP + sw_chunk(row, 4 * half + c)) =
-              make_uint4(lo[4 * c], lo[4 * c + 1], lo[4 * c + 2], lo[4 * c + 3]);
-        }
-      }
+      umma::wait_st();
       if (j == nchunks - 1 && nkeys - j * kKeys < kKeys) {
         // V rows of keys >= nkeys are never attended (P = 0) but may hold
         // non-finite bytes (slots past the context, blocks not loaded): clear
@@ -407,40 +442,52 @@ __global__ void __launch_bounds__(kThreads, 1)
           *reinterpret_cast<uint4*>(sV + (rem >> 3) * (kKeys * 128) + r * 128 +
                                     ((rem & 7) << 4)) = make_uint4(0u, 0u, 0u, 0u);
         }
+        fence_proxy_async_smem();
       }
-      fence_proxy_async_smem();
       umma::fence_before_sync();
       __syncwarp();
-      if (lane == 0) mbar_arrive(smem_addr(p_bar + (j & 1)));
+      if (lane == 0) mbar_arrive(smem_addr(p_bar + j % kSBufs));
     }
 
     ok &= mbar_wait_bounded(smem_addr(pv_bar + ((nchunks - 1) & 1)), ((nchunks - 1) >> 1) & 1);
     umma::fence_after_sync();
     launch_dependents();
-    // ---- the row's sum over both key halves, then out = O / l
-    float* rb = red + (nchunks & 1) * (2 * kRows);
-    rb[half * kRows + row] = l;
-    named_bar_sync(1 + quarter, 64);
-    const float lt = l + rb[(1 - half) * kRows + row];
+    // ---- merge the two halves' (max, sum, O); thread (row, part) writes
+    // output columns [part * D/2, +D/2)
+    float* rb = red;  // [2 (max, sum)][kSplit][kRows]
+    rb[part * kRows + row] = m;
+    rb[(kSplit + part) * kRows + row] = l;
+    named_bar_sync(1 + quarter, 32 * kSplit);
+    const float m0 = rb[row], m1 = rb[kRows + row];
+    const float mm = fmaxf(m0, m1);
+    const float w0 = m0 == -INFINITY ? 0.f : ex2_approx(m0 - mm);
+    const float w1 = m1 == -INFINITY ? 0.f : ex2_approx(m1 - mm);
+    const float lt = rb[kSplit * kRows + row] * w0 + rb[(kSplit + 1) * kRows + row] * w1;
     const float inv = (row_valid && lt > 0.f) ? 1.0f / lt : 0.f;
+    const float c0 = w0 * inv, c1 = w1 * inv;
     uint16_t* out = static_cast<uint16_t*>(p.out) +
                     (static_cast<size_t>(q0 + t0 + (row_valid ? my_t : 0)) * p.num_q_heads +
                      kvh * G + my_g) *
                         D +
-                    half * (D / 2);
+                    part * (D / 2);
+    const uint32_t tO0 = tmem + L::kOCol + part * (D / 2) + lane_base;
 #pragma unroll
     for (int c = 0; c < D / 64; ++c) {
-      float o[32];
-      umma::ld32(tOh + c * 32, o);
+      float a0[32], a1[32];
+      umma::ld32(tO0 + c * 32, a0);
+      umma::ld32(tO0 + D + c * 32, a1);
       umma::wait_ld();
       if (row_valid) {
 #pragma unroll
         for (int q4 = 0; q4 < 4; ++q4) {
+          float v[8];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) v[e] = a0[8 * q4 + e] * c0 + a1[8 * q4 + e] * c1;
           uint4 w;
-          w.x = pack2<kBf16>(o[8 * q4] * inv, o[8 * q4 + 1] * inv);
-          w.y = pack2<kBf16>(o[8 * q4 + 2] * inv, o[8 * q4 + 3] * inv);
-          w.z = pack2<kBf16>(o[8 * q4 + 4] * inv, o[8 * q4 + 5] * inv);
-          w.w = pack2<kBf16>(o[8 * q4 + 6] * inv, o[8 * q4 + 7] * inv);
+          w.x = pack2<kBf16>(v[0], v[1]);
+          w.y = pack2<kBf16>(v[2], v[3]);
+          w.z = pack2<kBf16>(v[4], v[5]);
+          w.w = pack2<kBf16>(v[6], v[7]);
           *reinterpret_cast<uint4*>(out + c * 32 + 8 * q4) = w;
         }
       }
