@@ -289,12 +289,12 @@ kvp_status kvp_attention_decode_fp8(void* out, const void* q, kvp_dtype q_dtype,
  * Sources: "ATB KV Cache management", "Prefix Caching" (requests that share a
  * system prompt reuse its cached K/V, and only their own tokens are computed);
  * "ATB PagedAttention", "ATB 的 PagedAttention 实现" (the page-table walk).
- *   q, out        [T, num_q_heads, D] of `dtype`, T = query_start[batch] rows;
+ *   q, out        [T, num_q_heads, D] of `dtype`, T = num_query_tokens rows;
  *                 16-byte aligned.  out rows outside every request's range
  *                 are not written.
  *   query_start   [batch + 1] int32 (device), non-decreasing, query_start[0]
  *                 = 0: request b's query rows are query_start[b] ..
- *                 query_start[b+1] - 1.
+ *                 query_start[b+1] - 1, all below num_query_tokens.
  *   context_lens  [batch] int32 (device): n, the request's tokens in the cache
  *                 INCLUDING this chunk (append the chunk's K/V first).  Query
  *                 row i of request b (L = its row count) sits at position
@@ -305,16 +305,18 @@ kvp_status kvp_attention_decode_fp8(void* out, const void* q, kvp_dtype q_dtype,
  * num_q_heads / num_kv_heads must divide 128 (KVP_ERR_UNSUPPORTED otherwise).
  * Device-side errors (*dev_status): KVP_ERR_BAD_BLOCK when a block id is out of
  * range, L > n, n > max_blocks_per_seq * 16 or L > max_query_len (the rows of
- * the offending request that are reached are written as zeros);
+ * the offending request that are reached are written as zeros), or when a
+ * request's rows reach past num_query_tokens (nothing of it is written);
  * KVP_ERR_TIMEOUT when a pipeline wait gave up.  Computed on the tensor cores
  * with float32 accumulation; no workspace.
  */
 kvp_status kvp_attention_prefill(void* out, const void* q, const void* k_cache,
                                  const void* v_cache, const int32_t* block_tables,
                                  int32_t max_blocks_per_seq, const int32_t* context_lens,
-                                 const int32_t* query_start, int32_t batch, int32_t num_q_heads,
-                                 int32_t max_query_len, float scale, kvp_cache_desc cache,
-                                 kvp_dtype dtype, int32_t* dev_status, kvp_stream_t stream);
+                                 const int32_t* query_start, int32_t num_query_tokens,
+                                 int32_t batch, int32_t num_q_heads, int32_t max_query_len,
+                                 float scale, kvp_cache_desc cache, kvp_dtype dtype,
+                                 int32_t* dev_status, kvp_stream_t stream);
 
 /*
  * kvp_attention_decode_noalloc -- kvp_attention_decode for callers that cannot

@@ -82,8 +82,8 @@ SIGNATURES = {
                                         _F, _D, _I32, _P, _SZ, _I32, _P, _P]),
     "kvp_attention_decode_noalloc": (_I32, [_P, _P, _P, _P, _P, _I32, _P, _I32, _I32, _F, _D,
                                             _I32, _I32, _P, _P]),
-    "kvp_attention_prefill": (_I32, [_P, _P, _P, _P, _P, _I32, _P, _P, _I32, _I32, _I32, _F,
-                                     _D, _I32, _P, _P]),
+    "kvp_attention_prefill": (_I32, [_P, _P, _P, _P, _P, _I32, _P, _P, _I32, _I32, _I32, _I32,
+                                     _F, _D, _I32, _P, _P]),
     "kvp_read_status": (_I32, [_P, _P]),
     "kvp_bm_create": (_P, [_I32, _I32, _I64]),
     "kvp_bm_destroy": (None, [_P]),
@@ -357,11 +357,13 @@ def kvp_attention_prefill(out, q, k_cache, v_cache, block_tables, context_lens, 
     _need_cuda(out, q, k_cache, v_cache, block_tables, context_lens, query_start, status)
     if q.dtype != k_cache.dtype or out.dtype != q.dtype:
         raise TypeError("q, out and the pools must share one dtype")
-    _, Hq, _ = (int(x) for x in q.shape)
+    T, Hq, _ = (int(x) for x in q.shape)
+    if int(out.shape[0]) < T:
+        raise ValueError("out needs as many rows as q")
     B = int(context_lens.shape[0])
     _check(lib.kvp_attention_prefill(
         _ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
-        int(block_tables.shape[1]), _ptr(context_lens), _ptr(query_start), B, Hq,
+        int(block_tables.shape[1]), _ptr(context_lens), _ptr(query_start), T, B, Hq,
         int(max_query_len), float(scale), cache_desc(k_cache), _dtype_code(q), _ptr(status),
         _stream_ptr(stream)), "kvp_attention_prefill")
 

@@ -3,6 +3,7 @@
 // kernel dispatch.  Nothing here allocates device memory.
 #include <cudaTypedefs.h>
 
+#include <algorithm>
 #include <cmath>
 #include <cstdint>
 #include <mutex>
@@ -66,6 +67,26 @@ kvp_status make_pool_map(CUtensorMap* map, const void* base, const kvp_cache_des
          box_bytes == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
          CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? KVP_OK : KVP_ERR_CUDA;
+}
+
+// TMA descriptor over q viewed as [T tokens][Hq heads][D]: a box of 64
+// elements x `group` heads x `box_tokens` tokens lands in shared memory as
+// 128-byte swizzled rows ordered (token, head) -- the K-major operand layout.
+kvp_status make_q_map(CUtensorMap* map, const void* q, int num_tokens, int num_q_heads,
+                      int head_dim, int group, int box_tokens) {
+  auto fn = encode_fn();
+  if (fn == nullptr) return KVP_ERR_CUDA;
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(head_dim), static_cast<cuuint64_t>(num_q_heads),
+                        static_cast<cuuint64_t>(num_tokens)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(head_dim) * 2,
+                           static_cast<cuuint64_t>(num_q_heads) * head_dim * 2};
+  cuuint32_t box[3] = {64, static_cast<cuuint32_t>(group), static_cast<cuuint32_t>(box_tokens)};
+  cuuint32_t estr[3] = {1, 1, 1};
+  const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT16, 3, const_cast<void*>(q), dims,
+                        strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? KVP_OK : KVP_ERR_CUDA;
 }
 
@@ -430,19 +451,21 @@ kvp_status kvp_attention_decode_fp8(void* out, const void* q, kvp_dtype q_dtype,
 kvp_status kvp_attention_prefill(void* out, const void* q, const void* k_cache,
                                  const void* v_cache, const int32_t* block_tables,
                                  int32_t max_blocks_per_seq, const int32_t* context_lens,
-                                 const int32_t* query_start, int32_t batch, int32_t num_q_heads,
-                                 int32_t max_query_len, float scale, kvp_cache_desc cache,
-                                 kvp_dtype dtype, int32_t* dev_status, kvp_stream_t stream) {
+                                 const int32_t* query_start, int32_t num_query_tokens,
+                                 int32_t batch, int32_t num_q_heads, int32_t max_query_len,
+                                 float scale, kvp_cache_desc cache, kvp_dtype dtype,
+                                 int32_t* dev_status, kvp_stream_t stream) {
   const kvp_status st = check_desc(cache);
   if (st != KVP_OK) return st;
   if (dtype != KVP_F16 && dtype != KVP_BF16) return KVP_ERR_INVALID_ARG;
-  if (batch < 0 || num_q_heads <= 0 || max_blocks_per_seq <= 0 || max_query_len < 0)
+  if (batch < 0 || num_q_heads <= 0 || max_blocks_per_seq <= 0 || max_query_len < 0 ||
+      num_query_tokens < 0)
     return KVP_ERR_INVALID_ARG;
   if (num_q_heads % cache.num_kv_heads != 0) return KVP_ERR_INVALID_ARG;
   if (!std::isfinite(scale)) return KVP_ERR_INVALID_ARG;
   const int group = num_q_heads / cache.num_kv_heads;
   if (128 % group != 0) return KVP_ERR_UNSUPPORTED;  // a 128-row tile holds whole groups
-  if (batch == 0 || max_query_len == 0) return KVP_OK;
+  if (batch == 0 || max_query_len == 0 || num_query_tokens == 0) return KVP_OK;
   if (!out || !q || !k_cache || !v_cache || !block_tables || !context_lens || !query_start)
     return KVP_ERR_INVALID_ARG;
   if (!aligned(out, 16) || !aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16))
@@ -451,8 +474,12 @@ kvp_status kvp_attention_prefill(void* out, const void* q, const void* k_cache,
   if (tiles > 0x7fffffffll || cache.num_kv_heads > 65535 || batch > 65535)
     return KVP_ERR_UNSUPPORTED;
 
-  CUtensorMap tk, tv;
-  kvp_status r = make_pool_map(&tk, k_cache, cache, 2);
+  const int box_tokens = std::min(128 / group, static_cast<int>(num_query_tokens));
+  CUtensorMap tq, tk, tv;
+  kvp_status r = make_q_map(&tq, q, num_query_tokens, num_q_heads, cache.head_dim, group,
+                            box_tokens);
+  if (r != KVP_OK) return r;
+  r = make_pool_map(&tk, k_cache, cache, 2);
   if (r != KVP_OK) return r;
   r = make_pool_map(&tv, v_cache, cache, 2);
   if (r != KVP_OK) return r;
@@ -470,8 +497,10 @@ kvp_status kvp_attention_prefill(void* out, const void* q, const void* k_cache,
   p.num_blocks = cache.num_blocks;
   p.max_blocks = max_blocks_per_seq;
   p.group = group;
+  p.num_tokens = num_query_tokens;
+  p.q_box_tokens = box_tokens;
   p.scale_log2 = scale * 1.4426950408889634f;
-  return from_cuda(launch_prefill(p, tk, tv, dtype == KVP_BF16, static_cast<int>(tiles),
+  return from_cuda(launch_prefill(p, tq, tk, tv, dtype == KVP_BF16, static_cast<int>(tiles),
                                   reinterpret_cast<cudaStream_t>(stream)));
 }
 

@@ -58,6 +58,8 @@ struct PrefillParams {
   int32_t* status;               // nullable
   int32_t batch, num_q_heads, num_kv_heads, head_dim, num_blocks, max_blocks;
   int32_t group;                 // Hq / Hkv (divides 128)
+  int32_t num_tokens;            // T, rows of q and out
+  int32_t q_box_tokens;          // tokens per Q tile copy: min(128 / group, T)
   float scale_log2;              // scale * log2(e)
 };
 
@@ -77,8 +79,8 @@ cudaError_t launch_decode_mma_int8(const DecodeParams& p, const CUtensorMap& tk,
 cudaError_t launch_decode_mma_fp8(const DecodeParams& p, const CUtensorMap& tk,
                                   const CUtensorMap& tv, int grid_x, cudaStream_t s);
 cudaError_t launch_decode_reduce(const DecodeParams& p, cudaStream_t s);
-cudaError_t launch_prefill(const PrefillParams& p, const CUtensorMap& tk, const CUtensorMap& tv,
-                           bool bf16, int grid_x, cudaStream_t s);
+cudaError_t launch_prefill(const PrefillParams& p, const CUtensorMap& tq, const CUtensorMap& tk,
+                           const CUtensorMap& tv, bool bf16, int grid_x, cudaStream_t s);
 
 // Launch `kernel` on stream `s` with programmatic stream serialisation, so its
 // CTAs can be scheduled while the previous kernel drains (every kernel of this

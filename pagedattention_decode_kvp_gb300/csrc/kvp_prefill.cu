@@ -69,8 +69,8 @@ struct PrefillLayout {
   static constexpr uint32_t kRedOff = kVOff + kVStages * kKV;  // [2][kSplit][kRows] float
   static constexpr uint32_t kTblOff = kRedOff + 2 * kSplit * kRows * 4;  // [kTableCap] int32
   static constexpr uint32_t kBarOff = kTblOff + kTableCap * 4;
-  // kfull[], vfull[], kempty[], vempty[], s[], p[], pv[2]
-  static constexpr int kBars = 2 * (kKStages + kVStages) + 2 * kSBufs + 2;
+  // kfull[], vfull[], kempty[], vempty[], s[], p[], pv[2], q
+  static constexpr int kBars = 2 * (kKStages + kVStages) + 2 * kSBufs + 3;
   // + 1024 bytes of alignment slack, the barriers and the TMEM address slot
   static constexpr size_t kSmem = 1024 + kBarOff + kBars * 8 + 16;
   // TMEM columns: score buffer i at [64 i, 64 i + 64) (key half h's P is
@@ -123,7 +123,8 @@ __device__ __forceinline__ void zero_tile_rows(const PrefillParams& p, int kvh, 
 // block table is on chip, while the softmax warps load Q.
 template <bool kBf16, int D>
 __global__ void __launch_bounds__(kThreads, 1)
-    prefill_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmk,
+    prefill_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmq,
+                   const __grid_constant__ CUtensorMap tmk,
                    const __grid_constant__ CUtensorMap tmv) {
   using namespace dev;
   using L = PrefillLayout<kBf16, D>;
@@ -143,7 +144,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* s_bar = ve_bar + kVStages;                               // [kSBufs]
   uint64_t* p_bar = s_bar + kSBufs;                                  // [kSBufs]
   uint64_t* pv_bar = p_bar + kSBufs;                                 // [2]
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(pv_bar + 2);
+  uint64_t* q_bar = pv_bar + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(q_bar + 1);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const bool mma_warp = warp == kMmaWarp;
@@ -164,6 +166,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (tile == gridDim.x - 1 && tid == 0 && qlen > static_cast<int>(gridDim.x) * tok_per_tile)
     set_status(p.status, kErrBadBlock);
   if (qlen <= 0 || t0 >= qlen) return;
+  if (q0 < 0 || q0 + qlen > p.num_tokens) {  // rows outside q / out: touch nothing
+    if (tid == 0) set_status(p.status, kErrBadBlock);
+    return;
+  }
   const int ntok = min(tok_per_tile, qlen - t0);
   if (qlen > n || n > p.max_blocks * kBlockSize) {
     zero_tile_rows<D>(p, kvh, q0, t0, ntok);
@@ -183,7 +189,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int i = 0; i < kSBufs; ++i) mbar_init(smem_addr(p_bar + i), kSoftmaxWarps);
     mbar_init(smem_addr(pv_bar), 1);
     mbar_init(smem_addr(pv_bar + 1), 1);
+    mbar_init(smem_addr(q_bar), 1);
     fence_barrier_init();
+    // ---- Q tile by TMA, straight into the K-major swizzled layout: a box of
+    // (64 elements, G heads, 128 / G tokens) puts (token t, head g) at row
+    // t * G + g.  Tokens past T read as zeros; rows past the tile's own tokens
+    // are never used.
+    const uint32_t qb = smem_addr(q_bar);
+    mbar_arrive_expect_tx(
+        qb, static_cast<uint32_t>(L::kHalves * 64 * G * p.q_box_tokens * 2));
+#pragma unroll
+    for (int hf = 0; hf < L::kHalves; ++hf)
+      tma_load_3d(smem_addr(sQ + hf * (kRows * 128)), &tmq, hf * 64, kvh * G, q0 + t0, qb);
   }
   // range-check every block id the tile reads; the first kTableCap are kept on
   // chip so the copy issuers never wait on a global load
@@ -196,6 +213,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (__syncthreads_or(bad)) {
     zero_tile_rows<D>(p, kvh, q0, t0, ntok);
     if (tid == 0) set_status(p.status, kErrBadBlock);
+    mbar_wait_bounded(smem_addr(q_bar), 0);  // no copy may land after the exit
     return;
   }
 
@@ -237,26 +255,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   // copies do not queue ahead of the Q loads
   if (producer) produce(0);
 
-  // ---- Q tile: row r = (query token r / G, query head r % G), K-major
-  // swizzled; softmax thread (row, part) stores half of its row
+  // ---- tile row r = (query token r / G, query head r % G)
   const int my_t = row / G;
   const int my_g = row % G;
   const bool row_valid = warp < kSoftmaxWarps && my_t < ntok;
-  if (warp < kSoftmaxWarps) {
-    const uint4* src =
-        reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.q) +
-                                       (static_cast<size_t>(q0 + t0 + (row_valid ? my_t : 0)) *
-                                            p.num_q_heads +
-                                        kvh * G + my_g) *
-                                           D);
-#pragma unroll
-    for (int i = 0; i < D / (8 * kSplit); ++i) {
-      const int c = part * (D / (8 * kSplit)) + i;
-      const uint4 v = row_valid ? src[c] : make_uint4(0u, 0u, 0u, 0u);
-      *reinterpret_cast<uint4*>(sQ + (c >> 3) * (kRows * 128) + sw_chunk(row, c)) = v;
-    }
-    fence_proxy_async_smem();  // Q is read by the tensor core (async proxy)
-  } else if (mma_warp) {
+  if (mma_warp) {
     umma::alloc(smem_addr(tmem_slot), L::kTmemCols);
   }
   umma::fence_before_sync();
@@ -297,6 +300,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
       };
 
+      ok &= mbar_wait_bounded(smem_addr(q_bar), 0);
       for (int c = 0; c < min(kAhead, nchunks); ++c) issue_s(c);
       for (int j = 0; j < nchunks; ++j) {
         ok &= mbar_wait_bounded(smem_addr(p_bar + j % kSBufs), (j / kSBufs) & 1);
@@ -500,23 +504,23 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 template <bool kBf16, int D>
-cudaError_t launch_prefill_t(const PrefillParams& p, const CUtensorMap& tk, const CUtensorMap& tv,
-                             int grid_x, cudaStream_t s) {
+cudaError_t launch_prefill_t(const PrefillParams& p, const CUtensorMap& tq, const CUtensorMap& tk,
+                             const CUtensorMap& tv, int grid_x, cudaStream_t s) {
   constexpr size_t smem = PrefillLayout<kBf16, D>::kSmem;
   cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(&prefill_kernel<kBf16, D>), smem);
   if (e != cudaSuccess) return e;
   const dim3 grid(grid_x, p.num_kv_heads, p.batch);
-  return launch_pdl(prefill_kernel<kBf16, D>, grid, dim3(kThreads), smem, s, p, tk, tv);
+  return launch_pdl(prefill_kernel<kBf16, D>, grid, dim3(kThreads), smem, s, p, tq, tk, tv);
 }
 
 }  // namespace
 
-cudaError_t launch_prefill(const PrefillParams& p, const CUtensorMap& tk, const CUtensorMap& tv,
-                           bool bf16, int grid_x, cudaStream_t s) {
-  if (!bf16 && p.head_dim == 64) return launch_prefill_t<false, 64>(p, tk, tv, grid_x, s);
-  if (!bf16 && p.head_dim == 128) return launch_prefill_t<false, 128>(p, tk, tv, grid_x, s);
-  if (bf16 && p.head_dim == 64) return launch_prefill_t<true, 64>(p, tk, tv, grid_x, s);
-  if (bf16 && p.head_dim == 128) return launch_prefill_t<true, 128>(p, tk, tv, grid_x, s);
+cudaError_t launch_prefill(const PrefillParams& p, const CUtensorMap& tq, const CUtensorMap& tk,
+                           const CUtensorMap& tv, bool bf16, int grid_x, cudaStream_t s) {
+  if (!bf16 && p.head_dim == 64) return launch_prefill_t<false, 64>(p, tq, tk, tv, grid_x, s);
+  if (!bf16 && p.head_dim == 128) return launch_prefill_t<false, 128>(p, tq, tk, tv, grid_x, s);
+  if (bf16 && p.head_dim == 64) return launch_prefill_t<true, 64>(p, tq, tk, tv, grid_x, s);
+  if (bf16 && p.head_dim == 128) return launch_prefill_t<true, 128>(p, tq, tk, tv, grid_x, s);
   return cudaErrorInvalidValue;
 }
 

@@ -214,3 +214,19 @@ def test_context_beyond_the_staged_table():
                                    w.query_start, w.scale, rows=rows)
     got = out.cpu()[torch.from_numpy(t).long(), torch.from_numpy(h).long()]
     assert_close(got, ref, "context beyond the staged table")
+
+
+def test_rows_past_num_query_tokens_set_status_and_write_nothing():
+    """query_start says request 1 owns rows 40..99 but q / out hold 60 rows:
+    the request is skipped (status), request 0 is computed normally."""
+    w = workloads.make_prefill(B=2, Hq=8, Hkv=2, D=128, lens=[40, 100], qlens=[40, 60],
+                               num_blocks=20, dtype=torch.float16, seed=12)
+    q = w.q[:60].clone()
+    out = torch.full((60, w.Hq, w.D), 5.0, dtype=w.dtype, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    run_gpu(w, status, out=out, q=q)
+    assert kvp.kvp_read_status(status) == kvp.KVP_ERR_BAD_BLOCK
+    assert bool((out[40:] == 5.0).all())
+    ref = oracle.attention_prefill(w.q[:40], w.k_pool, w.v_pool, w.block_tables[:1],
+                                   w.context_lens[:1], w.query_start[:2], w.scale)
+    assert_close(out[:40], ref, "request before the overflowing one")
