@@ -16,7 +16,8 @@
 //     in shared memory: TMA copies (128-byte swizzle, the layout the tensor
 //     core reads directly) issued by two producer warps, one per tensor.
 //   * One thread issues the tensor-core work: S = Q K^T (tcgen05.mma, M=128,
-//     N=64, K=D) into TMEM score buffers three chunks ahead of the softmax,
+//     N=64, K=D, Q held in TMEM so only K is read from shared memory) into
+//     TMEM score buffers two chunks ahead of the softmax,
 //     and O += P V (M=128, N=D, K=64) into TMEM accumulators, so the tensor
 //     core works while the CUDA cores exponentiate.
 //   * Two threads own each query row (TMEM lane): each takes 32 of every
@@ -61,7 +62,7 @@ struct PrefillLayout {
   // stage once its P V is; depths fill the shared memory left by Q and P.
   static constexpr int kKStages = D == 64 ? 8 : 5;
   static constexpr int kVStages = D == 64 ? 8 : 5;
-  static constexpr int kAhead = 3;                        // S computed 3 chunks ahead
+  static constexpr int kAhead = 2;                        // S computed 2 chunks ahead
   static constexpr int kSBufs = kAhead + 1;               // TMEM score (then P) buffers
   static constexpr uint32_t kQOff = 0;
   static constexpr uint32_t kKOff = kQ;
@@ -69,18 +70,19 @@ struct PrefillLayout {
   static constexpr uint32_t kRedOff = kVOff + kVStages * kKV;  // [2][kSplit][kRows] float
   static constexpr uint32_t kTblOff = kRedOff + 2 * kSplit * kRows * 4;  // [kTableCap] int32
   static constexpr uint32_t kBarOff = kTblOff + kTableCap * 4;
-  // kfull[], vfull[], kempty[], vempty[], s[], p[], pv[2], q
-  static constexpr int kBars = 2 * (kKStages + kVStages) + 2 * kSBufs + 3;
+  // kfull[], vfull[], kempty[], vempty[], s[], p[], pv[2], q, q in TMEM
+  static constexpr int kBars = 2 * (kKStages + kVStages) + 2 * kSBufs + 4;
   // + 1024 bytes of alignment slack, the barriers and the TMEM address slot
   static constexpr size_t kSmem = 1024 + kBarOff + kBars * 8 + 16;
   // TMEM columns: score buffer i at [64 i, 64 i + 64) (key half h's P is
   // written over its scores at [64 i + 32 h, +16), its bf16 residual at
-  // [64 i + 32 h + 16, +16)); the O accumulator of
-  // key half h at [256 + h D, 256 + (h+1) D).  The shared memory keeps a
-  // second CTA off the SM, so all 512 columns are free.
+  // [64 i + 32 h + 16, +16)); the Q tile (16-bit pairs) at [192, 192 + D/2);
+  // the O accumulator of key half h at [256 + h D, 256 + (h+1) D).  The
+  // shared memory keeps a second CTA off the SM, so all 512 columns are free.
+  static constexpr uint32_t kQCol = kSBufs * kKeys;
   static constexpr uint32_t kOCol = 256;
   static constexpr uint32_t kTmemCols = 512;
-  static_assert(kSBufs * kKeys <= static_cast<int>(kOCol), "score buffers overlap O");
+  static_assert(kQCol + D / 2 <= kOCol, "score buffers and Q overlap O");
   static_assert(kOCol + kSplit * D <= kTmemCols, "O accumulators exceed TMEM");
   static_assert(2 * (kSmem + 1024) > kSmemPerSm, "TMEM budget assumes one CTA per SM");
   static_assert(kSmem <= 232448, "exceeds the per-block shared-memory limit");
@@ -144,8 +146,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* s_bar = ve_bar + kVStages;                               // [kSBufs]
   uint64_t* p_bar = s_bar + kSBufs;                                  // [kSBufs]
   uint64_t* pv_bar = p_bar + kSBufs;                                 // [2]
-  uint64_t* q_bar = pv_bar + 2;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(q_bar + 1);
+  uint64_t* q_bar = pv_bar + 2;      // Q tile landed in shared memory
+  uint64_t* qt_bar = q_bar + 1;      // Q copied into TMEM (8 arrivals)
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(qt_bar + 1);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const bool mma_warp = warp == kMmaWarp;
@@ -190,6 +193,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(smem_addr(pv_bar), 1);
     mbar_init(smem_addr(pv_bar + 1), 1);
     mbar_init(smem_addr(q_bar), 1);
+    mbar_init(smem_addr(qt_bar), kSoftmaxWarps);
     fence_barrier_init();
     // ---- Q tile by TMA, straight into the K-major swizzled layout: a box of
     // (64 elements, G heads, 128 / G tokens) puts (token t, head g) at row
@@ -279,7 +283,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       // shared-memory descriptors are built once; an operand at byte offset o
       // from a base is the base descriptor plus o >> 4 (the start-address
       // field, which never carries: every address is below 256 KB)
-      const uint64_t q_desc = umma::smem_desc_sw128(smem_addr(sQ), 16, 1024);
       const uint64_t k_desc = umma::smem_desc_sw128(smem_addr(sm + L::kKOff), 16, 1024);
       const uint64_t v_desc = umma::smem_desc_sw128(smem_addr(sm + L::kVOff), kKeys * 128, 1024);
       auto issue_s = [&](int c) {  // wait for chunk c's K, S(c) = Q K(c)^T, free the K stage
@@ -290,9 +293,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (elect_one()) {
 #pragma unroll
           for (int s = 0; s < D / 16; ++s) {
-            const uint32_t qoff = (s >> 2) * (kRows * 128) + (s & 3) * 32;
             const uint32_t koff = (s >> 2) * (kKeys * 128) + (s & 3) * 32;
-            umma::mma_f16(d, q_desc + (qoff >> 4), kd + (koff >> 4), kIdS, s > 0 ? 1u : 0u);
+            umma::mma_f16_tmem_a(d, tmem + L::kQCol + s * 8, kd + (koff >> 4), kIdS,
+                                 s > 0 ? 1u : 0u);
           }
           umma::commit(smem_addr(s_bar + c % kSBufs));
           umma::commit(smem_addr(ke_bar + c % kKStages));
@@ -300,7 +303,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
       };
 
-      ok &= mbar_wait_bounded(smem_addr(q_bar), 0);
+      ok &= mbar_wait_bounded(smem_addr(qt_bar), 0);
+      umma::fence_after_sync();
       for (int c = 0; c < min(kAhead, nchunks); ++c) issue_s(c);
       for (int j = 0; j < nchunks; ++j) {
         ok &= mbar_wait_bounded(smem_addr(p_bar + j % kSBufs), (j / kSBufs) & 1);
@@ -346,6 +350,30 @@ __global__ void __launch_bounds__(kThreads, 1)
     float m = -INFINITY, l = 0.f;  // this key half's running max (log2 units) and sum
     const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
     const uint32_t tOp = tmem + L::kOCol + part * D + lane_base;  // this half's O row
+    {
+      // Q row `row`, elements [part * D/2, +D/2), from the swizzled tile into
+      // TMEM as 16-bit pairs (the A operand of S = Q K^T)
+      ok &= mbar_wait_bounded(smem_addr(q_bar), 0);
+#pragma unroll
+      for (int g = 0; g < D / 64; ++g) {
+        uint32_t w[16];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int c = part * (D / 16) + g * 4 + i;  // 16-byte chunk of the row
+          const uint4 v =
+              *reinterpret_cast<const uint4*>(sQ + (c >> 3) * (kRows * 128) + sw_chunk(row, c));
+          w[4 * i] = v.x;
+          w[4 * i + 1] = v.y;
+          w[4 * i + 2] = v.z;
+          w[4 * i + 3] = v.w;
+        }
+        umma::st16_bits(tmem + L::kQCol + part * (D / 4) + g * 16 + lane_base, w);
+      }
+      umma::wait_st();
+      umma::fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_addr(qt_bar));
+    }
     auto o_scale = [&](float alpha) {  // this half's O row *= alpha
 #pragma unroll
       for (int c = 0; c < D / 32; ++c) {
