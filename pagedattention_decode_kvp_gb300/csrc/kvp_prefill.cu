@@ -43,7 +43,7 @@ namespace {
 constexpr int kRows = 128;                            // M: query rows per CTA
 constexpr int kKeys = 64;                             // key tokens per chunk (4 blocks)
 constexpr int kSplit = 2;                             // softmax threads per query row
-constexpr int kKeysPerThread = kKeys / kSplit;        // 32 keys of each chunk
+constexpr int kKeysPerThread = kKeys / kSplit;        // keys of each chunk per thread
 constexpr int kSoftmaxWarps = 4 * kSplit;             // kSplit per TMEM lane quarter
 constexpr int kSoftmaxThreads = kSoftmaxWarps * 32;
 constexpr int kMmaWarp = kSoftmaxWarps;               // issues the tensor-core work
@@ -60,9 +60,9 @@ struct PrefillLayout {
   static constexpr uint32_t kKV = kKeys * D * 2;          // one K or V tile
   // Separate K and V rings: a K stage is free once its S is computed, a V
   // stage once its P V is; depths fill the shared memory left by Q and P.
-  static constexpr int kKStages = D == 64 ? 8 : 5;
-  static constexpr int kVStages = D == 64 ? 8 : 5;
-  static constexpr int kAhead = 2;                        // S computed 2 chunks ahead
+  static constexpr int kKStages = kKeys == 64 ? (D == 64 ? 8 : 5) : (D == 64 ? 5 : 3);
+  static constexpr int kVStages = kKeys == 64 ? (D == 64 ? 8 : 5) : (D == 64 ? 5 : 2);
+  static constexpr int kAhead = kKeys == 64 ? 2 : 1;      // chunks S runs ahead
   static constexpr int kSBufs = kAhead + 1;               // TMEM score (then P) buffers
   static constexpr uint32_t kQOff = 0;
   static constexpr uint32_t kKOff = kQ;
@@ -82,7 +82,11 @@ struct PrefillLayout {
   static constexpr uint32_t kQCol = kSBufs * kKeys;
   static constexpr uint32_t kOCol = 256;
   static constexpr uint32_t kTmemCols = 512;
-  static_assert(kQCol + D / 2 <= kOCol, "score buffers and Q overlap O");
+  // Q goes to TMEM when it fits beside the score buffers (an N=64 score MMA
+  // reading both operands from shared memory is bound by its bandwidth; at
+  // N=128 the two are balanced and Q stays in shared memory)
+  static constexpr bool kQInTmem = kQCol + D / 2 <= kOCol;
+  static_assert(kQCol <= kOCol, "score buffers overlap O");
   static_assert(kOCol + kSplit * D <= kTmemCols, "O accumulators exceed TMEM");
   static_assert(2 * (kSmem + 1024) > kSmemPerSm, "TMEM budget assumes one CTA per SM");
   static_assert(kSmem <= 232448, "exceeds the per-block shared-memory limit");
@@ -283,6 +287,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // shared-memory descriptors are built once; an operand at byte offset o
       // from a base is the base descriptor plus o >> 4 (the start-address
       // field, which never carries: every address is below 256 KB)
+      const uint64_t q_desc = umma::smem_desc_sw128(smem_addr(sQ), 16, 1024);
       const uint64_t k_desc = umma::smem_desc_sw128(smem_addr(sm + L::kKOff), 16, 1024);
       const uint64_t v_desc = umma::smem_desc_sw128(smem_addr(sm + L::kVOff), kKeys * 128, 1024);
       auto issue_s = [&](int c) {  // wait for chunk c's K, S(c) = Q K(c)^T, free the K stage
@@ -294,8 +299,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int s = 0; s < D / 16; ++s) {
             const uint32_t koff = (s >> 2) * (kKeys * 128) + (s & 3) * 32;
-            umma::mma_f16_tmem_a(d, tmem + L::kQCol + s * 8, kd + (koff >> 4), kIdS,
-                                 s > 0 ? 1u : 0u);
+            if constexpr (L::kQInTmem) {
+              umma::mma_f16_tmem_a(d, tmem + L::kQCol + s * 8, kd + (koff >> 4), kIdS,
+                                   s > 0 ? 1u : 0u);
+            } else {
+              const uint32_t qoff = (s >> 2) * (kRows * 128) + (s & 3) * 32;
+              umma::mma_f16(d, q_desc + (qoff >> 4), kd + (koff >> 4), kIdS, s > 0 ? 1u : 0u);
+            }
           }
           umma::commit(smem_addr(s_bar + c % kSBufs));
           umma::commit(smem_addr(ke_bar + c % kKStages));
@@ -303,7 +313,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
       };
 
-      ok &= mbar_wait_bounded(smem_addr(qt_bar), 0);
+      ok &= mbar_wait_bounded(smem_addr(L::kQInTmem ? qt_bar : q_bar), 0);
       umma::fence_after_sync();
       for (int c = 0; c < min(kAhead, nchunks); ++c) issue_s(c);
       for (int j = 0; j < nchunks; ++j) {
@@ -350,7 +360,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     float m = -INFINITY, l = 0.f;  // this key half's running max (log2 units) and sum
     const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
     const uint32_t tOp = tmem + L::kOCol + part * D + lane_base;  // this half's O row
-    {
+    if constexpr (L::kQInTmem) {
       // Q row `row`, elements [part * D/2, +D/2), from the swizzled tile into
       // TMEM as 16-bit pairs (the A operand of S = Q K^T)
       ok &= mbar_wait_bounded(smem_addr(q_bar), 0);
