@@ -41,7 +41,7 @@ namespace kvp {
 namespace {
 
 constexpr int kRows = 128;                            // M: query rows per CTA
-constexpr int kKeys = 64;                             // key tokens per chunk (4 blocks)
+constexpr int kKeys = 128;                            // key tokens per chunk (8 blocks)
 constexpr int kSplit = 2;                             // softmax threads per query row
 constexpr int kKeysPerThread = kKeys / kSplit;        // keys of each chunk per thread
 constexpr int kSoftmaxWarps = 4 * kSplit;             // kSplit per TMEM lane quarter
@@ -62,13 +62,13 @@ struct PrefillLayout {
   // stage once its P V is; depths fill the shared memory left by Q and P.
   static constexpr int kKStages = kKeys == 64 ? (D == 64 ? 8 : 5) : (D == 64 ? 5 : 3);
   static constexpr int kVStages = kKeys == 64 ? (D == 64 ? 8 : 5) : (D == 64 ? 5 : 2);
-  static constexpr int kAhead = kKeys == 64 ? 2 : 1;      // chunks S runs ahead
+  static constexpr int kAhead = 2;                        // chunks S runs ahead
   static constexpr int kSBufs = kAhead + 1;               // TMEM score (then P) buffers
   static constexpr uint32_t kQOff = 0;
   static constexpr uint32_t kKOff = kQ;
   static constexpr uint32_t kVOff = kKOff + kKStages * kKV;
-  static constexpr uint32_t kRedOff = kVOff + kVStages * kKV;  // [2][kSplit][kRows] float
-  static constexpr uint32_t kTblOff = kRedOff + 2 * kSplit * kRows * 4;  // [kTableCap] int32
+  static constexpr uint32_t kRedOff = kVOff + kVStages * kKV;  // [4][kSplit][kRows] float
+  static constexpr uint32_t kTblOff = kRedOff + 4 * kSplit * kRows * 4;  // [kTableCap] int32
   static constexpr uint32_t kBarOff = kTblOff + kTableCap * 4;
   // kfull[], vfull[], kempty[], vempty[], s[], p[], pv[2], q, q in TMEM
   static constexpr int kBars = 2 * (kKStages + kVStages) + 2 * kSBufs + 4;
@@ -79,15 +79,18 @@ struct PrefillLayout {
   // [64 i + 32 h + 16, +16)); the Q tile (16-bit pairs) at [192, 192 + D/2);
   // the O accumulator of key half h at [256 + h D, 256 + (h+1) D).  The
   // shared memory keeps a second CTA off the SM, so all 512 columns are free.
+  // 128-key chunks share one O accumulator between a row's two threads (their
+  // row max is exchanged once per chunk); 64-key chunks keep one per thread
+  static constexpr bool kSharedO = kKeys > 64;
   static constexpr uint32_t kQCol = kSBufs * kKeys;
-  static constexpr uint32_t kOCol = 256;
+  static constexpr uint32_t kOCol = kSharedO ? kSBufs * kKeys : 256;
   static constexpr uint32_t kTmemCols = 512;
   // Q goes to TMEM when it fits beside the score buffers (an N=64 score MMA
   // reading both operands from shared memory is bound by its bandwidth; at
   // N=128 the two are balanced and Q stays in shared memory)
   static constexpr bool kQInTmem = kQCol + D / 2 <= kOCol;
   static_assert(kQCol <= kOCol, "score buffers overlap O");
-  static_assert(kOCol + kSplit * D <= kTmemCols, "O accumulators exceed TMEM");
+  static_assert(kOCol + (kSharedO ? 1 : kSplit) * D <= kTmemCols, "O accumulators exceed TMEM");
   static_assert(2 * (kSmem + 1024) > kSmemPerSm, "TMEM budget assumes one CTA per SM");
   static_assert(kSmem <= 232448, "exceeds the per-block shared-memory limit");
 };
@@ -323,15 +326,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t pa = tmem + (j % kSBufs) * kKeys;  // P of chunk j (TMEM)
         const uint64_t vd = v_desc + (((j % kVStages) * L::kKV) >> 4);
         if (elect_one()) {
-          // key half h (16-key steps t = 0, 1) into O accumulator h
+          // key half h (16-key steps t) into O accumulator h (or the shared one)
 #pragma unroll
           for (int h = 0; h < kSplit; ++h) {
 #pragma unroll
             for (int t = 0; t < kKeysPerThread / 16; ++t) {
-              const uint32_t o_acc = tmem + L::kOCol + h * D;
+              const uint32_t o_acc = tmem + L::kOCol + (L::kSharedO ? 0 : h * D);
               const uint32_t a = pa + h * kKeysPerThread + t * 8;
               const uint64_t b = vd + (((h * kKeysPerThread + t * 16) * 128) >> 4);
-              umma::mma_f16_tmem_a(o_acc, a, b, kIdO, (j > 0 || t > 0) ? 1u : 0u);
+              const bool first = j == 0 && t == 0 && (!L::kSharedO || h == 0);
+              umma::mma_f16_tmem_a(o_acc, a, b, kIdO, first ? 0u : 1u);
               if constexpr (kBf16)
                 umma::mma_f16_tmem_a(o_acc, a + kKeysPerThread / 2, b, kIdO, 1u);
             }
@@ -359,7 +363,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     const float mul = pos_scale ? sl2 : 1.0f;
     float m = -INFINITY, l = 0.f;  // this key half's running max (log2 units) and sum
     const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
-    const uint32_t tOp = tmem + L::kOCol + part * D + lane_base;  // this half's O row
+    // the O columns this thread rescales: its own accumulator's row, or its
+    // half of the shared accumulator's row
+    constexpr int kOCols = L::kSharedO ? D / 2 : D;
+    const uint32_t tOp =
+        tmem + L::kOCol + (L::kSharedO ? part * (D / 2) : part * D) + lane_base;
     if constexpr (L::kQInTmem) {
       // Q row `row`, elements [part * D/2, +D/2), from the swizzled tile into
       // TMEM as 16-bit pairs (the A operand of S = Q K^T)
@@ -384,9 +392,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_addr(qt_bar));
     }
-    auto o_scale = [&](float alpha) {  // this half's O row *= alpha
+    auto o_scale = [&](float alpha) {  // this thread's O columns *= alpha
 #pragma unroll
-      for (int c = 0; c < D / 32; ++c) {
+      for (int c = 0; c < kOCols / 32; ++c) {
         float o[32];
         umma::ld32(tOp + c * 32, o);
         umma::wait_ld();
@@ -425,7 +433,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         mx2 = fmaxf(mx2, fmaxf(s[k + 4], s[k + 5]));
         mx3 = fmaxf(mx3, fmaxf(s[k + 6], s[k + 7]));
       }
-      const float rowmax = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * mul;
+      float rowmax = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * mul;
+      if constexpr (L::kSharedO) {  // one max per row: the partner holds the other keys
+        float* rb = red + (j & 1) * (kSplit * kRows);
+        rb[part * kRows + row] = rowmax;
+        named_bar_sync(1 + quarter, 32 * kSplit);
+        rowmax = fmaxf(rowmax, rb[(1 - part) * kRows + row]);
+      }
       const float mnew = fmaxf(m, rowmax);
       const bool grow = mnew > m + 8.0f;  // lazy: rescale only when the max grows by > 2^8
       const float alpha = grow ? ex2_approx(m - mnew) : 1.0f;
@@ -496,7 +510,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     launch_dependents();
     // ---- merge the two halves' (max, sum, O); thread (row, part) writes
     // output columns [part * D/2, +D/2)
-    float* rb = red;  // [2 (max, sum)][kSplit][kRows]
+    float* rb = red + 2 * kSplit * kRows;  // [2 (max, sum)][kSplit][kRows]
     rb[part * kRows + row] = m;
     rb[(kSplit + part) * kRows + row] = l;
     named_bar_sync(1 + quarter, 32 * kSplit);
@@ -517,7 +531,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int c = 0; c < D / 64; ++c) {
       float a0[32], a1[32];
       umma::ld32(tO0 + c * 32, a0);
-      umma::ld32(tO0 + D + c * 32, a1);
+      if constexpr (L::kSharedO) {  // one accumulator, equal maxima: c0 = c1
+#pragma unroll
+        for (int e = 0; e < 32; ++e) a1[e] = 0.f;
+      } else {
+        umma::ld32(tO0 + D + c * 32, a1);
+      }
       umma::wait_ld();
       if (row_valid) {
 #pragma unroll
