@@ -62,7 +62,9 @@ struct PrefillLayout {
   // stage once its P V is; depths fill the shared memory left by Q and P.
   static constexpr int kKStages = kKeys == 64 ? (D == 64 ? 8 : 5) : (D == 64 ? 5 : 3);
   static constexpr int kVStages = kKeys == 64 ? (D == 64 ? 8 : 5) : (D == 64 ? 5 : 2);
-  static constexpr int kAhead = 2;                        // chunks S runs ahead
+  // chunks S runs ahead of the softmax (the MMA thread issues S(j + kAhead)
+  // before it waits for the softmax of chunk j)
+  static constexpr int kAhead = kKeys > 64 ? 1 : 2;
   static constexpr int kSBufs = kAhead + 1;               // TMEM score (then P) buffers
   static constexpr uint32_t kQOff = 0;
   static constexpr uint32_t kKOff = kQ;
@@ -74,16 +76,18 @@ struct PrefillLayout {
   static constexpr int kBars = 2 * (kKStages + kVStages) + 2 * kSBufs + 4;
   // + 1024 bytes of alignment slack, the barriers and the TMEM address slot
   static constexpr size_t kSmem = 1024 + kBarOff + kBars * 8 + 16;
-  // TMEM columns: score buffer i at [64 i, 64 i + 64) (key half h's P is
-  // written over its scores at [64 i + 32 h, +16), its bf16 residual at
-  // [64 i + 32 h + 16, +16)); the Q tile (16-bit pairs) at [192, 192 + D/2);
-  // the O accumulator of key half h at [256 + h D, 256 + (h+1) D).  The
-  // shared memory keeps a second CTA off the SM, so all 512 columns are free.
-  // 128-key chunks share one O accumulator between a row's two threads (their
-  // row max is exchanged once per chunk); 64-key chunks keep one per thread
+  // TMEM columns: score buffer i at [kKeys i, kKeys (i+1)) (key half h's P
+  // is written over its own scores at [kKeys i + kKeys/2 h, +kKeys/4), its
+  // bf16 residual right after); then the Q tile (16-bit pairs, D/2 columns)
+  // when it fits; the O accumulator(s) at kOCol.  The shared memory keeps a
+  // second CTA off the SM, so all 512 columns are free.
+  // 128-key chunks (two score buffers, Q at 256, O at 512 - D) share one O
+  // accumulator between a row's two threads, whose row max is exchanged once
+  // per chunk; 64-key chunks (three buffers, Q at 192, O at 256) keep one O
+  // accumulator per thread (at 256 + h D).
   static constexpr bool kSharedO = kKeys > 64;
   static constexpr uint32_t kQCol = kSBufs * kKeys;
-  static constexpr uint32_t kOCol = kSharedO ? kSBufs * kKeys : 256;
+  static constexpr uint32_t kOCol = kSharedO ? 512 - D : 256;
   static constexpr uint32_t kTmemCols = 512;
   // Q goes to TMEM when it fits beside the score buffers (an N=64 score MMA
   // reading both operands from shared memory is bound by its bandwidth; at
@@ -125,10 +129,10 @@ __device__ __forceinline__ void zero_tile_rows(const PrefillParams& p, int kvh, 
 //   s[c % kSBufs]         MMA -> softmax      S of chunk c in TMEM buffer c % kSBufs
 //   p[c % kSBufs]         softmax -> MMA      P of chunk c written over it (8 arrivals)
 //   pv[c % 2]             MMA -> softmax, MMA O += P V of chunk c complete
-// Per chunk j the MMA thread waits p(j) and V(j), issues P V(j), then -- once
-// P V(j-1) has read its P -- S(j + kAhead) into chunk j-1's buffer.  The
-// softmax of chunk j needs only S(j); O is touched (lazy rescale, after
-// P V(j-1)) only when a row's max jumps.  The producers start as soon as the
+// Per chunk j the MMA thread -- once P V(j-1) has read its P -- issues
+// S(j + kAhead) into chunk j-1's buffer, then waits p(j) and V(j) and issues
+// P V(j).  The softmax of chunk j needs only S(j); O is touched (lazy rescale,
+// after P V(j-1)) only when a row's max jumps.  The producers start as soon as the
 // block table is on chip, while the softmax warps load Q.
 template <bool kBf16, int D>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -320,6 +324,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       umma::fence_after_sync();
       for (int c = 0; c < min(kAhead, nchunks); ++c) issue_s(c);
       for (int j = 0; j < nchunks; ++j) {
+        // S(j+kAhead) goes over chunk j-1's P: once P V(j-1) has read it, the
+        // tensor core computes it while the softmax works on chunk j
+        if (j + kAhead < nchunks) {
+          if (j >= 1)
+            ok &= mbar_wait_bounded(smem_addr(pv_bar + ((j - 1) & 1)), ((j - 1) >> 1) & 1);
+          issue_s(j + kAhead);
+        }
         ok &= mbar_wait_bounded(smem_addr(p_bar + j % kSBufs), (j / kSBufs) & 1);
         ok &= mbar_wait_bounded(smem_addr(vf_bar + j % kVStages), (j / kVStages) & 1);
         umma::fence_after_sync();
@@ -344,12 +355,6 @@ __global__ void __launch_bounds__(kThreads, 1)
           umma::commit(smem_addr(ve_bar + j % kVStages));
         }
         __syncwarp();
-        // S(j+kAhead) goes over chunk j-1's P: wait until P V(j-1) has read it
-        if (j + kAhead < nchunks) {
-          if (j >= 1)
-            ok &= mbar_wait_bounded(smem_addr(pv_bar + ((j - 1) & 1)), ((j - 1) >> 1) & 1);
-          issue_s(j + kAhead);
-        }
       }
     }
     __syncwarp();
