@@ -109,3 +109,29 @@ def test_product_fails_loudly_without_library(monkeypatch, tmp_path):
     monkeypatch.setattr(kvp, "LIB_PATH", str(tmp_path / "missing.so"))
     with pytest.raises(RuntimeError, match="not built"):
         kvp.load_library()
+
+
+def test_prefill_invalid_arguments_fail_before_any_launch(lib):
+    P = None
+    inf = float("inf")
+
+    def call(hq=8, d=None, T=64, batch=2, mql=32, scale=0.125, dtype=0):
+        desc = _desc() if d is None else d
+        return lib.kvp_attention_prefill(P, P, P, P, P, 16, P, P, T, batch, hq, mql, scale, desc,
+                                         dtype, P, P)
+    # group (Hq / Hkv) must divide the 128-row tile; Hq must be a multiple of Hkv
+    assert call(hq=_desc().num_kv_heads * 3) == kvp.KVP_ERR_UNSUPPORTED
+    assert call(hq=_desc().num_kv_heads + 1) == kvp.KVP_ERR_INVALID_ARG
+    # unsupported head_dim / block size, bad dtype, non-finite scale, negative sizes
+    assert call(d=_desc(d=80)) == kvp.KVP_ERR_UNSUPPORTED
+    assert call(d=_desc(bs=32)) == kvp.KVP_ERR_UNSUPPORTED
+    assert call(dtype=2) == kvp.KVP_ERR_INVALID_ARG
+    assert call(scale=inf) == kvp.KVP_ERR_INVALID_ARG
+    assert call(T=-1) == kvp.KVP_ERR_INVALID_ARG
+    assert call(mql=-1) == kvp.KVP_ERR_INVALID_ARG
+    # null buffers with work to do
+    assert call() == kvp.KVP_ERR_INVALID_ARG
+    # nothing to do: no-ops even with null buffers
+    assert call(batch=0) == kvp.KVP_OK
+    assert call(mql=0) == kvp.KVP_OK
+    assert call(T=0) == kvp.KVP_OK
