@@ -7,32 +7,33 @@
 // chunk's queries (their K/V already appended); query i of the chunk sits at
 // position n - L + i and attends causally to positions 0 .. n - L + i through
 // the block table.  Unlike the decode, this is a dense contraction: a 128-row
-// query tile against 64-key tiles.
+// query tile against 128-key tiles.
 //
 // Design (one CTA of 11 warps per (request, kv head, 128-row query tile)):
 //   * Tile rows are (query token, query head of the kv head's group) pairs, so
 //     every K/V byte a tile reads serves the whole GQA group.
-//   * K/V arrive in 64-key chunks (4 blocks) through separate K and V rings
+//   * K/V arrive in 128-key chunks (8 blocks) through separate K and V rings
 //     in shared memory: TMA copies (128-byte swizzle, the layout the tensor
 //     core reads directly) issued by two producer warps, one per tensor.
 //   * One thread issues the tensor-core work: S = Q K^T (tcgen05.mma, M=128,
-//     N=64, K=D, Q held in TMEM so only K is read from shared memory) into
-//     TMEM score buffers two chunks ahead of the softmax,
-//     and O += P V (M=128, N=D, K=64) into TMEM accumulators, so the tensor
-//     core works while the CUDA cores exponentiate.
-//   * Two threads own each query row (TMEM lane): each takes 32 of every
-//     chunk's 64 keys, applies the causal mask and the scale, and keeps its own
-//     running max and sum in registers, with its own O accumulator in TMEM
-//     (P V is split by key half) -- no exchange between them until the end,
-//     where the two (max, sum, O) are merged.  The running max is updated
-//     lazily: only when it grows by more than 2^8 is the O accumulator
-//     rescaled in TMEM (exact: numerator and denominator share the stale max).
-//   * P stays in tensor memory: each thread writes its 32 probabilities,
+//     N=128, K=D; Q held in TMEM so only K is read from shared memory) into
+//     one of two TMEM score buffers -- S of chunk j+1 is issued before the
+//     softmax of chunk j is awaited -- and O += P V (M=128, N=D, K=128) into
+//     a TMEM accumulator, so the tensor core works while the CUDA cores
+//     exponentiate.
+//   * Two threads own each query row (TMEM lane): each takes 64 of every
+//     chunk's 128 keys, applies the causal mask and the scale; the two
+//     exchange their chunk max once per chunk, keep the row's running max and
+//     their partial sums in registers, and share one O accumulator in TMEM
+//     (each rescales half of its columns).  The running max is updated
+//     lazily: only when it grows by more than 2^8 is O rescaled (exact:
+//     numerator and denominator share the stale max).
+//   * P stays in tensor memory: each thread writes its 64 probabilities,
 //     packed as 16-bit pairs, over the scores it has read (fp16; bf16 as a
 //     high part plus a bf16 residual so P keeps ~16 bits), and P V takes its
 //     A operand from TMEM -- no shared-memory round trip, no proxy fence.
-//   * At the end the two threads of a row merge their (max, sum, O) and each
-//     writes half of the output row.
+//   * At the end the two threads of a row add their sums and each writes half
+//     of the output row.
 #include "kvp_device.cuh"
 #include "kvp_internal.h"
 #include "kvp_umma.cuh"
@@ -42,6 +43,8 @@ namespace {
 
 constexpr int kRows = 128;                            // M: query rows per CTA
 constexpr int kKeys = 128;                            // key tokens per chunk (8 blocks)
+// (64-key chunks were measured slower: an N = 64 score MMA costs nearly as
+// much as an N = 128 one, so per key the single issuing thread does more)
 constexpr int kSplit = 2;                             // softmax threads per query row
 constexpr int kKeysPerThread = kKeys / kSplit;        // keys of each chunk per thread
 constexpr int kSoftmaxWarps = 4 * kSplit;             // kSplit per TMEM lane quarter
@@ -59,12 +62,12 @@ struct PrefillLayout {
   static constexpr uint32_t kQ = kRows * D * 2;           // Q tile
   static constexpr uint32_t kKV = kKeys * D * 2;          // one K or V tile
   // Separate K and V rings: a K stage is free once its S is computed, a V
-  // stage once its P V is; depths fill the shared memory left by Q and P.
-  static constexpr int kKStages = kKeys == 64 ? (D == 64 ? 8 : 5) : (D == 64 ? 5 : 3);
-  static constexpr int kVStages = kKeys == 64 ? (D == 64 ? 8 : 5) : (D == 64 ? 5 : 2);
-  // chunks S runs ahead of the softmax (the MMA thread issues S(j + kAhead)
-  // before it waits for the softmax of chunk j)
-  static constexpr int kAhead = kKeys > 64 ? 1 : 2;
+  // stage once its P V is; depths fill the shared memory left by Q.
+  static constexpr int kKStages = D == 64 ? 5 : 3;
+  static constexpr int kVStages = D == 64 ? 5 : 2;
+  // S runs one chunk ahead of the softmax: the MMA thread issues S(j + 1)
+  // before it waits for the softmax of chunk j
+  static constexpr int kAhead = 1;
   static constexpr int kSBufs = kAhead + 1;               // TMEM score (then P) buffers
   static constexpr uint32_t kQOff = 0;
   static constexpr uint32_t kKOff = kQ;
@@ -76,25 +79,16 @@ struct PrefillLayout {
   static constexpr int kBars = 2 * (kKStages + kVStages) + 2 * kSBufs + 4;
   // + 1024 bytes of alignment slack, the barriers and the TMEM address slot
   static constexpr size_t kSmem = 1024 + kBarOff + kBars * 8 + 16;
-  // TMEM columns: score buffer i at [kKeys i, kKeys (i+1)) (key half h's P
-  // is written over its own scores at [kKeys i + kKeys/2 h, +kKeys/4), its
-  // bf16 residual right after); then the Q tile (16-bit pairs, D/2 columns)
-  // when it fits; the O accumulator(s) at kOCol.  The shared memory keeps a
-  // second CTA off the SM, so all 512 columns are free.
-  // 128-key chunks (two score buffers, Q at 256, O at 512 - D) share one O
-  // accumulator between a row's two threads, whose row max is exchanged once
-  // per chunk; 64-key chunks (three buffers, Q at 192, O at 256) keep one O
-  // accumulator per thread (at 256 + h D).
-  static constexpr bool kSharedO = kKeys > 64;
+  // TMEM columns: score buffer i at [128 i, 128 (i+1)) (key half h's P is
+  // written over its own scores at [128 i + 64 h, +32), its bf16 residual
+  // right after); the Q tile (16-bit pairs) at [256, 256 + D/2), so the score
+  // MMAs read only K from shared memory; the O accumulator, shared by a row's
+  // two threads, at [512 - D, 512).  The shared memory keeps a second CTA off
+  // the SM, so all 512 columns are free.
   static constexpr uint32_t kQCol = kSBufs * kKeys;
-  static constexpr uint32_t kOCol = kSharedO ? 512 - D : 256;
+  static constexpr uint32_t kOCol = 512 - D;
   static constexpr uint32_t kTmemCols = 512;
-  // Q goes to TMEM when it fits beside the score buffers (an N=64 score MMA
-  // reading both operands from shared memory is bound by its bandwidth; at
-  // N=128 the two are balanced and Q stays in shared memory)
-  static constexpr bool kQInTmem = kQCol + D / 2 <= kOCol;
-  static_assert(kQCol <= kOCol, "score buffers overlap O");
-  static_assert(kOCol + (kSharedO ? 1 : kSplit) * D <= kTmemCols, "O accumulators exceed TMEM");
+  static_assert(kQCol + D / 2 <= kOCol, "score buffers and Q overlap O");
   static_assert(2 * (kSmem + 1024) > kSmemPerSm, "TMEM budget assumes one CTA per SM");
   static_assert(kSmem <= 232448, "exceeds the per-block shared-memory limit");
 };
@@ -116,10 +110,9 @@ __device__ __forceinline__ void zero_tile_rows(const PrefillParams& p, int kvh, 
 }
 
 // Warp roles: warps 0-7 run the softmax -- warp w serves query rows
-// 32*(w%4) .. +31 (the TMEM lanes it may access) for keys [32*(w/4), +32) of
-// each chunk, accumulated into O accumulator w/4; warp 8 issues the
-// tensor-core instructions; warps 9 and 10 are producers of the K and the V
-// tiles.  The MMA and producer warps run their loops converged (waits and
+// 32*(w%4) .. +31 (the TMEM lanes it may access) for keys [64*(w/4), +64) of
+// each chunk and O columns [D/2*(w/4), +D/2); warp 8 issues the tensor-core
+// instructions; warps 9 and 10 are producers of the K and the V tiles.  The MMA and producer warps run their loops converged (waits and
 // address arithmetic warp-uniform) and issue from one elected lane.
 // Hand-offs (mbarriers; every wait is at most one phase behind its barrier):
 //   kfull[c % kKStages]   producer -> MMA     chunk c's K landed (1 arrival + bytes)
@@ -294,7 +287,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       // shared-memory descriptors are built once; an operand at byte offset o
       // from a base is the base descriptor plus o >> 4 (the start-address
       // field, which never carries: every address is below 256 KB)
-      const uint64_t q_desc = umma::smem_desc_sw128(smem_addr(sQ), 16, 1024);
       const uint64_t k_desc = umma::smem_desc_sw128(smem_addr(sm + L::kKOff), 16, 1024);
       const uint64_t v_desc = umma::smem_desc_sw128(smem_addr(sm + L::kVOff), kKeys * 128, 1024);
       auto issue_s = [&](int c) {  // wait for chunk c's K, S(c) = Q K(c)^T, free the K stage
@@ -306,13 +298,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int s = 0; s < D / 16; ++s) {
             const uint32_t koff = (s >> 2) * (kKeys * 128) + (s & 3) * 32;
-            if constexpr (L::kQInTmem) {
-              umma::mma_f16_tmem_a(d, tmem + L::kQCol + s * 8, kd + (koff >> 4), kIdS,
-                                   s > 0 ? 1u : 0u);
-            } else {
-              const uint32_t qoff = (s >> 2) * (kRows * 128) + (s & 3) * 32;
-              umma::mma_f16(d, q_desc + (qoff >> 4), kd + (koff >> 4), kIdS, s > 0 ? 1u : 0u);
-            }
+            umma::mma_f16_tmem_a(d, tmem + L::kQCol + s * 8, kd + (koff >> 4), kIdS,
+                                 s > 0 ? 1u : 0u);
           }
           umma::commit(smem_addr(s_bar + c % kSBufs));
           umma::commit(smem_addr(ke_bar + c % kKStages));
@@ -320,7 +307,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
       };
 
-      ok &= mbar_wait_bounded(smem_addr(L::kQInTmem ? qt_bar : q_bar), 0);
+      ok &= mbar_wait_bounded(smem_addr(qt_bar), 0);
       umma::fence_after_sync();
       for (int c = 0; c < min(kAhead, nchunks); ++c) issue_s(c);
       for (int j = 0; j < nchunks; ++j) {
@@ -337,15 +324,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t pa = tmem + (j % kSBufs) * kKeys;  // P of chunk j (TMEM)
         const uint64_t vd = v_desc + (((j % kVStages) * L::kKV) >> 4);
         if (elect_one()) {
-          // key half h (16-key steps t) into O accumulator h (or the shared one)
+          // key half h (16-key steps t), P read where thread (row, h) wrote it
 #pragma unroll
           for (int h = 0; h < kSplit; ++h) {
 #pragma unroll
             for (int t = 0; t < kKeysPerThread / 16; ++t) {
-              const uint32_t o_acc = tmem + L::kOCol + (L::kSharedO ? 0 : h * D);
+              const uint32_t o_acc = tmem + L::kOCol;
               const uint32_t a = pa + h * kKeysPerThread + t * 8;
               const uint64_t b = vd + (((h * kKeysPerThread + t * 16) * 128) >> 4);
-              const bool first = j == 0 && t == 0 && (!L::kSharedO || h == 0);
+              const bool first = j == 0 && h == 0 && t == 0;
               umma::mma_f16_tmem_a(o_acc, a, b, kIdO, first ? 0u : 1u);
               if constexpr (kBf16)
                 umma::mma_f16_tmem_a(o_acc, a + kKeysPerThread / 2, b, kIdO, 1u);
@@ -368,12 +355,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     const float mul = pos_scale ? sl2 : 1.0f;
     float m = -INFINITY, l = 0.f;  // this key half's running max (log2 units) and sum
     const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
-    // the O columns this thread rescales: its own accumulator's row, or its
-    // half of the shared accumulator's row
-    constexpr int kOCols = L::kSharedO ? D / 2 : D;
-    const uint32_t tOp =
-        tmem + L::kOCol + (L::kSharedO ? part * (D / 2) : part * D) + lane_base;
-    if constexpr (L::kQInTmem) {
+    // the O columns this thread rescales and writes: its half of the row
+    constexpr int kOCols = D / 2;
+    const uint32_t tOp = tmem + L::kOCol + part * (D / 2) + lane_base;
+    {
       // Q row `row`, elements [part * D/2, +D/2), from the swizzled tile into
       // TMEM as 16-bit pairs (the A operand of S = Q K^T)
       ok &= mbar_wait_bounded(smem_addr(q_bar), 0);
@@ -439,7 +424,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         mx3 = fmaxf(mx3, fmaxf(s[k + 6], s[k + 7]));
       }
       float rowmax = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * mul;
-      if constexpr (L::kSharedO) {  // one max per row: the partner holds the other keys
+      {  // one max per row: the partner thread holds the row's other keys
         float* rb = red + (j & 1) * (kSplit * kRows);
         rb[part * kRows + row] = rowmax;
         named_bar_sync(1 + quarter, 32 * kSplit);
@@ -513,47 +498,31 @@ __global__ void __launch_bounds__(kThreads, 1)
     ok &= mbar_wait_bounded(smem_addr(pv_bar + ((nchunks - 1) & 1)), ((nchunks - 1) >> 1) & 1);
     umma::fence_after_sync();
     launch_dependents();
-    // ---- merge the two halves' (max, sum, O); thread (row, part) writes
-    // output columns [part * D/2, +D/2)
-    float* rb = red + 2 * kSplit * kRows;  // [2 (max, sum)][kSplit][kRows]
-    rb[part * kRows + row] = m;
-    rb[(kSplit + part) * kRows + row] = l;
+    // ---- the row's sum over both key halves (their max is shared), then
+    // out = O / l; thread (row, part) writes output columns [part * D/2, +D/2)
+    float* rb = red + 2 * kSplit * kRows;
+    rb[part * kRows + row] = l;
     named_bar_sync(1 + quarter, 32 * kSplit);
-    const float m0 = rb[row], m1 = rb[kRows + row];
-    const float mm = fmaxf(m0, m1);
-    const float w0 = m0 == -INFINITY ? 0.f : ex2_approx(m0 - mm);
-    const float w1 = m1 == -INFINITY ? 0.f : ex2_approx(m1 - mm);
-    const float lt = rb[kSplit * kRows + row] * w0 + rb[(kSplit + 1) * kRows + row] * w1;
+    const float lt = rb[row] + rb[kRows + row];
     const float inv = (row_valid && lt > 0.f) ? 1.0f / lt : 0.f;
-    const float c0 = w0 * inv, c1 = w1 * inv;
     uint16_t* out = static_cast<uint16_t*>(p.out) +
                     (static_cast<size_t>(q0 + t0 + (row_valid ? my_t : 0)) * p.num_q_heads +
                      kvh * G + my_g) *
                         D +
                     part * (D / 2);
-    const uint32_t tO0 = tmem + L::kOCol + part * (D / 2) + lane_base;
 #pragma unroll
     for (int c = 0; c < D / 64; ++c) {
-      float a0[32], a1[32];
-      umma::ld32(tO0 + c * 32, a0);
-      if constexpr (L::kSharedO) {  // one accumulator, equal maxima: c0 = c1
-#pragma unroll
-        for (int e = 0; e < 32; ++e) a1[e] = 0.f;
-      } else {
-        umma::ld32(tO0 + D + c * 32, a1);
-      }
+      float o[32];
+      umma::ld32(tOp + c * 32, o);
       umma::wait_ld();
       if (row_valid) {
 #pragma unroll
         for (int q4 = 0; q4 < 4; ++q4) {
-          float v[8];
-#pragma unroll
-          for (int e = 0; e < 8; ++e) v[e] = a0[8 * q4 + e] * c0 + a1[8 * q4 + e] * c1;
           uint4 w;
-          w.x = pack2<kBf16>(v[0], v[1]);
-          w.y = pack2<kBf16>(v[2], v[3]);
-          w.z = pack2<kBf16>(v[4], v[5]);
-          w.w = pack2<kBf16>(v[6], v[7]);
+          w.x = pack2<kBf16>(o[8 * q4] * inv, o[8 * q4 + 1] * inv);
+          w.y = pack2<kBf16>(o[8 * q4 + 2] * inv, o[8 * q4 + 3] * inv);
+          w.z = pack2<kBf16>(o[8 * q4 + 4] * inv, o[8 * q4 + 5] * inv);
+          w.w = pack2<kBf16>(o[8 * q4 + 6] * inv, o[8 * q4 + 7] * inv);
           *reinterpret_cast<uint4*>(out + c * 32 + 8 * q4) = w;
         }
       }
