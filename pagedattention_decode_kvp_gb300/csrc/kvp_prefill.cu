@@ -9,31 +9,33 @@
 // the block table.  Unlike the decode, this is a dense contraction: a 128-row
 // query tile against 128-key tiles.
 //
-// Design (one CTA of 11 warps per (request, kv head, 128-row query tile)):
+// Design: a persistent kernel, one CTA of 11 warps per SM, walking a list of
+// (request, kv head, 128-row query tile) work items:
 //   * Tile rows are (query token, query head of the kv head's group) pairs, so
 //     every K/V byte a tile reads serves the whole GQA group.
 //   * K/V arrive in 128-key chunks (8 blocks) through separate K and V rings
 //     in shared memory: TMA copies (128-byte swizzle, the layout the tensor
-//     core reads directly) issued by two producer warps, one per tensor.
-//   * One thread issues the tensor-core work: S = Q K^T (tcgen05.mma, M=128,
+//     core reads directly) issued by two producer warps, one per tensor.  The
+//     rings run on across tiles, so the next tile's copies overlap the end of
+//     the current one; each tile's Q travels through the K ring ahead of its
+//     K chunks.
+//   * One warp issues the tensor-core work: S = Q K^T (tcgen05.mma, M=128,
 //     N=128, K=D; Q held in TMEM so only K is read from shared memory) into
-//     one of two TMEM score buffers -- S of chunk j+1 is issued before the
-//     softmax of chunk j is awaited -- and O += P V (M=128, N=D, K=128) into
-//     a TMEM accumulator, so the tensor core works while the CUDA cores
-//     exponentiate.
-//   * Two threads own each query row (TMEM lane): each takes 64 of every
-//     chunk's 128 keys, applies the causal mask and the scale; the two
-//     exchange their chunk max once per chunk, keep the row's running max and
-//     their partial sums in registers, and share one O accumulator in TMEM
-//     (each rescales half of its columns).  The running max is updated
-//     lazily: only when it grows by more than 2^8 is O rescaled (exact:
-//     numerator and denominator share the stale max).
-//   * P stays in tensor memory: each thread writes its 64 probabilities,
-//     packed as 16-bit pairs, over the scores it has read (fp16; bf16 as a
-//     high part plus a bf16 residual so P keeps ~16 bits), and P V takes its
-//     A operand from TMEM -- no shared-memory round trip, no proxy fence.
-//   * At the end the two threads of a row add their sums and each writes half
-//     of the output row.
+//     two TMEM score buffers, and O += P V (M=128, N=D, K=128) into a TMEM
+//     accumulator, so the tensor core works while the CUDA cores exponentiate.
+//   * Eight softmax warps, each owning 16 query rows (TMEM lanes): a row is
+//     spread over four lanes of one warp, each holding 32 of every chunk's
+//     128 scores (the 16-lane TMEM load shape), so a row's max and sum need
+//     only two shuffles and no warp waits on another.  The running max is
+//     updated lazily: only when it grows by more than 2^8 is O rescaled
+//     (exact: numerator and denominator share the stale max).
+//   * P stays in tensor memory, packed as 16-bit pairs in key order (fp16;
+//     bf16 as a high part plus a bf16 residual so P keeps ~16 bits), and P V
+//     takes its A operand from TMEM -- no shared-memory round trip.
+//   * At the end of a tile each row's four lanes add their sums and write the
+//     row.  TMEM, barriers and tensor maps are set up once per CTA.
+#include <algorithm>
+
 #include "kvp_device.cuh"
 #include "kvp_internal.h"
 #include "kvp_umma.cuh"
@@ -41,108 +43,211 @@
 namespace kvp {
 namespace {
 
-constexpr int kRows = 128;                            // M: query rows per CTA
+constexpr int kRows = 128;                            // M: query rows per tile
 constexpr int kKeys = 128;                            // key tokens per chunk (8 blocks)
 // (64-key chunks were measured slower: an N = 64 score MMA costs nearly as
 // much as an N = 128 one, so per key the single issuing thread does more)
-constexpr int kSplit = 2;                             // softmax threads per query row
-constexpr int kKeysPerThread = kKeys / kSplit;        // keys of each chunk per thread
-constexpr int kSoftmaxWarps = 4 * kSplit;             // kSplit per TMEM lane quarter
+// Softmax warps: two per TMEM lane quarter, each owning 16 query rows; a row
+// is spread over four consecutive lanes of one warp (the 16-lane TMEM shapes)
+constexpr int kSoftmaxWarps = 8;
 constexpr int kSoftmaxThreads = kSoftmaxWarps * 32;
 constexpr int kMmaWarp = kSoftmaxWarps;               // issues the tensor-core work
 // TMA issue: one warp streams K tiles, one V tiles
 constexpr int kProducerWarps = 2;
 constexpr int kThreads = kSoftmaxThreads + 32 + kProducerWarps * 32;
 constexpr int kSmemPerSm = 233472;                    // shared memory of one SM (bytes)
-constexpr int kTableCap = 1024;                       // block ids staged on chip per tile
+// Work items are scanned in windows of kWindow candidates (one per softmax
+// thread); only those with rows are visited
+constexpr int kWindow = kSoftmaxThreads;
 
 template <bool kBf16, int D>
 struct PrefillLayout {
   static constexpr int kHalves = D / 64;                  // 64-element K-major halves
-  static constexpr uint32_t kQ = kRows * D * 2;           // Q tile
-  static constexpr uint32_t kKV = kKeys * D * 2;          // one K or V tile
-  // Separate K and V rings: a K stage is free once its S is computed, a V
-  // stage once its P V is; depths fill the shared memory left by Q.
-  static constexpr int kKStages = D == 64 ? 5 : 3;
-  static constexpr int kVStages = D == 64 ? 5 : 2;
-  // S runs one chunk ahead of the softmax: the MMA thread issues S(j + 1)
-  // before it waits for the softmax of chunk j
-  static constexpr int kAhead = 1;
-  static constexpr int kSBufs = kAhead + 1;               // TMEM score (then P) buffers
-  static constexpr uint32_t kQOff = 0;
-  static constexpr uint32_t kKOff = kQ;
+  static constexpr uint32_t kKV = kKeys * D * 2;          // one K, V or Q tile (kRows == kKeys)
+  // Separate K and V rings: a K stage is free once its S is computed (a Q
+  // stage once Q is in TMEM), a V stage once its P V is; the depths fill the
+  // shared memory, to ride out the copy latency under load.
+  static constexpr int kKStages = D == 64 ? 7 : 3;
+  static constexpr int kVStages = D == 64 ? 6 : 3;
+  static constexpr int kSBufs = 2;                        // TMEM score buffers
+  static constexpr uint32_t kKOff = 0;
   static constexpr uint32_t kVOff = kKOff + kKStages * kKV;
-  static constexpr uint32_t kRedOff = kVOff + kVStages * kKV;  // [4][kSplit][kRows] float
-  static constexpr uint32_t kTblOff = kRedOff + 4 * kSplit * kRows * 4;  // [kTableCap] int32
-  static constexpr uint32_t kBarOff = kTblOff + kTableCap * 4;
-  // kfull[], vfull[], kempty[], vempty[], s[], p[], pv[2], q, q in TMEM
+  // output staging: row r (D 16-bit values) at r * kStgStride; the 16 bytes
+  // of padding make one-row-per-lane 16-byte writes conflict-free
+  static constexpr uint32_t kStgStride = D * 2 + 16;
+  static constexpr uint32_t kStgOff = kVOff + kVStages * kKV;
+  static constexpr uint32_t kRedOff = kStgOff + kRows * kStgStride;  // [kRows] row sums
+  static constexpr uint32_t kMaskOff = kRedOff + kRows * 4;  // [kWindow / 32] work-item bits
+  static constexpr uint32_t kBarOff = kMaskOff + kWindow / 8;
+  // kfull[], vfull[], kempty[], vempty[], s[], p[], pv[2], q in TMEM, MMA done
   static constexpr int kBars = 2 * (kKStages + kVStages) + 2 * kSBufs + 4;
-  // + 1024 bytes of alignment slack, the barriers and the TMEM address slot
-  static constexpr size_t kSmem = 1024 + kBarOff + kBars * 8 + 16;
-  // TMEM columns: score buffer i at [128 i, 128 (i+1)) (key half h's P is
-  // written over its own scores at [128 i + 64 h, +32), its bf16 residual
-  // right after); the Q tile (16-bit pairs) at [256, 256 + D/2), so the score
-  // MMAs read only K from shared memory; the O accumulator, shared by a row's
-  // two threads, at [512 - D, 512).  The shared memory keeps a second CTA off
-  // the SM, so all 512 columns are free.
+  // + the barriers and the TMEM address slot.  The swizzled tiles need a
+  // 1024-byte aligned base, which the kernel checks instead of reserving slack.
+  static constexpr size_t kSmem = kBarOff + kBars * 8 + 16;
+  // TMEM columns: score buffer i at [128 i, 128 (i+1)); the Q tile (16-bit
+  // pairs) at [256, 256 + D/2), so the score MMAs read only K from shared
+  // memory; O at [512 - D, 512).  P is 16-bit pairs in key order (64
+  // columns; the bf16 residual 64 columns on).  Where it fits, P has columns
+  // of its own right after Q, so a score buffer is free again as soon as the
+  // softmax has read it and S(j + 2) queues on the tensor core right behind
+  // P V(j); otherwise (bf16, D = 128) P is written over the scores it came
+  // from, and S(j + 1) waits until P V(j - 1) has read it.  The shared memory
+  // keeps a second CTA off the SM, so all 512 columns are free.
   static constexpr uint32_t kQCol = kSBufs * kKeys;
+  static constexpr uint32_t kPCols = kBf16 ? 128 : 64;
   static constexpr uint32_t kOCol = 512 - D;
+  static constexpr bool kPSep = kQCol + D / 2 + kPCols <= kOCol;
+  static constexpr uint32_t kPCol = kQCol + D / 2;        // (kPSep only)
   static constexpr uint32_t kTmemCols = 512;
   static_assert(kQCol + D / 2 <= kOCol, "score buffers and Q overlap O");
-  static_assert(2 * (kSmem + 1024) > kSmemPerSm, "TMEM budget assumes one CTA per SM");
+  static_assert(2 * kSmem > kSmemPerSm, "TMEM budget assumes one CTA per SM");
   static_assert(kSmem <= 232448, "exceeds the per-block shared-memory limit");
 };
 
-// Swizzled offset of 16-byte chunk c of row r in a 128-byte-row tile.
-__device__ __forceinline__ uint32_t sw_chunk(int r, int c) {
-  return static_cast<uint32_t>(r * 128 + (((c & 7) ^ (r & 7)) << 4));
+// shared -> global bulk copy (async proxy), tracked by this thread's bulk groups
+__device__ __forceinline__ void bulk_store(void* gdst, uint32_t ssrc, uint32_t bytes) {
+  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(gdst),
+               "r"(ssrc), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit() {
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+// this thread's bulk copies have read their shared-memory sources
+__device__ __forceinline__ void bulk_wait_read() {
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+// ... and have completed
+__device__ __forceinline__ void bulk_wait_all() {
+  asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
 }
 
+// Named barrier over `nthreads` threads that also ANDs a flag across them.
+__device__ __forceinline__ bool named_bar_and(uint32_t id, uint32_t nthreads, bool v) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 p, %1, 0;\n\t"
+      "bar.red.and.pred q, %2, %3, p;\n\t"
+      "selp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"(static_cast<uint32_t>(v)), "r"(id), "r"(nthreads)
+      : "memory");
+  return r != 0;
+}
+
+// One work item: tile x of request b's query chunk against kv head kvh.
+struct Tile {
+  int b, kvh, q0, qlen, n, t0, ntok, pos0, nkeys, nblk, nchunks;
+  bool lens_bad;   // lengths out of range: rows are zeroed, nothing is read
+  int32_t status;  // error to record for this item (0 = none)
+};
+
+// The request lengths a work item needs, loaded ahead of its turn.
+struct ItemLens {
+  int q0, q1, n;
+};
+
+// Work item `id` of tiles_x * batch * num_kv_heads: the last query tiles of
+// every request first (they attend to the most keys), then the earlier ones.
+__device__ __forceinline__ ItemLens load_lens(const PrefillParams& p, long long id) {
+  const long long per_x = static_cast<long long>(p.batch) * p.num_kv_heads;
+  const int b = static_cast<int>(id % per_x) / p.num_kv_heads;
+  return ItemLens{p.query_start[b], p.query_start[b + 1], p.context_lens[b]};
+}
+
+// Returns false when the item has no rows (the request's chunk is shorter).
+__device__ __forceinline__ bool decode_tile(const PrefillParams& p, int tiles_x, long long id,
+                                            const ItemLens& lens, Tile& t) {
+  const long long per_x = static_cast<long long>(p.batch) * p.num_kv_heads;
+  const int x = tiles_x - 1 - static_cast<int>(id / per_x);
+  const int r = static_cast<int>(id % per_x);
+  t.b = r / p.num_kv_heads;
+  t.kvh = r % p.num_kv_heads;
+  t.status = 0;
+  t.nchunks = 0;
+  t.lens_bad = false;
+  t.q0 = lens.q0;
+  t.qlen = lens.q1 - lens.q0;
+  t.n = lens.n;
+  const int tok_per_tile = kRows / p.group;
+  t.t0 = x * tok_per_tile;
+  // rows past the launch's coverage (a chunk longer than its maximum length)
+  if (x == 0 && t.kvh == 0 && t.qlen > tiles_x * tok_per_tile) t.status = kErrBadBlock;
+  if (t.qlen <= 0 || t.t0 >= t.qlen) return t.status != 0;
+  if (t.q0 < 0 || t.q0 + t.qlen > p.num_tokens) {  // rows outside q / out: touch nothing
+    t.status = kErrBadBlock;
+    t.ntok = 0;
+    return true;
+  }
+  t.ntok = min(tok_per_tile, t.qlen - t.t0);
+  if (t.qlen > t.n || t.n > p.max_blocks * kBlockSize) {
+    t.lens_bad = true;
+    t.status = kErrBadBlock;
+    return true;
+  }
+  t.pos0 = t.n - t.qlen + t.t0;  // position of the tile's first query token
+  t.nkeys = t.pos0 + t.ntok;     // keys needed: 0 .. nkeys - 1
+  t.nblk = (t.nkeys + kBlockSize - 1) / kBlockSize;
+  t.nchunks = (t.nkeys + kKeys - 1) / kKeys;
+  return true;
+}
+
+// Zeroes the output rows of a tile (threads [0, nthreads) of the block).
 template <int D>
-__device__ __forceinline__ void zero_tile_rows(const PrefillParams& p, int kvh, int q0, int t0,
-                                               int ntok) {
+__device__ __forceinline__ void zero_tile_rows(const PrefillParams& p, const Tile& t,
+                                               int nthreads) {
   const int G = p.group;
   uint16_t* out = static_cast<uint16_t*>(p.out);
-  for (int idx = threadIdx.x; idx < ntok * G * D; idx += blockDim.x) {
-    const int t = idx / (G * D), g = (idx / D) % G, d = idx % D;
-    out[(static_cast<size_t>(q0 + t0 + t) * p.num_q_heads + kvh * G + g) * D + d] = 0;
+  for (int idx = threadIdx.x; idx < t.ntok * G * D; idx += nthreads) {
+    const int tk = idx / (G * D), g = (idx / D) % G, d = idx % D;
+    out[(static_cast<size_t>(t.q0 + t.t0 + tk) * p.num_q_heads + t.kvh * G + g) * D + d] = 0;
   }
 }
 
 // Warp roles: warps 0-7 run the softmax -- warp w serves query rows
-// 32*(w%4) .. +31 (the TMEM lanes it may access) for keys [64*(w/4), +64) of
-// each chunk and O columns [D/2*(w/4), +D/2); warp 8 issues the tensor-core
-// instructions; warps 9 and 10 are producers of the K and the V tiles.  The MMA and producer warps run their loops converged (waits and
-// address arithmetic warp-uniform) and issue from one elected lane.
+// 32*(w%4) + 16*(w/4) .. +15 (within the TMEM lanes it may access), all keys
+// of each chunk and all O columns, and warps 0-3 move each tile's Q from
+// shared memory into TMEM; warp 8 issues the tensor-core instructions; warps
+// 9 and 10 are producers of the K (and Q) and the V tiles.  The MMA and
+// producer warps run their loops converged (waits and address arithmetic
+// warp-uniform) and issue from one elected lane.  Every role walks the same
+// work items and counts K-ring slots, V-ring slots, chunks and tiles alike,
+// so the barrier phases agree without any exchange.
 // Hand-offs (mbarriers; every wait is at most one phase behind its barrier):
-//   kfull[c % kKStages]   producer -> MMA     chunk c's K landed (1 arrival + bytes)
-//   vfull[c % kVStages]   producers -> MMA    chunk c's V landed
-//   kempty[c % kKStages]  MMA -> producers    S(c) done: K stage free
-//   vempty[c % kVStages]  MMA -> producers    P V(c) done: V stage free
-//   s[c % kSBufs]         MMA -> softmax      S of chunk c in TMEM buffer c % kSBufs
-//   p[c % kSBufs]         softmax -> MMA      P of chunk c written over it (8 arrivals)
-//   pv[c % 2]             MMA -> softmax, MMA O += P V of chunk c complete
-// Per chunk j the MMA thread -- once P V(j-1) has read its P -- issues
-// S(j + kAhead) into chunk j-1's buffer, then waits p(j) and V(j) and issues
-// P V(j).  The softmax of chunk j needs only S(j); O is touched (lazy rescale,
-// after P V(j-1)) only when a row's max jumps.  The producers start as soon as the
-// block table is on chip, while the softmax warps load Q.
+//   kfull[k % kKStages]   producer -> MMA, softmax  K chunk / Q tile landed
+//   vfull[v % kVStages]   producer -> MMA     V chunk landed
+//   kempty[k % kKStages]  MMA -> producer     S done (or Q in TMEM): stage free
+//   vempty[v % kVStages]  MMA -> producer     P V done: V stage free
+//   s[g % 2]              MMA -> softmax      S of chunk g in TMEM buffer g % 2
+//   p[g % 2]              softmax -> MMA      S(g) read, P(g) written (8 arrivals)
+//   pv[g % 2]             MMA -> softmax      O += P V of chunk g complete
+//   qt                    softmax -> MMA      the tile's Q in TMEM (8 arrivals)
+// (g counts chunks over all of the CTA's tiles, k and v count ring slots.)
+// With P in its own TMEM columns the MMA warp issues S of a tile's first two
+// chunks once its Q is in TMEM, then per chunk g waits p(g) and V(g), issues
+// P V(g) and S(g + 2) into chunk g's score buffer; the softmax of chunk g
+// needs S(g), and P V(g-1) complete before it writes P and (lazy rescale,
+// only when a row's max jumps) O.  With P over the scores, S(g) waits until
+// P V(g-2) has read the buffer.  The first P V of a tile overwrites O, which
+// the softmax warps have read out before they release that chunk's P.
 template <bool kBf16, int D>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmq,
                    const __grid_constant__ CUtensorMap tmk,
-                   const __grid_constant__ CUtensorMap tmv) {
+                   const __grid_constant__ CUtensorMap tmv, const int tiles_x) {
   using namespace dev;
   using L = PrefillLayout<kBf16, D>;
   constexpr int kKStages = L::kKStages;
   constexpr int kVStages = L::kVStages;
   constexpr int kSBufs = L::kSBufs;
-  constexpr int kAhead = L::kAhead;
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* sm = align1024(smem_raw);
-  uint8_t* sQ = sm + L::kQOff;
-  float* red = reinterpret_cast<float*>(sm + L::kRedOff);
-  int32_t* stbl = reinterpret_cast<int32_t*>(sm + L::kTblOff);
+  constexpr bool kPSep = L::kPSep;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* sm = smem_raw;
+  if ((smem_addr(sm) & 1023u) != 0) {  // the swizzled tiles need it; never seen
+    if (threadIdx.x == 0) set_status(p.status, KVP_ERR_UNSUPPORTED);
+    return;
+  }
   uint64_t* kf_bar = reinterpret_cast<uint64_t*>(sm + L::kBarOff);  // [kKStages]
   uint64_t* vf_bar = kf_bar + kKStages;                              // [kVStages]
   uint64_t* ke_bar = vf_bar + kVStages;                              // [kKStages]
@@ -150,45 +255,21 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* s_bar = ve_bar + kVStages;                               // [kSBufs]
   uint64_t* p_bar = s_bar + kSBufs;                                  // [kSBufs]
   uint64_t* pv_bar = p_bar + kSBufs;                                 // [2]
-  uint64_t* q_bar = pv_bar + 2;      // Q tile landed in shared memory
-  uint64_t* qt_bar = q_bar + 1;      // Q copied into TMEM (8 arrivals)
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(qt_bar + 1);
+  uint64_t* qt_bar = pv_bar + 2;     // the tile's Q copied into TMEM
+  uint64_t* done_bar = qt_bar + 1;   // every tensor-core op of the CTA complete
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done_bar + 1);
+  uint8_t* stg = sm + L::kStgOff;                                    // output staging
+  float* red = reinterpret_cast<float*>(sm + L::kRedOff);            // row sums
+  uint32_t* mask = reinterpret_cast<uint32_t*>(sm + L::kMaskOff);    // items with rows
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const bool mma_warp = warp == kMmaWarp;
   const bool producer = warp > kMmaWarp;
-  const int quarter = warp & 3;
-  const int part = (warp >> 2) & (kSplit - 1);  // which key half / O accumulator
-  const int row = quarter * 32 + lane;
-  const int b = blockIdx.z, kvh = blockIdx.y, tile = blockIdx.x;
   const int G = p.group;
-  const int tok_per_tile = kRows / G;
+  const long long items = static_cast<long long>(tiles_x) * p.batch * p.num_kv_heads;
 
-  grid_dependency_wait();
-  const int q0 = p.query_start[b];
-  const int qlen = p.query_start[b + 1] - q0;
-  const int n = p.context_lens[b];
-  const int t0 = tile * tok_per_tile;
-  // rows past the grid's coverage (a chunk longer than the launch's maximum)
-  if (tile == gridDim.x - 1 && tid == 0 && qlen > static_cast<int>(gridDim.x) * tok_per_tile)
-    set_status(p.status, kErrBadBlock);
-  if (qlen <= 0 || t0 >= qlen) return;
-  if (q0 < 0 || q0 + qlen > p.num_tokens) {  // rows outside q / out: touch nothing
-    if (tid == 0) set_status(p.status, kErrBadBlock);
-    return;
-  }
-  const int ntok = min(tok_per_tile, qlen - t0);
-  if (qlen > n || n > p.max_blocks * kBlockSize) {
-    zero_tile_rows<D>(p, kvh, q0, t0, ntok);
-    if (tid == 0) set_status(p.status, kErrBadBlock);
-    return;
-  }
-  const int pos0 = n - qlen + t0;  // position of this tile's first query token
-  const int nkeys = pos0 + ntok;   // keys needed: 0 .. nkeys - 1
-  const int nblk = (nkeys + kBlockSize - 1) / kBlockSize;
-  const int nchunks = (nkeys + kKeys - 1) / kKeys;
-  const int32_t* tbl = p.block_tables + static_cast<size_t>(b) * p.max_blocks;
   if (mma_warp && lane == 0) {
+    prefetch_tensormap(&tmq);
     prefetch_tensormap(&tmk);
     prefetch_tensormap(&tmv);
     for (int i = 0; i < 2 * (kKStages + kVStages) + kSBufs; ++i)
@@ -196,292 +277,349 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int i = 0; i < kSBufs; ++i) mbar_init(smem_addr(p_bar + i), kSoftmaxWarps);
     mbar_init(smem_addr(pv_bar), 1);
     mbar_init(smem_addr(pv_bar + 1), 1);
-    mbar_init(smem_addr(q_bar), 1);
-    mbar_init(smem_addr(qt_bar), kSoftmaxWarps);
+    mbar_init(smem_addr(qt_bar), 1);
+    mbar_init(smem_addr(done_bar), 1);
     fence_barrier_init();
-    // ---- Q tile by TMA, straight into the K-major swizzled layout: a box of
-    // (64 elements, G heads, 128 / G tokens) puts (token t, head g) at row
-    // t * G + g.  Tokens past T read as zeros; rows past the tile's own tokens
-    // are never used.
-    const uint32_t qb = smem_addr(q_bar);
-    mbar_arrive_expect_tx(
-        qb, static_cast<uint32_t>(L::kHalves * 64 * G * p.q_box_tokens * 2));
-#pragma unroll
-    for (int hf = 0; hf < L::kHalves; ++hf)
-      tma_load_3d(smem_addr(sQ + hf * (kRows * 128)), &tmq, hf * 64, kvh * G, q0 + t0, qb);
   }
-  // range-check every block id the tile reads; the first kTableCap are kept on
-  // chip so the copy issuers never wait on a global load
-  bool bad = false;
-  for (int i = tid; i < nblk; i += kThreads) {
-    const int id = tbl[i];
-    bad |= (id < 0) || (id >= p.num_blocks);
-    if (i < kTableCap) stbl[i] = id;
-  }
-  if (__syncthreads_or(bad)) {
-    zero_tile_rows<D>(p, kvh, q0, t0, ntok);
-    if (tid == 0) set_status(p.status, kErrBadBlock);
-    mbar_wait_bounded(smem_addr(q_bar), 0);  // no copy may land after the exit
-    return;
-  }
+  if (mma_warp) umma::alloc(smem_addr(tmem_slot), L::kTmemCols);
+  umma::fence_before_sync();
+  __syncthreads();
+  umma::fence_after_sync();
+  const uint32_t tmem = *tmem_slot;
+  grid_dependency_wait();
+  bool ok = true;
 
-  // ---- producers: warp 9 streams the K tiles, warp 10 the V tiles
+  // ---- per-role state, kept across work items
+  // producers: warp 9 streams each tile's Q and K chunks, warp 10 its V chunks
   const bool is_k = warp == kMmaWarp + 1;
   const CUtensorMap* map = is_k ? &tmk : &tmv;
   const int nst = is_k ? kKStages : kVStages;
   uint64_t* full = is_k ? kf_bar : vf_bar;
   uint64_t* empty = is_k ? ke_bar : ve_bar;
   const uint32_t ring = smem_addr(sm + (is_k ? L::kKOff : L::kVOff));
-  auto produce = [&](int c) {  // the whole warp; one lane issues the copies
-    const int st = c % nst;
-    bool fine = true;
-    if (c >= nst) fine = mbar_wait_bounded(smem_addr(empty + st), ((c / nst) - 1) & 1);
-    const int blk0 = c * (kKeys / kBlockSize);
-    const int nb = min(kKeys / kBlockSize, nblk - blk0);
-    int my_id = 0;
-    if (lane < nb) my_id = blk0 + lane < kTableCap ? stbl[blk0 + lane] : tbl[blk0 + lane];
-    int ids[kKeys / kBlockSize];
-#pragma unroll
-    for (int i = 0; i < kKeys / kBlockSize; ++i) ids[i] = __shfl_sync(0xffffffffu, my_id, i);
-    if (elect_one()) {
-      const uint32_t bar = smem_addr(full + st);
-      mbar_arrive_expect_tx(bar, static_cast<uint32_t>(nb * L::kHalves * 2048));
-#pragma unroll
-      for (int i = 0; i < kKeys / kBlockSize; ++i) {
-        if (i < nb) {
-          const int y = (ids[i] * p.num_kv_heads + kvh) * kBlockSize;
-#pragma unroll
-          for (int hf = 0; hf < L::kHalves; ++hf)
-            tma_load_2d(ring + st * L::kKV + i * 2048 + hf * (kKeys * 128), map, hf * 64, y, bar);
-        }
-      }
-    }
-    __syncwarp();
-    return fine;
-  };
-  // chunk 0 goes out at once; the rest waits until Q is staged, so the first
-  // copies do not queue ahead of the Q loads
-  if (producer) produce(0);
+  uint32_t slot = 0;  // ring slots used so far
+  // MMA warp and softmax warps: K slots, V slots, chunks and tiles so far
+  uint32_t kc = 0, vc = 0, gc = 0, tc = 0;
+  constexpr uint32_t kIdS = umma::instr_desc_f16(kRows, kKeys, kBf16, false, false);
+  constexpr uint32_t kIdO = umma::instr_desc_f16(kRows, D, kBf16, false, true);
+  // shared-memory descriptors are built once; an operand at byte offset o
+  // from a base is the base descriptor plus o >> 4 (the start-address field,
+  // which never carries: every address is below 256 KB)
+  const uint64_t k_desc = umma::smem_desc_sw128(smem_addr(sm + L::kKOff), 16, 1024);
+  const uint64_t v_desc = umma::smem_desc_sw128(smem_addr(sm + L::kVOff), kKeys * 128, 1024);
+  // softmax: scores are scaled inside the exponent's FMA when the scale is
+  // positive (max and mask commute with it); otherwise they are scaled first
+  const float sl2 = p.scale_log2;
+  const bool pos_scale = sl2 > 0.f;
+  const float mul = pos_scale ? sl2 : 1.0f;
+  const int quarter = warp & 3;  // TMEM lanes 32 * quarter .. + 31
+  // this thread's two tile rows (row r = query token r / G, head r % G) and 32
+  // of each chunk's 128 keys, as the 16x256b TMEM shape hands them out: rows
+  // base + lane/4 and base + lane/4 + 8 (base = 32 * quarter + 16 * (warp /
+  // 4)), keys 8k + 2 (lane % 4) and the next of each group of eight (k = 0..15)
+  const int base = quarter * 32 + (warp >> 2) * 16;
+  const int ra = base + (lane >> 2), rb = ra + 8;
+  const int c2 = 2 * (lane & 3);
+  const uint32_t lane_base = static_cast<uint32_t>(base) << 16;
+  const uint32_t tO = tmem + L::kOCol + lane_base;
 
-  // ---- tile row r = (query token r / G, query head r % G)
-  const int my_t = row / G;
-  const int my_g = row % G;
-  const bool row_valid = warp < kSoftmaxWarps && my_t < ntok;
-  if (mma_warp) {
-    umma::alloc(smem_addr(tmem_slot), L::kTmemCols);
-  }
-  umma::fence_before_sync();
-  __syncthreads();
-  umma::fence_after_sync();
-  const uint32_t tmem = *tmem_slot;
-  bool ok = true;
-
-  if (producer) {
-    for (int c = 1; c < nchunks; ++c) ok &= produce(c);
-  } else if (mma_warp) {
-    // the whole warp runs this loop (waits and descriptor arithmetic stay
-    // warp-uniform); one elected lane issues each group of tensor instructions
-    {
-      constexpr uint32_t kIdS = umma::instr_desc_f16(kRows, kKeys, kBf16, false, false);
-      constexpr uint32_t kIdO = umma::instr_desc_f16(kRows, D, kBf16, false, true);
-      // shared-memory descriptors are built once; an operand at byte offset o
-      // from a base is the base descriptor plus o >> 4 (the start-address
-      // field, which never carries: every address is below 256 KB)
-      const uint64_t k_desc = umma::smem_desc_sw128(smem_addr(sm + L::kKOff), 16, 1024);
-      const uint64_t v_desc = umma::smem_desc_sw128(smem_addr(sm + L::kVOff), kKeys * 128, 1024);
-      auto issue_s = [&](int c) {  // wait for chunk c's K, S(c) = Q K(c)^T, free the K stage
-        ok &= mbar_wait_bounded(smem_addr(kf_bar + c % kKStages), (c / kKStages) & 1);
-        umma::fence_after_sync();
-        const uint64_t kd = k_desc + (((c % kKStages) * L::kKV) >> 4);
-        const uint32_t d = tmem + (c % kSBufs) * kKeys;
-        if (elect_one()) {
-#pragma unroll
-          for (int s = 0; s < D / 16; ++s) {
-            const uint32_t koff = (s >> 2) * (kKeys * 128) + (s & 3) * 32;
-            umma::mma_f16_tmem_a(d, tmem + L::kQCol + s * 8, kd + (koff >> 4), kIdS,
-                                 s > 0 ? 1u : 0u);
-          }
-          umma::commit(smem_addr(s_bar + c % kSBufs));
-          umma::commit(smem_addr(ke_bar + c % kKStages));
-        }
-        __syncwarp();
-      };
-
-      ok &= mbar_wait_bounded(smem_addr(qt_bar), 0);
-      umma::fence_after_sync();
-      for (int c = 0; c < min(kAhead, nchunks); ++c) issue_s(c);
-      for (int j = 0; j < nchunks; ++j) {
-        // S(j+kAhead) goes over chunk j-1's P: once P V(j-1) has read it, the
-        // tensor core computes it while the softmax works on chunk j
-        if (j + kAhead < nchunks) {
-          if (j >= 1)
-            ok &= mbar_wait_bounded(smem_addr(pv_bar + ((j - 1) & 1)), ((j - 1) >> 1) & 1);
-          issue_s(j + kAhead);
-        }
-        ok &= mbar_wait_bounded(smem_addr(p_bar + j % kSBufs), (j / kSBufs) & 1);
-        ok &= mbar_wait_bounded(smem_addr(vf_bar + j % kVStages), (j / kVStages) & 1);
-        umma::fence_after_sync();
-        const uint32_t pa = tmem + (j % kSBufs) * kKeys;  // P of chunk j (TMEM)
-        const uint64_t vd = v_desc + (((j % kVStages) * L::kKV) >> 4);
-        if (elect_one()) {
-          // key half h (16-key steps t), P read where thread (row, h) wrote it
-#pragma unroll
-          for (int h = 0; h < kSplit; ++h) {
-#pragma unroll
-            for (int t = 0; t < kKeysPerThread / 16; ++t) {
-              const uint32_t o_acc = tmem + L::kOCol;
-              const uint32_t a = pa + h * kKeysPerThread + t * 8;
-              const uint64_t b = vd + (((h * kKeysPerThread + t * 16) * 128) >> 4);
-              const bool first = j == 0 && h == 0 && t == 0;
-              umma::mma_f16_tmem_a(o_acc, a, b, kIdO, first ? 0u : 1u);
-              if constexpr (kBf16)
-                umma::mma_f16_tmem_a(o_acc, a + kKeysPerThread / 2, b, kIdO, 1u);
-            }
-          }
-          umma::commit(smem_addr(pv_bar + (j & 1)));
-          umma::commit(smem_addr(ve_bar + j % kVStages));
-        }
-        __syncwarp();
-      }
-    }
-    __syncwarp();
-    launch_dependents();
-  } else {
-    const int qpos = pos0 + my_t;
-    const float sl2 = p.scale_log2;
-    // scores are scaled inside the exponent's FMA when the scale is positive
-    // (max and mask commute with it); otherwise they are scaled first
-    const bool pos_scale = sl2 > 0.f;
-    const float mul = pos_scale ? sl2 : 1.0f;
-    float m = -INFINITY, l = 0.f;  // this key half's running max (log2 units) and sum
-    const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
-    // the O columns this thread rescales and writes: its half of the row
-    constexpr int kOCols = D / 2;
-    const uint32_t tOp = tmem + L::kOCol + part * (D / 2) + lane_base;
-    {
-      // Q row `row`, elements [part * D/2, +D/2), from the swizzled tile into
-      // TMEM as 16-bit pairs (the A operand of S = Q K^T)
-      ok &= mbar_wait_bounded(smem_addr(q_bar), 0);
-#pragma unroll
-      for (int g = 0; g < D / 64; ++g) {
-        uint32_t w[16];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const int c = part * (D / 16) + g * 4 + i;  // 16-byte chunk of the row
-          const uint4 v =
-              *reinterpret_cast<const uint4*>(sQ + (c >> 3) * (kRows * 128) + sw_chunk(row, c));
-          w[4 * i] = v.x;
-          w[4 * i + 1] = v.y;
-          w[4 * i + 2] = v.z;
-          w[4 * i + 3] = v.w;
-        }
-        umma::st16_bits(tmem + L::kQCol + part * (D / 4) + g * 16 + lane_base, w);
-      }
-      umma::wait_st();
-      umma::fence_before_sync();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(smem_addr(qt_bar));
-    }
-    auto o_scale = [&](float alpha) {  // this thread's O columns *= alpha
-#pragma unroll
-      for (int c = 0; c < kOCols / 32; ++c) {
-        float o[32];
-        umma::ld32(tOp + c * 32, o);
-        umma::wait_ld();
-#pragma unroll
-        for (int i = 0; i < 32; ++i) o[i] *= alpha;
-        umma::st32(tOp + c * 32, o);
-      }
-      umma::wait_st();
+  // ---- producers: one work item (the whole warp; one lane issues the copies)
+  auto produce_item = [&](const Tile& t) {
+    const int32_t* tbl = p.block_tables + static_cast<size_t>(t.b) * p.max_blocks;
+    auto take = [&](uint32_t c) {  // wait until slot c's stage is free
+      if (c >= static_cast<uint32_t>(nst))
+        ok &= mbar_wait_bounded(smem_addr(empty + c % nst), ((c / nst) - 1) & 1);
+      return ok;
     };
-    for (int j = 0; j < nchunks; ++j) {
-      ok &= mbar_wait_bounded(smem_addr(s_bar + j % kSBufs), (j / kSBufs) & 1);
+    if (is_k) {
+      // Q tile: a box of (64 elements, G heads, 128 / G tokens) puts (token
+      // t, head g) at row t * G + g of the K-major swizzled layout.  Tokens
+      // past T read as zeros; rows past the tile's own tokens are never used.
+      if (!take(slot)) return;
+      const int st = slot % nst;
+      if (elect_one()) {
+        const uint32_t bar = smem_addr(full + st);
+        mbar_arrive_expect_tx(bar,
+                              static_cast<uint32_t>(L::kHalves * 64 * G * p.q_box_tokens * 2));
+#pragma unroll
+        for (int hf = 0; hf < L::kHalves; ++hf)
+          tma_load_3d(ring + st * L::kKV + hf * (kRows * 128), &tmq, hf * 64, t.kvh * G,
+                      t.q0 + t.t0, bar);
+      }
+      __syncwarp();
+      ++slot;
+    }
+    for (int c = 0; c < t.nchunks; ++c, ++slot) {
+      const int blk0 = c * (kKeys / kBlockSize);
+      const int nb = min(kKeys / kBlockSize, t.nblk - blk0);
+      // block ids of the chunk (lane i holds block blk0 + i); an id out of
+      // range is replaced by block 0 -- the tile is flagged and its rows
+      // zeroed by the softmax warps -- so no copy ever leaves the pool
+      int my_id = 0;
+      if (lane < nb) {
+        my_id = tbl[blk0 + lane];
+        if (my_id < 0 || my_id >= p.num_blocks) my_id = 0;
+      }
+      if (!take(slot)) return;
+      const int st = slot % nst;
+      int ids[kKeys / kBlockSize];
+#pragma unroll
+      for (int i = 0; i < kKeys / kBlockSize; ++i) ids[i] = __shfl_sync(0xffffffffu, my_id, i);
+      if (elect_one()) {
+        const uint32_t bar = smem_addr(full + st);
+        mbar_arrive_expect_tx(bar, static_cast<uint32_t>(nb * L::kHalves * 2048));
+#pragma unroll
+        for (int i = 0; i < kKeys / kBlockSize; ++i) {
+          if (i < nb) {
+            const int y = (ids[i] * p.num_kv_heads + t.kvh) * kBlockSize;
+#pragma unroll
+            for (int hf = 0; hf < L::kHalves; ++hf)
+              tma_load_2d(ring + st * L::kKV + i * 2048 + hf * (kKeys * 128), map, hf * 64, y,
+                          bar);
+          }
+        }
+      }
+      __syncwarp();
+    }
+  };
+
+  // ---- MMA warp: one work item.  The whole warp runs it (waits and
+  // descriptor arithmetic stay warp-uniform); one elected lane issues each
+  // group of tensor instructions.
+  // S(g) = Q K^T from K slot k into score buffer g % 2; frees the K stage
+  auto issue_s = [&](uint32_t k, uint32_t g) {
+    ok &= mbar_wait_bounded(smem_addr(kf_bar + k % kKStages), (k / kKStages) & 1);
+    umma::fence_after_sync();
+    const uint64_t kd = k_desc + (((k % kKStages) * L::kKV) >> 4);
+    const uint32_t d = tmem + (g % kSBufs) * kKeys;
+    if (elect_one()) {
+#pragma unroll
+      for (int s = 0; s < D / 16; ++s) {
+        const uint32_t koff = (s >> 2) * (kKeys * 128) + (s & 3) * 32;
+        umma::mma_f16_tmem_a(d, tmem + L::kQCol + s * 8, kd + (koff >> 4), kIdS, s > 0 ? 1u : 0u);
+      }
+      umma::commit(smem_addr(s_bar + g % kSBufs));
+      umma::commit(smem_addr(ke_bar + k % kKStages));
+    }
+    __syncwarp();
+  };
+  // with P over the scores, S(g) waits until P V(g-2) has read buffer g % 2
+  auto s_buffer_free = [&](uint32_t g) {
+    if (!kPSep && g >= 2)
+      ok &= mbar_wait_bounded(smem_addr(pv_bar + (g & 1)), ((g - 2) >> 1) & 1);
+  };
+  auto mma_item = [&](const Tile& t) {
+    const int n = t.nchunks;
+    // ---- Q into TMEM straight from its K-ring stage (tcgen05.cp, the same
+    // K-major swizzled operand the score MMAs would read), once every S of
+    // the previous tile -- the last one is the latest -- has read the old Q
+    ok &= mbar_wait_bounded(smem_addr(kf_bar + kc % kKStages), (kc / kKStages) & 1);
+    if (gc > 0) ok &= mbar_wait_bounded(smem_addr(s_bar + (gc - 1) % kSBufs), ((gc - 1) / kSBufs) & 1);
+    umma::fence_after_sync();
+    if (elect_one()) {
+      const uint64_t qd = k_desc + (((kc % kKStages) * L::kKV) >> 4);
+#pragma unroll
+      for (int s = 0; s < D / 16; ++s) {
+        const uint32_t qoff = (s >> 2) * (kRows * 128) + (s & 3) * 32;
+        umma::cp_128x256b(tmem + L::kQCol + s * 8, qd + (qoff >> 4));
+      }
+      umma::commit(smem_addr(qt_bar));
+      umma::commit(smem_addr(ke_bar + kc % kKStages));  // the Q stage is free once copied
+    }
+    __syncwarp();
+    ok &= mbar_wait_bounded(smem_addr(qt_bar), tc & 1);
+    umma::fence_after_sync();
+    const uint32_t k0 = kc + 1;  // K slot of chunk 0
+    for (int c = 0; c < min(kPSep ? kSBufs : 1, n); ++c) {
+      s_buffer_free(gc + c);
+      issue_s(k0 + c, gc + c);
+    }
+    for (int j = 0; j < n && ok; ++j) {
+      const uint32_t g = gc + j;
+      if (!kPSep && j + 1 < n) {
+        // S(g+1) goes over P(g-1): once P V(g-1) has read it, the tensor core
+        // computes it while the softmax works on chunk g
+        s_buffer_free(g + 1);
+        issue_s(k0 + j + 1, g + 1);
+      }
+      ok &= mbar_wait_bounded(smem_addr(p_bar + g % kSBufs), (g / kSBufs) & 1);
+      ok &= mbar_wait_bounded(smem_addr(vf_bar + (vc + j) % kVStages), ((vc + j) / kVStages) & 1);
       umma::fence_after_sync();
-      float s[kKeysPerThread];
-      const uint32_t tS = tmem + (j % kSBufs) * kKeys + part * kKeysPerThread + lane_base;
+      // P of chunk g (TMEM)
+      const uint32_t pa = tmem + (kPSep ? L::kPCol : (g % kSBufs) * kKeys);
+      const uint64_t vd = v_desc + ((((vc + j) % kVStages) * L::kKV) >> 4);
+      if (elect_one()) {
+        // 16-key steps u: P at 8 columns per step (its bf16 residual 64 on)
 #pragma unroll
-      for (int c = 0; c < kKeysPerThread / 32; ++c)
-        umma::ld32(tS + c * 32, *reinterpret_cast<float(*)[32]>(s + c * 32));
+        for (int u = 0; u < kKeys / 16; ++u) {
+          const uint32_t a = pa + u * 8;
+          const uint64_t bd = vd + (((u * 16) * 128) >> 4);
+          umma::mma_f16_tmem_a(tmem + L::kOCol, a, bd, kIdO, (j > 0 || u > 0) ? 1u : 0u);
+          if constexpr (kBf16) umma::mma_f16_tmem_a(tmem + L::kOCol, a + kKeys / 2, bd, kIdO, 1u);
+        }
+        umma::commit(smem_addr(pv_bar + (g & 1)));
+        umma::commit(smem_addr(ve_bar + (vc + j) % kVStages));
+      }
+      __syncwarp();
+      // S(g+2) takes chunk g's score buffer (read by the softmax before it
+      // released P(g)) and queues behind P V(g)
+      if (kPSep && j + kSBufs < n) issue_s(k0 + j + kSBufs, g + kSBufs);
+    }
+    kc += 1 + n;
+    vc += n;
+    gc += n;
+    ++tc;
+  };
+
+  // ---- softmax warps: one work item
+  auto softmax_item = [&](const Tile& t) {
+    if (t.status != 0 && tid == 0) set_status(p.status, t.status);
+    if (t.nchunks == 0) {
+      if (t.lens_bad) zero_tile_rows<D>(p, t, kSoftmaxThreads);
+      return;
+    }
+    const int n = t.nchunks;
+    // block ids the tile reads, range-checked at its end (loads in flight
+    // meanwhile); ids past the first 128 blocks are checked there directly
+    const int32_t* tbl = p.block_tables + static_cast<size_t>(t.b) * p.max_blocks;
+    int bid_pre[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) bid_pre[u] = lane + 32 * u < t.nblk ? tbl[lane + 32 * u] : 0;
+    const bool va = ra / G < t.ntok, vb = rb / G < t.ntok;
+    const int qpa = t.pos0 + ra / G, qpb = t.pos0 + rb / G;
+    float ma = -INFINITY, mb = -INFINITY, la = 0.f, lb = 0.f;  // running max, partial sums
+    for (int j = 0; j < n && ok; ++j) {
+      const uint32_t g = gc + j;
+      ok &= mbar_wait_bounded(smem_addr(s_bar + g % kSBufs), (g / kSBufs) & 1);
+      umma::fence_after_sync();
+      const uint32_t tS = tmem + (g % kSBufs) * kKeys + lane_base;
+      uint32_t raw[2][32];
+#pragma unroll
+      for (int hc = 0; hc < 2; ++hc) umma::ld_16x256b_x8(tS + hc * 64, raw[hc]);
       umma::wait_ld();
-      const int kbase = j * kKeys + part * kKeysPerThread;
-      if (j * kKeys + kKeys - 1 > pos0) {  // chunk reaches past some row's position
+      float s[2][32];  // [half of the chunk][register of the 16x256b shape]
 #pragma unroll
-        for (int k = 0; k < kKeysPerThread; ++k)
-          s[k] = (row_valid && kbase + k <= qpos) ? s[k] : -INFINITY;
+      for (int hc = 0; hc < 2; ++hc)
+#pragma unroll
+        for (int i = 0; i < 32; ++i) s[hc][i] = __uint_as_float(raw[hc][i]);
+      // register 4k + 2r + e of half hc: row (r ? rb : ra), key 128j + 64hc + 8k + c2 + e
+      if (j * kKeys + kKeys - 1 > t.pos0) {  // chunk reaches past some row's position
+#pragma unroll
+        for (int hc = 0; hc < 2; ++hc)
+#pragma unroll
+          for (int k = 0; k < 8; ++k)
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+              const int key = j * kKeys + hc * 64 + 8 * k + c2 + e;
+              float& sa = s[hc][4 * k + e];
+              float& sb = s[hc][4 * k + 2 + e];
+              sa = (va && key <= qpa) ? sa : -INFINITY;
+              sb = (vb && key <= qpb) ? sb : -INFINITY;
+            }
       }
       if (!pos_scale) {
 #pragma unroll
-        for (int k = 0; k < kKeysPerThread; ++k)
-          s[k] = s[k] == -INFINITY ? -INFINITY : s[k] * sl2;
-      }
-      float mx0 = fmaxf(s[0], s[1]), mx1 = fmaxf(s[2], s[3]);
-      float mx2 = fmaxf(s[4], s[5]), mx3 = fmaxf(s[6], s[7]);
+        for (int hc = 0; hc < 2; ++hc)
 #pragma unroll
-      for (int k = 8; k < kKeysPerThread; k += 8) {
-        mx0 = fmaxf(mx0, fmaxf(s[k], s[k + 1]));
-        mx1 = fmaxf(mx1, fmaxf(s[k + 2], s[k + 3]));
-        mx2 = fmaxf(mx2, fmaxf(s[k + 4], s[k + 5]));
-        mx3 = fmaxf(mx3, fmaxf(s[k + 6], s[k + 7]));
+          for (int i = 0; i < 32; ++i)
+            s[hc][i] = s[hc][i] == -INFINITY ? -INFINITY : s[hc][i] * sl2;
       }
-      float rowmax = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * mul;
-      {  // one max per row: the partner thread holds the row's other keys
-        float* rb = red + (j & 1) * (kSplit * kRows);
-        rb[part * kRows + row] = rowmax;
-        named_bar_sync(1 + quarter, 32 * kSplit);
-        rowmax = fmaxf(rowmax, rb[(1 - part) * kRows + row]);
-      }
-      const float mnew = fmaxf(m, rowmax);
-      const bool grow = mnew > m + 8.0f;  // lazy: rescale only when the max grows by > 2^8
-      const float alpha = grow ? ex2_approx(m - mnew) : 1.0f;
-      if (grow) {
-        l *= alpha;
-        m = mnew;
-      }
-      // ---- P over this thread's scores in TMEM (it has read them all); a
-      // half whose keys are all masked so far (m = -inf) gets P = 0
-      const float negm = m == -INFINITY ? 0.f : -m;
-      float ps0 = 0.f, ps1 = 0.f, ps2 = 0.f, ps3 = 0.f;
+      // ---- row maxima: this thread's 32 keys of each row, then the row's
+      // four lanes (xor 1, 2)
+      float xa0 = -INFINITY, xa1 = -INFINITY, xb0 = -INFINITY, xb1 = -INFINITY;
 #pragma unroll
-      for (int sub = 0; sub < kKeysPerThread / 32; ++sub) {
-        uint32_t hi[16], lo[16];
+      for (int hc = 0; hc < 2; ++hc)
 #pragma unroll
-        for (int k = 0; k < 32; k += 4) {
-          const float* sk = s + sub * 32 + k;
-          const float p0 = ex2_approx(fmaf(sk[0], mul, negm));
-          const float p1 = ex2_approx(fmaf(sk[1], mul, negm));
-          const float p2 = ex2_approx(fmaf(sk[2], mul, negm));
-          const float p3 = ex2_approx(fmaf(sk[3], mul, negm));
-          ps0 += p0;
-          ps1 += p1;
-          ps2 += p2;
-          ps3 += p3;
-          hi[k / 2] = pack2<kBf16>(p0, p1);
-          hi[k / 2 + 1] = pack2<kBf16>(p2, p3);
+        for (int k = 0; k < 8; ++k) {
+          xa0 = fmaxf(xa0, s[hc][4 * k]);
+          xa1 = fmaxf(xa1, s[hc][4 * k + 1]);
+          xb0 = fmaxf(xb0, s[hc][4 * k + 2]);
+          xb1 = fmaxf(xb1, s[hc][4 * k + 3]);
+        }
+      float mxa = fmaxf(xa0, xa1), mxb = fmaxf(xb0, xb1);
+      mxa = fmaxf(mxa, __shfl_xor_sync(0xffffffffu, mxa, 1));
+      mxb = fmaxf(mxb, __shfl_xor_sync(0xffffffffu, mxb, 1));
+      mxa = fmaxf(mxa, __shfl_xor_sync(0xffffffffu, mxa, 2));
+      mxb = fmaxf(mxb, __shfl_xor_sync(0xffffffffu, mxb, 2));
+      const float mna = fmaxf(ma, mxa * mul), mnb = fmaxf(mb, mxb * mul);
+      // lazy: rescale only when a row's max grows by more than 2^8
+      const bool ga = mna > ma + 8.0f, gb = mnb > mb + 8.0f;
+      const float aa = ga ? ex2_approx(ma - mna) : 1.0f;
+      const float ab = gb ? ex2_approx(mb - mnb) : 1.0f;
+      if (ga) {
+        la *= aa;
+        ma = mna;
+      }
+      if (gb) {
+        lb *= ab;
+        mb = mnb;
+      }
+      // ---- P in key order: the pair (8k + c2, +1) of half hc is P column
+      // 32hc + 4k + lane%4, which is where the 16x128b store puts repetition
+      // k.  A row with all keys masked so far (m = -inf) gets P = 0.
+      const float nma = ma == -INFINITY ? 0.f : -ma;
+      const float nmb = mb == -INFINITY ? 0.f : -mb;
+      uint32_t hi[2][16], lo[2][16];
+#pragma unroll
+      for (int hc = 0; hc < 2; ++hc) {
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const float pa0 = ex2_approx(fmaf(s[hc][4 * k], mul, nma));
+          const float pa1 = ex2_approx(fmaf(s[hc][4 * k + 1], mul, nma));
+          const float pb0 = ex2_approx(fmaf(s[hc][4 * k + 2], mul, nmb));
+          const float pb1 = ex2_approx(fmaf(s[hc][4 * k + 3], mul, nmb));
+          la += pa0 + pa1;
+          lb += pb0 + pb1;
+          hi[hc][2 * k] = pack2<kBf16>(pa0, pa1);
+          hi[hc][2 * k + 1] = pack2<kBf16>(pb0, pb1);
           if constexpr (kBf16) {
-            const float2 h01 = unpack2<true>(hi[k / 2]);
-            const float2 h23 = unpack2<true>(hi[k / 2 + 1]);
-            lo[k / 2] = pack2<true>(p0 - h01.x, p1 - h01.y);
-            lo[k / 2 + 1] = pack2<true>(p2 - h23.x, p3 - h23.y);
+            const float2 ha = unpack2<true>(hi[hc][2 * k]);
+            const float2 hb = unpack2<true>(hi[hc][2 * k + 1]);
+            lo[hc][2 * k] = pack2<true>(pa0 - ha.x, pa1 - ha.y);
+            lo[hc][2 * k + 1] = pack2<true>(pb0 - hb.x, pb1 - hb.y);
           }
         }
-        umma::st16_bits(tS + sub * 16, hi);
-        if constexpr (kBf16) umma::st16_bits(tS + kKeysPerThread / 2 + sub * 16, lo);
       }
-      l += (ps0 + ps1) + (ps2 + ps3);
-      // ---- O: rescale the rows whose max jumped, once P V(j-1) is in it
-      if (__any_sync(0xffffffffu, grow && j > 0)) {
-        ok &= mbar_wait_bounded(smem_addr(pv_bar + ((j - 1) & 1)), ((j - 1) >> 1) & 1);
+      // P V(g-1) must have read its P (own columns) and added into O before
+      // either is written: waited for only where needed, after the exponentials
+      const bool rescale = __any_sync(0xffffffffu, (ga || gb) && j > 0);
+      if (g > 0 && (kPSep || rescale)) {
+        ok &= mbar_wait_bounded(smem_addr(pv_bar + ((g - 1) & 1)), ((g - 1) >> 1) & 1);
         umma::fence_after_sync();
-        o_scale(alpha);
+      }
+      // P over the scores it came from (all read above), or in its own columns
+      const uint32_t tP = kPSep ? tmem + L::kPCol + lane_base : tS;
+#pragma unroll
+      for (int hc = 0; hc < 2; ++hc) {
+        umma::st_16x128b_x8(tP + hc * 32, hi[hc]);
+        if constexpr (kBf16) umma::st_16x128b_x8(tP + kKeys / 2 + hc * 32, lo[hc]);
+      }
+      // ---- O: rescale the rows whose max jumped
+      if (rescale) {
+#pragma unroll
+        for (int c = 0; c < D / 64; ++c) {
+          uint32_t o[32];
+          umma::ld_16x256b_x8(tO + c * 64, o);
+          umma::wait_ld();
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            o[4 * k] = __float_as_uint(__uint_as_float(o[4 * k]) * aa);
+            o[4 * k + 1] = __float_as_uint(__uint_as_float(o[4 * k + 1]) * aa);
+            o[4 * k + 2] = __float_as_uint(__uint_as_float(o[4 * k + 2]) * ab);
+            o[4 * k + 3] = __float_as_uint(__uint_as_float(o[4 * k + 3]) * ab);
+          }
+          umma::st_16x256b_x8(tO + c * 64, o);
+        }
       }
       umma::wait_st();
-      if (j == nchunks - 1 && nkeys - j * kKeys < kKeys) {
+      if (j == n - 1 && t.nkeys - j * kKeys < kKeys) {
         // V rows of keys >= nkeys are never attended (P = 0) but may hold
         // non-finite bytes (slots past the context, blocks not loaded): clear
         // them once the chunk's copies have landed
-        ok &= mbar_wait_bounded(smem_addr(vf_bar + j % kVStages), (j / kVStages) & 1);
-        uint8_t* sV = sm + L::kVOff + (j % kVStages) * L::kKV;
-        const int first = nkeys - j * kKeys;
+        const uint32_t v = vc + j;
+        ok &= mbar_wait_bounded(smem_addr(vf_bar + v % kVStages), (v / kVStages) & 1);
+        uint8_t* sV = sm + L::kVOff + (v % kVStages) * L::kKV;
+        const int first = t.nkeys - j * kKeys;
         for (int idx = tid; idx < (kKeys - first) * L::kHalves * 8; idx += kSoftmaxThreads) {
           const int r = first + idx / (L::kHalves * 8);
           const int rem = idx % (L::kHalves * 8);
@@ -492,56 +630,173 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       umma::fence_before_sync();
       __syncwarp();
-      if (lane == 0) mbar_arrive(smem_addr(p_bar + j % kSBufs));
+      if (lane == 0) mbar_arrive(smem_addr(p_bar + g % kSBufs));
     }
-
-    ok &= mbar_wait_bounded(smem_addr(pv_bar + ((nchunks - 1) & 1)), ((nchunks - 1) >> 1) & 1);
+    // ---- out = O / l.  Range-check every block id the tile read (each warp
+    // for itself): a tile that met an out-of-range id writes zeros.  Every
+    // softmax warp gets here, even after a failed wait, so that the named
+    // barriers below always complete; the first one also agrees on whether
+    // all waits succeeded.
+    bool bad = false;
+#pragma unroll
+    for (int u = 0; u < 4; ++u)
+      bad |= lane + 32 * u < t.nblk && (bid_pre[u] < 0 || bid_pre[u] >= p.num_blocks);
+    for (int i = lane + 128; i < t.nblk; i += 32) {
+      const int bid = tbl[i];
+      bad |= (bid < 0) || (bid >= p.num_blocks);
+    }
+    const uint32_t gl = gc + n - 1;
+    if (ok) ok = mbar_wait_bounded(smem_addr(pv_bar + (gl & 1)), (gl >> 1) & 1);
     umma::fence_after_sync();
-    launch_dependents();
-    // ---- the row's sum over both key halves (their max is shared), then
-    // out = O / l; thread (row, part) writes output columns [part * D/2, +D/2)
-    float* rb = red + 2 * kSplit * kRows;
-    rb[part * kRows + row] = l;
-    named_bar_sync(1 + quarter, 32 * kSplit);
-    const float lt = rb[row] + rb[kRows + row];
-    const float inv = (row_valid && lt > 0.f) ? 1.0f / lt : 0.f;
-    uint16_t* out = static_cast<uint16_t*>(p.out) +
-                    (static_cast<size_t>(q0 + t0 + (row_valid ? my_t : 0)) * p.num_q_heads +
-                     kvh * G + my_g) *
-                        D +
-                    part * (D / 2);
+    bad = __any_sync(0xffffffffu, bad);
+    if (bad && tid == 0) set_status(p.status, kErrBadBlock);
+    // row sums: the four lanes of a row, then through shared memory to the
+    // thread that writes the row out
+    la += __shfl_xor_sync(0xffffffffu, la, 1);
+    lb += __shfl_xor_sync(0xffffffffu, lb, 1);
+    la += __shfl_xor_sync(0xffffffffu, la, 2);
+    lb += __shfl_xor_sync(0xffffffffu, lb, 2);
+    if ((lane & 3) == 0) {
+      red[ra] = la;
+      red[rb] = lb;
+    }
+    // the previous tile's row copies have read the staging buffer
+    if (warp < 4) bulk_wait_read();
+    ok = named_bar_and(1, kSoftmaxThreads, ok);
+    // thread (warp w, lane) finishes half w / 4 of row 32 (w % 4) + lane: O
+    // read with the one-lane-per-row TMEM shape, scaled, packed, staged
+    if (ok) {
+      const int r = quarter * 32 + lane;
+      const int hf = warp >> 2;
+      const float lr = red[r];
+      const float inv = lr > 0.f ? 1.0f / lr : 0.f;
+      const uint32_t tOr = tmem + L::kOCol + hf * (D / 2) + (static_cast<uint32_t>(quarter * 32) << 16);
+      float o[D / 2];
 #pragma unroll
-    for (int c = 0; c < D / 64; ++c) {
-      float o[32];
-      umma::ld32(tOp + c * 32, o);
+      for (int c = 0; c < D / 64; ++c)
+        umma::ld32(tOr + c * 32, *reinterpret_cast<float(*)[32]>(o + c * 32));
       umma::wait_ld();
-      if (row_valid) {
+      uint8_t* srow = stg + r * L::kStgStride + hf * D;
 #pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4) {
-          uint4 w;
-          w.x = pack2<kBf16>(o[8 * q4] * inv, o[8 * q4 + 1] * inv);
-          w.y = pack2<kBf16>(o[8 * q4 + 2] * inv, o[8 * q4 + 3] * inv);
-          w.z = pack2<kBf16>(o[8 * q4 + 4] * inv, o[8 * q4 + 5] * inv);
-          w.w = pack2<kBf16>(o[8 * q4 + 6] * inv, o[8 * q4 + 7] * inv);
-          *reinterpret_cast<uint4*>(out + c * 32 + 8 * q4) = w;
-        }
+      for (int c = 0; c < D / 16; ++c) {  // 16-byte chunk: 8 values
+        uint4 v;
+        v.x = bad ? 0u : pack2<kBf16>(o[8 * c] * inv, o[8 * c + 1] * inv);
+        v.y = bad ? 0u : pack2<kBf16>(o[8 * c + 2] * inv, o[8 * c + 3] * inv);
+        v.z = bad ? 0u : pack2<kBf16>(o[8 * c + 4] * inv, o[8 * c + 5] * inv);
+        v.w = bad ? 0u : pack2<kBf16>(o[8 * c + 6] * inv, o[8 * c + 7] * inv);
+        *reinterpret_cast<uint4*>(srow + 16 * c) = v;
       }
     }
+    fence_proxy_async_smem();
+    named_bar_sync(1, kSoftmaxThreads);
+    // one bulk copy per valid row (warps 0-3: row 32 w + lane)
+    if (ok && warp < 4) {
+      const int r = quarter * 32 + lane;
+      if (r / G < t.ntok) {
+        uint16_t* orow = static_cast<uint16_t*>(p.out) +
+                         (static_cast<size_t>(t.q0 + t.t0 + r / G) * p.num_q_heads +
+                          t.kvh * G + r % G) * D;
+        bulk_store(orow, smem_addr(stg + r * L::kStgStride), D * 2);
+      }
+      bulk_commit();
+    }
+    vc += n;
+    gc += n;
+  };
+
+  // ---- every role walks the same work items: the candidates id =
+  // blockIdx.x + k * gridDim.x, a window of kWindow at a time; the softmax
+  // warps mark those with rows, and each role visits the marked ones in
+  // order, loading the next item's lengths while it works on the current one
+  const long long ncand = (items - blockIdx.x + gridDim.x - 1) / gridDim.x;
+  for (long long w0 = 0; w0 < ncand; w0 += kWindow) {
+    if (warp < kSoftmaxWarps) {
+      bool has = false;
+      const long long k = w0 + tid;
+      if (k < ncand) {
+        Tile t;
+        const long long id = blockIdx.x + k * gridDim.x;
+        has = decode_tile(p, tiles_x, id, load_lens(p, id), t);
+      }
+      const uint32_t bits = __ballot_sync(0xffffffffu, has);
+      if (lane == 0) mask[warp] = bits;
+    }
+    __syncthreads();
+    // next marked candidate after k (-1: none)
+    auto next_item = [&](int k) {
+      for (int wd = (k + 1) >> 5; wd < kWindow / 32; ++wd) {
+        uint32_t m = mask[wd];
+        if (wd == ((k + 1) >> 5)) m &= 0xffffffffu << ((k + 1) & 31);
+        if (m) return wd * 32 + __ffs(m) - 1;
+      }
+      return -1;
+    };
+    auto id_of = [&](int k) { return blockIdx.x + (w0 + k) * gridDim.x; };
+    int k = next_item(-1);
+    ItemLens lens = k >= 0 ? load_lens(p, id_of(k)) : ItemLens{0, 0, 0};
+    while (k >= 0) {
+      const int kn = next_item(k);
+      const ItemLens cur = lens;
+      if (kn >= 0) lens = load_lens(p, id_of(kn));  // in flight meanwhile
+      Tile t;
+      decode_tile(p, tiles_x, id_of(k), cur, t);
+      if (ok) {
+        if (producer) {
+          if (t.nchunks > 0) produce_item(t);
+        } else if (mma_warp) {
+          if (t.nchunks > 0) mma_item(t);
+        } else {
+          softmax_item(t);
+        }
+      }
+      k = kn;
+    }
+    __syncthreads();  // the mask is rewritten for the next window
   }
+
+  if (producer) {
+    // no copy may land after the exit: wait (bounded) for the last slots
+    const uint32_t first = slot > static_cast<uint32_t>(nst) ? slot - nst : 0;
+    for (uint32_t c = first; c < slot; ++c)
+      mbar_wait_bounded(smem_addr(full + c % nst), (c / nst) & 1);
+  } else if (mma_warp) {
+    // every tensor-core op issued by this warp has completed before TMEM is
+    // released
+    if (elect_one()) umma::commit(smem_addr(done_bar));
+    __syncwarp();
+    mbar_wait_bounded(smem_addr(done_bar), 0);
+  }
+  if (warp < 4) bulk_wait_all();  // the output rows have landed
+  launch_dependents();
   umma::fence_before_sync();
   __syncthreads();
   if (mma_warp) umma::dealloc(tmem, L::kTmemCols);
   if (!__syncthreads_and(ok) && tid == 0) set_status(p.status, kErrTimeout);
 }
 
+int sm_count() {
+  static int cached[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 1;
+  if (dev >= 0 && dev < 64 && cached[dev] > 0) return cached[dev];
+  int n = 1;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n < 1)
+    n = 1;
+  if (dev >= 0 && dev < 64) cached[dev] = n;
+  return n;
+}
+
 template <bool kBf16, int D>
 cudaError_t launch_prefill_t(const PrefillParams& p, const CUtensorMap& tq, const CUtensorMap& tk,
-                             const CUtensorMap& tv, int grid_x, cudaStream_t s) {
+                             const CUtensorMap& tv, int tiles_x, cudaStream_t s) {
   constexpr size_t smem = PrefillLayout<kBf16, D>::kSmem;
   cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(&prefill_kernel<kBf16, D>), smem);
   if (e != cudaSuccess) return e;
-  const dim3 grid(grid_x, p.num_kv_heads, p.batch);
-  return launch_pdl(prefill_kernel<kBf16, D>, grid, dim3(kThreads), smem, s, p, tq, tk, tv);
+  // one CTA per SM walks the work items (shared memory keeps it to one)
+  const long long items = static_cast<long long>(tiles_x) * p.batch * p.num_kv_heads;
+  const int grid = static_cast<int>(std::min<long long>(items, sm_count()));
+  return launch_pdl(prefill_kernel<kBf16, D>, dim3(grid), dim3(kThreads), smem, s, p, tq, tk, tv,
+                    tiles_x);
 }
 
 }  // namespace
