@@ -104,24 +104,6 @@ struct PrefillLayout {
   static_assert(kSmem <= 232448, "exceeds the per-block shared-memory limit");
 };
 
-// shared -> global bulk copy (async proxy), tracked by this thread's bulk groups
-__device__ __forceinline__ void bulk_store(void* gdst, uint32_t ssrc, uint32_t bytes) {
-  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(gdst),
-               "r"(ssrc), "r"(bytes)
-               : "memory");
-}
-__device__ __forceinline__ void bulk_commit() {
-  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
-}
-// this thread's bulk copies have read their shared-memory sources
-__device__ __forceinline__ void bulk_wait_read() {
-  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
-}
-// ... and have completed
-__device__ __forceinline__ void bulk_wait_all() {
-  asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
-}
-
 // Named barrier over `nthreads` threads that also ANDs a flag across them.
 __device__ __forceinline__ bool named_bar_and(uint32_t id, uint32_t nthreads, bool v) {
   uint32_t r;
@@ -150,18 +132,20 @@ struct ItemLens {
 
 // Work item `id` of tiles_x * batch * num_kv_heads: the last query tiles of
 // every request first (they attend to the most keys), then the earlier ones.
-__device__ __forceinline__ ItemLens load_lens(const PrefillParams& p, long long id) {
-  const long long per_x = static_cast<long long>(p.batch) * p.num_kv_heads;
-  const int b = static_cast<int>(id % per_x) / p.num_kv_heads;
+// (The launch keeps the number of items below 2^31, so item arithmetic is
+// 32-bit.)
+__device__ __forceinline__ ItemLens load_lens(const PrefillParams& p, int id) {
+  const int per_x = p.batch * p.num_kv_heads;
+  const int b = (id % per_x) / p.num_kv_heads;
   return ItemLens{p.query_start[b], p.query_start[b + 1], p.context_lens[b]};
 }
 
 // Returns false when the item has no rows (the request's chunk is shorter).
-__device__ __forceinline__ bool decode_tile(const PrefillParams& p, int tiles_x, long long id,
+__device__ __forceinline__ bool decode_tile(const PrefillParams& p, int tiles_x, int id,
                                             const ItemLens& lens, Tile& t) {
-  const long long per_x = static_cast<long long>(p.batch) * p.num_kv_heads;
-  const int x = tiles_x - 1 - static_cast<int>(id / per_x);
-  const int r = static_cast<int>(id % per_x);
+  const int per_x = p.batch * p.num_kv_heads;
+  const int x = tiles_x - 1 - id / per_x;
+  const int r = id % per_x;
   t.b = r / p.num_kv_heads;
   t.kvh = r % p.num_kv_heads;
   t.status = 0;
@@ -266,7 +250,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const bool mma_warp = warp == kMmaWarp;
   const bool producer = warp > kMmaWarp;
   const int G = p.group;
-  const long long items = static_cast<long long>(tiles_x) * p.batch * p.num_kv_heads;
+  const int items = tiles_x * p.batch * p.num_kv_heads;  // < 2^31 (checked at launch)
 
   if (mma_warp && lane == 0) {
     prefetch_tensormap(&tmq);
@@ -660,8 +644,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       red[ra] = la;
       red[rb] = lb;
     }
-    // the previous tile's row copies have read the staging buffer
-    if (warp < 4) bulk_wait_read();
+    // (every thread has read the previous tile's staged rows: it passed the
+    // barrier below only after its own reads)
     ok = named_bar_and(1, kSoftmaxThreads, ok);
     // thread (warp w, lane) finishes half w / 4 of row 32 (w % 4) + lane: O
     // read with the one-lane-per-row TMEM shape, scaled, packed, staged
@@ -687,18 +671,22 @@ __global__ void __launch_bounds__(kThreads, 1)
         *reinterpret_cast<uint4*>(srow + 16 * c) = v;
       }
     }
-    fence_proxy_async_smem();
     named_bar_sync(1, kSoftmaxThreads);
-    // one bulk copy per valid row (warps 0-3: row 32 w + lane)
-    if (ok && warp < 4) {
-      const int r = quarter * 32 + lane;
-      if (r / G < t.ntok) {
-        uint16_t* orow = static_cast<uint16_t*>(p.out) +
-                         (static_cast<size_t>(t.q0 + t.t0 + r / G) * p.num_q_heads +
-                          t.kvh * G + r % G) * D;
-        bulk_store(orow, smem_addr(stg + r * L::kStgStride), D * 2);
+    // the staged rows out with coalesced 16-byte stores: each warp writes
+    // kRowsPerStep rows per step, a row's D * 2 bytes over consecutive lanes
+    if (ok) {
+      constexpr int kLanesPerRow = D * 2 / 16;
+      constexpr int kRowsPerStep = 32 / kLanesPerRow;
+      const int sub = lane / kLanesPerRow, ch = lane % kLanesPerRow;
+      for (int r = warp * kRowsPerStep + sub; r < kRows; r += kSoftmaxWarps * kRowsPerStep) {
+        if (r / G < t.ntok) {
+          const uint4 v = *reinterpret_cast<const uint4*>(stg + r * L::kStgStride + ch * 16);
+          uint16_t* orow = static_cast<uint16_t*>(p.out) +
+                           (static_cast<size_t>(t.q0 + t.t0 + r / G) * p.num_q_heads +
+                            t.kvh * G + r % G) * D;
+          *reinterpret_cast<uint4*>(orow + ch * 8) = v;
+        }
       }
-      bulk_commit();
     }
     vc += n;
     gc += n;
@@ -708,14 +696,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   // blockIdx.x + k * gridDim.x, a window of kWindow at a time; the softmax
   // warps mark those with rows, and each role visits the marked ones in
   // order, loading the next item's lengths while it works on the current one
-  const long long ncand = (items - blockIdx.x + gridDim.x - 1) / gridDim.x;
-  for (long long w0 = 0; w0 < ncand; w0 += kWindow) {
+  const int ncand = (items - static_cast<int>(blockIdx.x) + static_cast<int>(gridDim.x) - 1) /
+                    static_cast<int>(gridDim.x);
+  for (int w0 = 0; w0 < ncand; w0 += kWindow) {
     if (warp < kSoftmaxWarps) {
       bool has = false;
-      const long long k = w0 + tid;
+      const int k = w0 + tid;
       if (k < ncand) {
         Tile t;
-        const long long id = blockIdx.x + k * gridDim.x;
+        const int id = static_cast<int>(blockIdx.x) + k * static_cast<int>(gridDim.x);
         has = decode_tile(p, tiles_x, id, load_lens(p, id), t);
       }
       const uint32_t bits = __ballot_sync(0xffffffffu, has);
@@ -731,7 +720,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       return -1;
     };
-    auto id_of = [&](int k) { return blockIdx.x + (w0 + k) * gridDim.x; };
+    auto id_of = [&](int k) {
+      return static_cast<int>(blockIdx.x) + (w0 + k) * static_cast<int>(gridDim.x);
+    };
     int k = next_item(-1);
     ItemLens lens = k >= 0 ? load_lens(p, id_of(k)) : ItemLens{0, 0, 0};
     while (k >= 0) {
@@ -766,7 +757,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
     mbar_wait_bounded(smem_addr(done_bar), 0);
   }
-  if (warp < 4) bulk_wait_all();  // the output rows have landed
   launch_dependents();
   umma::fence_before_sync();
   __syncthreads();
@@ -794,6 +784,7 @@ cudaError_t launch_prefill_t(const PrefillParams& p, const CUtensorMap& tq, cons
   if (e != cudaSuccess) return e;
   // one CTA per SM walks the work items (shared memory keeps it to one)
   const long long items = static_cast<long long>(tiles_x) * p.batch * p.num_kv_heads;
+  if (items >= (1ll << 31)) return cudaErrorInvalidValue;  // item arithmetic is 32-bit
   const int grid = static_cast<int>(std::min<long long>(items, sm_count()));
   return launch_pdl(prefill_kernel<kBf16, D>, dim3(grid), dim3(kThreads), smem, s, p, tq, tk, tv,
                     tiles_x);
