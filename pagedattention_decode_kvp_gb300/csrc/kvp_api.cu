@@ -483,6 +483,10 @@ kvp_status kvp_attention_prefill(void* out, const void* q, const void* k_cache,
   if (r != KVP_OK) return r;
   r = make_pool_map(&tv, v_cache, cache, 2);
   if (r != KVP_OK) return r;
+  // out has q's shape [T, Hq, D]: full tiles leave through the same box
+  CUtensorMap to;
+  r = make_q_map(&to, out, num_query_tokens, num_q_heads, cache.head_dim, group, box_tokens);
+  if (r != KVP_OK) return r;
   PrefillParams p{};
   p.out = out;
   p.q = q;
@@ -500,7 +504,7 @@ kvp_status kvp_attention_prefill(void* out, const void* q, const void* k_cache,
   p.num_tokens = num_query_tokens;
   p.q_box_tokens = box_tokens;
   p.scale_log2 = scale * 1.4426950408889634f;
-  return from_cuda(launch_prefill(p, tq, tk, tv, dtype == KVP_BF16, static_cast<int>(tiles),
+  return from_cuda(launch_prefill(p, tq, tk, tv, to, dtype == KVP_BF16, static_cast<int>(tiles),
                                   reinterpret_cast<cudaStream_t>(stream)));
 }
 

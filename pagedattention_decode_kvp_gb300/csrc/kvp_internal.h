@@ -80,7 +80,8 @@ cudaError_t launch_decode_mma_fp8(const DecodeParams& p, const CUtensorMap& tk,
                                   const CUtensorMap& tv, int grid_x, cudaStream_t s);
 cudaError_t launch_decode_reduce(const DecodeParams& p, cudaStream_t s);
 cudaError_t launch_prefill(const PrefillParams& p, const CUtensorMap& tq, const CUtensorMap& tk,
-                           const CUtensorMap& tv, bool bf16, int grid_x, cudaStream_t s);
+                           const CUtensorMap& tv, const CUtensorMap& to, bool bf16, int grid_x,
+                           cudaStream_t s);
 
 // Launch `kernel` on stream `s` with programmatic stream serialisation, so its
 // CTAs can be scheduled while the previous kernel drains (every kernel of this

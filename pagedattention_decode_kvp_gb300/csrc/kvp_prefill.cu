@@ -72,11 +72,11 @@ struct PrefillLayout {
   static constexpr int kSBufs = 2;                        // TMEM score buffers
   static constexpr uint32_t kKOff = 0;
   static constexpr uint32_t kVOff = kKOff + kKStages * kKV;
-  // output staging: row r (D 16-bit values) at r * kStgStride; the 16 bytes
-  // of padding make one-row-per-lane 16-byte writes conflict-free
-  static constexpr uint32_t kStgStride = D * 2 + 16;
+  // output staging: the O tile in the layout of a Q tile (64-column halves,
+  // 128-byte rows, 128-byte swizzle) -- what the output's TMA store reads,
+  // and conflict-free for one-row-per-lane 16-byte writes
   static constexpr uint32_t kStgOff = kVOff + kVStages * kKV;
-  static constexpr uint32_t kRedOff = kStgOff + kRows * kStgStride;  // [kRows] row sums
+  static constexpr uint32_t kRedOff = kStgOff + kKV;  // [kRows] row sums
   static constexpr uint32_t kMaskOff = kRedOff + kRows * 4;  // [kWindow / 32] work-item bits
   static constexpr uint32_t kBarOff = kMaskOff + kWindow / 8;
   // kfull[], vfull[], kempty[], vempty[], s[], p[], pv[2], q in TMEM, MMA done
@@ -103,6 +103,32 @@ struct PrefillLayout {
   static_assert(2 * kSmem > kSmemPerSm, "TMEM budget assumes one CTA per SM");
   static_assert(kSmem <= 232448, "exceeds the per-block shared-memory limit");
 };
+
+// Swizzled offset of 16-byte chunk c (of 8) of row r in a 128-byte-row tile.
+__device__ __forceinline__ uint32_t sw_chunk(int r, int c) {
+  return static_cast<uint32_t>(r * 128 + (((c & 7) ^ (r & 7)) << 4));
+}
+
+// 3-D tiled tensor store shared -> global (this thread's bulk group).
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, uint32_t src, int32_t x,
+                                             int32_t y, int32_t z) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
+          reinterpret_cast<uint64_t>(map)),
+      "r"(src), "r"(x), "r"(y), "r"(z)
+      : "memory");
+}
+__device__ __forceinline__ void bulk_commit() {
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+// this thread's bulk stores have read their shared-memory sources
+__device__ __forceinline__ void bulk_wait_read() {
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+// ... and have completed
+__device__ __forceinline__ void bulk_wait_all() {
+  asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
 
 // Named barrier over `nthreads` threads that also ANDs a flag across them.
 __device__ __forceinline__ bool named_bar_and(uint32_t id, uint32_t nthreads, bool v) {
@@ -219,7 +245,8 @@ template <bool kBf16, int D>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmq,
                    const __grid_constant__ CUtensorMap tmk,
-                   const __grid_constant__ CUtensorMap tmv, const int tiles_x) {
+                   const __grid_constant__ CUtensorMap tmv,
+                   const __grid_constant__ CUtensorMap tmo, const int tiles_x) {
   using namespace dev;
   using L = PrefillLayout<kBf16, D>;
   constexpr int kKStages = L::kKStages;
@@ -256,6 +283,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     prefetch_tensormap(&tmq);
     prefetch_tensormap(&tmk);
     prefetch_tensormap(&tmv);
+    prefetch_tensormap(&tmo);
     for (int i = 0; i < 2 * (kKStages + kVStages) + kSBufs; ++i)
       mbar_init(smem_addr(kf_bar + i), 1);
     for (int i = 0; i < kSBufs; ++i) mbar_init(smem_addr(p_bar + i), kSoftmaxWarps);
@@ -644,43 +672,62 @@ __global__ void __launch_bounds__(kThreads, 1)
       red[ra] = la;
       red[rb] = lb;
     }
-    // (every thread has read the previous tile's staged rows: it passed the
-    // barrier below only after its own reads)
+    // the previous tile's staged rows have been read: by every thread (it
+    // passed the barrier below only after its own reads) and by the TMA
+    // store thread 0 issued
+    if (tid == 0) bulk_wait_read();
     ok = named_bar_and(1, kSoftmaxThreads, ok);
-    // thread (warp w, lane) finishes half w / 4 of row 32 (w % 4) + lane: O
-    // read with the one-lane-per-row TMEM shape, scaled, packed, staged
+    // thread (warp w, lane) finishes columns [D/2 (w / 4), +D/2) of row
+    // 32 (w % 4) + lane: O read with the one-lane-per-row TMEM shape, scaled,
+    // packed and staged
     if (ok) {
       const int r = quarter * 32 + lane;
       const int hf = warp >> 2;
       const float lr = red[r];
       const float inv = lr > 0.f ? 1.0f / lr : 0.f;
-      const uint32_t tOr = tmem + L::kOCol + hf * (D / 2) + (static_cast<uint32_t>(quarter * 32) << 16);
+      const uint32_t tOr =
+          tmem + L::kOCol + hf * (D / 2) + (static_cast<uint32_t>(quarter * 32) << 16);
       float o[D / 2];
 #pragma unroll
       for (int c = 0; c < D / 64; ++c)
         umma::ld32(tOr + c * 32, *reinterpret_cast<float(*)[32]>(o + c * 32));
       umma::wait_ld();
-      uint8_t* srow = stg + r * L::kStgStride + hf * D;
 #pragma unroll
       for (int c = 0; c < D / 16; ++c) {  // 16-byte chunk: 8 values
+        const int cc = hf * (D / 16) + c;  // chunk of the full row
         uint4 v;
         v.x = bad ? 0u : pack2<kBf16>(o[8 * c] * inv, o[8 * c + 1] * inv);
         v.y = bad ? 0u : pack2<kBf16>(o[8 * c + 2] * inv, o[8 * c + 3] * inv);
         v.z = bad ? 0u : pack2<kBf16>(o[8 * c + 4] * inv, o[8 * c + 5] * inv);
         v.w = bad ? 0u : pack2<kBf16>(o[8 * c + 6] * inv, o[8 * c + 7] * inv);
-        *reinterpret_cast<uint4*>(srow + 16 * c) = v;
+        *reinterpret_cast<uint4*>(stg + (cc >> 3) * (kRows * 128) + sw_chunk(r, cc)) = v;
       }
     }
+    fence_proxy_async_smem();
     named_bar_sync(1, kSoftmaxThreads);
-    // the staged rows out with coalesced 16-byte stores: each warp writes
-    // kRowsPerStep rows per step, a row's D * 2 bytes over consecutive lanes
     if (ok) {
-      constexpr int kLanesPerRow = D * 2 / 16;
-      constexpr int kRowsPerStep = 32 / kLanesPerRow;
-      const int sub = lane / kLanesPerRow, ch = lane % kLanesPerRow;
-      for (int r = warp * kRowsPerStep + sub; r < kRows; r += kSoftmaxWarps * kRowsPerStep) {
-        if (r / G < t.ntok) {
-          const uint4 v = *reinterpret_cast<const uint4*>(stg + r * L::kStgStride + ch * 16);
+      if (t.ntok == kRows / G) {
+        // a full tile: one TMA store per 64-column half, (token, head) rows
+        // as the Q tile came in
+        if (tid == 0) {
+#pragma unroll
+          for (int hf = 0; hf < L::kHalves; ++hf)
+            tma_store_3d(&tmo, smem_addr(stg + hf * (kRows * 128)), hf * 64, t.kvh * G,
+                         t.q0 + t.t0);
+          bulk_commit();
+        }
+      } else {
+        // a partial tile (its box would cover later tokens): the valid rows
+        // with coalesced 16-byte stores, a row's D * 2 bytes over consecutive
+        // lanes
+        constexpr int kLanesPerRow = D * 2 / 16;
+        constexpr int kRowsPerStep = 32 / kLanesPerRow;
+        const int sub = lane / kLanesPerRow, ch = lane % kLanesPerRow;
+        const int nrows = t.ntok * G;
+#pragma unroll 4
+        for (int r = warp * kRowsPerStep + sub; r < nrows; r += kSoftmaxWarps * kRowsPerStep) {
+          const uint4 v = *reinterpret_cast<const uint4*>(stg + (ch >> 3) * (kRows * 128) +
+                                                          sw_chunk(r, ch));
           uint16_t* orow = static_cast<uint16_t*>(p.out) +
                            (static_cast<size_t>(t.q0 + t.t0 + r / G) * p.num_q_heads +
                             t.kvh * G + r % G) * D;
@@ -757,6 +804,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
     mbar_wait_bounded(smem_addr(done_bar), 0);
   }
+  if (tid == 0) bulk_wait_all();  // the output tiles have landed
   launch_dependents();
   umma::fence_before_sync();
   __syncthreads();
@@ -778,7 +826,8 @@ int sm_count() {
 
 template <bool kBf16, int D>
 cudaError_t launch_prefill_t(const PrefillParams& p, const CUtensorMap& tq, const CUtensorMap& tk,
-                             const CUtensorMap& tv, int tiles_x, cudaStream_t s) {
+                             const CUtensorMap& tv, const CUtensorMap& to, int tiles_x,
+                             cudaStream_t s) {
   constexpr size_t smem = PrefillLayout<kBf16, D>::kSmem;
   cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(&prefill_kernel<kBf16, D>), smem);
   if (e != cudaSuccess) return e;
@@ -787,17 +836,18 @@ cudaError_t launch_prefill_t(const PrefillParams& p, const CUtensorMap& tq, cons
   if (items >= (1ll << 31)) return cudaErrorInvalidValue;  // item arithmetic is 32-bit
   const int grid = static_cast<int>(std::min<long long>(items, sm_count()));
   return launch_pdl(prefill_kernel<kBf16, D>, dim3(grid), dim3(kThreads), smem, s, p, tq, tk, tv,
-                    tiles_x);
+                    to, tiles_x);
 }
 
 }  // namespace
 
 cudaError_t launch_prefill(const PrefillParams& p, const CUtensorMap& tq, const CUtensorMap& tk,
-                           const CUtensorMap& tv, bool bf16, int grid_x, cudaStream_t s) {
-  if (!bf16 && p.head_dim == 64) return launch_prefill_t<false, 64>(p, tq, tk, tv, grid_x, s);
-  if (!bf16 && p.head_dim == 128) return launch_prefill_t<false, 128>(p, tq, tk, tv, grid_x, s);
-  if (bf16 && p.head_dim == 64) return launch_prefill_t<true, 64>(p, tq, tk, tv, grid_x, s);
-  if (bf16 && p.head_dim == 128) return launch_prefill_t<true, 128>(p, tq, tk, tv, grid_x, s);
+                           const CUtensorMap& tv, const CUtensorMap& to, bool bf16, int grid_x,
+                           cudaStream_t s) {
+  if (!bf16 && p.head_dim == 64) return launch_prefill_t<false, 64>(p, tq, tk, tv, to, grid_x, s);
+  if (!bf16 && p.head_dim == 128) return launch_prefill_t<false, 128>(p, tq, tk, tv, to, grid_x, s);
+  if (bf16 && p.head_dim == 64) return launch_prefill_t<true, 64>(p, tq, tk, tv, to, grid_x, s);
+  if (bf16 && p.head_dim == 128) return launch_prefill_t<true, 128>(p, tq, tk, tv, to, grid_x, s);
   return cudaErrorInvalidValue;
 }
 
