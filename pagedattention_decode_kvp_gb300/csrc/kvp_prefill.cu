@@ -130,6 +130,39 @@ __device__ __forceinline__ void bulk_wait_all() {
   asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
 }
 
+// Three-input max; packed two-lane fp32 arithmetic (each lane rounds as the
+// scalar instruction would).
+__device__ __forceinline__ float max3f(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+__device__ __forceinline__ uint64_t f2pack(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ float2 f2unpack(uint64_t x) {
+  float2 r;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(r.x), "=f"(r.y) : "l"(x));
+  return r;
+}
+__device__ __forceinline__ uint64_t ffma2(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t r;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+  return r;
+}
+__device__ __forceinline__ uint64_t fadd2(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ uint64_t fmul2(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+
 // Named barrier over `nthreads` threads that also ANDs a flag across them.
 __device__ __forceinline__ bool named_bar_and(uint32_t id, uint32_t nthreads, bool v) {
   uint32_t r;
@@ -499,7 +532,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int u = 0; u < 4; ++u) bid_pre[u] = lane + 32 * u < t.nblk ? tbl[lane + 32 * u] : 0;
     const bool va = ra / G < t.ntok, vb = rb / G < t.ntok;
     const int qpa = t.pos0 + ra / G, qpb = t.pos0 + rb / G;
-    float ma = -INFINITY, mb = -INFINITY, la = 0.f, lb = 0.f;  // running max, partial sums
+    float ma = -INFINITY, mb = -INFINITY;  // running row maxima
+    uint64_t la2 = 0, lb2 = 0;             // partial row sums, two per row (packed; fp16)
+    float la = 0.f, lb = 0.f;              // partial row sums (bf16)
     for (int j = 0; j < n && ok; ++j) {
       const uint32_t g = gc + j;
       ok &= mbar_wait_bounded(smem_addr(s_bar + g % kSBufs), (g / kSBufs) & 1);
@@ -536,17 +571,17 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int i = 0; i < 32; ++i)
             s[hc][i] = s[hc][i] == -INFINITY ? -INFINITY : s[hc][i] * sl2;
       }
-      // ---- row maxima: this thread's 32 keys of each row, then the row's
-      // four lanes (xor 1, 2)
+      // ---- row maxima: this thread's 32 keys of each row (three-input
+      // max, two chains per row), then the row's four lanes (xor 1, 2)
       float xa0 = -INFINITY, xa1 = -INFINITY, xb0 = -INFINITY, xb1 = -INFINITY;
 #pragma unroll
       for (int hc = 0; hc < 2; ++hc)
 #pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          xa0 = fmaxf(xa0, s[hc][4 * k]);
-          xa1 = fmaxf(xa1, s[hc][4 * k + 1]);
-          xb0 = fmaxf(xb0, s[hc][4 * k + 2]);
-          xb1 = fmaxf(xb1, s[hc][4 * k + 3]);
+        for (int k = 0; k < 8; k += 2) {
+          xa0 = max3f(xa0, s[hc][4 * k], s[hc][4 * k + 1]);
+          xa1 = max3f(xa1, s[hc][4 * k + 4], s[hc][4 * k + 5]);
+          xb0 = max3f(xb0, s[hc][4 * k + 2], s[hc][4 * k + 3]);
+          xb1 = max3f(xb1, s[hc][4 * k + 6], s[hc][4 * k + 7]);
         }
       float mxa = fmaxf(xa0, xa1), mxb = fmaxf(xb0, xb1);
       mxa = fmaxf(mxa, __shfl_xor_sync(0xffffffffu, mxa, 1));
@@ -559,29 +594,48 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float aa = ga ? ex2_approx(ma - mna) : 1.0f;
       const float ab = gb ? ex2_approx(mb - mnb) : 1.0f;
       if (ga) {
+        la2 = fmul2(la2, f2pack(aa, aa));
         la *= aa;
         ma = mna;
       }
       if (gb) {
+        lb2 = fmul2(lb2, f2pack(ab, ab));
         lb *= ab;
         mb = mnb;
       }
       // ---- P in key order: the pair (8k + c2, +1) of half hc is P column
       // 32hc + 4k + lane%4, which is where the 16x128b store puts repetition
       // k.  A row with all keys masked so far (m = -inf) gets P = 0.
+      // (pairs of keys go through the packed two-lane FMA and add)
       const float nma = ma == -INFINITY ? 0.f : -ma;
       const float nmb = mb == -INFINITY ? 0.f : -mb;
+      const uint64_t mul2 = f2pack(mul, mul);
+      const uint64_t nma2 = f2pack(nma, nma), nmb2 = f2pack(nmb, nmb);
       uint32_t hi[2][16], lo[2][16];
 #pragma unroll
       for (int hc = 0; hc < 2; ++hc) {
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
-          const float pa0 = ex2_approx(fmaf(s[hc][4 * k], mul, nma));
-          const float pa1 = ex2_approx(fmaf(s[hc][4 * k + 1], mul, nma));
-          const float pb0 = ex2_approx(fmaf(s[hc][4 * k + 2], mul, nmb));
-          const float pb1 = ex2_approx(fmaf(s[hc][4 * k + 3], mul, nmb));
-          la += pa0 + pa1;
-          lb += pb0 + pb1;
+          float pa0, pa1, pb0, pb1;
+          if constexpr (!kBf16) {
+            const float2 ta =
+                f2unpack(ffma2(f2pack(s[hc][4 * k], s[hc][4 * k + 1]), mul2, nma2));
+            const float2 tb =
+                f2unpack(ffma2(f2pack(s[hc][4 * k + 2], s[hc][4 * k + 3]), mul2, nmb2));
+            pa0 = ex2_approx(ta.x);
+            pa1 = ex2_approx(ta.y);
+            pb0 = ex2_approx(tb.x);
+            pb1 = ex2_approx(tb.y);
+            la2 = fadd2(la2, f2pack(pa0, pa1));
+            lb2 = fadd2(lb2, f2pack(pb0, pb1));
+          } else {  // (the bf16 residuals leave no registers for the pairs)
+            pa0 = ex2_approx(fmaf(s[hc][4 * k], mul, nma));
+            pa1 = ex2_approx(fmaf(s[hc][4 * k + 1], mul, nma));
+            pb0 = ex2_approx(fmaf(s[hc][4 * k + 2], mul, nmb));
+            pb1 = ex2_approx(fmaf(s[hc][4 * k + 3], mul, nmb));
+            la += pa0 + pa1;
+            lb += pb0 + pb1;
+          }
           hi[hc][2 * k] = pack2<kBf16>(pa0, pa1);
           hi[hc][2 * k + 1] = pack2<kBf16>(pb0, pb1);
           if constexpr (kBf16) {
@@ -664,6 +718,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (bad && tid == 0) set_status(p.status, kErrBadBlock);
     // row sums: the four lanes of a row, then through shared memory to the
     // thread that writes the row out
+    if constexpr (!kBf16) {
+      la = f2unpack(la2).x + f2unpack(la2).y;
+      lb = f2unpack(lb2).x + f2unpack(lb2).y;
+    }
     la += __shfl_xor_sync(0xffffffffu, la, 1);
     lb += __shfl_xor_sync(0xffffffffu, lb, 1);
     la += __shfl_xor_sync(0xffffffffu, la, 2);
