@@ -300,15 +300,21 @@ kvp_status kvp_attention_decode_fp8(void* out, const void* q, kvp_dtype q_dtype,
  *                 row i of request b (L = its row count) sits at position
  *                 n - L + i and attends to positions 0 .. n - L + i:
  *                 out = sum_j softmax_j(scale * q.K_j) V_j (causal mask).
- *   max_query_len an upper bound on every request's L; it sizes the grid.
+ *   max_query_len an upper bound on every request's L; with the batch and
+ *                 the kv heads it sizes the list of 128-row work items
+ *                 (ceil(max_query_len * G / 128) per request and kv head),
+ *                 which must stay below 2^31 (KVP_ERR_UNSUPPORTED otherwise).
  *   k/v cache, block_tables, max_blocks_per_seq, cache: as kvp_attention_decode.
  * num_q_heads / num_kv_heads must divide 128 (KVP_ERR_UNSUPPORTED otherwise).
  * Device-side errors (*dev_status): KVP_ERR_BAD_BLOCK when a block id is out of
- * range, L > n, n > max_blocks_per_seq * 16 or L > max_query_len (the rows of
- * the offending request that are reached are written as zeros), or when a
- * request's rows reach past num_query_tokens (nothing of it is written);
- * KVP_ERR_TIMEOUT when a pipeline wait gave up.  Computed on the tensor cores
- * with float32 accumulation; no workspace.
+ * range (every 128-row tile that reads one is written as zeros), when L > n,
+ * n > max_blocks_per_seq * 16 or L > max_query_len (the request's rows that
+ * are reached are written as zeros), or when a request's rows reach past
+ * num_query_tokens (nothing of it is written); KVP_ERR_TIMEOUT when a pipeline
+ * wait gave up; KVP_ERR_UNSUPPORTED if the device placed the kernel's shared
+ * memory off a 1024-byte boundary (nothing is computed; not expected).
+ * Computed on the tensor cores with float32 accumulation by one persistent
+ * block per SM; no workspace.
  */
 kvp_status kvp_attention_prefill(void* out, const void* q, const void* k_cache,
                                  const void* v_cache, const int32_t* block_tables,

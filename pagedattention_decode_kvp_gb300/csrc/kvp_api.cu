@@ -471,8 +471,7 @@ kvp_status kvp_attention_prefill(void* out, const void* q, const void* k_cache,
   if (!aligned(out, 16) || !aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16))
     return KVP_ERR_INVALID_ARG;
   const long long tiles = (static_cast<long long>(max_query_len) * group + 127) / 128;
-  if (tiles > 0x7fffffffll || cache.num_kv_heads > 65535 || batch > 65535)
-    return KVP_ERR_UNSUPPORTED;
+  if (tiles * batch * cache.num_kv_heads > 0x7fffffffll) return KVP_ERR_UNSUPPORTED;
 
   const int box_tokens = std::min(128 / group, static_cast<int>(num_query_tokens));
   CUtensorMap tq, tk, tv;

@@ -133,5 +133,11 @@ def test_prefill_invalid_arguments_fail_before_any_launch(lib):
     assert call() == kvp.KVP_ERR_INVALID_ARG
     # nothing to do: no-ops even with null buffers
     assert call(batch=0) == kvp.KVP_OK
+    # a work list of 2^31 or more 128-row items is refused before any launch
+    # (fake, aligned, never dereferenced buffer addresses)
+    A = ctypes.c_void_p(1 << 20)
+    big = lib.kvp_attention_prefill(A, A, A, A, A, 16, A, A, 64, 65535, _desc().num_kv_heads,
+                                    0x7fffffff, 0.125, _desc(), 0, A, P)
+    assert big == kvp.KVP_ERR_UNSUPPORTED
     assert call(mql=0) == kvp.KVP_OK
     assert call(T=0) == kvp.KVP_OK
