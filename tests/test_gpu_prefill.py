@@ -4,10 +4,11 @@ called through the C ABI, against the fp64 CPU oracle on the same seeded inputs.
 Bar: within 3e-3 absolute OR 1e-2 relative of the oracle, element by element
 (the same bar as the decode: fp16/bf16 inputs, fp32 accumulation, P rounded to
 the input type -- bf16 P carried as a high part plus a bf16 residual).
-Cases span several 128-row query tiles and 64-key chunks with ragged tails, a
+Cases span several 128-row query tiles and 128-key chunks with ragged tails
+(full tiles leave through a TMA store, partial ones through plain stores), a
 whole-prompt prefill, chunks that start mid-context, single-token chunks, empty
-chunks, NaN in every pool slot no request owns, and the data errors the header
-documents."""
+chunks, NaN in every pool slot no request owns, a sparse work list longer than
+one scan window per block, and the data errors the header documents."""
 import numpy as np
 import pytest
 import torch
@@ -199,9 +200,10 @@ def test_prefix_prefill_workload_full_size_sampled():
 
 
 def test_context_beyond_the_staged_table():
-    """A 17000-token context (1063 blocks) reaches past the block ids a tile
-    keeps on chip; the chunk's last rows read those blocks from the table in
-    global memory.  Sampled rows against the oracle."""
+    """A 17000-token context (1063 blocks) reaches past the 128 block ids the
+    softmax warps load ahead for their range check (the rest are checked at
+    the tile's end) and past any short table.  Sampled rows against the
+    oracle."""
     w = workloads.make_prefill(B=2, Hq=8, Hkv=2, D=128, lens=[17000, 300], qlens=[150, 300],
                                num_blocks=1100, dtype=torch.float16, seed=31)
     out = run_gpu(w)
@@ -230,3 +232,31 @@ def test_rows_past_num_query_tokens_set_status_and_write_nothing():
     ref = oracle.attention_prefill(w.q[:40], w.k_pool, w.v_pool, w.block_tables[:1],
                                    w.context_lens[:1], w.query_start[:2], w.scale)
     assert_close(out[:40], ref, "request before the overflowing one")
+
+
+def test_sparse_work_list_spans_several_windows():
+    """100 requests with G = 8 and one 1024-token chunk among chunks of at most
+    64 tokens: max_query_len makes 64 tiles per (request, kv head), 51 200 work
+    items, so each persistent block scans more than one window of candidates
+    and skips most of them.  Sampled rows (every request's first and last row
+    among them) against the oracle."""
+    rng = np.random.default_rng(41)
+    qlens = [int(x) for x in rng.integers(1, 65, size=100)]
+    qlens[37] = 1024
+    lens = [q + int(p) for q, p in zip(qlens, rng.integers(0, 200, size=100))]
+    nb = sum(-(-n // 16) for n in lens) + 8
+    w = workloads.make_prefill(B=100, Hq=64, Hkv=8, D=64, lens=lens, qlens=qlens, num_blocks=nb,
+                               dtype=torch.float16, seed=43)
+    assert w.max_query_len == 1024
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out = run_gpu(w, status)
+    assert kvp.kvp_read_status(status) == kvp.KVP_OK
+    qs = w.query_start.cpu().numpy()
+    t = list(rng.integers(0, w.T, size=128)) + [int(x) for x in qs[:-1]] + \
+        [int(x) - 1 for x in qs[1:]]
+    h = list(rng.integers(0, w.Hq, size=len(t)))
+    rows = np.stack([np.array(t), np.array(h)], axis=1).astype(np.int32)
+    ref = oracle.attention_prefill(w.q, w.k_pool, w.v_pool, w.block_tables, w.context_lens,
+                                   w.query_start, w.scale, rows=rows)
+    got = out.cpu()[torch.tensor(t).long(), torch.tensor(h).long()]
+    assert_close(got, ref, "sparse work list")
