@@ -437,7 +437,8 @@ def run_ours(args):
     # the fused partition pass also moves the appended rows (read source, write slot)
     partial_bytes = dbytes["partial_pass"] + (append_bytes(w) if step.fused else 0)
     achieved = partial_bytes / (partial_ms / 1e3) / 1e9
-    traffic = profiled_traffic(args.workload)
+    # the committed counters are for the full-size workload only
+    traffic = None if args.batch else profiled_traffic(args.workload)
     res = {
         "metric": METRIC,
         "value": round(value, 2),
@@ -694,7 +695,8 @@ def run_prefill(args):
         "query_tokens_per_s": round(q_tokens_per_s, 1),
         "roofline": {"bound": "tensor", "achieved": round(achieved, 3), "peak": peak,
                      "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
-                     "traffic": profiled_traffic(args.workload, PREFILL_SOURCES),
+                     "traffic": (None if args.batch
+                                 else profiled_traffic(args.workload, PREFILL_SOURCES)),
                      "kernel": "prefill_kernel", "peak_source": peak_src,
                      "algorithmic_flops_per_launch": flops,
                      "launch_ms": round(kernel_ms, 5)},
