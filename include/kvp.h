@@ -361,6 +361,18 @@ kvp_status kvp_attention_decode_noalloc(void* out, const void* q, const void* k_
                                         kvp_stream_t stream);
 
 /*
+ * kvp_selftest_wait_timeout -- a diagnostic (the pages have no counterpart):
+ * launches one block that waits, through the same bounded mbarrier wait every
+ * pipeline of this library uses, on a barrier that nothing arrives on, and
+ * gives up after `limit_ns` nanoseconds of wall-clock time (1e3 .. 5e9), as
+ * the kernels do after 2 s when a copy or a hand-off never comes.  The wait
+ * records KVP_ERR_TIMEOUT in *dev_status (if it still holds KVP_OK); nothing
+ * faults and the stream stays usable.  Returns KVP_ERR_INVALID_ARG for a null
+ * status or a limit outside the range, KVP_ERR_CUDA if the launch fails.
+ */
+kvp_status kvp_selftest_wait_timeout(int32_t* dev_status, int64_t limit_ns, kvp_stream_t stream);
+
+/*
  * kvp_read_status -- synchronise `stream`, read the device status word and
  * return it as a kvp_status (KVP_ERR_CUDA if the read fails).  Does not reset
  * the word; write 0 to it to clear.

@@ -85,6 +85,7 @@ SIGNATURES = {
     "kvp_attention_prefill": (_I32, [_P, _P, _P, _P, _P, _I32, _P, _P, _I32, _I32, _I32, _I32,
                                      _F, _D, _I32, _P, _P]),
     "kvp_read_status": (_I32, [_P, _P]),
+    "kvp_selftest_wait_timeout": (_I32, [_P, _I64, _P]),
     "kvp_bm_create": (_P, [_I32, _I32, _I64]),
     "kvp_bm_destroy": (None, [_P]),
     "kvp_bm_allocate": (_I32, [_P, _I64, _I32, _I32]),
@@ -366,6 +367,15 @@ def kvp_attention_prefill(out, q, k_cache, v_cache, block_tables, context_lens, 
         int(block_tables.shape[1]), _ptr(context_lens), _ptr(query_start), T, B, Hq,
         int(max_query_len), float(scale), cache_desc(k_cache), _dtype_code(q), _ptr(status),
         _stream_ptr(stream)), "kvp_attention_prefill")
+
+
+def kvp_selftest_wait_timeout(status, limit_ns, stream=None):
+    """Run the library's bounded mbarrier wait on a barrier nothing arrives
+    on, giving up after limit_ns: it records KVP_ERR_TIMEOUT in `status`."""
+    _need_cuda(status)
+    _check(load_library().kvp_selftest_wait_timeout(_ptr(status), int(limit_ns),
+                                                     _stream_ptr(stream)),
+           "kvp_selftest_wait_timeout")
 
 
 def kvp_read_status(status, stream=None) -> int:

@@ -30,6 +30,7 @@ SOURCES = [
     "kvp_prefill.cu",
     "kvp_block_manager.cpp",
     "kvp_noalloc.cu",
+    "kvp_selftest.cu",
 ]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC,-O3",

@@ -507,6 +507,14 @@ kvp_status kvp_attention_prefill(void* out, const void* q, const void* k_cache,
                                   reinterpret_cast<cudaStream_t>(stream)));
 }
 
+kvp_status kvp_selftest_wait_timeout(int32_t* dev_status, int64_t limit_ns,
+                                     kvp_stream_t stream) {
+  if (dev_status == nullptr || limit_ns < 1000 || limit_ns > 5000000000ll)
+    return KVP_ERR_INVALID_ARG;
+  return from_cuda(launch_selftest_wait(dev_status, static_cast<uint64_t>(limit_ns),
+                                        reinterpret_cast<cudaStream_t>(stream)));
+}
+
 kvp_status kvp_read_status(const int32_t* dev_status, kvp_stream_t stream) {
   if (dev_status == nullptr) return KVP_ERR_INVALID_ARG;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);

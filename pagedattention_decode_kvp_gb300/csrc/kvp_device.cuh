@@ -111,15 +111,17 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 }
 
 // Wait for the phase with `parity` to complete, giving up after about
-// kWaitTimeoutNs of wall-clock time (and after a hard iteration cap), so a lost
-// transfer can never hang the GPU.  Returns false on timeout.
+// `limit_ns` of wall-clock time (kWaitTimeoutNs unless a self-test asks for
+// less) and after a hard iteration cap, so a lost transfer can never hang the
+// GPU.  Returns false on timeout.
 constexpr uint64_t kWaitTimeoutNs = 2000000000ull;
-__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity) {
+__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
+                                                  uint64_t limit_ns = kWaitTimeoutNs) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_timer_ns();
   for (uint32_t i = 0; i < (1u << 28); ++i) {
     if (mbar_try_wait(bar, parity)) return true;
-    if ((i & 63u) == 63u && global_timer_ns() - t0 > kWaitTimeoutNs) return false;
+    if ((i & 63u) == 63u && global_timer_ns() - t0 > limit_ns) return false;
   }
   return false;
 }

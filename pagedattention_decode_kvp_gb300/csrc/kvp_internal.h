@@ -79,6 +79,10 @@ cudaError_t launch_decode_mma_int8(const DecodeParams& p, const CUtensorMap& tk,
 cudaError_t launch_decode_mma_fp8(const DecodeParams& p, const CUtensorMap& tk,
                                   const CUtensorMap& tv, int grid_x, cudaStream_t s);
 cudaError_t launch_decode_reduce(const DecodeParams& p, cudaStream_t s);
+// Self-test of the bounded wait: one block waits on a barrier nothing arrives
+// on, for at most limit_ns, and records kErrTimeout when it gives up.
+cudaError_t launch_selftest_wait(int32_t* status, uint64_t limit_ns, cudaStream_t s);
+
 cudaError_t launch_prefill(const PrefillParams& p, const CUtensorMap& tq, const CUtensorMap& tk,
                            const CUtensorMap& tv, const CUtensorMap& to, bool bf16, int grid_x,
                            cudaStream_t s);

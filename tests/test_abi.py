@@ -111,6 +111,13 @@ def test_product_fails_loudly_without_library(monkeypatch, tmp_path):
         kvp.load_library()
 
 
+def test_selftest_wait_checks_its_arguments_before_launch(lib):
+    A = ctypes.c_void_p(1 << 20)
+    assert lib.kvp_selftest_wait_timeout(None, 1_000_000, None) == kvp.KVP_ERR_INVALID_ARG
+    assert lib.kvp_selftest_wait_timeout(A, 0, None) == kvp.KVP_ERR_INVALID_ARG
+    assert lib.kvp_selftest_wait_timeout(A, 6_000_000_000, None) == kvp.KVP_ERR_INVALID_ARG
+
+
 def test_prefill_invalid_arguments_fail_before_any_launch(lib):
     P = None
     inf = float("inf")
