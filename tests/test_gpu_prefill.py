@@ -58,7 +58,10 @@ def run_gpu(w, status=None, max_query_len=None, out=None, q=None):
 # token, an empty chunk, exact multiples of 64 and 128.
 CASES = [(300, 300), (1030, 200), (17, 1), (50, 0), (64, 64), (129, 129), (200, 37),
          (16, 16), (1, 1), (520, 130)]
-SHAPES = [(4, 4, 128), (8, 2, 64), (16, 2, 128), (8, 1, 128), (32, 4, 64)]
+# (Hq, Hkv, D): groups G = 1, 4, 8 and the extremes 32 (4 tokens per 128-row
+# tile) and 128 (one token with all its heads per tile)
+SHAPES = [(4, 4, 128), (8, 2, 64), (16, 2, 128), (8, 1, 128), (32, 4, 64), (64, 2, 64),
+          (128, 1, 64)]
 
 
 @pytest.mark.parametrize("dtype", [torch.float16, torch.bfloat16])
