@@ -475,3 +475,36 @@ def test_prefill_single_token_chunks_equal_decode():
     pre = oracle.attention_prefill(q, kp, vp, tables, lens, [0, 1, 2], 0.2)
     dec = oracle.attention_decode(q, kp, vp, tables, lens, 0.2)
     np.testing.assert_allclose(pre, dec, rtol=1e-13, atol=1e-14)
+
+
+def test_prefill_first_query_of_a_prompt_returns_v0():
+    """A whole-prompt prefill's first query sits at position 0 and attends to
+    key 0 alone: its output is V[0] exactly (widened), whatever q and K hold."""
+    g = torch.Generator().manual_seed(62)
+    lens = [37]
+    q = torch.randn(37, 4, 64, generator=g).half()
+    K = torch.randn(1, 2, 37, 64, generator=g).half()
+    V = torch.randn(1, 2, 37, 64, generator=g).half()
+    kp, vp, tables = _paged_from_dense(K, V, lens, 8, seed=7)
+    out = oracle.attention_prefill(q, kp, vp, tables, lens, [0, 37], 0.125)
+    for h in range(4):  # query heads 0, 1 read kv head 0; 2, 3 read kv head 1
+        assert np.array_equal(out[0, h], V[0, h // 2, 0].double().numpy())
+
+
+def test_prefill_never_reads_keys_after_the_query():
+    """Causality: changing K/V at positions past a query's own leaves its row
+    bit-identical, and changes the rows that can see them."""
+    g = torch.Generator().manual_seed(63)
+    lens, L = [50], 20              # queries at positions 30 .. 49
+    q = torch.randn(L, 4, 64, generator=g).half()
+    K = torch.randn(1, 2, 50, 64, generator=g).half()
+    V = torch.randn(1, 2, 50, 64, generator=g).half()
+    kp, vp, tables = _paged_from_dense(K, V, lens, 8, seed=8)
+    base = oracle.attention_prefill(q, kp, vp, tables, lens, [0, L], 0.125)
+    K2, V2 = K.clone(), V.clone()
+    K2[:, :, 40:] = torch.randn(1, 2, 10, 64, generator=g).half()
+    V2[:, :, 40:] = torch.randn(1, 2, 10, 64, generator=g).half()
+    kp2, vp2, _ = _paged_from_dense(K2, V2, lens, 8, seed=8)
+    moved = oracle.attention_prefill(q, kp2, vp2, tables, lens, [0, L], 0.125)
+    assert np.array_equal(base[:10], moved[:10])       # positions 30 .. 39
+    assert not np.allclose(base[10:], moved[10:])      # positions 40 .. 49 see the change
