@@ -6,7 +6,14 @@ the workload has them), append of the step's new tokens (INT8-quantising for the
 INT8 workload), paged decode attention (partition pass + reduce).  Inputs are
 resident in HBM when the timed region starts; `value` is whole-job achieved HBM
 GB/s over the step's algorithmic bytes, timed with CUDA events on the launching
-stream.  Prints ONE JSON line (rank 0).
+stream around the K steps only; the dominant kernel's own time (the roofline
+numerator) comes from a separate pass of the same steps with events around it.
+Prints ONE JSON line (rank 0).
+
+The default run (llama7b, the configuration the metric is quoted on) also
+times, each in a timed region of its own, the GQA-70B, INT8 and FP8 long-context
+and prefix-sharing decode workloads and the prefix-cached prompt pass
+(prefix_prefill, TFLOP/s on the tensor roofline), under "workloads".
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
   python bench.py --impl reference ...   # the CPU oracle on the host cores
@@ -344,6 +351,180 @@ def cpu_oracle_baseline(w, host_k, host_v, host_ks=None, host_vs=None, rows=None
             "rows": len(rows), "cores": oracle.num_threads(), "elt": elt}
 
 
+def timed_region(run, steps, world, dev, local):
+    """K steps bracketed by a barrier and a device synchronize on both sides,
+    timed by two CUDA events on the launching stream (nothing else is recorded
+    inside the region, so the kernels' programmatic launch overlap is kept);
+    nvidia-smi clocks are sampled meanwhile.  Returns (max-over-ranks ms,
+    clock summary)."""
+    stream = torch.cuda.current_stream()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        start.record(stream)
+        for _ in range(steps):
+            run()
+        end.record(stream)
+        torch.cuda.synchronize()
+    barrier(world)
+    return max_over_ranks(start.elapsed_time(end), world, dev), clk.summary()
+
+
+def kernel_pass(run_ev, steps) -> float:
+    """Mean duration (ms) of the step's dominant kernel over a separate pass of
+    K steps, from events recorded right before and right after it on the
+    launching stream."""
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(steps)]
+    torch.cuda.synchronize()
+    for i in range(steps):
+        run_ev(evs[i])
+    torch.cuda.synchronize()
+    return statistics.mean(e0.elapsed_time(e1) for e0, e1 in evs)
+
+
+def check_status(kvp, status, what):
+    st = kvp.kvp_read_status(status)
+    if st != kvp.KVP_OK:
+        raise RuntimeError(f"{what}: device status {kvp.kvp_status_string(st)}")
+
+
+def dtype_name(w) -> str:
+    base = {torch.float16: "f16", torch.bfloat16: "bf16"}[w.dtype]
+    if w.kv_int8:
+        return base + (" (fp8 e4m3 KV)" if w.kv_fp8 else " (int8 KV)")
+    return base
+
+
+def measure_decode(name, args, kvp, world, dev, local, headline):
+    """Build one decode workload on the device, warm up, time K steps (outer
+    events only), then time its partition kernel in a separate pass.  Returns
+    (workload, step, measurement dict)."""
+    w = workloads.make(name, device=dev, nan_sentinel=False,
+                       batch=args.batch if headline else None,
+                       contiguity=args.contiguity if headline else None)
+    step = Step(w, kvp, dev, args.partition_blocks if headline else 0, fused=not args.unfused)
+    lens = [int(x) for x in w.context_lens]
+    dbytes = decode_bytes(w, lens)
+    sbytes = dbytes["call"] + append_bytes(w) + copy_bytes(w)
+    for _ in range(args.warmup):
+        step.run()
+    torch.cuda.synchronize()
+    check_status(kvp, step.status, f"{name} after warm-up")
+    elapsed_ms, clocks = timed_region(step.run, args.steps, world, dev, local)
+    partial_ms = kernel_pass(step.run, args.steps)
+    check_status(kvp, step.status, f"{name} after the timed steps")
+    total_bytes = sum_over_ranks(sbytes * args.steps, world, dev)
+    value = total_bytes / (elapsed_ms / 1e3) / 1e9
+    tokens_per_s = sum_over_ranks(sum(lens) * args.steps, world, dev) / (elapsed_ms / 1e3)
+    peak, peak_src = measured_peak()
+    # the fused partition pass also moves the appended rows (read source, write slot)
+    partial_bytes = dbytes["partial_pass"] + (append_bytes(w) if step.fused else 0)
+    achieved = partial_bytes / (partial_ms / 1e3) / 1e9
+    # the committed counters are for the full-size workloads only
+    full_size = not (headline and (args.batch or args.contiguity is not None))
+    traffic = profiled_traffic(name) if full_size else None
+    m = {
+        "value": round(value, 2),
+        "unit": "GB/s",
+        "ms_per_step": round(elapsed_ms / args.steps, 5),
+        "tokens_per_s": round(tokens_per_s, 1),
+        "pct_of_peak": round(100 * value / peak, 2),
+        "dtype": dtype_name(w),
+        "config": {"workload": w.name + (f" (batch {w.B})" if headline and args.batch else ""),
+                   "batch": w.B, "q_heads": w.Hq, "kv_heads": w.Hkv, "head_dim": w.D,
+                   "block_size": 16, "num_blocks": w.num_blocks, "context_tokens": sum(lens),
+                   "max_context": max(lens), "new_tokens": int(w.slot_mapping.numel()),
+                   "cow_pairs": int(w.cow_pairs.shape[0]) if w.cow_pairs is not None else 0,
+                   "partition_blocks": step.part_blocks,
+                   "append": "fused into the decode" if step.fused else "separate kernel",
+                   "l2": ("inputs larger than L2: {:.2f} GB of K/V per step vs 129 MB L2"
+                          .format(dbytes["kv"] / 1e9)) if dbytes["kv"] > 4 * L2_BYTES else
+                         "inputs partly L2-resident (L2 reuse is part of this workload)",
+                   "parallelism": "replicas" if world > 1 else "single GPU"},
+        "step_bytes": sbytes,
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak,
+                     "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": traffic,
+                     "kernel": "decode_partial_kernel", "peak_source": peak_src,
+                     "algorithmic_bytes_per_launch": partial_bytes,
+                     "launch_ms": round(partial_ms, 5),
+                     "timing": "kernel events in a separate pass of the same steps"},
+        "gpu_launches": step.launches_per_step() * args.steps,
+        "clocks": clocks,
+    }
+    if "contiguous_share" in w.info:
+        m["config"]["contiguous_share"] = round(w.info["contiguous_share"], 4)
+    if w.kv_int8:
+        m["prefill_quantise"] = step.prefill
+    return w, step, m, total_bytes
+
+
+def decode_cpu_baseline(w, step, rows_all, rows_one):
+    """The oracle as it stands on the host cores: `rows_all` (request, head)
+    rows on every core (median of three runs) and `rows_one` rows on one core."""
+    import oracle
+    oracle.build()
+    w_host = workloads.Workload(**{k: (v.cpu() if isinstance(v, torch.Tensor) else v)
+                                   for k, v in w.__dict__.items()})
+    hk, hv = step.kp.cpu(), step.vp.cpu()
+    if w.kv_fp8:
+        hk, hv = hk.view(torch.float8_e4m3fn), hv.view(torch.float8_e4m3fn)
+    hks = step.ks.cpu() if w.kv_int8 else None
+    hvs = step.vs.cpu() if w.kv_int8 else None
+    rows = sample_rows(w, rows_all)
+    runs = [cpu_oracle_baseline(w_host, hk, hv, hks, hvs, rows) for _ in range(3)]
+    cb = sorted(runs, key=lambda r: r["seconds"])[1]
+    res = {"value": round(cb["bytes"] / cb["seconds"] / 1e9, 4), "unit": "GB/s",
+           "cores": cb["cores"], "kind": "oracle",
+           "sample": f"{cb['rows']} of {w.B * w.Hq} (request, query head) rows of one decode "
+                     f"call, median of 3 runs, {cb['seconds']:.2f} s each"}
+    if rows_one:
+        threads = oracle.num_threads()
+        oracle.set_num_threads(1)
+        try:
+            c1 = cpu_oracle_baseline(w_host, hk, hv, hks, hvs, sample_rows(w, rows_one))
+        finally:
+            oracle.set_num_threads(threads)
+        res["value_1core"] = round(c1["bytes"] / c1["seconds"] / 1e9, 4)
+        res["sample_1core"] = (f"{c1['rows']} (request, query head) rows on 1 core, "
+                               f"{c1['seconds']:.2f} s")
+    return res
+
+
+def run_e2e(step, host_keys, args, world, dev, unit_total, unit_scale, unit):
+    """The same steps end to end through the public API: every step copies its
+    inputs in from pinned host memory and its output back, then waits."""
+    host = {k: getattr(step, k).cpu().pin_memory() for k in host_keys
+            if getattr(step, k, None) is not None}
+    out_host = torch.empty(step.out.shape, dtype=step.out.dtype).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = out_host.numel() * out_host.element_size()
+
+    def e2e_step():
+        for k, t in host.items():
+            getattr(step, k).copy_(t, non_blocking=True)
+        step.run()
+        out_host.copy_(step.out, non_blocking=True)
+        torch.cuda.current_stream().synchronize()
+
+    for _ in range(args.warmup):
+        e2e_step()
+    barrier(world)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        e2e_step()
+    e2e_s = max_over_ranks(time.perf_counter() - t0, world, dev)
+    barrier(world)
+    return {"value": round(unit_total / e2e_s / unit_scale, 3), "unit": unit,
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "ms_per_step": round(e2e_s * 1e3 / args.steps, 4)}
+
+
+EXTRA_DECODE = ("gqa70b", "int8long", "fp8long", "prefix")
+EXTRA_PREFILL = ("prefix_prefill",)
+
+
 def run_ours(args):
     import pagedattention_decode_kvp_gb300 as kvp
     from pagedattention_decode_kvp_gb300 import _build
@@ -360,144 +541,49 @@ def run_ours(args):
     barrier(world)
     kvp.load_library()
 
-    w = workloads.make(args.workload, device=dev, nan_sentinel=False, batch=args.batch,
-                       contiguity=args.contiguity)
-    step = Step(w, kvp, dev, args.partition_blocks, fused=not args.unfused)
-    lens = [int(x) for x in w.context_lens]
-    dbytes = decode_bytes(w, lens)
-    sbytes = dbytes["call"] + append_bytes(w) + copy_bytes(w)
-    kv_total = sum(lens)
-    stream = torch.cuda.current_stream()
-
-    for _ in range(args.warmup):
-        step.run()
-    torch.cuda.synchronize()
-    st = kvp.kvp_read_status(step.status)
-    if st != kvp.KVP_OK:
-        raise RuntimeError(f"device status after warm-up: {kvp.kvp_status_string(st)}")
-
-    # ---- timed region: K steps, events on the launching stream
-    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-           for _ in range(args.steps)]
-    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    barrier(world)
-    torch.cuda.synchronize()
-    with ClockSampler(local) as clk:
-        start.record(stream)
-        for i in range(args.steps):
-            step.run(evs[i])
-        end.record(stream)
-        torch.cuda.synchronize()
-    barrier(world)
-    elapsed_ms = start.elapsed_time(end)
-    partial_ms = statistics.mean(e0.elapsed_time(e1) for e0, e1 in evs)
-    elapsed_ms = max_over_ranks(elapsed_ms, world, dev)
-    ms_per_step = elapsed_ms / args.steps
-    total_bytes = sum_over_ranks(sbytes * args.steps, world, dev)
-    value = total_bytes / (elapsed_ms / 1e3) / 1e9
-    tokens_per_s = sum_over_ranks(kv_total * args.steps, world, dev) / (elapsed_ms / 1e3)
-
-    # ---- end to end through the public API with host buffers
+    w, step, m, total_bytes = measure_decode(args.workload, args, kvp, world, dev, local, True)
     e2e = None
     if not args.no_e2e:
-        host = {k: getattr(step, k).cpu().pin_memory() for k in
-                ("q", "tables", "lens", "slots", "new_k", "new_v")}
-        if step.pairs is not None:
-            host["pairs"] = step.pairs.cpu().pin_memory()
-        out_host = torch.empty(step.out.shape, dtype=step.out.dtype).pin_memory()
-        h2d = sum(t.numel() * t.element_size() for t in host.values())
-        d2h = out_host.numel() * out_host.element_size()
+        e2e = run_e2e(step, ("q", "tables", "lens", "slots", "new_k", "new_v", "pairs"), args,
+                      world, dev, total_bytes, 1e9, "GB/s")
 
-        def e2e_step():
-            for k, t in host.items():
-                getattr(step, k).copy_(t, non_blocking=True)
-            step.run()
-            out_host.copy_(step.out, non_blocking=True)
-            torch.cuda.current_stream().synchronize()
+    res = {"metric": METRIC, "value": m["value"], "unit": "GB/s", "n_gpus": world,
+           "steps": args.steps, "warmup": args.warmup, "ms_per_step": m["ms_per_step"],
+           "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+           "dtype": m["dtype"],
+           "data": "synthetic (seeded N(0,1), shapes of the pages' workloads)",
+           "config": m["config"], "tokens_per_s": m["tokens_per_s"],
+           "pct_of_peak": m["pct_of_peak"], "step_bytes": m["step_bytes"],
+           "roofline": m["roofline"], "e2e": e2e, "gpu_launches": m["gpu_launches"],
+           "clocks": m["clocks"]}
+    if "prefill_quantise" in m:
+        res["prefill_quantise"] = m["prefill_quantise"]
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        res["cpu_baseline"] = decode_cpu_baseline(w, step, args.cpu_rows, args.cpu_rows_1core)
+    del step, w
+    torch.cuda.empty_cache()
 
-        for _ in range(args.warmup):
-            e2e_step()
-        barrier(world)
-        t0 = time.perf_counter()
-        for _ in range(args.steps):
-            e2e_step()
-        e2e_s = max_over_ranks(time.perf_counter() - t0, world, dev)
-        barrier(world)
-        e2e = {"value": round(total_bytes / e2e_s / 1e9, 2), "unit": "GB/s",
-               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-               "ms_per_step": round(e2e_s * 1e3 / args.steps, 4)}
+    # the other workloads of the same method, each timed the same way in this run
+    extras = {}
+    if args.extras:
+        for name in EXTRA_DECODE:
+            ew, estep, em, _ = measure_decode(name, args, kvp, world, dev, local, False)
+            if rank == 0 and world == 1 and not args.no_cpu_baseline:
+                em["cpu_baseline"] = decode_cpu_baseline(ew, estep, 16 if ew.kv_int8 else 64, 0)
+            extras[name] = em
+            del estep, ew
+            torch.cuda.empty_cache()
+        for name in EXTRA_PREFILL:
+            pw, pstep, pm, _ = measure_prefill(name, args, kvp, world, dev, local, False)
+            if rank == 0 and world == 1 and not args.no_cpu_baseline:
+                pm["cpu_baseline"] = prefill_cpu_baseline(pw, pstep, 1024)
+            extras[name] = pm
+            del pstep, pw
+            torch.cuda.empty_cache()
+        res["workloads"] = extras
 
-    if rank != 0:
-        if world > 1:
-            import torch.distributed as dist
-            dist.destroy_process_group()
-        return
-
-    peak, peak_src = measured_peak()
-    # the fused partition pass also moves the appended rows (read source, write slot)
-    partial_bytes = dbytes["partial_pass"] + (append_bytes(w) if step.fused else 0)
-    achieved = partial_bytes / (partial_ms / 1e3) / 1e9
-    # the committed counters are for the full-size workload only
-    traffic = None if args.batch else profiled_traffic(args.workload)
-    res = {
-        "metric": METRIC,
-        "value": round(value, 2),
-        "unit": "GB/s",
-        "n_gpus": world,
-        "steps": args.steps,
-        "warmup": args.warmup,
-        "ms_per_step": round(ms_per_step, 5),
-        "higher_is_better": True,
-        "scaling": "weak",
-        "vs_baseline": None,
-        "dtype": {torch.float16: "f16", torch.bfloat16: "bf16"}[w.dtype] + (
-            (" (fp8 e4m3 KV)" if w.kv_fp8 else " (int8 KV)") if w.kv_int8 else ""),
-        "data": "synthetic (seeded N(0,1), shapes of the pages' workloads)",
-        "config": {"workload": w.name + (f" (batch {w.B})" if args.batch else ""), "batch": w.B, "q_heads": w.Hq, "kv_heads": w.Hkv,
-                   "head_dim": w.D, "block_size": 16, "num_blocks": w.num_blocks,
-                   "context_tokens": kv_total, "max_context": max(lens),
-                   "new_tokens": int(w.slot_mapping.numel()),
-                   "cow_pairs": int(w.cow_pairs.shape[0]) if w.cow_pairs is not None else 0,
-                   "partition_blocks": step.part_blocks,
-                   "append": "fused into the decode" if step.fused else "separate kernel",
-                   "l2": ("inputs larger than L2: {:.2f} GB of K/V per step vs 129 MB L2"
-                          .format(dbytes["kv"] / 1e9)) if dbytes["kv"] > 4 * L2_BYTES else
-                         "inputs partly L2-resident (L2 reuse is part of this workload)",
-                   "parallelism": "replicas" if world > 1 else "single GPU"},
-        "tokens_per_s": round(tokens_per_s, 1),
-        "pct_of_peak": round(100 * value / peak, 2),
-        "step_bytes": sbytes,
-        "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak,
-                     "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": traffic,
-                     "kernel": "decode_partial_kernel", "peak_source": peak_src,
-                     "algorithmic_bytes_per_launch": partial_bytes,
-                     "launch_ms": round(partial_ms, 5)},
-        "e2e": e2e,
-        "gpu_launches": step.launches_per_step() * args.steps,
-        "clocks": clk.summary(),
-    }
-    if w.kv_int8:
-        res["prefill_int8"] = step.prefill
-    if "contiguous_share" in w.info:
-        res["config"]["contiguous_share"] = round(w.info["contiguous_share"], 4)
-
-    if world == 1 and not args.no_cpu_baseline:
-        import oracle
-        oracle.build()
-        w_host = workloads.Workload(**{k: (v.cpu() if isinstance(v, torch.Tensor) else v)
-                                       for k, v in w.__dict__.items()})
-        hk, hv = step.kp.cpu(), step.vp.cpu()
-        if w.kv_fp8:
-            hk, hv = hk.view(torch.float8_e4m3fn), hv.view(torch.float8_e4m3fn)
-        hks = step.ks.cpu() if w.kv_int8 else None
-        hvs = step.vs.cpu() if w.kv_int8 else None
-        rows = sample_rows(w, args.cpu_rows)
-        cb = cpu_oracle_baseline(w_host, hk, hv, hks, hvs, rows)
-        res["cpu_baseline"] = {"value": round(cb["bytes"] / cb["seconds"] / 1e9, 4),
-                               "unit": "GB/s", "cores": cb["cores"], "kind": "oracle",
-                               "sample": f"{cb['rows']} of {w.B * w.Hq} (request, query head) "
-                                         f"rows of one decode call, {cb['seconds']:.2f} s"}
-    print(json.dumps(res))
+    if rank == 0:
+        print(json.dumps(res))
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()
@@ -587,6 +673,67 @@ def cpu_oracle_prefill(w, host_k, host_v, rows):
             "cores": oracle.num_threads()}
 
 
+def measure_prefill(name, args, kvp, world, dev, local, headline):
+    """Build a prefill workload on the device, warm up, time K steps (outer
+    events only), then time the prefill kernel in a separate pass."""
+    w = workloads.make_prefill_named(name, device=dev, nan_sentinel=False,
+                                     batch=args.batch if headline else None)
+    step = PrefillStep(w, kvp, dev)
+    flops, pairs = prefill_work(w)
+    for _ in range(args.warmup):
+        step.run()
+    torch.cuda.synchronize()
+    check_status(kvp, step.status, f"{name} after warm-up")
+    elapsed_ms, clocks = timed_region(step.run, args.steps, world, dev, local)
+    kernel_ms = kernel_pass(step.run, args.steps)
+    check_status(kvp, step.status, f"{name} after the timed steps")
+    total_flops = sum_over_ranks(flops * args.steps, world, dev)
+    value = total_flops / (elapsed_ms / 1e3) / 1e12
+    q_tokens_per_s = sum_over_ranks(w.T * args.steps, world, dev) / (elapsed_ms / 1e3)
+    peak, peak_src = measured_tensor_peak()
+    achieved = flops / (kernel_ms / 1e3) / 1e12
+    full_size = not (headline and args.batch)
+    m = {
+        "value": round(value, 3),
+        "unit": "TFLOP/s",
+        "ms_per_step": round(elapsed_ms / args.steps, 5),
+        "query_tokens_per_s": round(q_tokens_per_s, 1),
+        "dtype": {torch.float16: "f16", torch.bfloat16: "bf16"}[w.dtype],
+        "config": {"workload": w.name + (f" (batch {w.B})" if headline and args.batch else ""),
+                   "batch": w.B, "q_heads": w.Hq, "kv_heads": w.Hkv, "head_dim": w.D,
+                   "block_size": 16, "num_blocks": w.num_blocks, "query_tokens": w.T,
+                   "prefix_tokens": w.info.get("prefix_tokens"),
+                   "context_tokens": int(w.context_lens.sum()),
+                   "attended_pairs_per_head": pairs,
+                   "l2": "K/V of the shared prefix is L2-resident across requests (prefix "
+                         "reuse is part of this workload); the chunk's append writes "
+                         "{:.2f} GB per step".format(step.append_bytes() / 1e9),
+                   "parallelism": "replicas" if world > 1 else "single GPU"},
+        "roofline": {"bound": "tensor", "achieved": round(achieved, 3), "peak": peak,
+                     "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
+                     "traffic": profiled_traffic(name, PREFILL_SOURCES) if full_size else None,
+                     "kernel": "prefill_kernel", "peak_source": peak_src,
+                     "algorithmic_flops_per_launch": flops,
+                     "launch_ms": round(kernel_ms, 5),
+                     "timing": "kernel events in a separate pass of the same steps"},
+        "gpu_launches": 2 * args.steps,
+        "clocks": clocks,
+    }
+    return w, step, m, total_flops
+
+
+def prefill_cpu_baseline(w, step, nrows):
+    import oracle
+    oracle.build()
+    wh = workloads.PrefillWorkload(**{k: (v.cpu() if isinstance(v, torch.Tensor) else v)
+                                      for k, v in w.__dict__.items()})
+    cb = cpu_oracle_prefill(wh, step.kp.cpu(), step.vp.cpu(), prefill_sample_rows(wh, nrows))
+    return {"value": round(cb["flops"] / cb["seconds"] / 1e12, 6), "unit": "TFLOP/s",
+            "cores": cb["cores"], "kind": "oracle",
+            "sample": f"{cb['rows']} of {w.T * w.Hq} (query row, head) pairs of one prefill "
+                      f"call, {cb['seconds']:.2f} s"}
+
+
 def run_prefill(args):
     import pagedattention_decode_kvp_gb300 as kvp
     from pagedattention_decode_kvp_gb300 import _build
@@ -603,119 +750,23 @@ def run_prefill(args):
     barrier(world)
     kvp.load_library()
 
-    w = workloads.make_prefill_named(args.workload, device=dev, nan_sentinel=False,
-                                     batch=args.batch)
-    step = PrefillStep(w, kvp, dev)
-    flops, pairs = prefill_work(w)
-    stream = torch.cuda.current_stream()
-    for _ in range(args.warmup):
-        step.run()
-    torch.cuda.synchronize()
-    st = kvp.kvp_read_status(step.status)
-    if st != kvp.KVP_OK:
-        raise RuntimeError(f"device status after warm-up: {kvp.kvp_status_string(st)}")
-
-    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-           for _ in range(args.steps)]
-    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    barrier(world)
-    torch.cuda.synchronize()
-    with ClockSampler(local) as clk:
-        start.record(stream)
-        for i in range(args.steps):
-            step.run(evs[i])
-        end.record(stream)
-        torch.cuda.synchronize()
-    barrier(world)
-    elapsed_ms = max_over_ranks(start.elapsed_time(end), world, dev)
-    kernel_ms = statistics.mean(e0.elapsed_time(e1) for e0, e1 in evs)
-    ms_per_step = elapsed_ms / args.steps
-    total_flops = sum_over_ranks(flops * args.steps, world, dev)
-    value = total_flops / (elapsed_ms / 1e3) / 1e12
-    q_tokens_per_s = sum_over_ranks(w.T * args.steps, world, dev) / (elapsed_ms / 1e3)
-
+    w, step, m, total_flops = measure_prefill(args.workload, args, kvp, world, dev, local, True)
     e2e = None
     if not args.no_e2e:
-        host = {k: getattr(step, k).cpu().pin_memory() for k in
-                ("q", "tables", "lens", "qs", "slots", "new_k", "new_v")}
-        out_host = torch.empty(step.out.shape, dtype=step.out.dtype).pin_memory()
-        h2d = sum(t.numel() * t.element_size() for t in host.values())
-        d2h = out_host.numel() * out_host.element_size()
-
-        def e2e_step():
-            for k, t in host.items():
-                getattr(step, k).copy_(t, non_blocking=True)
-            step.run()
-            out_host.copy_(step.out, non_blocking=True)
-            torch.cuda.current_stream().synchronize()
-
-        for _ in range(args.warmup):
-            e2e_step()
-        barrier(world)
-        t0 = time.perf_counter()
-        for _ in range(args.steps):
-            e2e_step()
-        e2e_s = max_over_ranks(time.perf_counter() - t0, world, dev)
-        barrier(world)
-        e2e = {"value": round(total_flops / e2e_s / 1e12, 3), "unit": "TFLOP/s",
-               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-               "ms_per_step": round(e2e_s * 1e3 / args.steps, 4)}
-
-    if rank != 0:
-        if world > 1:
-            import torch.distributed as dist
-            dist.destroy_process_group()
-        return
-
-    peak, peak_src = measured_tensor_peak()
-    achieved = flops / (kernel_ms / 1e3) / 1e12
-    res = {
-        "metric": PREFILL_METRIC,
-        "value": round(value, 3),
-        "unit": "TFLOP/s",
-        "n_gpus": world,
-        "steps": args.steps,
-        "warmup": args.warmup,
-        "ms_per_step": round(ms_per_step, 5),
-        "higher_is_better": True,
-        "scaling": "weak",
-        "vs_baseline": None,
-        "dtype": "f16",
-        "data": "synthetic (seeded N(0,1), shapes of the pages' prefix-sharing workload)",
-        "config": {"workload": w.name + (f" (batch {w.B})" if args.batch else ""), "batch": w.B,
-                   "q_heads": w.Hq, "kv_heads": w.Hkv, "head_dim": w.D, "block_size": 16,
-                   "num_blocks": w.num_blocks, "query_tokens": w.T,
-                   "prefix_tokens": w.info.get("prefix_tokens"),
-                   "context_tokens": int(w.context_lens.sum()),
-                   "attended_pairs_per_head": pairs,
-                   "l2": "K/V of the shared prefix is L2-resident across requests (prefix "
-                         "reuse is part of this workload); the chunk's append writes "
-                         "{:.2f} GB per step".format(step.append_bytes() / 1e9),
-                   "parallelism": "replicas" if world > 1 else "single GPU"},
-        "query_tokens_per_s": round(q_tokens_per_s, 1),
-        "roofline": {"bound": "tensor", "achieved": round(achieved, 3), "peak": peak,
-                     "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
-                     "traffic": (None if args.batch
-                                 else profiled_traffic(args.workload, PREFILL_SOURCES)),
-                     "kernel": "prefill_kernel", "peak_source": peak_src,
-                     "algorithmic_flops_per_launch": flops,
-                     "launch_ms": round(kernel_ms, 5)},
-        "e2e": e2e,
-        "gpu_launches": 2 * args.steps,
-        "clocks": clk.summary(),
-    }
-    if world == 1 and not args.no_cpu_baseline:
-        import oracle
-        oracle.build()
-        wh = workloads.PrefillWorkload(**{k: (v.cpu() if isinstance(v, torch.Tensor) else v)
-                                          for k, v in w.__dict__.items()})
-        cb = cpu_oracle_prefill(wh, step.kp.cpu(), step.vp.cpu(),
-                                prefill_sample_rows(wh, args.cpu_rows))
-        res["cpu_baseline"] = {"value": round(cb["flops"] / cb["seconds"] / 1e12, 6),
-                               "unit": "TFLOP/s", "cores": cb["cores"], "kind": "oracle",
-                               "sample": f"{cb['rows']} of {w.T * w.Hq} (query row, head) "
-                                         f"pairs of one prefill call, {cb['seconds']:.2f} s"}
-    print(json.dumps(res))
+        e2e = run_e2e(step, ("q", "tables", "lens", "qs", "slots", "new_k", "new_v"), args,
+                      world, dev, total_flops, 1e12, "TFLOP/s")
+    res = {"metric": PREFILL_METRIC, "value": m["value"], "unit": "TFLOP/s", "n_gpus": world,
+           "steps": args.steps, "warmup": args.warmup, "ms_per_step": m["ms_per_step"],
+           "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+           "dtype": m["dtype"],
+           "data": "synthetic (seeded N(0,1), shapes of the pages' prefix-sharing workload)",
+           "config": m["config"], "query_tokens_per_s": m["query_tokens_per_s"],
+           "roofline": m["roofline"], "e2e": e2e, "gpu_launches": m["gpu_launches"],
+           "clocks": m["clocks"]}
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        res["cpu_baseline"] = prefill_cpu_baseline(w, step, args.cpu_rows)
+    if rank == 0:
+        print(json.dumps(res))
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()
@@ -829,6 +880,12 @@ def main():
     ap.add_argument("--unfused", action="store_true",
                     help="append with kvp_append, then decode (default: the fused entry point "
                          "where every request appends one token at its last position)")
+    ap.add_argument("--cpu-rows-1core", type=int, default=128,
+                    help="(request, head) rows the CPU oracle times on one core (0 = skip)")
+    ap.add_argument("--no-extras", action="store_true",
+                    help="time only the named workload (default for llama7b: also gqa70b, "
+                         "int8long, fp8long, prefix and prefix_prefill, each in its own "
+                         "timed region, reported under \"workloads\")")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
@@ -839,7 +896,10 @@ def main():
         if prefill:
             args.cpu_rows = 8192 if args.impl == "ours" else 2048
         else:
-            args.cpu_rows = 256 if args.impl == "ours" else 64
+            args.cpu_rows = 1024 if args.impl == "ours" else 64
+    args.extras = (not args.no_extras and args.workload == "llama7b" and args.batch is None
+                   and args.contiguity is None and args.partition_blocks == 0
+                   and not args.unfused)
     if args.impl == "reference":
         (run_reference_prefill if prefill else run_reference)(args)
     else:

@@ -343,9 +343,13 @@ kvp_status kvp_attention_prefill(void* out, const void* q, const void* k_cache,
  *   - Returns KVP_ERR_SCRATCH_LIMIT, before launching anything, when these sizes
  *     need more than KVP_NOALLOC_SCRATCH_BYTES of workspace
  *     (kvp_decode_workspace_bytes tells how much they need).
- *   - The first call on each device looks up the scratch array's device address
- *     (cudaGetSymbolAddress, with that device current); make that first call
- *     before any stream capture.
+ *   - The first call on each device that needs partials looks up the scratch
+ *     array's device address (cudaGetSymbolAddress, with that device current);
+ *     make that first call before any stream capture.  The address is cached
+ *     per device and per context: after a device reset (or from a new context)
+ *     the next such call looks it up again, so it too belongs before any
+ *     capture.  Calls whose contexts fit one partition, and calls with
+ *     arguments the decode rejects, never look it up.
  *   - Every call, on any stream, shares the one array: calls that overlap on the
  *     GPU race and corrupt each other's results.  Serialise them (one stream, or
  *     events).  The array keeps the last call's contents; nothing in it needs to

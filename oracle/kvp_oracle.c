@@ -332,23 +332,29 @@ void orc_quantize_int8_fixed(const uint16_t* src, int src_kind, long long n, flo
  * ------------------------------------------------------------------------- */
 void orc_quantize_fp8(const uint16_t* src, int src_kind, long long rows, int D, uint8_t* q,
                       float* scale_out) {
-#pragma omp parallel for schedule(static)
-  for (long long r = 0; r < rows; ++r) {
-    const uint16_t* x16 = src + (size_t)r * D;
-    float amax = 0.0f;
-    for (int j = 0; j < D; ++j) {
-      float x = (float)(src_kind == ORC_BF16 ? orc_bf16_to_f64(x16[j]) : orc_f16_to_f64(x16[j]));
-      float a = fabsf(x);
-      if (a > amax) amax = a;
+  /* the float32 divisions round to nearest-even, as in the INT8 quantisers;
+   * the floating-point environment is per thread, so each worker sets it */
+#pragma omp parallel
+  {
+    fesetround(FE_TONEAREST);
+#pragma omp for schedule(static)
+    for (long long r = 0; r < rows; ++r) {
+      const uint16_t* x16 = src + (size_t)r * D;
+      float amax = 0.0f;
+      for (int j = 0; j < D; ++j) {
+        float x = (float)(src_kind == ORC_BF16 ? orc_bf16_to_f64(x16[j]) : orc_f16_to_f64(x16[j]));
+        float a = fabsf(x);
+        if (a > amax) amax = a;
+      }
+      volatile float s = amax / 448.0f;
+      float sc = (s > 0.0f) ? s : 1.0f;
+      for (int j = 0; j < D; ++j) {
+        float x = (float)(src_kind == ORC_BF16 ? orc_bf16_to_f64(x16[j]) : orc_f16_to_f64(x16[j]));
+        volatile float ratio = x / sc;
+        q[(size_t)r * D + j] = orc_f32_to_e4m3(ratio);
+      }
+      scale_out[r] = sc;
     }
-    volatile float s = amax / 448.0f;
-    float sc = (s > 0.0f) ? s : 1.0f;
-    for (int j = 0; j < D; ++j) {
-      float x = (float)(src_kind == ORC_BF16 ? orc_bf16_to_f64(x16[j]) : orc_f16_to_f64(x16[j]));
-      volatile float ratio = x / sc;
-      q[(size_t)r * D + j] = orc_f32_to_e4m3(ratio);
-    }
-    scale_out[r] = sc;
   }
 }
 

@@ -277,6 +277,7 @@ int32_t kvp_version(void) { return 100; }  // 0.1.0
 kvp_status kvp_append(const void* key, const void* value, void* k_cache, void* v_cache,
                       const int32_t* slot_mapping, int32_t num_tokens, kvp_cache_desc cache,
                       kvp_dtype dtype, int32_t* dev_status, kvp_stream_t stream) {
+  KVP_NVTX_RANGE("kvp_append");
   const kvp_status ds = check_desc(cache);
   if (ds != KVP_OK) return ds;
   if (num_tokens < 0 || (dtype != KVP_F16 && dtype != KVP_BF16)) return KVP_ERR_INVALID_ARG;
@@ -292,6 +293,7 @@ kvp_status kvp_append_int8(const void* key, const void* value, kvp_dtype src_dty
                            int8_t* k_cache, int8_t* v_cache, float* k_scale, float* v_scale,
                            const int32_t* slot_mapping, int32_t num_tokens, kvp_cache_desc cache,
                            int32_t* dev_status, kvp_stream_t stream) {
+  KVP_NVTX_RANGE("kvp_append_int8");
   const kvp_status ds = check_desc(cache);
   if (ds != KVP_OK) return ds;
   if (num_tokens < 0 || (src_dtype != KVP_F16 && src_dtype != KVP_BF16))
@@ -312,6 +314,7 @@ kvp_status kvp_append_int8_fixed(const void* key, const void* value, kvp_dtype s
                                  float* v_scale_pool, float k_scale, float v_scale,
                                  const int32_t* slot_mapping, int32_t num_tokens,
                                  kvp_cache_desc cache, int32_t* dev_status, kvp_stream_t stream) {
+  KVP_NVTX_RANGE("kvp_append_int8_fixed");
   const kvp_status ds = check_desc(cache);
   if (ds != KVP_OK) return ds;
   if (num_tokens < 0 || (src_dtype != KVP_F16 && src_dtype != KVP_BF16))
@@ -334,6 +337,7 @@ kvp_status kvp_append_fp8(const void* key, const void* value, kvp_dtype src_dtyp
                           uint8_t* k_cache, uint8_t* v_cache, float* k_scale, float* v_scale,
                           const int32_t* slot_mapping, int32_t num_tokens, kvp_cache_desc cache,
                           int32_t* dev_status, kvp_stream_t stream) {
+  KVP_NVTX_RANGE("kvp_append_fp8");
   const kvp_status ds = check_desc(cache);
   if (ds != KVP_OK) return ds;
   if (num_tokens < 0 || (src_dtype != KVP_F16 && src_dtype != KVP_BF16))
@@ -352,6 +356,7 @@ kvp_status kvp_append_fp8(const void* key, const void* value, kvp_dtype src_dtyp
 kvp_status kvp_copy_blocks(void* k_cache, void* v_cache, float* k_scale, float* v_scale,
                            int32_t cache_elem_bytes, const int32_t* pairs, int32_t num_pairs,
                            kvp_cache_desc cache, int32_t* dev_status, kvp_stream_t stream) {
+  KVP_NVTX_RANGE("kvp_copy_blocks");
   const kvp_status ds = check_desc(cache);
   if (ds != KVP_OK) return ds;
   if (num_pairs < 0 || (cache_elem_bytes != 1 && cache_elem_bytes != 2))
@@ -391,6 +396,7 @@ kvp_status kvp_attention_decode(void* out, const void* q, const void* k_cache,
                                 kvp_cache_desc cache, kvp_dtype dtype, int32_t partition_blocks,
                                 void* workspace, size_t workspace_bytes, int32_t phases,
                                 int32_t* dev_status, kvp_stream_t stream) {
+  KVP_NVTX_RANGE("kvp_attention_decode");
   if (dtype != KVP_F16 && dtype != KVP_BF16) return KVP_ERR_INVALID_ARG;
   return decode_common(out, q, dtype == KVP_BF16, dtype == KVP_BF16 ? 1 : 0, k_cache, v_cache,
                        nullptr, nullptr, block_tables, max_blocks_per_seq, context_lens, batch,
@@ -407,6 +413,7 @@ kvp_status kvp_append_attention_decode(const void* key, const void* value, void*
                                        void* workspace, size_t workspace_bytes,
                                        int32_t phases, int32_t* dev_status,
                                        kvp_stream_t stream) {
+  KVP_NVTX_RANGE("kvp_append_attention_decode");
   if (dtype != KVP_F16 && dtype != KVP_BF16) return KVP_ERR_INVALID_ARG;
   if (batch > 0 && (!key || !value || !aligned(key, 16) || !aligned(value, 16)))
     return KVP_ERR_INVALID_ARG;
@@ -425,6 +432,7 @@ kvp_status kvp_attention_decode_int8(void* out, const void* q, kvp_dtype q_dtype
                                      int32_t partition_blocks, void* workspace,
                                      size_t workspace_bytes, int32_t phases,
                                      int32_t* dev_status, kvp_stream_t stream) {
+  KVP_NVTX_RANGE("kvp_attention_decode_int8");
   if (q_dtype != KVP_F16 && q_dtype != KVP_BF16) return KVP_ERR_INVALID_ARG;
   return decode_common(out, q, q_dtype == KVP_BF16, 2, k_cache, v_cache, k_scale, v_scale,
                        block_tables, max_blocks_per_seq, context_lens, batch, num_q_heads, scale,
@@ -441,6 +449,7 @@ kvp_status kvp_attention_decode_fp8(void* out, const void* q, kvp_dtype q_dtype,
                                     int32_t partition_blocks, void* workspace,
                                     size_t workspace_bytes, int32_t phases, int32_t* dev_status,
                                     kvp_stream_t stream) {
+  KVP_NVTX_RANGE("kvp_attention_decode_fp8");
   if (q_dtype != KVP_F16 && q_dtype != KVP_BF16) return KVP_ERR_INVALID_ARG;
   return decode_common(out, q, q_dtype == KVP_BF16, 3, k_cache, v_cache, k_scale, v_scale,
                        block_tables, max_blocks_per_seq, context_lens, batch, num_q_heads, scale,
@@ -455,6 +464,7 @@ kvp_status kvp_attention_prefill(void* out, const void* q, const void* k_cache,
                                  int32_t batch, int32_t num_q_heads, int32_t max_query_len,
                                  float scale, kvp_cache_desc cache, kvp_dtype dtype,
                                  int32_t* dev_status, kvp_stream_t stream) {
+  KVP_NVTX_RANGE("kvp_attention_prefill");
   const kvp_status st = check_desc(cache);
   if (st != KVP_OK) return st;
   if (dtype != KVP_F16 && dtype != KVP_BF16) return KVP_ERR_INVALID_ARG;
@@ -509,6 +519,7 @@ kvp_status kvp_attention_prefill(void* out, const void* q, const void* k_cache,
 
 kvp_status kvp_selftest_wait_timeout(int32_t* dev_status, int64_t limit_ns,
                                      kvp_stream_t stream) {
+  KVP_NVTX_RANGE("kvp_selftest_wait_timeout");
   if (dev_status == nullptr || limit_ns < 1000 || limit_ns > 5000000000ll)
     return KVP_ERR_INVALID_ARG;
   return from_cuda(launch_selftest_wait(dev_status, static_cast<uint64_t>(limit_ns),
@@ -516,6 +527,7 @@ kvp_status kvp_selftest_wait_timeout(int32_t* dev_status, int64_t limit_ns,
 }
 
 kvp_status kvp_read_status(const int32_t* dev_status, kvp_stream_t stream) {
+  KVP_NVTX_RANGE("kvp_read_status");
   if (dev_status == nullptr) return KVP_ERR_INVALID_ARG;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   int32_t v = 0;

@@ -4,6 +4,7 @@
 
 #include <cuda.h>
 #include <cuda_runtime.h>
+#include <nvtx3/nvToolsExt.h>
 #include <stdint.h>
 
 #include <utility>
@@ -11,6 +12,18 @@
 #include "kvp.h"
 
 namespace kvp {
+
+// An NVTX range named after the entry point, open for the rest of the scope,
+// so a profiler's timeline and its kernel filters (e.g. ncu --nvtx-include
+// "kvp_attention_decode/") see each C-ABI call.  NVTX v3 is header-only; with
+// no tool attached a push or pop is a check of one function pointer.
+struct NvtxRange {
+  explicit NvtxRange(const char* name) { nvtxRangePushA(name); }
+  ~NvtxRange() { nvtxRangePop(); }
+  NvtxRange(const NvtxRange&) = delete;
+  NvtxRange& operator=(const NvtxRange&) = delete;
+};
+#define KVP_NVTX_RANGE(name) ::kvp::NvtxRange kvp_nvtx_range_(name)
 
 constexpr int kBlockSize = 16;       // tokens per cache block
 constexpr int kWarps = 4;            // consumer warps per decode CTA

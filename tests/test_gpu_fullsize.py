@@ -4,10 +4,9 @@ Each decode workload (llama7b, gqa70b, prefix, int8long, fp8long) is drawn on
 the host, run once through ``bench.Step`` (same entry points, fused or not,
 same automatic split-context partitions), and checked against the oracle fed
 the same host inputs: the appended slots, copy-on-write blocks and 8-bit codes
-/ scales bit-exact; the attention output on sampled (request, head) rows --
-first and last requests and a seeded random sample -- within 3e-3 absolute OR
-1e-2 relative of the fp64 oracle.  Inputs given to the oracle never come from
-the GPU.
+/ scales bit-exact; the attention output of every (request, head) row, element
+by element, within 3e-3 absolute OR 1e-2 relative of the fp64 oracle.  Inputs
+given to the oracle never come from the GPU.
 """
 import numpy as np
 import pytest
@@ -39,15 +38,6 @@ def assert_close(got, ref, what):
         i = np.unravel_index(np.argmax(np.where(ok, 0, err)), err.shape)
         raise AssertionError(f"{what}: {int((~ok).sum())} elements out of tolerance; worst at "
                              f"{i}: gpu {g[i]} ref {ref[i]} (max abs err {err.max():.3e})")
-
-
-def sample_rows(w, n_random=20, seed=0):
-    rng = np.random.default_rng(seed)
-    rows = [(0, h) for h in range(min(4, w.Hq))]
-    rows += [(w.B - 1, w.Hq - 1 - h) for h in range(min(4, w.Hq))]
-    for _ in range(n_random):
-        rows.append((int(rng.integers(w.B)), int(rng.integers(w.Hq))))
-    return rows
 
 
 def slot_rows(pool, slots):
@@ -83,11 +73,8 @@ def test_16bit_workload_full_size(name):
     gv = slot_rows(step.vp.cpu(), w.slot_mapping)
     assert torch.equal(gk.view(torch.int16), slot_rows(okp, w.slot_mapping).view(torch.int16))
     assert torch.equal(gv.view(torch.int16), slot_rows(ovp, w.slot_mapping).view(torch.int16))
-    rows = sample_rows(w, seed=len(name))
-    ref = oracle.attention_decode(w.q, okp, ovp, w.block_tables, w.context_lens, w.scale,
-                                  rows=rows)
-    got = torch.stack([step.out[b, h] for b, h in rows])
-    assert_close(got, ref, f"{name} full size")
+    ref = oracle.attention_decode(w.q, okp, ovp, w.block_tables, w.context_lens, w.scale)
+    assert_close(step.out, ref, f"{name} full size, every row")
 
 
 @pytest.mark.parametrize("name", ["int8long", "fp8long"])
@@ -117,8 +104,6 @@ def test_8bit_workload_full_size(name):
     for gpu, ref in ((step.ks, oks), (step.vs, ovs)):
         assert torch.equal(slot_rows(gpu.cpu(), probe).view(torch.int32),
                            slot_rows(ref, probe).view(torch.int32))
-    rows = sample_rows(w, n_random=12, seed=7)
     ref = oracle.attention_decode(w.q, okc, ovc, w.block_tables, w.context_lens, w.scale,
-                                  k_scale=oks, v_scale=ovs, rows=rows)
-    got = torch.stack([step.out[b, h] for b, h in rows])
-    assert_close(got, ref, f"{name} full size")
+                                  k_scale=oks, v_scale=ovs)
+    assert_close(step.out, ref, f"{name} full size, every row")

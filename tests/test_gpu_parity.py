@@ -95,7 +95,6 @@ def test_tiny_workload_full_parity():
     ref = oracle.attention_decode(w.q, okp, ovp, w.block_tables, w.context_lens, w.scale)
     assert_attn_close(out, ref, "tiny")
     # context_len 1 returns V_0 exactly
-    assert same_bits(out[0], okp.new_empty(0)) or True
     blk = int(w.block_tables[0, 0])
     v0 = ovp[blk, :, 0, :]  # [Hkv, D]
     G = w.Hq // w.Hkv

@@ -182,18 +182,24 @@ def test_prefill_rejects_unsupported_groups():
 def test_prefix_prefill_workload_full_size_sampled():
     """The benchmarked prefix-cached prompt pass at full size (128 requests,
     33K query tokens, 1030-token shared prefix), through the same call the
-    bench times, on sampled (row, head) outputs."""
+    bench times: every head of each request's first and last query rows and a
+    random sample of the rest, against the oracle."""
     w = workloads.make_prefill_named("prefix_prefill", device="cuda", nan_sentinel=True)
     out = torch.empty((w.T, w.Hq, w.D), dtype=w.dtype, device="cuda")
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
     kvp.kvp_attention_prefill(out, w.q, w.k_pool, w.v_pool, w.block_tables, w.context_lens,
                               w.query_start, w.max_query_len, w.scale, status=status)
     assert kvp.kvp_read_status(status) == kvp.KVP_OK
-    rng = np.random.default_rng(17)
-    t = rng.integers(0, w.T, size=256)
-    h = rng.integers(0, w.Hq, size=256)
+    # every head of each request's first and last query rows (the fewest and
+    # the most attended keys, at both ends of every tile walk), plus a seeded
+    # random sample of interior (row, head) pairs
     qs = w.query_start.cpu().numpy()
-    t[:3] = [0, int(qs[1]) - 1, w.T - 1]  # first row, end of the first chunk, last row
+    ends = np.unique(np.concatenate([qs[:-1], qs[1:] - 1]))
+    t = np.repeat(ends, w.Hq)
+    h = np.tile(np.arange(w.Hq), len(ends))
+    rng = np.random.default_rng(17)
+    t = np.concatenate([t, rng.integers(0, w.T, size=2048)])
+    h = np.concatenate([h, rng.integers(0, w.Hq, size=2048)])
     rows = np.stack([t, h], axis=1).astype(np.int32)
     ref = oracle.attention_prefill(w.q.cpu(), w.k_pool.cpu(), w.v_pool.cpu(),
                                    w.block_tables.cpu(), w.context_lens.cpu(),

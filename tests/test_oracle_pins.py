@@ -2,11 +2,13 @@
 
 Each test checks the oracle against something other than itself: an exhaustive
 enumeration, a library routine (torch float64 softmax / matmul, NumPy indexing),
-a closed form, or an independent restatement of the quantiser with NumPy's own
-primitives.  A plausible slip in the oracle (wrong head group, dropped scale,
+a closed form, or the quantiser's definition written out in exact rational
+arithmetic (plus properties any correct abs-max quantiser has).  A plausible slip in the oracle (wrong head group, dropped scale,
 transposed operand, wrong slot arithmetic, wrong rounding) fails at least one.
 """
 import math
+import struct
+from fractions import Fraction
 
 import numpy as np
 import pytest
@@ -245,29 +247,72 @@ def test_int8_decode_equals_dense_on_dequantised_values():
 
 
 # ------------------------------------------------------------ INT8 quantiser
-def _numpy_per_channel_quantiser(x16: np.ndarray):
-    """Restatement of the per-channel branch of the quantiser with NumPy's own
-    primitives: abs-max over the last axis in float32, /127, zero scale -> 1,
-    round (half to even), clip to [-128, 127], cast to int8."""
-    x = x16.astype(np.float32)
-    amax = np.max(np.abs(x), axis=-1, keepdims=True)
-    scale = (amax / np.float32(127.0)).astype(np.float32)
-    scale = np.where(scale > 0, scale, np.float32(1.0)).astype(np.float32)
-    codes = np.clip(np.round(x / scale), -128, 127).astype(np.int8)
-    return codes, scale[..., 0]
+def _f32(v: float) -> float:
+    """The float32 nearest to the double v (ties to even)."""
+    return struct.unpack("f", struct.pack("f", v))[0]
+
+
+def _quantise_rows_by_definition(x, qmax=127, fixed_scale=None):
+    """The INT8 rule written out from its definition ("KV Cache 优化与显存管理",
+    三: scale = abs-max / 127 per token and head, zero scale -> 1, codes =
+    x / scale rounded half to even, clipped to [-128, 127]) with exact
+    rational arithmetic instead of float32 arrays: every float32 quotient is
+    the exact quotient rounded once to double and once to float32, which
+    equals rounding it directly to float32 because a double carries more than
+    2 * 24 + 2 bits (Figueroa, "When is double rounding innocuous?", 1995).
+    Python's round() is half-to-even.  Returns (codes [rows, D] int8, scales
+    [rows] float32)."""
+    rows = [[float(v) for v in r] for r in np.asarray(x, dtype=np.float64)]
+    codes = np.zeros((len(rows), len(rows[0]) if rows else 0), dtype=np.int8)
+    scales = np.zeros(len(rows), dtype=np.float32)
+    for i, r in enumerate(rows):
+        if fixed_scale is None:
+            amax = max(abs(v) for v in r)
+            s = _f32(float(Fraction(amax) / qmax))
+            s = s if s > 0 else 1.0
+        else:
+            s = _f32(fixed_scale)
+        for j, v in enumerate(r):
+            q = round(_f32(float(Fraction(v) / Fraction(s))))
+            codes[i, j] = min(127, max(-128, q))
+        scales[i] = s
+    return codes, scales
 
 
 @pytest.mark.parametrize("dtype", [torch.float16, torch.bfloat16])
-def test_quantiser_matches_numpy_restatement(dtype):
+def test_quantiser_matches_its_definition(dtype):
     g = torch.Generator().manual_seed(15)
-    x = (torch.randn(400, 128, generator=g) * torch.rand(400, 1, generator=g) * 3).to(dtype)
+    x = (torch.randn(160, 128, generator=g) * torch.rand(160, 1, generator=g) * 3).to(dtype)
     x[3] = 0
     x[4, :7] = 0
     x[5] = 1e-3
     codes, scales = oracle.quantize_int8(x)
-    ref_codes, ref_scales = _numpy_per_channel_quantiser(x.float().numpy())
+    ref_codes, ref_scales = _quantise_rows_by_definition(x.float().numpy())
     assert np.array_equal(codes, ref_codes)
     assert np.array_equal(scales.view(np.uint32), ref_scales.view(np.uint32))
+
+
+def test_quantiser_properties():
+    """Properties any correct per-row abs-max quantiser has, independent of
+    how it is written: each code times its scale is within half a scale of the
+    source value, the abs-max element maps to +-127, the scale is the float32
+    nearest to abs-max / 127 (its neighbours are farther), and codes stay in
+    [-127, 127]."""
+    g = torch.Generator().manual_seed(21)
+    x = (torch.randn(300, 64, generator=g) * torch.rand(300, 1, generator=g) * 10).half()
+    codes, scales = oracle.quantize_int8(x)
+    xf = x.double().numpy()
+    sc = scales.astype(np.float64)[:, None]
+    assert np.all(np.abs(codes * sc - xf) <= sc * (0.5 + 2.0 ** -20))
+    amax_at = np.argmax(np.abs(xf), axis=1)
+    assert np.all(np.abs(codes[np.arange(len(xf)), amax_at]) == 127)
+    for i in range(len(xf)):
+        exact = Fraction(float(np.abs(xf[i]).max())) / 127
+        s = np.float32(scales[i])
+        d = abs(Fraction(float(s)) - exact)
+        for nb in (np.nextafter(s, np.float32(0)), np.nextafter(s, np.float32(np.inf))):
+            assert d <= abs(Fraction(float(nb)) - exact)
+    assert codes.min() >= -127 and codes.max() <= 127
 
 
 def test_quantiser_special_rows():
@@ -332,7 +377,8 @@ def test_append_int8_matches_quantise_then_scatter():
     slots = torch.tensor([5, -1, 63], dtype=torch.int32)
     c, s = oracle.append_int8(codes, scales, src, slots)
     c, s = c.numpy(), s.numpy()
-    qc, qs = _numpy_per_channel_quantiser(src.float().numpy())
+    qc, qs = _quantise_rows_by_definition(src.float().numpy().reshape(-1, D))
+    qc, qs = qc.reshape(3, Hkv, D), qs.reshape(3, Hkv)
     assert np.array_equal(c[0, :, 5], qc[0]) and np.array_equal(c[3, :, 15], qc[2])
     assert np.array_equal(s[0, :, 5], qs[0]) and np.array_equal(s[3, :, 15], qs[2])
     assert int(np.count_nonzero(s)) == 2 * Hkv
@@ -380,12 +426,12 @@ def test_fp8_quantiser_matches_library_restatement():
     assert codes[3].tolist() == [0] * 128 and scales[3] == 1.0
 
 
-def test_fixed_scale_int8_matches_numpy_restatement():
+def test_fixed_scale_int8_matches_its_definition():
     g = torch.Generator().manual_seed(42)
     x = (torch.randn(64, 128, generator=g) * 3).half()
     s = 0.0375
     got = oracle.quantize_int8_fixed(x, s)
-    ref = np.clip(np.round(x.float().numpy() / np.float32(s)), -128, 127).astype(np.int8)
+    ref, _ = _quantise_rows_by_definition(x.float().numpy(), fixed_scale=s)
     assert np.array_equal(got, ref)
     big = torch.full((1, 8), 60000.0, dtype=torch.float16)
     assert oracle.quantize_int8_fixed(big, 1.0).tolist() == [[127] * 8]   # clip

@@ -43,8 +43,11 @@ def test_noalloc_matches_workspace_decode_on_two_calls_in_a_row(lib):
     ws = torch.empty(need // 4 + 4, dtype=torch.float32, device="cuda")
     kvp.kvp_attention_decode(ref, q, kp, vp, bt, cl, w.scale, workspace=ws)
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
-    for _ in range(2):
-        out = torch.full_like(q, float("nan"))
+    # every buffer the calls write is allocated up front, so nothing below
+    # but the entry point itself could take device memory
+    outs = [torch.full_like(q, float("nan")) for _ in range(3)]
+
+    def call(out):
         st = lib.kvp_attention_decode_noalloc(
             out.data_ptr(), q.data_ptr(), kp.data_ptr(), vp.data_ptr(), bt.data_ptr(),
             w.max_blocks, cl.data_ptr(), w.B, w.Hq, ctypes.c_float(w.scale), desc,
@@ -52,6 +55,13 @@ def test_noalloc_matches_workspace_decode_on_two_calls_in_a_row(lib):
         assert st == kvp.KVP_OK
         torch.cuda.synchronize()
         assert kvp.kvp_read_status(status) == kvp.KVP_OK
+
+    call(outs[0])  # the first call on this device looks up the scratch address
+    free_before = torch.cuda.mem_get_info()[0]
+    for out in outs[1:]:  # two more calls in a row
+        call(out)
+    assert torch.cuda.mem_get_info()[0] == free_before  # no device memory was taken
+    for out in outs:
         assert torch.isfinite(out.float()).all()
         assert _close(out, ref)
 
