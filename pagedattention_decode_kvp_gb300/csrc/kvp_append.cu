@@ -43,40 +43,77 @@ __global__ void __launch_bounds__(256)
   vc[dst] = value[src];
 }
 
-// Codes rint(x_e / s) for 8 elements, x / s being the IEEE float32 quotient,
-// packed 4 per word.  r = x * (1/s) is within 2e-5 of x / s for |x / s| <=
-// 127.0001 (two roundings of relative size 2^-24), and RN(x / s) within 8e-6
-// of it, so whenever r lies more than 1e-4 from a half-integer both round to
-// the same integer; only elements inside that band take the exact quotient.
-// The clip to [-128, 127] of the definition never binds: s = RN(amax / 127)
-// keeps |x / s| <= 127 * (1 + 2^-23), which rounds to at most 127.
+// Codes rint(x_e / s) of 8 elements, x / s being the IEEE float32 quotient,
+// packed 4 per word (low byte first).
+//
+// Fast path: with r = x * (1/s), fma(x, 1/s, 1.5 * 2^23) rounds r once to an
+// integer k, half to even, held in the low mantissa bits (|r| < 2^22), so the
+// low byte of its bit pattern is k as an int8; d = fma(x, 1/s, -k) is r - k.
+// r is within 2e-5 of x / s for |x / s| <= 127.0001 (1/s is a correctly
+// rounded reciprocal; the product is exact inside the FMA), and RN(x / s)
+// within 8e-6 of x / s, so whenever |d| < 0.5 - 1e-4 both round to the same
+// integer.  Elements inside that band around a half-integer take the exact
+// quotient instead.  Pairs of elements go through the packed two-lane FMA.
+// kClip (a caller's fixed scale, where x / s may be anything) clamps r to
+// [-1024, 1024] first, so the rounding trick stays in range, and clips the
+// codes to [-128, 127]; clamped elements fail the band test and take the
+// exact path.  Without kClip the clip never binds: s = RN(amax / 127) keeps
+// |x / s| <= 127 * (1 + 2^-23), which rounds to at most 127.
 template <bool kClip>
 __device__ __forceinline__ void quantise8(const float (&x)[8], float s, float inv,
                                           uint32_t (&packed)[2]) {
-  int q[8];
-  bool near_tie = false;
+  constexpr float kMagic = 12582912.0f;   // 1.5 * 2^23
+  constexpr float kBand = 0.5f - 1.0e-4f;
+  uint32_t bits[8];
+  float d[8];
+  const uint64_t inv2 = dev::f2pack(inv, inv);
+  const uint64_t magic2 = dev::f2pack(kMagic, kMagic);
+  const uint64_t nmagic2 = dev::f2pack(-kMagic, -kMagic);
 #pragma unroll
-  for (int e = 0; e < 8; ++e) {
-    const float r = x[e] * inv;
-    const float rr = rintf(r);
-    q[e] = static_cast<int>(rr);
-    near_tie |= fabsf(r - rr) > 0.5f - 1.0e-4f;
-  }
-  if (near_tie) {
-#pragma unroll
-    for (int e = 0; e < 8; ++e) {
-      const float r = x[e] * inv;
-      if (fabsf(r - rintf(r)) > 0.5f - 1.0e-4f) q[e] = __float2int_rn(__fdiv_rn(x[e], s));
+  for (int e = 0; e < 8; e += 2) {
+    const uint64_t x2 = dev::f2pack(x[e], x[e + 1]);
+    uint64_t m2;
+    if constexpr (kClip) {
+      const float2 r = dev::f2unpack(dev::fmul2(x2, inv2));
+      m2 = dev::fadd2(dev::f2pack(fminf(fmaxf(r.x, -1024.f), 1024.f),
+                                  fminf(fmaxf(r.y, -1024.f), 1024.f)), magic2);
+    } else {
+      m2 = dev::ffma2(x2, inv2, magic2);
+    }
+    const uint64_t k2 = dev::fadd2(m2, nmagic2);                 // exact
+    const uint64_t nk2 = dev::f2pack(-dev::f2unpack(k2).x, -dev::f2unpack(k2).y);
+    const float2 dd = dev::f2unpack(dev::ffma2(x2, inv2, nk2));  // r - k
+    d[e] = dd.x;
+    d[e + 1] = dd.y;
+    float2 k = dev::f2unpack(k2);
+    if constexpr (kClip) {
+      k.x = fminf(fmaxf(k.x, -128.f), 127.f);
+      k.y = fminf(fmaxf(k.y, -128.f), 127.f);
+      bits[e] = static_cast<uint32_t>(static_cast<int>(k.x));
+      bits[e + 1] = static_cast<uint32_t>(static_cast<int>(k.y));
+    } else {
+      const float2 m = dev::f2unpack(m2);
+      bits[e] = __float_as_uint(m.x);
+      bits[e + 1] = __float_as_uint(m.y);
     }
   }
-  if constexpr (kClip) {  // a fixed scale can put x / s outside [-128, 127]
+  const float dmax = fmaxf(dev::max3f(fabsf(d[0]), fabsf(d[1]), fabsf(d[2])),
+                           fmaxf(dev::max3f(fabsf(d[3]), fabsf(d[4]), fabsf(d[5])),
+                                 fmaxf(fabsf(d[6]), fabsf(d[7]))));
+  if (dmax > kBand) {  // rare: some element sits near a half-integer
 #pragma unroll
-    for (int e = 0; e < 8; ++e) q[e] = min(127, max(-128, q[e]));
+    for (int e = 0; e < 8; ++e) {
+      if (fabsf(d[e]) > kBand) {
+        int q = __float2int_rn(__fdiv_rn(x[e], s));
+        if constexpr (kClip) q = min(127, max(-128, q));
+        bits[e] = static_cast<uint32_t>(q);
+      }
+    }
   }
 #pragma unroll
   for (int w = 0; w < 2; ++w) {
-    const uint32_t lo = __byte_perm(q[4 * w], q[4 * w + 1], 0x0040);
-    const uint32_t hi = __byte_perm(q[4 * w + 2], q[4 * w + 3], 0x0040);
+    const uint32_t lo = __byte_perm(bits[4 * w], bits[4 * w + 1], 0x0040);
+    const uint32_t hi = __byte_perm(bits[4 * w + 2], bits[4 * w + 3], 0x0040);
     packed[w] = __byte_perm(lo, hi, 0x5410);
   }
 }
@@ -95,13 +132,19 @@ __device__ __forceinline__ void quantise8_fp8(const float (&x)[8], float s, uint
 
 enum class QuantMode { kInt8, kInt8Fixed, kFp8 };
 
-// Quantise-and-scatter.  One group of D/8 lanes per (token, head) row, each
-// lane owning 8 elements (one 16-byte load of K and of V); grid =
-// (ceil(T / tokens per CTA), Hkv).
+// Quantise-and-scatter.  Eight lanes per (token, head) row, four rows per
+// warp; lane j of a row owns the 16-byte chunks j, j + 8, ... of its K and of
+// its V row (8 elements each, D / 64 chunks), so every load and store
+// instruction covers whole rows' contiguous bytes.  grid = (ceil(T / 32),
+// Hkv).
 //   kInt8:      scale = amax / 127 (1 if not > 0), code = rint(x / scale)
 //   kInt8Fixed: the given scale, code = clip(rint(x / scale), -128, 127)
 //   kFp8:       scale = amax / 448 (1 if not > 0), code = E4M3(x / scale)
-// and the scale is stored beside the codes.
+// and the scale is stored beside the codes.  The abs-max runs on the packed
+// 16-bit source pairs (exact) and K's and V's travel in one shuffle word.
+constexpr int kQuantLanes = 8;
+constexpr int kQuantRowsPerCta = 256 / kQuantLanes;
+
 template <bool kBf16, int D, QuantMode kMode>
 __global__ void __launch_bounds__(256)
     append_quant_kernel(const uint4* __restrict__ key, const uint4* __restrict__ value,
@@ -109,52 +152,47 @@ __global__ void __launch_bounds__(256)
                         float* __restrict__ ks, float* __restrict__ vs, float fixed_ks,
                         float fixed_vs, const int32_t* __restrict__ slots, int num_tokens,
                         int num_kv_heads, int num_slots, int32_t* status) {
-  constexpr int L = D / 8;
-  constexpr int kTokens = 256 / L;
+  constexpr int kChunks = D / 64;     // 16-byte chunks per lane, of K and of V
+  constexpr int kRowChunks = D / 8;   // 16-byte chunks per row
   dev::grid_dependency_wait();
   dev::launch_dependents();
-  const int t = blockIdx.x * kTokens + static_cast<int>(threadIdx.x) / L;
-  const int sub = threadIdx.x % L;
+  const int t = blockIdx.x * kQuantRowsPerCta + static_cast<int>(threadIdx.x) / kQuantLanes;
+  const int sub = threadIdx.x % kQuantLanes;
   const int h = blockIdx.y;
   const bool in = t < num_tokens;
   int slot = -1;
-  float xk[8], xv[8];
+  uint4 rk[kChunks], rv[kChunks];
 #pragma unroll
-  for (int e = 0; e < 8; ++e) xk[e] = xv[e] = 0.f;
+  for (int c = 0; c < kChunks; ++c) rk[c] = rv[c] = make_uint4(0u, 0u, 0u, 0u);
   if (in) {
     slot = slots[t];
-    const size_t src = (static_cast<size_t>(t) * num_kv_heads + h) * L + sub;
-    const uint4 rk = key[src];
-    const uint4 rv = value[src];
-    const uint32_t wk[4] = {rk.x, rk.y, rk.z, rk.w};
-    const uint32_t wv[4] = {rv.x, rv.y, rv.z, rv.w};
+    const size_t src = (static_cast<size_t>(t) * num_kv_heads + h) * kRowChunks + sub;
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const float2 a = dev::unpack2<kBf16>(wk[i]);
-      const float2 c = dev::unpack2<kBf16>(wv[i]);
-      xk[2 * i] = a.x;
-      xk[2 * i + 1] = a.y;
-      xv[2 * i] = c.x;
-      xv[2 * i + 1] = c.y;
+    for (int c = 0; c < kChunks; ++c) {
+      rk[c] = key[src + c * kQuantLanes];
+      rv[c] = value[src + c * kQuantLanes];
     }
   }
   float sk = fixed_ks, sv = fixed_vs;
   if constexpr (kMode != QuantMode::kInt8Fixed) {
-    float ak = 0.f, av = 0.f;
+    uint32_t mk = 0u, mv = 0u;
 #pragma unroll
-    for (int e = 0; e < 8; ++e) {
-      ak = fmaxf(ak, fabsf(xk[e]));
-      av = fmaxf(av, fabsf(xv[e]));
+    for (int c = 0; c < kChunks; ++c) {
+      mk = dev::absmax2<kBf16>(mk, dev::absmax2<kBf16>(dev::absmax2<kBf16>(rk[c].x, rk[c].y),
+                                                       dev::absmax2<kBf16>(rk[c].z, rk[c].w)));
+      mv = dev::absmax2<kBf16>(mv, dev::absmax2<kBf16>(dev::absmax2<kBf16>(rv[c].x, rv[c].y),
+                                                       dev::absmax2<kBf16>(rv[c].z, rv[c].w)));
     }
+    // K's two halves in the low half-word, V's in the high one
+    uint32_t kv = dev::absmax2<kBf16>(__byte_perm(mk, mv, 0x5410), __byte_perm(mk, mv, 0x7632));
 #pragma unroll
-    for (int o = L / 2; o >= 1; o >>= 1) {
-      ak = fmaxf(ak, __shfl_xor_sync(0xffffffffu, ak, o));
-      av = fmaxf(av, __shfl_xor_sync(0xffffffffu, av, o));
-    }
+    for (int o = kQuantLanes / 2; o >= 1; o >>= 1)
+      kv = dev::absmax2<kBf16>(kv, __shfl_xor_sync(0xffffffffu, kv, o));
+    const float2 a = dev::unpack2<kBf16>(kv);
     // float32 IEEE division for the scale, as the quantiser is defined
     const float qmax = kMode == QuantMode::kFp8 ? 448.0f : 127.0f;
-    sk = __fdiv_rn(ak, qmax);
-    sv = __fdiv_rn(av, qmax);
+    sk = __fdiv_rn(a.x, qmax);
+    sv = __fdiv_rn(a.y, qmax);
     sk = sk > 0.f ? sk : 1.0f;
     sv = sv > 0.f ? sv : 1.0f;
   }
@@ -163,18 +201,36 @@ __global__ void __launch_bounds__(256)
     if (sub == 0 && h == 0) dev::set_status(status, kErrBadBlock);
     return;
   }
-  uint32_t pk[2], pv[2];
-  if constexpr (kMode == QuantMode::kFp8) {
-    quantise8_fp8(xk, sk, pk);
-    quantise8_fp8(xv, sv, pv);
-  } else {
-    quantise8<kMode == QuantMode::kInt8Fixed>(xk, sk, __frcp_rn(sk), pk);
-    quantise8<kMode == QuantMode::kInt8Fixed>(xv, sv, __frcp_rn(sv), pv);
-  }
   const size_t srow = (static_cast<size_t>(slot / kBlockSize) * num_kv_heads + h) * kBlockSize +
                       slot % kBlockSize;
-  *reinterpret_cast<uint2*>(kc + srow * D + sub * 8) = make_uint2(pk[0], pk[1]);
-  *reinterpret_cast<uint2*>(vc + srow * D + sub * 8) = make_uint2(pv[0], pv[1]);
+  const float ik = kMode == QuantMode::kFp8 ? 0.f : __frcp_rn(sk);
+  const float iv = kMode == QuantMode::kFp8 ? 0.f : __frcp_rn(sv);
+#pragma unroll
+  for (int c = 0; c < kChunks; ++c) {
+    float xk[8], xv[8];
+    const uint32_t wk[4] = {rk[c].x, rk[c].y, rk[c].z, rk[c].w};
+    const uint32_t wv[4] = {rv[c].x, rv[c].y, rv[c].z, rv[c].w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float2 fk = dev::unpack2<kBf16>(wk[i]);
+      const float2 fv = dev::unpack2<kBf16>(wv[i]);
+      xk[2 * i] = fk.x;
+      xk[2 * i + 1] = fk.y;
+      xv[2 * i] = fv.x;
+      xv[2 * i + 1] = fv.y;
+    }
+    uint32_t pk[2], pv[2];
+    if constexpr (kMode == QuantMode::kFp8) {
+      quantise8_fp8(xk, sk, pk);
+      quantise8_fp8(xv, sv, pv);
+    } else {
+      quantise8<kMode == QuantMode::kInt8Fixed>(xk, sk, ik, pk);
+      quantise8<kMode == QuantMode::kInt8Fixed>(xv, sv, iv, pv);
+    }
+    const size_t off = srow * D + (sub + c * kQuantLanes) * 8;
+    *reinterpret_cast<uint2*>(kc + off) = make_uint2(pk[0], pk[1]);
+    *reinterpret_cast<uint2*>(vc + off) = make_uint2(pv[0], pv[1]);
+  }
   if (sub == 0) {
     ks[srow] = sk;
     vs[srow] = sv;
@@ -252,8 +308,7 @@ cudaError_t launch_quant(const void* key, const void* value, bool src_bf16, void
   const auto* v = static_cast<const uint4*>(value);
   auto* kd = static_cast<uint8_t*>(k_cache);
   auto* vd = static_cast<uint8_t*>(v_cache);
-  const int tokens_per_cta = 256 / (c.head_dim / 8);
-  const dim3 grid((num_tokens + tokens_per_cta - 1) / tokens_per_cta, c.num_kv_heads);
+  const dim3 grid((num_tokens + kQuantRowsPerCta - 1) / kQuantRowsPerCta, c.num_kv_heads);
 #define KVP_Q_CASE(BF, DD)                                                                     \
   if (src_bf16 == BF && c.head_dim == DD)                                                      \
     return launch_pdl(append_quant_kernel<BF, DD, kMode>, grid, dim3(256), 0, s, k, v, kd, vd, \

@@ -224,6 +224,40 @@ __device__ __forceinline__ float ex2_approx(float x) {
   return y;
 }
 
+// ----------------------------------------------------------------- packed fp32
+// Three-input max; packed two-lane fp32 arithmetic (each lane rounds as the
+// scalar instruction would).
+__device__ __forceinline__ float max3f(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+__device__ __forceinline__ uint64_t f2pack(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ float2 f2unpack(uint64_t x) {
+  float2 r;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(r.x), "=f"(r.y) : "l"(x));
+  return r;
+}
+__device__ __forceinline__ uint64_t ffma2(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t r;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+  return r;
+}
+__device__ __forceinline__ uint64_t fadd2(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ uint64_t fmul2(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+
 // ----------------------------------------------------------------- packing
 template <bool kBf16>
 __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
@@ -262,6 +296,24 @@ __device__ __forceinline__ uint16_t from_float(float x) {
   } else {
     __half v = __float2half_rn(x);
     return *reinterpret_cast<uint16_t*>(&v);
+  }
+}
+
+// Element-wise max of |a| and |b| for two packed 16-bit floats (fp16 or
+// bf16): the sign bits are cleared, then the pairs compared as floats.  Exact
+// (no rounding); a NaN operand yields the other one.
+template <bool kBf16>
+__device__ __forceinline__ uint32_t absmax2(uint32_t a, uint32_t b) {
+  a &= 0x7fff7fffu;
+  b &= 0x7fff7fffu;
+  if constexpr (kBf16) {
+    const __nv_bfloat162 r = __hmax2(*reinterpret_cast<const __nv_bfloat162*>(&a),
+                                     *reinterpret_cast<const __nv_bfloat162*>(&b));
+    return *reinterpret_cast<const uint32_t*>(&r);
+  } else {
+    const __half2 r = __hmax2(*reinterpret_cast<const __half2*>(&a),
+                              *reinterpret_cast<const __half2*>(&b));
+    return *reinterpret_cast<const uint32_t*>(&r);
   }
 }
 

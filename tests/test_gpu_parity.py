@@ -216,6 +216,65 @@ def test_append_int8_bit_exact(src_dtype, D):
     assert same_bits(gvc, ovc) and same_bits(gvs, ovs)
 
 
+def _tie_rows(src_dtype, D, n_rows, seed):
+    """Rows that put many elements on or next to a half-integer of x / scale:
+    (a) amax = 127 * 2^e, so scale = 2^e exactly and (k + 1/2) * 2^e are exact
+    ties; (b) the same values moved by one unit in the last place either way;
+    (c) arbitrary maxima with elements rounded from (k + 1/2) * amax / 127,
+    which land within a few units in the last place of a tie."""
+    g = torch.Generator().manual_seed(seed)
+    rows = torch.empty(n_rows, D, dtype=torch.float32)
+    for r in range(n_rows):
+        kind = r % 3
+        e = int(torch.randint(-10, 6, (1,), generator=g))
+        k = torch.randint(-127, 127, (D,), generator=g).float()
+        if kind < 2:
+            x = ((k + 0.5) * 2.0 ** e).to(src_dtype)
+            if kind == 1:  # one unit in the last place up or down
+                bits = x.view(torch.int16)
+                step = torch.randint(0, 2, (D,), generator=g, dtype=torch.int16) * 2 - 1
+                x = (bits + step).view(src_dtype)
+            x[0] = 127.0 * 2.0 ** e
+        else:
+            amax = float(torch.rand(1, generator=g)) * 30 + 0.01
+            x = ((k + 0.5) * (amax / 127.0)).to(src_dtype)
+            x[0] = -amax
+        x = x.float()
+        x = x[torch.randperm(D, generator=g)]  # the abs-max anywhere in the row
+        rows[r] = x
+    return rows.to(src_dtype)
+
+
+@pytest.mark.parametrize("src_dtype", [torch.float16, torch.bfloat16])
+@pytest.mark.parametrize("D", [64, 128])
+def test_append_int8_ties_and_near_ties_bit_exact(src_dtype, D):
+    """The quantiser's codes come from a rounded product on the fast path and
+    from the IEEE quotient next to a half-integer; rows built on and around
+    ties check both against the oracle's float32 division, bit for bit."""
+    Hkv, NB = 2, 256
+    x = _tie_rows(src_dtype, D, 2 * 1536, seed=D + (src_dtype == torch.bfloat16))
+    key = x[:1536].view(768, Hkv, D)
+    value = x[1536:].view(768, Hkv, D)
+    T = key.shape[0]
+    g = torch.Generator().manual_seed(5)
+    slots = torch.randperm(NB * 16, generator=g)[:T].to(torch.int32)
+    kc = torch.zeros(NB, Hkv, 16, D, dtype=torch.int8)
+    vc = torch.zeros_like(kc)
+    ks = torch.zeros(NB, Hkv, 16)
+    vs = torch.zeros(NB, Hkv, 16)
+    gkc, gvc, gks, gvs = kc.cuda(), vc.cuda(), ks.cuda(), vs.cuda()
+    kvp.kvp_append_int8(key.cuda(), value.cuda(), gkc, gvc, gks, gvs, slots.cuda())
+    torch.cuda.synchronize()
+    okc, oks = oracle.append_int8(kc, ks, key, slots)
+    ovc, ovs = oracle.append_int8(vc, vs, value, slots)
+    assert same_bits(gks, oks) and same_bits(gvs, ovs)
+    assert same_bits(gkc, okc) and same_bits(gvc, ovc)
+    # the rows really exercise ties: many exact x.5 quotients among them
+    q = key.float().view(-1, D) / torch.from_numpy(
+        oracle.quantize_int8(key.view(-1, D))[1])[:, None]
+    assert int(((q - q.floor()) == 0.5).sum()) > 1000
+
+
 def int8_workload(B, Hq, Hkv, D, lens, NB, q_dtype, seed, max_blocks=None):
     w = workloads.make_custom(B=B, Hq=Hq, Hkv=Hkv, D=D, lens=lens, num_blocks=NB,
                               dtype=q_dtype, kv_int8=True, seed=seed, max_blocks=max_blocks)
