@@ -217,8 +217,10 @@ class ClockSampler:
 class Step:
     """Device buffers of one workload and the step through the public API."""
 
-    def __init__(self, w, kvp, dev, partition_blocks=0, fused=False):
+    def __init__(self, w, kvp, dev, partition_blocks=0, fused=False, merge_runs=False):
         self.w, self.kvp, self.dev = w, kvp, dev
+        # the run-merged fetch rides on the phases argument of every decode call
+        self.flags = kvp.KVP_DECODE_MERGE_RUNS if merge_runs else 0
         # the fused step needs one new token per request at position n - 1
         self.fused = fused and not w.kv_int8 and w.cow_pairs is None and \
             int(w.slot_mapping.numel()) == w.B
@@ -297,7 +299,8 @@ class Step:
             for i, ph in enumerate(phases):
                 kvp.kvp_append_attention_decode(self.new_k, self.new_v, self.out, self.q, self.kp,
                                                 self.vp, self.tables, self.lens, w.scale,
-                                                workspace=self.ws, phases=ph, status=self.status,
+                                                workspace=self.ws, phases=ph | self.flags,
+                                                status=self.status,
                                                 partition_blocks=self.pb_arg)
                 if ev is not None and i == 0:
                     ev[1].record()
@@ -319,12 +322,14 @@ class Step:
                 decode = kvp.kvp_attention_decode_fp8 if w.kv_fp8 else \
                     kvp.kvp_attention_decode_int8
                 decode(self.out, self.q, self.kp, self.vp, self.ks,
-                       self.vs, self.tables, self.lens, w.scale, workspace=self.ws, phases=ph,
-                       status=self.status, partition_blocks=self.pb_arg)
+                       self.vs, self.tables, self.lens, w.scale, workspace=self.ws,
+                       phases=ph | self.flags, status=self.status,
+                       partition_blocks=self.pb_arg)
             else:
                 kvp.kvp_attention_decode(self.out, self.q, self.kp, self.vp, self.tables,
-                                         self.lens, w.scale, workspace=self.ws, phases=ph,
-                                         status=self.status, partition_blocks=self.pb_arg)
+                                         self.lens, w.scale, workspace=self.ws,
+                                         phases=ph | self.flags, status=self.status,
+                                         partition_blocks=self.pb_arg)
             if ev is not None and i == 0:
                 ev[1].record()
 
@@ -434,7 +439,8 @@ def measure_decode(name, args, kvp, world, dev, local, headline):
     w = workloads.make(name, device=dev, nan_sentinel=False,
                        batch=args.batch if headline else None,
                        contiguity=args.contiguity if headline else None)
-    step = Step(w, kvp, dev, args.partition_blocks if headline else 0, fused=not args.unfused)
+    step = Step(w, kvp, dev, args.partition_blocks if headline else 0, fused=not args.unfused,
+                merge_runs=headline and args.merge_runs)
     lens = [int(x) for x in w.context_lens]
     dbytes = decode_bytes(w, lens)
     sbytes = dbytes["call"] + append_bytes(w) + copy_bytes(w)
@@ -469,6 +475,7 @@ def measure_decode(name, args, kvp, world, dev, local, headline):
                    "cow_pairs": int(w.cow_pairs.shape[0]) if w.cow_pairs is not None else 0,
                    "partition_blocks": step.part_blocks,
                    "append": "fused into the decode" if step.fused else "separate kernel",
+                   "fetch": "runs of consecutive blocks" if step.flags else "per block",
                    "l2": ("inputs larger than L2: {:.2f} GB of K/V per step vs 129 MB L2"
                           .format(dbytes["kv"] / 1e9)) if dbytes["kv"] > 4 * L2_BYTES else
                          "inputs partly L2-resident (L2 reuse is part of this workload)",
@@ -925,6 +932,9 @@ def main():
     ap.add_argument("--unfused", action="store_true",
                     help="append with kvp_append, then decode (default: the fused entry point "
                          "where every request appends one token at its last position)")
+    ap.add_argument("--merge-runs", action="store_true",
+                    help="decode with the run-merged fetch (one copy per run of up to 4 "
+                         "physically consecutive blocks)")
     ap.add_argument("--cpu-rows-1core", type=int, default=128,
                     help="(request, head) rows the CPU oracle times on one core (0 = skip)")
     ap.add_argument("--no-extras", action="store_true",
@@ -944,7 +954,7 @@ def main():
             args.cpu_rows = 1024 if args.impl == "ours" else 64
     args.extras = (not args.no_extras and args.workload == "llama7b" and args.batch is None
                    and args.contiguity is None and args.partition_blocks == 0
-                   and not args.unfused)
+                   and not args.unfused and not args.merge_runs)
     if args.impl == "reference":
         (run_reference_prefill if prefill else run_reference)(args)
     else:

@@ -86,7 +86,13 @@ enum {
   KVP_PHASE_PARTIAL = 1, /* per-partition pass: partial (m, l, o) to workspace,
                             or the final row for requests with one partition  */
   KVP_PHASE_REDUCE = 2,  /* merge of the partials into out                     */
-  KVP_PHASE_ALL = 3
+  KVP_PHASE_ALL = 3,
+  /* Flag, or'ed into `phases` of any decode entry point: fetch runs of
+   * physically consecutive blocks ("ATB KV Cache management", "显存碎片问题":
+   * contiguous-first allocation leaves most of a table as such runs) with one
+   * copy per run of up to 4 blocks instead of one per block.  Same results,
+   * bit for bit, as the default per-block fetch. */
+  KVP_DECODE_MERGE_RUNS = 8
 };
 
 /* Human-readable name of a status code (static storage). */

@@ -36,6 +36,7 @@ KVP_BF16 = 1
 KVP_PHASE_PARTIAL = 1
 KVP_PHASE_REDUCE = 2
 KVP_PHASE_ALL = 3
+KVP_DECODE_MERGE_RUNS = 8  # or'ed into `phases`: one copy per run of consecutive blocks
 BLOCK_SIZE = 16
 
 

@@ -70,6 +70,38 @@ kvp_status make_pool_map(CUtensorMap* map, const void* base, const kvp_cache_des
   return r == CUDA_SUCCESS ? KVP_OK : KVP_ERR_CUDA;
 }
 
+// TMA descriptor over a whole pool viewed as 5-D {row piece, 16 rows, pieces
+// per row, Hkv, NB} (a row piece is <= 128 bytes of a token row), whose box
+// {piece, 16, pieces, 1, run} lands `run` consecutive blocks' tiles of one kv
+// head in shared memory back to back, each laid out as a per-block box would
+// put it ([piece][16 rows][bytes], 128-byte swizzle for 128-byte pieces).
+kvp_status make_pool_run_map(CUtensorMap* map, const void* base, const kvp_cache_desc& c,
+                             int elem_bytes, int run) {
+  auto fn = encode_fn();
+  if (fn == nullptr) return KVP_ERR_CUDA;
+  const int row_bytes = c.head_dim * elem_bytes;
+  const int piece_bytes = row_bytes < 128 ? row_bytes : 128;
+  const int pieces = row_bytes / piece_bytes;
+  cuuint64_t dims[5] = {static_cast<cuuint64_t>(piece_bytes / elem_bytes),
+                        static_cast<cuuint64_t>(kBlockSize), static_cast<cuuint64_t>(pieces),
+                        static_cast<cuuint64_t>(c.num_kv_heads),
+                        static_cast<cuuint64_t>(c.num_blocks)};
+  cuuint64_t strides[4] = {static_cast<cuuint64_t>(row_bytes),
+                           static_cast<cuuint64_t>(piece_bytes),
+                           static_cast<cuuint64_t>(row_bytes) * kBlockSize,
+                           static_cast<cuuint64_t>(row_bytes) * kBlockSize * c.num_kv_heads};
+  cuuint32_t box[5] = {static_cast<cuuint32_t>(piece_bytes / elem_bytes),
+                       static_cast<cuuint32_t>(kBlockSize), static_cast<cuuint32_t>(pieces), 1,
+                       static_cast<cuuint32_t>(run)};
+  cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+  const CUresult r =
+      fn(map, elem_bytes == 2 ? CU_TENSOR_MAP_DATA_TYPE_UINT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8, 5,
+         const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+         piece_bytes == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? KVP_OK : KVP_ERR_CUDA;
+}
+
 // TMA descriptor over q viewed as [T tokens][Hq heads][D]: a box of 64
 // elements x `group` heads x `box_tokens` tokens lands in shared memory as
 // 128-byte swizzled rows ordered (token, head) -- the K-major operand layout.
@@ -179,6 +211,8 @@ kvp_status decode_common(void* out, const void* q, bool q_bf16, int kv_kind, con
   DecodeShape sh;
   const kvp_status st = shape_decode(batch, hq, c, max_blocks, partition_blocks, int8, &sh);
   if (st != KVP_OK) return st;
+  const bool merge_runs = (phases & KVP_DECODE_MERGE_RUNS) != 0;
+  phases &= ~KVP_DECODE_MERGE_RUNS;
   if (phases < 1 || phases > 3) return KVP_ERR_INVALID_ARG;
   if (!std::isfinite(scale)) return KVP_ERR_INVALID_ARG;
   if (batch == 0) return KVP_OK;
@@ -226,22 +260,31 @@ kvp_status decode_common(void* out, const void* q, bool q_bf16, int kv_kind, con
 
   if (phases & KVP_PHASE_PARTIAL) {
     const int eb = int8 ? 1 : 2;
-    CUtensorMap tk, tv;
-    kvp_status r = make_pool_map(&tk, kc, c, eb);
-    if (r != KVP_OK) return r;
-    r = make_pool_map(&tv, vc, c, eb);
+    DecodeMaps maps;
+    maps.merged = merge_runs;
+    kvp_status r = KVP_OK;
+    if (merge_runs) {
+      const int runs[3] = {1, 2, 4};
+      for (int i = 0; i < 3 && r == KVP_OK; ++i) {
+        r = make_pool_run_map(&maps.runs.k[i], kc, c, eb, runs[i]);
+        if (r == KVP_OK) r = make_pool_run_map(&maps.runs.v[i], vc, c, eb, runs[i]);
+      }
+    } else {
+      r = make_pool_map(&maps.k, kc, c, eb);
+      if (r == KVP_OK) r = make_pool_map(&maps.v, vc, c, eb);
+    }
     if (r != KVP_OK) return r;
     cudaError_t e;
     switch (sh.path) {
       case DecodePath::kSimt:
-        e = launch_decode_simt(p, tk, tv, kv_kind == 1, sh.max_parts, s);
+        e = launch_decode_simt(p, maps, kv_kind == 1, sh.max_parts, s);
         break;
       case DecodePath::kMma:
-        e = launch_decode_mma(p, tk, tv, kv_kind == 1, sh.max_parts, s);
+        e = launch_decode_mma(p, maps, kv_kind == 1, sh.max_parts, s);
         break;
       default:
-        e = kv_kind == 3 ? launch_decode_mma_fp8(p, tk, tv, sh.max_parts, s)
-                         : launch_decode_mma_int8(p, tk, tv, sh.max_parts, s);
+        e = kv_kind == 3 ? launch_decode_mma_fp8(p, maps, sh.max_parts, s)
+                         : launch_decode_mma_int8(p, maps, sh.max_parts, s);
         break;
     }
     if (e != cudaSuccess) return KVP_ERR_CUDA;

@@ -553,6 +553,19 @@ struct MmaInt8Path {
         vc[0] = rc.x; vc[1] = rc.y;
         vd[0] = rd.x; vd[1] = rd.y;
       }
+      if constexpr (kFp8) {
+        // E4M3 has NaN codes: V of tokens past the context (unused slots may
+        // hold any bytes) must not reach the product, where 0 * NaN = NaN
+        if (valid < 16) {
+#pragma unroll
+          for (int w = 0; w < kVw; ++w) {
+            va[w] = ta < valid ? va[w] : 0u;
+            vb[w] = tb < valid ? vb[w] : 0u;
+            vc[w] = tc < valid ? vc[w] : 0u;
+            vd[w] = td < valid ? vd[w] : 0u;
+          }
+        }
+      }
     }
     float ct[kMt][4];
 #pragma unroll
@@ -618,72 +631,85 @@ __device__ __forceinline__ void zero_rows(const DecodeParams& p, int b, int head
   for (int i = threadIdx.x; i < nheads * D; i += blockDim.x) out[i] = 0;
 }
 
+// What one decode CTA works on: request b, kv head kvh, query heads head0 ..
+// head0 + nheads - 1, and blocks blk0 .. blk0 + nb - 1 of the request's table
+// (partition `part` of nparts); tail_valid tokens in the sequence's last block.
+struct DecodeCta {
+  int part, kvh, b, head0, nheads, n, nparts, nb, tail_valid;
+  bool last_part;
+};
+
+// Shared memory of a decode CTA (1024-byte aligned stage area first).
+struct DecodeSmem {
+  uint8_t* stages;   // kWarps * kStagesPerWarp tiles of K then V
+  float* scales;     // per tile: 16 K scales, 16 V scales (8-bit pools)
+  uint64_t* bars;    // kWarps * kStagesPerWarp mbarriers
+  int32_t* tbl;      // the partition's block ids
+};
+
 template <class Path>
-__global__ void __launch_bounds__(kWarps * 32)
-    decode_partial_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmk,
-                          const __grid_constant__ CUtensorMap tmv) {
-  using namespace dev;
+__device__ __forceinline__ DecodeSmem decode_smem(uint8_t* smem_raw) {
   constexpr int S = kWarps * kStagesPerWarp;
-  constexpr int TB = Path::kTileBytes;
-  constexpr int SB = Path::kScaleStageBytes;
-  constexpr int H = Path::kHeads;
+  uint8_t* smem = dev::align1024(smem_raw);
+  DecodeSmem m;
+  m.stages = smem;
+  m.scales = reinterpret_cast<float*>(smem + S * 2 * Path::kTileBytes);
+  m.bars = reinterpret_cast<uint64_t*>(smem + S * 2 * Path::kTileBytes +
+                                       S * Path::kScaleStageBytes);
+  m.tbl = reinterpret_cast<int32_t*>(m.bars + S);
+  return m;
+}
+
+// Prologue shared by both pipelines: which work this CTA has, the partition's
+// block ids staged in shared memory and range-checked ("踩坑一": the page table
+// is copied on chip once, not looked up in HBM per page), and the fused
+// append.  Returns false when the CTA has nothing to stream (its rows are
+// already written or belong to another partition).  *any_bad: an id is out of
+// range.  `init_bars` runs on thread 0 before the barrier that publishes the
+// table.
+template <class Path, class InitBars>
+__device__ __forceinline__ bool decode_prologue(const DecodeParams& p, const DecodeSmem& sm,
+                                                DecodeCta& c, bool* any_bad,
+                                                InitBars init_bars) {
+  using namespace dev;
   constexpr int D = Path::kD;
-  constexpr int kRowBytes = D * Path::kElemBytes;
-  constexpr int kBoxBytes = kRowBytes < 128 ? kRowBytes : 128;  // inner extent of a TMA box
-  constexpr int kBoxes = kRowBytes / kBoxBytes;                 // TMA boxes per tile
-  static_assert(kWarps * H * (D + 2) * 4 <= S * 2 * TB, "merge area must fit in the stages");
-
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = align1024(smem_raw);
-  uint8_t* stages = smem;
-  float* scales = reinterpret_cast<float*>(smem + S * 2 * TB);
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S * 2 * TB + S * SB);
-  int32_t* tbl = reinterpret_cast<int32_t*>(bars + S);
-  __shared__ int cta_flag;
-
-  const int part = blockIdx.x;
-  const int kvh = blockIdx.y / p.qgroups;
+  c.part = blockIdx.x;
+  c.kvh = blockIdx.y / p.qgroups;
   const int qg = blockIdx.y % p.qgroups;
-  const int b = blockIdx.z;
-  const int head0 = kvh * p.group + qg * p.heads_per_cta;
-  const int nheads = min(p.heads_per_cta, p.group - qg * p.heads_per_cta);
-  const int warp = threadIdx.x >> 5;
-  const int lane = threadIdx.x & 31;
+  c.b = blockIdx.z;
+  c.head0 = c.kvh * p.group + qg * p.heads_per_cta;
+  c.nheads = min(p.heads_per_cta, p.group - qg * p.heads_per_cta);
 
   grid_dependency_wait();  // the previous kernel (e.g. the append) has landed
-  const int n = p.context_lens[b];
-  if (n <= 0 || n > p.max_blocks * kBlockSize) {
-    if (part == 0) {
-      zero_rows<D>(p, b, head0, nheads);
-      if (n != 0 && threadIdx.x == 0) set_status(p.status, kErrBadBlock);
+  c.n = p.context_lens[c.b];
+  if (c.n <= 0 || c.n > p.max_blocks * kBlockSize) {
+    if (c.part == 0) {
+      zero_rows<D>(p, c.b, c.head0, c.nheads);
+      if (c.n != 0 && threadIdx.x == 0) set_status(p.status, kErrBadBlock);
     }
-    return;
+    return false;
   }
-  const int nblk_seq = (n + kBlockSize - 1) / kBlockSize;
-  const int nparts = (nblk_seq + p.part_blocks - 1) / p.part_blocks;
-  const int blk0 = part * p.part_blocks;
-  if (blk0 >= nblk_seq) return;
-  const int nb = min(p.part_blocks, nblk_seq - blk0);
-  const bool last_part = blk0 + nb == nblk_seq;
-  const int tail_valid = n - (nblk_seq - 1) * kBlockSize;
+  const int nblk_seq = (c.n + kBlockSize - 1) / kBlockSize;
+  c.nparts = (nblk_seq + p.part_blocks - 1) / p.part_blocks;
+  const int blk0 = c.part * p.part_blocks;
+  if (blk0 >= nblk_seq) return false;
+  c.nb = min(p.part_blocks, nblk_seq - blk0);
+  c.last_part = blk0 + c.nb == nblk_seq;
+  c.tail_valid = c.n - (nblk_seq - 1) * kBlockSize;
 
   // ---- stage this partition's slice of the block table and check every id
   bool bad = false;
-  const int32_t* row = p.block_tables + static_cast<size_t>(b) * p.max_blocks + blk0;
-  for (int i = threadIdx.x; i < nb; i += blockDim.x) {
+  const int32_t* row = p.block_tables + static_cast<size_t>(c.b) * p.max_blocks + blk0;
+  for (int i = threadIdx.x; i < c.nb; i += blockDim.x) {
     const int id = row[i];
     bad |= (id < 0) || (id >= p.num_blocks);
-    tbl[i] = id;
+    sm.tbl[i] = id;
   }
   if (threadIdx.x == 0) {
-    cta_flag = 0;
-    prefetch_tensormap(&tmk);
-    prefetch_tensormap(&tmv);
-#pragma unroll
-    for (int s = 0; s < S; ++s) mbar_init(smem_addr(bars + s), 1);
+    init_bars();
     fence_barrier_init();
   }
-  const bool any_bad = __syncthreads_or(bad);
+  *any_bad = __syncthreads_or(bad);
 
   // ---- fused append: the new token of this request (position n-1) lies in
   // the sequence's last block, which only last-partition CTAs read; they write
@@ -691,109 +717,51 @@ __global__ void __launch_bounds__(kWarps * 32)
   // the TMA (async proxy) before any copy is issued.  CTAs of other query
   // groups of the same kv head write the same bytes.
   if constexpr (Path::kElemBytes == 2) {
-    if (p.new_k != nullptr && last_part && !any_bad) {
+    if (p.new_k != nullptr && c.last_part && !*any_bad) {
       constexpr int kChunks = D * 2 / 16;  // 16-byte chunks per row
       const size_t srow =
-          (static_cast<size_t>(tbl[nb - 1]) * p.num_kv_heads + kvh) * kBlockSize +
-          (n - 1) % kBlockSize;
-      const size_t nrow = static_cast<size_t>(b) * p.num_kv_heads + kvh;
+          (static_cast<size_t>(sm.tbl[c.nb - 1]) * p.num_kv_heads + c.kvh) * kBlockSize +
+          (c.n - 1) % kBlockSize;
+      const size_t nrow = static_cast<size_t>(c.b) * p.num_kv_heads + c.kvh;
       if (threadIdx.x < 2 * kChunks) {
-        const int c = threadIdx.x % kChunks;
+        const int ch = threadIdx.x % kChunks;
         const bool is_v = threadIdx.x >= kChunks;
         const uint4* src = static_cast<const uint4*>(is_v ? p.new_v : p.new_k) + nrow * kChunks;
         uint4* dst = reinterpret_cast<uint4*>(const_cast<void*>(is_v ? p.v_pool : p.k_pool)) +
                      srow * kChunks;
-        dst[c] = src[c];
+        dst[ch] = src[ch];
         fence_proxy_async_global();
       }
       __syncthreads();
     }
   }
+  return true;
+}
 
-  const float* ksrc = p.k_scale;
-  const float* vsrc = p.v_scale;
-  auto issue = [&](int j) {  // lane 0 of this warp: fetch the warp's j-th block
-    const int i = warp + j * kWarps;
-    const int stage = warp * kStagesPerWarp + (j % kStagesPerWarp);
-    const uint32_t bar = smem_addr(bars + stage);
-    uint8_t* kdst = stages + stage * 2 * TB;
-    uint8_t* vdst = kdst + TB;
-    const int y = (tbl[i] * p.num_kv_heads + kvh) * kBlockSize;
-    mbar_arrive_expect_tx(bar, 2 * TB + SB);
-#pragma unroll
-    for (int x = 0; x < kBoxes; ++x) {
-      const int xe = x * (kBoxBytes / Path::kElemBytes);
-      tma_load_2d(smem_addr(kdst + x * 16 * kBoxBytes), &tmk, xe, y, bar);
-      tma_load_2d(smem_addr(vdst + x * 16 * kBoxBytes), &tmv, xe, y, bar);
-    }
-    if constexpr (SB > 0) {
-      float* sdst = scales + stage * (SB / 4);
-      bulk_load(smem_addr(sdst), ksrc + y, 64, bar);
-      bulk_load(smem_addr(sdst + 16), vsrc + y, 64, bar);
-    }
-  };
-
-  typename Path::State st;
-  bool ok = !any_bad;
-  if (ok) {
-    Path::init(st, p, b, head0, nheads, lane);
-    const int my_blocks = nb > warp ? (nb - warp + kWarps - 1) / kWarps : 0;
-    const int prologue = my_blocks < kStagesPerWarp ? my_blocks : kStagesPerWarp;
-    if (lane == 0) {
-      for (int j = 0; j < prologue; ++j) issue(j);
-    }
-    int issued = prologue;
-    int j = 0;
-    for (; j < my_blocks; ++j) {
-      const int stage = warp * kStagesPerWarp + (j % kStagesPerWarp);
-      const bool landed = mbar_wait_bounded(smem_addr(bars + stage), (j / kStagesPerWarp) & 1);
-      if (!__all_sync(0xffffffffu, landed)) {
-        ok = false;
-        break;
-      }
-      const int i = warp + j * kWarps;
-      const int valid = (last_part && i == nb - 1) ? tail_valid : kBlockSize;
-      const uint8_t* kt = stages + stage * 2 * TB;
-      Path::consume(st, kt, kt + TB, scales + stage * (SB / 4), valid, lane, p.scale_log2);
-      __syncwarp();
-      if (j + kStagesPerWarp < my_blocks) {
-        if (lane == 0) {
-          fence_proxy_async_smem();
-          issue(j + kStagesPerWarp);
-        }
-        ++issued;
-      }
-    }
-    if (!ok) {
-      // A transfer did not land in time: wait (bounded) for this warp's copies
-      // still in flight so no TMA write outlives the CTA, then report.
-      if (lane == 0) {
-        for (int jj = j; jj < issued; ++jj) {
-          const int stage = warp * kStagesPerWarp + (jj % kStagesPerWarp);
-          mbar_wait_bounded(smem_addr(bars + stage), (jj / kStagesPerWarp) & 1);
-        }
-        set_status(p.status, kErrTimeout);
-        atomicExch(&cta_flag, 1);
-      }
-    }
-  } else if (threadIdx.x == 0) {
-    set_status(p.status, kErrBadBlock);
-  }
-
-  // ---- merge the warps' partial states (stage memory is free now)
-  launch_dependents();
-  __syncthreads();
-  const bool cta_bad = any_bad || cta_flag != 0;
-  float* mo = reinterpret_cast<float*>(smem);
+// Epilogue shared by both pipelines: merge the warps' partial states (the
+// stage memory is free by now) and write the output rows (single partition)
+// or this partition's (m, l, o) to the workspace.  cta_bad: a block id was out
+// of range or a transfer timed out; the rows are then zero (or L < 0 marks the
+// partition failed for the reduce).
+template <class Path>
+__device__ __forceinline__ void decode_epilogue(const DecodeParams& p, const DecodeSmem& sm,
+                                                const DecodeCta& c, typename Path::State& st,
+                                                bool cta_bad) {
+  using namespace dev;
+  constexpr int H = Path::kHeads;
+  constexpr int D = Path::kD;
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  float* mo = reinterpret_cast<float*>(sm.stages);
   float* mm = mo + kWarps * H * D;
   float* ml = mm + kWarps * H;
   if (!cta_bad) Path::finalize(st, mo + warp * H * D, mm + warp * H, ml + warp * H, lane);
   __syncthreads();
 
-  const size_t rowbase = static_cast<size_t>(b) * p.num_q_heads + head0;
-  if (nparts == 1) {
+  const size_t rowbase = static_cast<size_t>(c.b) * p.num_q_heads + c.head0;
+  if (c.nparts == 1) {
     uint16_t* out = static_cast<uint16_t*>(p.out) + rowbase * D;
-    for (int idx = threadIdx.x; idx < nheads * D; idx += blockDim.x) {
+    for (int idx = threadIdx.x; idx < c.nheads * D; idx += blockDim.x) {
       const int hh = idx / D, d = idx % D;
       float res = 0.f;
       if (!cta_bad) {
@@ -812,7 +780,7 @@ __global__ void __launch_bounds__(kWarps * 32)
       out[idx] = p.q_bf16 ? from_float<true>(res) : from_float<false>(res);
     }
   } else {
-    for (int idx = threadIdx.x; idx < nheads * D; idx += blockDim.x) {
+    for (int idx = threadIdx.x; idx < c.nheads * D; idx += blockDim.x) {
       const int hh = idx / D, d = idx % D;
       float M = -INFINITY, L = -1.f, acc = 0.f;  // L < 0 marks a failed partition
       if (!cta_bad) {
@@ -826,7 +794,7 @@ __global__ void __launch_bounds__(kWarps * 32)
           acc = fmaf(f, mo[(w * H + hh) * D + d], acc);
         }
       }
-      const size_t prow = (rowbase + hh) * p.max_parts + part;
+      const size_t prow = (rowbase + hh) * p.max_parts + c.part;
       p.ws_o[prow * D + d] = acc;
       if (d == 0) {
         p.ws_ml[2 * prow] = M;
@@ -836,15 +804,278 @@ __global__ void __launch_bounds__(kWarps * 32)
   }
 }
 
+// ---------------------------------------------------------------------------
+// Per-block fetch: each of the CTA's 4 warps owns a ring of 2 stages and
+// streams its own blocks w, w+4, ... (lane 0 issues the block's TMA boxes and
+// waits with the warp), independently of the other warps.
 template <class Path>
-cudaError_t launch_partial(const DecodeParams& p, const CUtensorMap& tk, const CUtensorMap& tv,
-                           int grid_x, cudaStream_t s) {
+__global__ void __launch_bounds__(kWarps * 32)
+    decode_partial_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmk,
+                          const __grid_constant__ CUtensorMap tmv) {
+  using namespace dev;
+  constexpr int S = kWarps * kStagesPerWarp;
+  constexpr int TB = Path::kTileBytes;
+  constexpr int SB = Path::kScaleStageBytes;
+  constexpr int H = Path::kHeads;
+  constexpr int D = Path::kD;
+  constexpr int kRowBytes = D * Path::kElemBytes;
+  constexpr int kBoxBytes = kRowBytes < 128 ? kRowBytes : 128;  // inner extent of a TMA box
+  constexpr int kBoxes = kRowBytes / kBoxBytes;                 // TMA boxes per tile
+  static_assert(kWarps * H * (D + 2) * 4 <= S * 2 * TB, "merge area must fit in the stages");
+
+  extern __shared__ uint8_t smem_raw[];
+  const DecodeSmem sm = decode_smem<Path>(smem_raw);
+  __shared__ int cta_flag;
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  DecodeCta c;
+  bool any_bad = false;
+  if (!decode_prologue<Path>(p, sm, c, &any_bad, [&] {
+        cta_flag = 0;
+        prefetch_tensormap(&tmk);
+        prefetch_tensormap(&tmv);
+#pragma unroll
+        for (int s = 0; s < S; ++s) mbar_init(smem_addr(sm.bars + s), 1);
+      }))
+    return;
+
+  const float* ksrc = p.k_scale;
+  const float* vsrc = p.v_scale;
+  auto issue = [&](int j) {  // lane 0 of this warp: fetch the warp's j-th block
+    const int i = warp + j * kWarps;
+    const int stage = warp * kStagesPerWarp + (j % kStagesPerWarp);
+    const uint32_t bar = smem_addr(sm.bars + stage);
+    uint8_t* kdst = sm.stages + stage * 2 * TB;
+    uint8_t* vdst = kdst + TB;
+    const int y = (sm.tbl[i] * p.num_kv_heads + c.kvh) * kBlockSize;
+    mbar_arrive_expect_tx(bar, 2 * TB + SB);
+#pragma unroll
+    for (int x = 0; x < kBoxes; ++x) {
+      const int xe = x * (kBoxBytes / Path::kElemBytes);
+      tma_load_2d(smem_addr(kdst + x * 16 * kBoxBytes), &tmk, xe, y, bar);
+      tma_load_2d(smem_addr(vdst + x * 16 * kBoxBytes), &tmv, xe, y, bar);
+    }
+    if constexpr (SB > 0) {
+      float* sdst = sm.scales + stage * (SB / 4);
+      bulk_load(smem_addr(sdst), ksrc + y, 64, bar);
+      bulk_load(smem_addr(sdst + 16), vsrc + y, 64, bar);
+    }
+  };
+
+  typename Path::State st;
+  bool ok = !any_bad;
+  if (ok) {
+    Path::init(st, p, c.b, c.head0, c.nheads, lane);
+    const int my_blocks = c.nb > warp ? (c.nb - warp + kWarps - 1) / kWarps : 0;
+    const int prologue = my_blocks < kStagesPerWarp ? my_blocks : kStagesPerWarp;
+    if (lane == 0) {
+      for (int j = 0; j < prologue; ++j) issue(j);
+    }
+    int issued = prologue;
+    int j = 0;
+    for (; j < my_blocks; ++j) {
+      const int stage = warp * kStagesPerWarp + (j % kStagesPerWarp);
+      const bool landed =
+          mbar_wait_bounded(smem_addr(sm.bars + stage), (j / kStagesPerWarp) & 1);
+      if (!__all_sync(0xffffffffu, landed)) {
+        ok = false;
+        break;
+      }
+      const int i = warp + j * kWarps;
+      const int valid = (c.last_part && i == c.nb - 1) ? c.tail_valid : kBlockSize;
+      const uint8_t* kt = sm.stages + stage * 2 * TB;
+      Path::consume(st, kt, kt + TB, sm.scales + stage * (SB / 4), valid, lane, p.scale_log2);
+      __syncwarp();
+      if (j + kStagesPerWarp < my_blocks) {
+        if (lane == 0) {
+          fence_proxy_async_smem();
+          issue(j + kStagesPerWarp);
+        }
+        ++issued;
+      }
+    }
+    if (!ok) {
+      // A transfer did not land in time: wait (bounded) for this warp's copies
+      // still in flight so no TMA write outlives the CTA, then report.
+      if (lane == 0) {
+        for (int jj = j; jj < issued; ++jj) {
+          const int stage = warp * kStagesPerWarp + (jj % kStagesPerWarp);
+          mbar_wait_bounded(smem_addr(sm.bars + stage), (jj / kStagesPerWarp) & 1);
+        }
+        set_status(p.status, kErrTimeout);
+        atomicExch(&cta_flag, 1);
+      }
+    }
+  } else if (threadIdx.x == 0) {
+    set_status(p.status, kErrBadBlock);
+  }
+
+  launch_dependents();
+  __syncthreads();
+  decode_epilogue<Path>(p, sm, c, st, any_bad || cta_flag != 0);
+}
+
+// ---------------------------------------------------------------------------
+// Run-merged fetch ("ATB KV Cache management", "显存碎片问题": blocks are
+// allocated contiguously first, so most of a request's table is runs of
+// consecutive physical blocks).  The CTA streams its blocks in groups of
+// kWarps consecutive table entries (warp w still consumes blocks w, w+4, ...,
+// so the softmax and the merge are those of the per-block pipeline); a group
+// stage holds the group's K tiles back to back, then its V tiles.  Thread 0
+// issues each group as maximal runs of 4, 2 or 1 physically consecutive
+// blocks, one TMA box per run and tensor (5-D maps {row piece, 16 rows,
+// pieces per row, Hkv, NB} whose box holds r whole tiles in the per-block
+// layout), so a contiguous group costs 2 copies instead of 2 per block and
+// row piece.  Barriers per group stage: full (the copies landed) and empty
+// (all 4 warps consumed their tiles: kWarps arrivals).
+template <class Path>
+__global__ void __launch_bounds__(kWarps * 32)
+    decode_merged_kernel(const DecodeParams p, const __grid_constant__ RunMaps maps) {
+  using namespace dev;
+  constexpr int kGS = kStagesPerWarp;  // group stages
+  constexpr int TB = Path::kTileBytes;
+  constexpr int SB = Path::kScaleStageBytes;
+  constexpr int H = Path::kHeads;
+  constexpr int D = Path::kD;
+  constexpr int kGroupBytes = 2 * kWarps * TB;
+  static_assert(kWarps == 4, "runs are cut into boxes of 4, 2 and 1 blocks");
+  static_assert(kWarps * H * (D + 2) * 4 <= kGS * kGroupBytes, "merge area must fit");
+
+  extern __shared__ uint8_t smem_raw[];
+  const DecodeSmem sm = decode_smem<Path>(smem_raw);
+  uint64_t* full = sm.bars;          // [kGS]
+  uint64_t* empty = sm.bars + kGS;   // [kGS]
+  __shared__ int cta_flag;
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  DecodeCta c;
+  bool any_bad = false;
+  if (!decode_prologue<Path>(p, sm, c, &any_bad, [&] {
+        cta_flag = 0;
+#pragma unroll
+        for (int r = 0; r < 3; ++r) {
+          prefetch_tensormap(&maps.k[r]);
+          prefetch_tensormap(&maps.v[r]);
+        }
+#pragma unroll
+        for (int s = 0; s < kGS; ++s) {
+          mbar_init(smem_addr(full + s), 1);
+          mbar_init(smem_addr(empty + s), kWarps);
+        }
+      }))
+    return;
+
+  const int ngroups = (c.nb + kWarps - 1) / kWarps;
+  // thread 0: fetch group g into group stage g % kGS
+  auto issue_group = [&](int g) {
+    const int st = g % kGS;
+    const int i0 = g * kWarps;
+    const int nt = min(kWarps, c.nb - i0);
+    const uint32_t bar = smem_addr(full + st);
+    uint8_t* kbase = sm.stages + st * kGroupBytes;
+    uint8_t* vbase = kbase + kWarps * TB;
+    mbar_arrive_expect_tx(bar, static_cast<uint32_t>(nt * (2 * TB + SB)));
+    for (int w = 0; w < nt;) {
+      const int id = sm.tbl[i0 + w];
+      int run = 1;
+      while (w + run < nt && run < kWarps && sm.tbl[i0 + w + run] == id + run) ++run;
+      const int box = run >= 4 ? 2 : (run >= 2 ? 1 : 0);  // map index: 4, 2 or 1 blocks
+      tma_load_5d(smem_addr(kbase + w * TB), &maps.k[box], 0, 0, 0, c.kvh, id, bar);
+      tma_load_5d(smem_addr(vbase + w * TB), &maps.v[box], 0, 0, 0, c.kvh, id, bar);
+      w += 1 << box;
+    }
+    if constexpr (SB > 0) {
+      for (int w = 0; w < nt; ++w) {
+        const int y = (sm.tbl[i0 + w] * p.num_kv_heads + c.kvh) * kBlockSize;
+        float* sdst = sm.scales + (st * kWarps + w) * (SB / 4);
+        bulk_load(smem_addr(sdst), p.k_scale + y, 64, bar);
+        bulk_load(smem_addr(sdst + 16), p.v_scale + y, 64, bar);
+      }
+    }
+  };
+
+  typename Path::State st;
+  bool ok = !any_bad;
+  if (ok) {
+    Path::init(st, p, c.b, c.head0, c.nheads, lane);
+    const int prologue = min(ngroups, kGS);
+    if (threadIdx.x == 0) {
+      for (int g = 0; g < prologue; ++g) issue_group(g);
+    }
+    int issued = prologue;
+    int g = 0;
+    for (; g < ngroups; ++g) {
+      const int gs = g % kGS;
+      const int i = g * kWarps + warp;
+      if (i < c.nb) {
+        const bool landed = mbar_wait_bounded(smem_addr(full + gs), (g / kGS) & 1);
+        if (!__all_sync(0xffffffffu, landed)) {
+          ok = false;
+          break;
+        }
+        const int valid = (c.last_part && i == c.nb - 1) ? c.tail_valid : kBlockSize;
+        const uint8_t* kt = sm.stages + gs * kGroupBytes + warp * TB;
+        Path::consume(st, kt, kt + kWarps * TB, sm.scales + (gs * kWarps + warp) * (SB / 4),
+                      valid, lane, p.scale_log2);
+      }
+      __syncwarp();
+      if (lane == 0) {
+        fence_proxy_async_smem();
+        mbar_arrive(smem_addr(empty + gs));
+      }
+      if (g + kGS < ngroups) {
+        if (threadIdx.x == 0) {
+          // every warp has read its tile of group g: refill the stage
+          if (mbar_wait_bounded(smem_addr(empty + gs), (g / kGS) & 1)) {
+            issue_group(g + kGS);
+          } else {
+            ok = false;
+          }
+        }
+        ++issued;
+        if (!__all_sync(0xffffffffu, ok)) break;
+      }
+    }
+    if (!ok) {
+      // A wait timed out: thread 0 waits (bounded) for the copies it issued
+      // that may still be in flight, so no TMA write outlives the CTA.
+      if (threadIdx.x == 0) {
+        for (int gg = max(0, issued - kGS); gg < issued; ++gg)
+          mbar_wait_bounded(smem_addr(full + gg % kGS), (gg / kGS) & 1);
+      }
+      if (lane == 0) {
+        set_status(p.status, kErrTimeout);
+        atomicExch(&cta_flag, 1);
+      }
+    }
+  } else if (threadIdx.x == 0) {
+    set_status(p.status, kErrBadBlock);
+  }
+
+  launch_dependents();
+  __syncthreads();
+  decode_epilogue<Path>(p, sm, c, st, any_bad || cta_flag != 0);
+}
+
+template <class Path>
+cudaError_t launch_partial(const DecodeParams& p, const DecodeMaps& m, int grid_x,
+                           cudaStream_t s) {
   const size_t smem = decode_smem_for<Path>(p.part_blocks);
-  cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(&decode_partial_kernel<Path>),
-                                   decode_smem_for<Path>(kMaxPartBlocks));
-  if (e != cudaSuccess) return e;
   const dim3 grid(grid_x, p.num_kv_heads * p.qgroups, p.batch);
-  return launch_pdl(decode_partial_kernel<Path>, grid, dim3(kWarps * 32), smem, s, p, tk, tv);
+  if (m.merged) {
+    const cudaError_t e = ensure_smem_attr(
+        reinterpret_cast<const void*>(&decode_merged_kernel<Path>),
+        decode_smem_for<Path>(kMaxPartBlocks));
+    if (e != cudaSuccess) return e;
+    return launch_pdl(decode_merged_kernel<Path>, grid, dim3(kWarps * 32), smem, s, p, m.runs);
+  }
+  const cudaError_t e = ensure_smem_attr(
+      reinterpret_cast<const void*>(&decode_partial_kernel<Path>),
+      decode_smem_for<Path>(kMaxPartBlocks));
+  if (e != cudaSuccess) return e;
+  return launch_pdl(decode_partial_kernel<Path>, grid, dim3(kWarps * 32), smem, s, p, m.k, m.v);
 }
 
 }  // namespace kvp

@@ -3,12 +3,12 @@
 
 namespace kvp {
 
-cudaError_t launch_decode_mma(const DecodeParams& p, const CUtensorMap& tk,
-                              const CUtensorMap& tv, bool kv_bf16, int grid_x, cudaStream_t s) {
-  if (!kv_bf16 && p.head_dim == 64) return launch_partial<MmaPath<false, 64>>(p, tk, tv, grid_x, s);
-  if (!kv_bf16 && p.head_dim == 128) return launch_partial<MmaPath<false, 128>>(p, tk, tv, grid_x, s);
-  if (kv_bf16 && p.head_dim == 64) return launch_partial<MmaPath<true, 64>>(p, tk, tv, grid_x, s);
-  if (kv_bf16 && p.head_dim == 128) return launch_partial<MmaPath<true, 128>>(p, tk, tv, grid_x, s);
+cudaError_t launch_decode_mma(const DecodeParams& p, const DecodeMaps& m, bool kv_bf16,
+                              int grid_x, cudaStream_t s) {
+  if (!kv_bf16 && p.head_dim == 64) return launch_partial<MmaPath<false, 64>>(p, m, grid_x, s);
+  if (!kv_bf16 && p.head_dim == 128) return launch_partial<MmaPath<false, 128>>(p, m, grid_x, s);
+  if (kv_bf16 && p.head_dim == 64) return launch_partial<MmaPath<true, 64>>(p, m, grid_x, s);
+  if (kv_bf16 && p.head_dim == 128) return launch_partial<MmaPath<true, 128>>(p, m, grid_x, s);
   return cudaErrorInvalidValue;
 }
 

@@ -3,12 +3,11 @@
 
 namespace kvp {
 
-cudaError_t launch_decode_simt(const DecodeParams& p, const CUtensorMap& tk,
-                               const CUtensorMap& tv, bool kv_bf16, int grid_x,
-                               cudaStream_t s) {
+cudaError_t launch_decode_simt(const DecodeParams& p, const DecodeMaps& m, bool kv_bf16,
+                               int grid_x, cudaStream_t s) {
 #define KVP_SIMT_CASE(BF, DD, GG)                                              \
   if (kv_bf16 == BF && p.head_dim == DD && p.heads_per_cta == GG)              \
-    return launch_partial<SimtPath<BF, DD, GG>>(p, tk, tv, grid_x, s);
+    return launch_partial<SimtPath<BF, DD, GG>>(p, m, grid_x, s);
   KVP_SIMT_CASE(false, 64, 1)
   KVP_SIMT_CASE(false, 64, 2)
   KVP_SIMT_CASE(false, 128, 1)

@@ -76,21 +76,36 @@ struct PrefillParams {
   float scale_log2;              // scale * log2(e)
 };
 
+// Pool maps of the run-merged decode fetch: 5-D views {row piece (<= 128
+// bytes), 16 rows, pieces per row, Hkv, NB} of a pool whose boxes hold whole
+// (block, kv head) tiles of 1, 2 and 4 consecutive blocks (index 0, 1, 2).
+struct RunMaps {
+  CUtensorMap k[3];
+  CUtensorMap v[3];
+};
+
+// Tensor maps of a decode launch: per-block fetch (2-D views [NB * Hkv * 16
+// rows, D], a box of 16 rows x <= 128 bytes) or run-merged fetch.
+struct DecodeMaps {
+  bool merged;
+  CUtensorMap k, v;  // per-block fetch
+  RunMaps runs;      // run-merged fetch
+};
+
 // Device error codes (mirror kvp_status).
 constexpr int32_t kErrBadBlock = KVP_ERR_BAD_BLOCK;
 constexpr int32_t kErrTimeout = KVP_ERR_TIMEOUT;
 
 // Host launchers implemented in the kernel translation units.  Each returns a
 // cudaError_t from the launch.
-cudaError_t launch_decode_simt(const DecodeParams& p, const CUtensorMap& tk,
-                               const CUtensorMap& tv, bool kv_bf16, int grid_x,
-                               cudaStream_t s);
-cudaError_t launch_decode_mma(const DecodeParams& p, const CUtensorMap& tk,
-                              const CUtensorMap& tv, bool kv_bf16, int grid_x, cudaStream_t s);
-cudaError_t launch_decode_mma_int8(const DecodeParams& p, const CUtensorMap& tk,
-                                   const CUtensorMap& tv, int grid_x, cudaStream_t s);
-cudaError_t launch_decode_mma_fp8(const DecodeParams& p, const CUtensorMap& tk,
-                                  const CUtensorMap& tv, int grid_x, cudaStream_t s);
+cudaError_t launch_decode_simt(const DecodeParams& p, const DecodeMaps& m, bool kv_bf16,
+                               int grid_x, cudaStream_t s);
+cudaError_t launch_decode_mma(const DecodeParams& p, const DecodeMaps& m, bool kv_bf16,
+                              int grid_x, cudaStream_t s);
+cudaError_t launch_decode_mma_int8(const DecodeParams& p, const DecodeMaps& m, int grid_x,
+                                   cudaStream_t s);
+cudaError_t launch_decode_mma_fp8(const DecodeParams& p, const DecodeMaps& m, int grid_x,
+                                  cudaStream_t s);
 cudaError_t launch_decode_reduce(const DecodeParams& p, cudaStream_t s);
 // Self-test of the bounded wait: one block waits on a barrier nothing arrives
 // on, for at most limit_ns, and records kErrTimeout when it gives up.

@@ -92,6 +92,12 @@ def test_invalid_arguments_fail_before_any_launch(lib):
     assert lib.kvp_attention_decode(*args(7, 3, 0)) == kvp.KVP_ERR_INVALID_ARG
     assert lib.kvp_attention_decode(*args(8, 3, 0)) == kvp.KVP_ERR_INVALID_ARG
     assert lib.kvp_attention_decode(*args(8, 4, 0)) == kvp.KVP_ERR_INVALID_ARG
+    # the run-merge flag alone names no phase; with a phase it passes the phase check
+    merge = kvp.KVP_DECODE_MERGE_RUNS
+    assert lib.kvp_attention_decode(*args(8, merge, 0)) == kvp.KVP_ERR_INVALID_ARG
+    assert lib.kvp_attention_decode(*args(8, merge | 16, 0)) == kvp.KVP_ERR_INVALID_ARG
+    zero_merge = (P, P, P, P, P, 16, P, 0, 8, 0.125, _desc(), 0, 0, P, 0, 3 | merge, P, P)
+    assert lib.kvp_attention_decode(*zero_merge) == kvp.KVP_OK
     big = (P, P, P, P, P, 256, P, 4, 8, 0.125, _desc(), 0, 0, P, 0, 3, P, P)
     assert lib.kvp_attention_decode(*big) == kvp.KVP_ERR_INVALID_ARG  # needs workspace
     # batch 0 is a no-op

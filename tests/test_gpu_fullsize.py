@@ -46,9 +46,9 @@ def slot_rows(pool, slots):
     return pool[s // 16, :, s % 16]
 
 
-def run_step(name):
+def run_step(name, merge_runs=False):
     w = workloads.make(name, device="cpu")
-    step = bench.Step(w, kvp, torch.device("cuda"), 0, fused=True)
+    step = bench.Step(w, kvp, torch.device("cuda"), 0, fused=True, merge_runs=merge_runs)
     step.run()
     torch.cuda.synchronize()
     assert kvp.kvp_read_status(step.status) == kvp.KVP_OK
@@ -107,3 +107,13 @@ def test_8bit_workload_full_size(name):
     ref = oracle.attention_decode(w.q, okc, ovc, w.block_tables, w.context_lens, w.scale,
                                   k_scale=oks, v_scale=ovs)
     assert_close(step.out, ref, f"{name} full size, every row")
+
+
+def test_gqa70b_full_size_run_merged_fetch():
+    """The GQA workload's tables are 85% runs of consecutive blocks: the
+    run-merged fetch at full size, every row against the oracle."""
+    w, step = run_step("gqa70b", merge_runs=True)
+    okp = oracle.append(w.k_pool, w.new_k, w.slot_mapping)
+    ovp = oracle.append(w.v_pool, w.new_v, w.slot_mapping)
+    ref = oracle.attention_decode(w.q, okp, ovp, w.block_tables, w.context_lens, w.scale)
+    assert_close(step.out, ref, "gqa70b full size, run-merged fetch")

@@ -436,7 +436,14 @@ def fp8_workload(B, Hq, Hkv, D, lens, NB, q_dtype, seed, max_blocks=None):
             used[int(w.block_tables[b, i // 16]), i % 16] = True
     ks[~used[:, None, :].expand_as(ks)] = float("nan")
     vs[~used[:, None, :].expand_as(vs)] = float("nan")
-    return w, torch.from_numpy(kc), torch.from_numpy(vc), ks, vs
+    # unused slots hold E4M3 NaN codes (0x7f, 0xff): an over-read, or a V code
+    # of a token past the context reaching the product, turns the output NaN
+    kc, vc = torch.from_numpy(kc), torch.from_numpy(vc)
+    unused = (~used)[:, None, :, None].expand_as(kc)
+    nan_codes = torch.where(torch.arange(D) % 2 == 0, 0x7f, 0xff).to(torch.uint8)
+    kc[unused] = nan_codes.expand_as(kc)[unused]
+    vc[unused] = nan_codes.expand_as(vc)[unused]
+    return w, kc, vc, ks, vs
 
 
 @pytest.mark.parametrize("q_dtype", [torch.float16, torch.bfloat16])
@@ -491,3 +498,94 @@ def test_fused_append_decode_equals_separate_calls(dtype, Hq, Hkv, D, partition_
     okp, ovp = oracle_pools_16(w)
     ref = oracle.attention_decode(w.q, okp, ovp, w.block_tables, w.context_lens, w.scale)
     assert_attn_close(out, ref, f"fused {dtype} {Hq}/{Hkv} D{D} pb{partition_blocks}")
+
+
+# --------------------------------------------------------------- run-merged fetch
+MERGE_CASES = [  # (kind, dtype, D, Hq, Hkv): every consumer of the decode
+    ("16", torch.float16, 128, 4, 4),     # CUDA cores, one query head per kv head
+    ("16", torch.bfloat16, 64, 16, 8),    # CUDA cores, two heads
+    ("16", torch.bfloat16, 128, 16, 2),   # tensor cores, 8 heads
+    ("16", torch.float16, 64, 24, 2),     # tensor cores, 12 heads (two query groups)
+    ("int8", torch.float16, 128, 16, 2),
+    ("int8", torch.bfloat16, 64, 8, 1),
+    ("fp8", torch.float16, 128, 16, 2),
+    ("fp8", torch.bfloat16, 64, 6, 2),
+]
+
+
+@pytest.mark.parametrize("kind,dtype,D,Hq,Hkv", MERGE_CASES)
+@pytest.mark.parametrize("p_run", [0.0, 0.85, 1.0])
+@pytest.mark.parametrize("partition_blocks", [0, 6])
+def test_merged_run_fetch_equals_per_block_fetch(kind, dtype, D, Hq, Hkv, p_run,
+                                                 partition_blocks):
+    """KVP_DECODE_MERGE_RUNS fetches runs of up to 4 physically consecutive
+    blocks with one copy each; every warp still consumes the same blocks in the
+    same order, so the output must equal the per-block fetch bit for bit, and
+    the oracle within tolerance.  Tables are scattered (no runs), 85% runs,
+    and one run per request; lengths put partial groups and partial blocks at
+    the ends of partitions."""
+    lens = [1, 16, 17, 64, 65, 300, 530, 0, 611]
+    w = workloads.make_custom(B=len(lens), Hq=Hq, Hkv=Hkv, D=D, lens=lens, num_blocks=200,
+                              dtype=dtype, kv_int8=kind != "16", contiguous_p=p_run,
+                              seed=D + Hq + int(10 * p_run), max_blocks=48)
+    ws = workspace_for(w, partition_blocks)
+    outs = []
+    if kind == "16":
+        kp, vp = w.k_pool.cuda(), w.v_pool.cuda()
+        kvp.kvp_append(w.new_k.cuda(), w.new_v.cuda(), kp, vp, w.slot_mapping.cuda())
+        for flags in (0, kvp.KVP_DECODE_MERGE_RUNS):
+            out = torch.full_like(w.q, float("nan"), device="cuda")
+            status = torch.zeros(1, dtype=torch.int32, device="cuda")
+            kvp.kvp_attention_decode(out, w.q.cuda(), kp, vp, w.block_tables.cuda(),
+                                     w.context_lens.cuda(), w.scale, workspace=ws,
+                                     partition_blocks=partition_blocks,
+                                     phases=kvp.KVP_PHASE_ALL | flags, status=status)
+            assert kvp.kvp_read_status(status) == kvp.KVP_OK
+            outs.append(out)
+        okp, ovp = oracle_pools_16(w)
+        ref = oracle.attention_decode(w.q, okp, ovp, w.block_tables, w.context_lens, w.scale)
+    else:
+        fp8 = kind == "fp8"
+        quant = oracle.quantize_fp8 if fp8 else oracle.quantize_int8
+        kc, ks = quant(w.k_pool)
+        vc, vs = quant(w.v_pool)
+        kc, vc = torch.from_numpy(kc), torch.from_numpy(vc)
+        ks, vs = torch.from_numpy(ks), torch.from_numpy(vs)
+        decode = kvp.kvp_attention_decode_fp8 if fp8 else kvp.kvp_attention_decode_int8
+        gkc, gvc, gks, gvs = kc.cuda(), vc.cuda(), ks.cuda(), vs.cuda()
+        for flags in (0, kvp.KVP_DECODE_MERGE_RUNS):
+            out = torch.full_like(w.q, float("nan"), device="cuda")
+            status = torch.zeros(1, dtype=torch.int32, device="cuda")
+            decode(out, w.q.cuda(), gkc, gvc, gks, gvs, w.block_tables.cuda(),
+                   w.context_lens.cuda(), w.scale, workspace=ws,
+                   partition_blocks=partition_blocks, phases=kvp.KVP_PHASE_ALL | flags,
+                   status=status)
+            assert kvp.kvp_read_status(status) == kvp.KVP_OK
+            outs.append(out)
+        if fp8:
+            kc, vc = kc.view(torch.float8_e4m3fn), vc.view(torch.float8_e4m3fn)
+        ref = oracle.attention_decode(w.q, kc, vc, w.block_tables, w.context_lens, w.scale,
+                                      k_scale=ks, v_scale=vs)
+    torch.cuda.synchronize()
+    assert same_bits(outs[0], outs[1]), "run-merged fetch differs from per-block fetch"
+    assert_attn_close(outs[1], ref, f"merged {kind} {dtype} D{D} {Hq}/{Hkv} p{p_run}")
+    assert torch.count_nonzero(outs[1][7]) == 0  # context 0 -> zero row
+
+
+def test_merged_run_fetch_bad_block_id_sets_status():
+    w = workloads.make_custom(B=2, Hq=8, Hkv=2, D=128, lens=[300, 200], num_blocks=64,
+                              dtype=torch.float16, contiguous_p=1.0, seed=12)
+    kp, vp = w.k_pool.cuda(), w.v_pool.cuda()
+    kvp.kvp_append(w.new_k.cuda(), w.new_v.cuda(), kp, vp, w.slot_mapping.cuda())
+    okp, ovp = oracle_pools_16(w)
+    w.block_tables[1, 3] = 64  # out of range, inside a run (after the appends)
+    out = torch.full_like(w.q, float("nan"), device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    kvp.kvp_attention_decode(out, w.q.cuda(), kp, vp, w.block_tables.cuda(),
+                             w.context_lens.cuda(), w.scale,
+                             phases=kvp.KVP_PHASE_ALL | kvp.KVP_DECODE_MERGE_RUNS, status=status)
+    assert kvp.kvp_read_status(status) == kvp.KVP_ERR_BAD_BLOCK
+    assert torch.count_nonzero(out[1]) == 0
+    ref = oracle.attention_decode(w.q[:1], okp, ovp, w.block_tables[:1], w.context_lens[:1],
+                                  w.scale)
+    assert_attn_close(out[:1], ref, "merged fetch, request with good ids")
