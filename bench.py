@@ -660,8 +660,9 @@ class PrefillStep:
     slots (kvp_append), then causal multi-query attention
     (kvp_attention_prefill)."""
 
-    def __init__(self, w, kvp, dev):
+    def __init__(self, w, kvp, dev, shared_blocks=0):
         self.w, self.kvp = w, kvp
+        self.shared = shared_blocks  # > 0: dense tiles over the shared prefix
         self.q = w.q.to(dev)
         self.kp, self.vp = w.k_pool.to(dev), w.v_pool.to(dev)
         self.tables = w.block_tables.to(dev)
@@ -691,7 +692,8 @@ class PrefillStep:
         if ev is not None:
             ev[0].record()
         kvp.kvp_attention_prefill(self.out, self.q, self.kp, self.vp, self.tables, self.lens,
-                                  self.qs, w.max_query_len, w.scale, status=self.status)
+                                  self.qs, w.max_query_len, w.scale,
+                                  shared_prefix_blocks=self.shared, status=self.status)
         if ev is not None:
             ev[1].record()
 
@@ -730,7 +732,8 @@ def measure_prefill(name, args, kvp, world, dev, local, headline):
     events only), then time the prefill kernel in a separate pass."""
     w = workloads.make_prefill_named(name, device=dev, nan_sentinel=False,
                                      batch=args.batch if headline else None)
-    step = PrefillStep(w, kvp, dev)
+    shared = 0 if (headline and args.per_request_tiles) else w.info.get("shared_blocks", 0)
+    step = PrefillStep(w, kvp, dev, shared)
     flops, pairs = prefill_work(w)
     for _ in range(args.warmup):
         step.run()
@@ -755,6 +758,8 @@ def measure_prefill(name, args, kvp, world, dev, local, headline):
                    "batch": w.B, "q_heads": w.Hq, "kv_heads": w.Hkv, "head_dim": w.D,
                    "block_size": 16, "num_blocks": w.num_blocks, "query_tokens": w.T,
                    "prefix_tokens": w.info.get("prefix_tokens"),
+                   "tiles": (f"dense over all requests' rows ({shared} shared prefix blocks)"
+                             if shared else "per request"),
                    "context_tokens": int(w.context_lens.sum()),
                    "attended_pairs_per_head": pairs,
                    "l2": "K/V of the shared prefix is L2-resident across requests (prefix "
@@ -935,6 +940,9 @@ def main():
     ap.add_argument("--merge-runs", action="store_true",
                     help="decode with the run-merged fetch (one copy per run of up to 4 "
                          "physically consecutive blocks)")
+    ap.add_argument("--per-request-tiles", action="store_true",
+                    help="prefill: 128-row tiles per request (default for prefix_prefill: "
+                         "dense tiles over the shared prefix)")
     ap.add_argument("--cpu-rows-1core", type=int, default=128,
                     help="(request, head) rows the CPU oracle times on one core (0 = skip)")
     ap.add_argument("--no-extras", action="store_true",

@@ -310,6 +310,21 @@ kvp_status kvp_attention_decode_fp8(void* out, const void* q, kvp_dtype q_dtype,
  *                 the kv heads it sizes the list of 128-row work items
  *                 (ceil(max_query_len * G / 128) per request and kv head),
  *                 which must stay below 2^31 (KVP_ERR_UNSUPPORTED otherwise).
+ *   shared_prefix_blocks  S >= 0.  S > 0 states that the first S entries of
+ *                 every request's block table (of the requests with query
+ *                 rows) name the same physical blocks -- a prompt prefix
+ *                 cached once and shared ("Prefix Caching") -- and that each
+ *                 such request holds n >= 16 * S tokens.  The rows of all
+ *                 requests are then packed into 128-row tiles of consecutive
+ *                 query tokens (no tile is padded at a request's end) and the
+ *                 prefix's whole 128-key chunks are read through one table;
+ *                 each request's other keys through its own.  Results are
+ *                 those of S = 0, bit for bit.  A table that disagrees on the
+ *                 first S entries, or n < 16 * S, is a data error
+ *                 (KVP_ERR_BAD_BLOCK; the tiles holding that request's rows
+ *                 are written as zeros).  With S > 0 the work items are
+ *                 ceil(num_query_tokens * G / 128) per kv head and
+ *                 max_query_len is not used to size them.
  *   k/v cache, block_tables, max_blocks_per_seq, cache: as kvp_attention_decode.
  * num_q_heads / num_kv_heads must divide 128 (KVP_ERR_UNSUPPORTED otherwise).
  * Device-side errors (*dev_status): KVP_ERR_BAD_BLOCK when a block id is out of
@@ -327,8 +342,9 @@ kvp_status kvp_attention_prefill(void* out, const void* q, const void* k_cache,
                                  int32_t max_blocks_per_seq, const int32_t* context_lens,
                                  const int32_t* query_start, int32_t num_query_tokens,
                                  int32_t batch, int32_t num_q_heads, int32_t max_query_len,
-                                 float scale, kvp_cache_desc cache, kvp_dtype dtype,
-                                 int32_t* dev_status, kvp_stream_t stream);
+                                 int32_t shared_prefix_blocks, float scale,
+                                 kvp_cache_desc cache, kvp_dtype dtype, int32_t* dev_status,
+                                 kvp_stream_t stream);
 
 /*
  * kvp_attention_decode_noalloc -- kvp_attention_decode for callers that cannot

@@ -84,7 +84,7 @@ SIGNATURES = {
     "kvp_attention_decode_noalloc": (_I32, [_P, _P, _P, _P, _P, _I32, _P, _I32, _I32, _F, _D,
                                             _I32, _I32, _P, _P]),
     "kvp_attention_prefill": (_I32, [_P, _P, _P, _P, _P, _I32, _P, _P, _I32, _I32, _I32, _I32,
-                                     _F, _D, _I32, _P, _P]),
+                                     _I32, _F, _D, _I32, _P, _P]),
     "kvp_read_status": (_I32, [_P, _P]),
     "kvp_selftest_wait_timeout": (_I32, [_P, _I64, _P]),
     "kvp_bm_create": (_P, [_I32, _I32, _I64]),
@@ -351,10 +351,13 @@ def kvp_attention_decode_noalloc(out, q, k_cache, v_cache, block_tables, context
 
 
 def kvp_attention_prefill(out, q, k_cache, v_cache, block_tables, context_lens, query_start,
-                          max_query_len, scale, *, status=None, stream=None) -> None:
+                          max_query_len, scale, *, shared_prefix_blocks=0, status=None,
+                          stream=None) -> None:
     """out[T, Hq, D] = causal multi-query paged attention of q[T, Hq, D] over
     fp16/bf16 pools; request b's rows are q[query_start[b]:query_start[b+1]]
-    and sit at the last positions of its context_lens[b] cached tokens."""
+    and sit at the last positions of its context_lens[b] cached tokens.
+    shared_prefix_blocks > 0: the first that many table entries of every
+    request are the same physical blocks (packs all rows into dense tiles)."""
     lib = load_library()
     _need_cuda(out, q, k_cache, v_cache, block_tables, context_lens, query_start, status)
     if q.dtype != k_cache.dtype or out.dtype != q.dtype:
@@ -366,8 +369,8 @@ def kvp_attention_prefill(out, q, k_cache, v_cache, block_tables, context_lens, 
     _check(lib.kvp_attention_prefill(
         _ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
         int(block_tables.shape[1]), _ptr(context_lens), _ptr(query_start), T, B, Hq,
-        int(max_query_len), float(scale), cache_desc(k_cache), _dtype_code(q), _ptr(status),
-        _stream_ptr(stream)), "kvp_attention_prefill")
+        int(max_query_len), int(shared_prefix_blocks), float(scale), cache_desc(k_cache),
+        _dtype_code(q), _ptr(status), _stream_ptr(stream)), "kvp_attention_prefill")
 
 
 def kvp_selftest_wait_timeout(status, limit_ns, stream=None):

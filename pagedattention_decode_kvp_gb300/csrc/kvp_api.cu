@@ -505,14 +505,16 @@ kvp_status kvp_attention_prefill(void* out, const void* q, const void* k_cache,
                                  int32_t max_blocks_per_seq, const int32_t* context_lens,
                                  const int32_t* query_start, int32_t num_query_tokens,
                                  int32_t batch, int32_t num_q_heads, int32_t max_query_len,
-                                 float scale, kvp_cache_desc cache, kvp_dtype dtype,
-                                 int32_t* dev_status, kvp_stream_t stream) {
+                                 int32_t shared_prefix_blocks, float scale,
+                                 kvp_cache_desc cache, kvp_dtype dtype, int32_t* dev_status,
+                                 kvp_stream_t stream) {
   KVP_NVTX_RANGE("kvp_attention_prefill");
   const kvp_status st = check_desc(cache);
   if (st != KVP_OK) return st;
   if (dtype != KVP_F16 && dtype != KVP_BF16) return KVP_ERR_INVALID_ARG;
   if (batch < 0 || num_q_heads <= 0 || max_blocks_per_seq <= 0 || max_query_len < 0 ||
-      num_query_tokens < 0)
+      num_query_tokens < 0 || shared_prefix_blocks < 0 ||
+      shared_prefix_blocks > max_blocks_per_seq)
     return KVP_ERR_INVALID_ARG;
   if (num_q_heads % cache.num_kv_heads != 0) return KVP_ERR_INVALID_ARG;
   if (!std::isfinite(scale)) return KVP_ERR_INVALID_ARG;
@@ -523,8 +525,13 @@ kvp_status kvp_attention_prefill(void* out, const void* q, const void* k_cache,
     return KVP_ERR_INVALID_ARG;
   if (!aligned(out, 16) || !aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16))
     return KVP_ERR_INVALID_ARG;
-  const long long tiles = (static_cast<long long>(max_query_len) * group + 127) / 128;
-  if (tiles * batch * cache.num_kv_heads > 0x7fffffffll) return KVP_ERR_UNSUPPORTED;
+  // work items: per-request 128-row tiles, or (a shared prefix) dense tiles
+  // over the whole batch's query rows
+  const bool dense = shared_prefix_blocks > 0;
+  const long long tiles = dense ? (static_cast<long long>(num_query_tokens) * group + 127) / 128
+                                : (static_cast<long long>(max_query_len) * group + 127) / 128;
+  if (tiles * (dense ? 1 : batch) * cache.num_kv_heads > 0x7fffffffll)
+    return KVP_ERR_UNSUPPORTED;
 
   const int box_tokens = std::min(128 / group, static_cast<int>(num_query_tokens));
   CUtensorMap tq, tk, tv;
@@ -556,6 +563,8 @@ kvp_status kvp_attention_prefill(void* out, const void* q, const void* k_cache,
   p.num_tokens = num_query_tokens;
   p.q_box_tokens = box_tokens;
   p.scale_log2 = scale * 1.4426950408889634f;
+  p.shared_blocks = shared_prefix_blocks;
+  p.prefix_chunks = shared_prefix_blocks * kBlockSize / 128;
   return from_cuda(launch_prefill(p, tq, tk, tv, to, dtype == KVP_BF16, static_cast<int>(tiles),
                                   reinterpret_cast<cudaStream_t>(stream)));
 }

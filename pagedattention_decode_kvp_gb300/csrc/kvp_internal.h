@@ -74,6 +74,9 @@ struct PrefillParams {
   int32_t num_tokens;            // T, rows of q and out
   int32_t q_box_tokens;          // tokens per Q tile copy: min(128 / group, T)
   float scale_log2;              // scale * log2(e)
+  int32_t shared_blocks;         // > 0: leading table entries shared by all requests
+                                 // (dense tiles over the whole batch's rows)
+  int32_t prefix_chunks;         // full 128-key chunks inside the shared prefix
 };
 
 // Pool maps of the run-merged decode fetch: 5-D views {row piece (<= 128

@@ -35,6 +35,7 @@
 //   * At the end of a tile each row's four lanes add their sums and write the
 //     row.  TMEM, barriers and tensor maps are set up once per CTA.
 #include <algorithm>
+#include <climits>
 
 #include "kvp_device.cuh"
 #include "kvp_internal.h"
@@ -144,61 +145,170 @@ __device__ __forceinline__ bool named_bar_and(uint32_t id, uint32_t nthreads, bo
   return r != 0;
 }
 
-// One work item: tile x of request b's query chunk against kv head kvh.
+// One work item.  Per-request tiles (no shared prefix): tokens t0 ..
+// t0 + ntok - 1 of request b's query chunk against kv head kvh.  Dense tiles
+// (a prefix of shared_blocks blocks that every request's table names alike):
+// 128 / G consecutive query tokens of the whole batch -- possibly of several
+// requests, b .. r1 -- against kv head kvh.  t0 is a row of q / out.
 struct Tile {
-  int b, kvh, q0, qlen, n, t0, ntok, pos0, nkeys, nblk, nchunks;
-  bool lens_bad;   // lengths out of range: rows are zeroed, nothing is read
-  int32_t status;  // error to record for this item (0 = none)
+  int kvh;
+  int t0, ntok;     // first query token (global row) and tokens in the tile
+  int b, r1;        // first and last request with rows in the tile
+  int nchunks;      // 128-key chunks the tile streams
+  int pos0, nkeys;  // per-request tiles: first token's position; keys needed
+  bool lens_bad;    // lengths out of range: rows are zeroed, nothing is read
+  int32_t status;   // error to record for this item (0 = none)
 };
 
-// The request lengths a work item needs, loaded ahead of its turn.
+// The request lengths a per-request work item needs, loaded ahead of its turn.
 struct ItemLens {
   int q0, q1, n;
 };
 
-// Work item `id` of tiles_x * batch * num_kv_heads: the last query tiles of
-// every request first (they attend to the most keys), then the earlier ones.
-// (The launch keeps the number of items below 2^31, so item arithmetic is
-// 32-bit.)
+// Work item `id`.  Per-request tiles: of tiles_x * batch * num_kv_heads, the
+// last query tiles of every request first (they attend to the most keys),
+// then the earlier ones.  Dense tiles: tile x = id / num_kv_heads, so the kv
+// heads of a tile run side by side and a request's own K/V stays in L2 for
+// the tiles after it.  (The launch keeps the number of items below 2^31, so
+// item arithmetic is 32-bit.)
+template <bool kDense>
 __device__ __forceinline__ ItemLens load_lens(const PrefillParams& p, int id) {
+  if constexpr (kDense) return ItemLens{0, 0, 0};  // dense tiles load their own
   const int per_x = p.batch * p.num_kv_heads;
   const int b = (id % per_x) / p.num_kv_heads;
   return ItemLens{p.query_start[b], p.query_start[b + 1], p.context_lens[b]};
 }
 
-// Returns false when the item has no rows (the request's chunk is shorter).
+// The request whose query rows hold token t (query_start is non-decreasing,
+// query_start[0] = 0; empty requests are skipped): the last r with
+// query_start[r] <= t.  Returns batch when t lies past every request.
+__device__ __forceinline__ int request_of(const PrefillParams& p, int t) {
+  int lo = 0, hi = p.batch;  // answer in [lo, hi]
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (p.query_start[mid] <= t) lo = mid; else hi = mid - 1;
+  }
+  return lo;
+}
+
+// A run of consecutive chunks read through one request's table.  owner < 0:
+// the shared prefix (read through the tile's first request's table; every row
+// attends to it, causally); otherwise request `owner`, and only its rows
+// attend.  Chunks start at key `key` and cover keys below `end`.  Dense
+// tiles visit their requests' own segments after the prefix; the lengths of
+// the next request to visit are loaded one segment ahead (nq0, nq1, nn), so
+// no walk waits on a global load at a segment boundary.
+struct ChunkWalk {
+  int owner;
+  const int32_t* tbl;
+  int key, end;
+  int r;              // dense tiles: the next request to visit
+  int nq0, nq1, nn;   // ... and its query range and length, in flight
+};
+
+__device__ __forceinline__ void walk_prefetch(const PrefillParams& p, const Tile& t,
+                                              ChunkWalk& w) {
+  if (w.r <= t.r1) {
+    w.nq0 = p.query_start[w.r];
+    w.nq1 = p.query_start[w.r + 1];
+    w.nn = p.context_lens[w.r];
+  }
+}
+
+// (dense tiles) The walk starts with the shared prefix's chunks.
+__device__ __forceinline__ void walk_start(const PrefillParams& p, const Tile& t, ChunkWalk& w) {
+  w.tbl = p.block_tables + static_cast<size_t>(t.b) * p.max_blocks;
+  w.key = 0;
+  w.owner = -1;
+  w.end = p.prefix_chunks * kKeys;
+  w.r = t.b;
+  walk_prefetch(p, t, w);
+}
+
+// The next chunk of the walk: its segment's owner, table and end stay in w,
+// its first key is returned (-1: the tile has no more chunks).  A request's
+// own segment covers keys [128 * prefix_chunks, its last row's position + 1)
+// for the rows it has in the tile (none: skipped; all inside the shared
+// chunks: empty).
+__device__ __forceinline__ int walk_next(const PrefillParams& p, const Tile& t, ChunkWalk& w) {
+  while (w.key >= w.end) {
+    if (w.r > t.r1) return -1;
+    const int r = w.r++;
+    const int q0 = w.nq0, q1 = w.nq1, n = w.nn;
+    walk_prefetch(p, t, w);
+    const int first = max(q0, t.t0), last = min(q1, t.t0 + t.ntok) - 1;
+    if (last < first) continue;
+    w.owner = r;
+    w.tbl = p.block_tables + static_cast<size_t>(r) * p.max_blocks;
+    w.key = p.prefix_chunks * kKeys;
+    w.end = n - (q1 - q0) + (last - q0) + 1;  // the last row's position + 1
+  }
+  const int key = w.key;
+  w.key += kKeys;
+  return key;
+}
+
+// Returns false when the item has no rows.
+template <bool kDense>
 __device__ __forceinline__ bool decode_tile(const PrefillParams& p, int tiles_x, int id,
                                             const ItemLens& lens, Tile& t) {
-  const int per_x = p.batch * p.num_kv_heads;
-  const int x = tiles_x - 1 - id / per_x;
-  const int r = id % per_x;
-  t.b = r / p.num_kv_heads;
-  t.kvh = r % p.num_kv_heads;
+  const int tok_per_tile = kRows / p.group;
   t.status = 0;
   t.nchunks = 0;
   t.lens_bad = false;
-  t.q0 = lens.q0;
-  t.qlen = lens.q1 - lens.q0;
-  t.n = lens.n;
-  const int tok_per_tile = kRows / p.group;
-  t.t0 = x * tok_per_tile;
+  if constexpr (kDense) {
+    const int x = id / p.num_kv_heads;
+    t.kvh = id % p.num_kv_heads;
+    t.t0 = x * tok_per_tile;
+    const int rows_end = p.query_start[p.batch];  // tokens past it belong to no request
+    if (x == 0 && t.kvh == 0 && rows_end > p.num_tokens) t.status = kErrBadBlock;
+    if (rows_end > p.num_tokens || t.t0 >= rows_end) {  // rows outside q / out: touch nothing
+      t.ntok = 0;
+      return t.status != 0;
+    }
+    t.ntok = min(tok_per_tile, rows_end - t.t0);
+    t.b = request_of(p, t.t0);
+    t.r1 = request_of(p, t.t0 + t.ntok - 1);
+    // every request with rows here: lengths in range, the whole shared prefix cached
+    for (int r = t.b; r <= t.r1; ++r) {
+      const int q0 = p.query_start[r], q1 = p.query_start[r + 1], n = p.context_lens[r];
+      if (q1 <= q0) continue;
+      if (q1 - q0 > n || n > p.max_blocks * kBlockSize || n < p.shared_blocks * kBlockSize)
+        t.lens_bad = true;
+    }
+    if (t.lens_bad) {
+      t.status = kErrBadBlock;
+      return true;
+    }
+    ChunkWalk w;
+    walk_start(p, t, w);
+    while (walk_next(p, t, w) >= 0) ++t.nchunks;
+    return true;
+  }
+  const int per_x = p.batch * p.num_kv_heads;
+  const int x = tiles_x - 1 - id / per_x;
+  const int r = id % per_x;
+  t.b = t.r1 = r / p.num_kv_heads;
+  t.kvh = r % p.num_kv_heads;
+  const int q0 = lens.q0, qlen = lens.q1 - lens.q0, n = lens.n;
+  const int tt = x * tok_per_tile;  // first token within the request's chunk
   // rows past the launch's coverage (a chunk longer than its maximum length)
-  if (x == 0 && t.kvh == 0 && t.qlen > tiles_x * tok_per_tile) t.status = kErrBadBlock;
-  if (t.qlen <= 0 || t.t0 >= t.qlen) return t.status != 0;
-  if (t.q0 < 0 || t.q0 + t.qlen > p.num_tokens) {  // rows outside q / out: touch nothing
+  if (x == 0 && t.kvh == 0 && qlen > tiles_x * tok_per_tile) t.status = kErrBadBlock;
+  if (qlen <= 0 || tt >= qlen) return t.status != 0;
+  if (q0 < 0 || q0 + qlen > p.num_tokens) {  // rows outside q / out: touch nothing
     t.status = kErrBadBlock;
     t.ntok = 0;
     return true;
   }
-  t.ntok = min(tok_per_tile, t.qlen - t.t0);
-  if (t.qlen > t.n || t.n > p.max_blocks * kBlockSize) {
+  t.t0 = q0 + tt;
+  t.ntok = min(tok_per_tile, qlen - tt);
+  if (qlen > n || n > p.max_blocks * kBlockSize) {
     t.lens_bad = true;
     t.status = kErrBadBlock;
     return true;
   }
-  t.pos0 = t.n - t.qlen + t.t0;  // position of the tile's first query token
+  t.pos0 = n - qlen + tt;        // position of the tile's first query token
   t.nkeys = t.pos0 + t.ntok;     // keys needed: 0 .. nkeys - 1
-  t.nblk = (t.nkeys + kBlockSize - 1) / kBlockSize;
   t.nchunks = (t.nkeys + kKeys - 1) / kKeys;
   return true;
 }
@@ -211,8 +321,29 @@ __device__ __forceinline__ void zero_tile_rows(const PrefillParams& p, const Til
   uint16_t* out = static_cast<uint16_t*>(p.out);
   for (int idx = threadIdx.x; idx < t.ntok * G * D; idx += nthreads) {
     const int tk = idx / (G * D), g = (idx / D) % G, d = idx % D;
-    out[(static_cast<size_t>(t.q0 + t.t0 + tk) * p.num_q_heads + t.kvh * G + g) * D + d] = 0;
+    out[(static_cast<size_t>(t.t0 + tk) * p.num_q_heads + t.kvh * G + g) * D + d] = 0;
   }
+
+}
+
+// Row `row` of tile t ((token row / G, head row % G) of the tile's tokens):
+// whether it is one of the tile's tokens, its request, and its position.
+template <bool kDense>
+__device__ __forceinline__ void row_info(const PrefillParams& p, const Tile& t, int row,
+                                         bool& valid, int& req, int& pos) {
+  const int tk = row / p.group;
+  valid = tk < t.ntok;
+  if constexpr (!kDense) {
+    req = t.b;
+    pos = t.pos0 + tk;
+    return;
+  }
+  const int tok = t.t0 + min(tk, t.ntok - 1);
+  int r = t.b;
+  while (r < t.r1 && p.query_start[r + 1] <= tok) ++r;  // tiles span few requests
+  const int q0 = p.query_start[r], q1 = p.query_start[r + 1];
+  req = r;
+  pos = p.context_lens[r] - (q1 - q0) + (tok - q0);
 }
 
 // Warp roles: warps 0-7 run the softmax -- warp w serves query rows
@@ -241,7 +372,7 @@ __device__ __forceinline__ void zero_tile_rows(const PrefillParams& p, const Til
 // only when a row's max jumps) O.  With P over the scores, S(g) waits until
 // P V(g-2) has read the buffer.  The first P V of a tile overwrites O, which
 // the softmax warps have read out before they release that chunk's P.
-template <bool kBf16, int D>
+template <bool kBf16, int D, bool kDense>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmq,
                    const __grid_constant__ CUtensorMap tmk,
@@ -277,7 +408,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const bool mma_warp = warp == kMmaWarp;
   const bool producer = warp > kMmaWarp;
   const int G = p.group;
-  const int items = tiles_x * p.batch * p.num_kv_heads;  // < 2^31 (checked at launch)
+  // < 2^31 (checked at launch)
+  const int items = tiles_x * (kDense ? 1 : p.batch) * p.num_kv_heads;
 
   if (mma_warp && lane == 0) {
     prefetch_tensormap(&tmq);
@@ -337,7 +469,6 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   // ---- producers: one work item (the whole warp; one lane issues the copies)
   auto produce_item = [&](const Tile& t) {
-    const int32_t* tbl = p.block_tables + static_cast<size_t>(t.b) * p.max_blocks;
     auto take = [&](uint32_t c) {  // wait until slot c's stage is free
       if (c >= static_cast<uint32_t>(nst))
         ok &= mbar_wait_bounded(smem_addr(empty + c % nst), ((c / nst) - 1) & 1);
@@ -356,20 +487,39 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int hf = 0; hf < L::kHalves; ++hf)
           tma_load_3d(ring + st * L::kKV + hf * (kRows * 128), &tmq, hf * 64, t.kvh * G,
-                      t.q0 + t.t0, bar);
+                      t.t0, bar);
       }
       __syncwarp();
       ++slot;
     }
-    for (int c = 0; c < t.nchunks; ++c, ++slot) {
-      const int blk0 = c * (kKeys / kBlockSize);
-      const int nb = min(kKeys / kBlockSize, t.nblk - blk0);
+    // the tile's chunks: per-request tiles read keys 0 .. nkeys - 1 of request
+    // b; dense tiles walk their segments
+    ChunkWalk cw;
+    if constexpr (kDense) {
+      walk_start(p, t, cw);
+    } else {
+      cw.tbl = p.block_tables + static_cast<size_t>(t.b) * p.max_blocks;
+      cw.key = 0;
+      cw.end = t.nkeys;
+    }
+    auto next_key = [&]() {
+      if constexpr (kDense) {
+        return walk_next(p, t, cw);
+      } else {
+        const int key = cw.key < cw.end ? cw.key : -1;
+        cw.key += kKeys;
+        return key;
+      }
+    };
+    for (int key = next_key(); key >= 0; key = next_key(), ++slot) {
+      const int blk0 = key / kBlockSize;
+      const int nb = (min(key + kKeys, cw.end) - key + kBlockSize - 1) / kBlockSize;
       // block ids of the chunk (lane i holds block blk0 + i); an id out of
       // range is replaced by block 0 -- the tile is flagged and its rows
       // zeroed by the softmax warps -- so no copy ever leaves the pool
       int my_id = 0;
       if (lane < nb) {
-        my_id = tbl[blk0 + lane];
+        my_id = cw.tbl[blk0 + lane];
         if (my_id < 0 || my_id >= p.num_blocks) my_id = 0;
       }
       if (!take(slot)) return;
@@ -491,18 +641,53 @@ __global__ void __launch_bounds__(kThreads, 1)
       return;
     }
     const int n = t.nchunks;
-    // block ids the tile reads, range-checked at its end (loads in flight
-    // meanwhile); ids past the first 128 blocks are checked there directly
-    const int32_t* tbl = p.block_tables + static_cast<size_t>(t.b) * p.max_blocks;
-    int bid_pre[4];
+    // this thread's two rows: valid (a token of the tile), request, position
+    bool va, vb;
+    int qa, qb, qpa, qpb;
+    row_info<kDense>(p, t, ra, va, qa, qpa);
+    row_info<kDense>(p, t, rb, vb, qb, qpb);
+    bool bad = false;
+    // per-request tiles: the block ids the tile reads, loaded now and range-
+    // checked at its end (ids past the first 128 are checked there directly)
+    int bid_pre[4] = {0, 0, 0, 0};
+    if constexpr (!kDense) {
+      const int32_t* tbl = p.block_tables + static_cast<size_t>(t.b) * p.max_blocks;
+      const int nblk = (t.nkeys + kBlockSize - 1) / kBlockSize;
 #pragma unroll
-    for (int u = 0; u < 4; ++u) bid_pre[u] = lane + 32 * u < t.nblk ? tbl[lane + 32 * u] : 0;
-    const bool va = ra / G < t.ntok, vb = rb / G < t.ntok;
-    const int qpa = t.pos0 + ra / G, qpb = t.pos0 + rb / G;
+      for (int u = 0; u < 4; ++u) bid_pre[u] = lane + 32 * u < nblk ? tbl[lane + 32 * u] : 0;
+    }
+    // dense tiles: every request with rows here must name the shared prefix's
+    // blocks as the first one does (each warp checks for itself); and this
+    // warp's valid rows are reduced once per tile so that every chunk's mask
+    // decision is warp-uniform: the smallest position, and the range of
+    // requests (a chunk of request R needs masks unless all rows are R's and
+    // lie at or past its last key)
+    int wq = INT_MAX, wr0 = INT_MAX, wr1 = -1;
+    if constexpr (kDense) {
+      if (t.r1 > t.b) {
+        const int32_t* t0 = p.block_tables + static_cast<size_t>(t.b) * p.max_blocks;
+        for (int k = lane; k < (t.r1 - t.b) * p.shared_blocks; k += 32) {
+          const int r = t.b + 1 + k / p.shared_blocks, i = k % p.shared_blocks;
+          if (p.query_start[r + 1] > p.query_start[r])
+            bad |= p.block_tables[static_cast<size_t>(r) * p.max_blocks + i] != t0[i];
+        }
+      }
+      if (va) { wq = qpa; wr0 = qa; wr1 = qa; }
+      if (vb) { wq = min(wq, qpb); wr0 = min(wr0, qb); wr1 = max(wr1, qb); }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        wq = min(wq, __shfl_xor_sync(0xffffffffu, wq, o));
+        wr0 = min(wr0, __shfl_xor_sync(0xffffffffu, wr0, o));
+        wr1 = max(wr1, __shfl_xor_sync(0xffffffffu, wr1, o));
+      }
+    }
     float ma = -INFINITY, mb = -INFINITY;  // running row maxima
     uint64_t la2 = 0, lb2 = 0;             // partial row sums, two per row (packed; fp16)
     float la = 0.f, lb = 0.f;              // partial row sums (bf16)
-    for (int j = 0; j < n && ok; ++j) {
+    // one chunk: chunk j of the tile, keys ck .. ck + 127 of which the first
+    // ckeys are read; `mask`: some row needs masks, then row a (b) keeps the
+    // keys <= qea (qeb) -- its position, or -1 where it attends to none
+    auto chunk = [&](int j, int ck, int ckeys, bool mask, int qea, int qeb) {
       const uint32_t g = gc + j;
       ok &= mbar_wait_bounded(smem_addr(s_bar + g % kSBufs), (g / kSBufs) & 1);
       umma::fence_after_sync();
@@ -516,19 +701,22 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int hc = 0; hc < 2; ++hc)
 #pragma unroll
         for (int i = 0; i < 32; ++i) s[hc][i] = __uint_as_float(raw[hc][i]);
-      // register 4k + 2r + e of half hc: row (r ? rb : ra), key 128j + 64hc + 8k + c2 + e
-      if (j * kKeys + kKeys - 1 > t.pos0) {  // chunk reaches past some row's position
+      // register 4k + 2r + e of half hc: row (r ? rb : ra), key ck + 64hc + 8k + c2 + e.
+      // A row attends to the chunk's keys at or before its position, and only
+      // to the shared prefix's or its own request's keys.  (Rows past the
+      // tile's tokens are never written; their scores need no mask.)
+      if (mask) {
 #pragma unroll
         for (int hc = 0; hc < 2; ++hc)
 #pragma unroll
           for (int k = 0; k < 8; ++k)
 #pragma unroll
             for (int e = 0; e < 2; ++e) {
-              const int key = j * kKeys + hc * 64 + 8 * k + c2 + e;
+              const int key = ck + hc * 64 + 8 * k + c2 + e;
               float& sa = s[hc][4 * k + e];
               float& sb = s[hc][4 * k + 2 + e];
-              sa = (va && key <= qpa) ? sa : -INFINITY;
-              sb = (vb && key <= qpb) ? sb : -INFINITY;
+              sa = key <= qea ? sa : -INFINITY;
+              sb = key <= qeb ? sb : -INFINITY;
             }
       }
       if (!pos_scale) {
@@ -645,14 +833,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       umma::wait_st();
-      if (j == n - 1 && t.nkeys - j * kKeys < kKeys) {
-        // V rows of keys >= nkeys are never attended (P = 0) but may hold
-        // non-finite bytes (slots past the context, blocks not loaded): clear
-        // them once the chunk's copies have landed
+      if (ckeys < kKeys) {
+        // V rows of keys past the segment are never attended (P = 0) but may
+        // hold non-finite bytes (slots past the context, blocks not loaded):
+        // clear them once the chunk's copies have landed
         const uint32_t v = vc + j;
         ok &= mbar_wait_bounded(smem_addr(vf_bar + v % kVStages), (v / kVStages) & 1);
         uint8_t* sV = sm + L::kVOff + (v % kVStages) * L::kKV;
-        const int first = t.nkeys - j * kKeys;
+        const int first = ckeys;
         for (int idx = tid; idx < (kKeys - first) * L::kHalves * 8; idx += kSoftmaxThreads) {
           const int r = first + idx / (L::kHalves * 8);
           const int rem = idx % (L::kHalves * 8);
@@ -664,20 +852,55 @@ __global__ void __launch_bounds__(kThreads, 1)
       umma::fence_before_sync();
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_addr(p_bar + g % kSBufs));
-    }
-    // ---- out = O / l.  Range-check every block id the tile read (each warp
-    // for itself): a tile that met an out-of-range id writes zeros.  Every
-    // softmax warp gets here, even after a failed wait, so that the named
-    // barriers below always complete; the first one also agrees on whether
-    // all waits succeeded.
-    bool bad = false;
+    };
+    if constexpr (kDense) {
+      // segments (outer) and their chunks (inner)
+      ChunkWalk cw;
+      walk_start(p, t, cw);
+      int j = 0;
+      while (j < n && ok) {
+        const int ck0 = walk_next(p, t, cw);
+        const int owner = cw.owner, end = cw.end;
+        cw.key = end;  // this segment is taken whole
+        const bool mixed = owner >= 0 && wr1 >= 0 && (wr0 != owner || wr1 != owner);
+        const int qea = (owner < 0 || qa == owner) ? qpa : -1;
+        const int qeb = (owner < 0 || qb == owner) ? qpb : -1;
+        for (int ck = ck0; ck < end && j < n && ok; ck += kKeys, ++j)
+          chunk(j, ck, min(kKeys, end - ck), mixed || ck + kKeys - 1 > wq, qea, qeb);
+      }
+      // every block id the tile read, range-checked segment by segment
+      walk_start(p, t, cw);
+      int k;
+      while ((k = walk_next(p, t, cw)) >= 0) {
+        const int b0 = k / kBlockSize, b1 = (cw.end + kBlockSize - 1) / kBlockSize;
+        for (int i = b0 + lane; i < b1; i += 32) {
+          const int id = cw.tbl[i];
+          bad |= (id < 0) || (id >= p.num_blocks);
+        }
+        cw.key = cw.end;  // the rest of this segment is covered
+      }
+    } else {
+      // one request: chunk j holds keys 128 j ..; a chunk needs masks once it
+      // reaches past the tile's first position (rows past the tile's tokens
+      // are never written and need none)
+      for (int j = 0; j < n && ok; ++j)
+        chunk(j, j * kKeys, min(kKeys, t.nkeys - j * kKeys), j * kKeys + kKeys - 1 > t.pos0,
+              va ? qpa : -1, vb ? qpb : -1);
+      const int32_t* tbl = p.block_tables + static_cast<size_t>(t.b) * p.max_blocks;
+      const int nblk = (t.nkeys + kBlockSize - 1) / kBlockSize;
 #pragma unroll
-    for (int u = 0; u < 4; ++u)
-      bad |= lane + 32 * u < t.nblk && (bid_pre[u] < 0 || bid_pre[u] >= p.num_blocks);
-    for (int i = lane + 128; i < t.nblk; i += 32) {
-      const int bid = tbl[i];
-      bad |= (bid < 0) || (bid >= p.num_blocks);
+      for (int u = 0; u < 4; ++u)
+        bad |= lane + 32 * u < nblk && (bid_pre[u] < 0 || bid_pre[u] >= p.num_blocks);
+      for (int i = lane + 128; i < nblk; i += 32) {
+        const int bid = tbl[i];
+        bad |= (bid < 0) || (bid >= p.num_blocks);
+      }
     }
+    // ---- out = O / l.  A tile that met an out-of-range block id (each warp
+    // checked every chunk's ids, and the shared prefix's, for itself) writes
+    // zeros.  Every softmax warp gets here, even after a failed wait, so that
+    // the named barriers below always complete; the first one also agrees on
+    // whether all waits succeeded.
     const uint32_t gl = gc + n - 1;
     if (ok) ok = mbar_wait_bounded(smem_addr(pv_bar + (gl & 1)), (gl >> 1) & 1);
     umma::fence_after_sync();
@@ -738,7 +961,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int hf = 0; hf < L::kHalves; ++hf)
             tma_store_3d(&tmo, smem_addr(stg + hf * (kRows * 128)), hf * 64, t.kvh * G,
-                         t.q0 + t.t0);
+                         t.t0);
           bulk_commit();
         }
       } else {
@@ -754,7 +977,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint4 v = *reinterpret_cast<const uint4*>(stg + (ch >> 3) * (kRows * 128) +
                                                           sw_chunk(r, ch));
           uint16_t* orow = static_cast<uint16_t*>(p.out) +
-                           (static_cast<size_t>(t.q0 + t.t0 + r / G) * p.num_q_heads +
+                           (static_cast<size_t>(t.t0 + r / G) * p.num_q_heads +
                             t.kvh * G + r % G) * D;
           *reinterpret_cast<uint4*>(orow + ch * 8) = v;
         }
@@ -777,7 +1000,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (k < ncand) {
         Tile t;
         const int id = static_cast<int>(blockIdx.x) + k * static_cast<int>(gridDim.x);
-        has = decode_tile(p, tiles_x, id, load_lens(p, id), t);
+        has = decode_tile<kDense>(p, tiles_x, id, load_lens<kDense>(p, id), t);
       }
       const uint32_t bits = __ballot_sync(0xffffffffu, has);
       if (lane == 0) mask[warp] = bits;
@@ -796,13 +1019,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       return static_cast<int>(blockIdx.x) + (w0 + k) * static_cast<int>(gridDim.x);
     };
     int k = next_item(-1);
-    ItemLens lens = k >= 0 ? load_lens(p, id_of(k)) : ItemLens{0, 0, 0};
+    ItemLens lens = k >= 0 ? load_lens<kDense>(p, id_of(k)) : ItemLens{0, 0, 0};
     while (k >= 0) {
       const int kn = next_item(k);
       const ItemLens cur = lens;
-      if (kn >= 0) lens = load_lens(p, id_of(kn));  // in flight meanwhile
+      if (kn >= 0) lens = load_lens<kDense>(p, id_of(kn));  // in flight meanwhile
       Tile t;
-      decode_tile(p, tiles_x, id_of(k), cur, t);
+      decode_tile<kDense>(p, tiles_x, id_of(k), cur, t);
       if (ok) {
         if (producer) {
           if (t.nchunks > 0) produce_item(t);
@@ -849,19 +1072,21 @@ int sm_count() {
   return n;
 }
 
-template <bool kBf16, int D>
+template <bool kBf16, int D, bool kDense>
 cudaError_t launch_prefill_t(const PrefillParams& p, const CUtensorMap& tq, const CUtensorMap& tk,
                              const CUtensorMap& tv, const CUtensorMap& to, int tiles_x,
                              cudaStream_t s) {
   constexpr size_t smem = PrefillLayout<kBf16, D>::kSmem;
-  cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(&prefill_kernel<kBf16, D>), smem);
+  cudaError_t e = ensure_smem_attr(
+      reinterpret_cast<const void*>(&prefill_kernel<kBf16, D, kDense>), smem);
   if (e != cudaSuccess) return e;
   // one CTA per SM walks the work items (shared memory keeps it to one)
-  const long long items = static_cast<long long>(tiles_x) * p.batch * p.num_kv_heads;
+  const long long items = static_cast<long long>(tiles_x) * (kDense ? 1 : p.batch) *
+                          p.num_kv_heads;
   if (items >= (1ll << 31)) return cudaErrorInvalidValue;  // item arithmetic is 32-bit
   const int grid = static_cast<int>(std::min<long long>(items, sm_count()));
-  return launch_pdl(prefill_kernel<kBf16, D>, dim3(grid), dim3(kThreads), smem, s, p, tq, tk, tv,
-                    to, tiles_x);
+  return launch_pdl(prefill_kernel<kBf16, D, kDense>, dim3(grid), dim3(kThreads), smem, s, p, tq,
+                    tk, tv, to, tiles_x);
 }
 
 }  // namespace
@@ -869,10 +1094,16 @@ cudaError_t launch_prefill_t(const PrefillParams& p, const CUtensorMap& tq, cons
 cudaError_t launch_prefill(const PrefillParams& p, const CUtensorMap& tq, const CUtensorMap& tk,
                            const CUtensorMap& tv, const CUtensorMap& to, bool bf16, int grid_x,
                            cudaStream_t s) {
-  if (!bf16 && p.head_dim == 64) return launch_prefill_t<false, 64>(p, tq, tk, tv, to, grid_x, s);
-  if (!bf16 && p.head_dim == 128) return launch_prefill_t<false, 128>(p, tq, tk, tv, to, grid_x, s);
-  if (bf16 && p.head_dim == 64) return launch_prefill_t<true, 64>(p, tq, tk, tv, to, grid_x, s);
-  if (bf16 && p.head_dim == 128) return launch_prefill_t<true, 128>(p, tq, tk, tv, to, grid_x, s);
+  const bool dense = p.shared_blocks > 0;
+#define KVP_PREFILL_CASE(BF, DD)                                                    \
+  if (bf16 == BF && p.head_dim == DD)                                              \
+    return dense ? launch_prefill_t<BF, DD, true>(p, tq, tk, tv, to, grid_x, s)    \
+                 : launch_prefill_t<BF, DD, false>(p, tq, tk, tv, to, grid_x, s);
+  KVP_PREFILL_CASE(false, 64)
+  KVP_PREFILL_CASE(false, 128)
+  KVP_PREFILL_CASE(true, 64)
+  KVP_PREFILL_CASE(true, 128)
+#undef KVP_PREFILL_CASE
   return cudaErrorInvalidValue;
 }
 

@@ -128,10 +128,10 @@ def test_prefill_invalid_arguments_fail_before_any_launch(lib):
     P = None
     inf = float("inf")
 
-    def call(hq=8, d=None, T=64, batch=2, mql=32, scale=0.125, dtype=0):
+    def call(hq=8, d=None, T=64, batch=2, mql=32, scale=0.125, dtype=0, shared=0):
         desc = _desc() if d is None else d
-        return lib.kvp_attention_prefill(P, P, P, P, P, 16, P, P, T, batch, hq, mql, scale, desc,
-                                         dtype, P, P)
+        return lib.kvp_attention_prefill(P, P, P, P, P, 16, P, P, T, batch, hq, mql, shared,
+                                         scale, desc, dtype, P, P)
     # group (Hq / Hkv) must divide the 128-row tile; Hq must be a multiple of Hkv
     assert call(hq=_desc().num_kv_heads * 3) == kvp.KVP_ERR_UNSUPPORTED
     assert call(hq=_desc().num_kv_heads + 1) == kvp.KVP_ERR_INVALID_ARG
@@ -142,6 +142,10 @@ def test_prefill_invalid_arguments_fail_before_any_launch(lib):
     assert call(scale=inf) == kvp.KVP_ERR_INVALID_ARG
     assert call(T=-1) == kvp.KVP_ERR_INVALID_ARG
     assert call(mql=-1) == kvp.KVP_ERR_INVALID_ARG
+    # the shared prefix is a count of table entries: 0 .. max_blocks_per_seq
+    assert call(shared=-1) == kvp.KVP_ERR_INVALID_ARG
+    assert call(shared=17) == kvp.KVP_ERR_INVALID_ARG
+    assert call(shared=16, batch=0) == kvp.KVP_OK
     # null buffers with work to do
     assert call() == kvp.KVP_ERR_INVALID_ARG
     # nothing to do: no-ops even with null buffers
@@ -150,7 +154,12 @@ def test_prefill_invalid_arguments_fail_before_any_launch(lib):
     # (fake, aligned, never dereferenced buffer addresses)
     A = ctypes.c_void_p(1 << 20)
     big = lib.kvp_attention_prefill(A, A, A, A, A, 16, A, A, 64, 65535, _desc().num_kv_heads,
-                                    0x7fffffff, 0.125, _desc(), 0, A, P)
+                                    0x7fffffff, 0, 0.125, _desc(), 0, A, P)
+    assert big == kvp.KVP_ERR_UNSUPPORTED
+    # dense tiles are counted from the query rows: 2^31 - 1 tokens of 128-head
+    # groups are 2^31 - 1 tiles for each of 8 kv heads
+    big = lib.kvp_attention_prefill(A, A, A, A, A, 16, A, A, 0x7fffffff, 4, 8 * 128, 16, 1,
+                                    0.125, _desc(hkv=8), 0, A, P)
     assert big == kvp.KVP_ERR_UNSUPPORTED
     assert call(mql=0) == kvp.KVP_OK
     assert call(T=0) == kvp.KVP_OK

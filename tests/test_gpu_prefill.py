@@ -8,7 +8,9 @@ Cases span several 128-row query tiles and 128-key chunks with ragged tails
 (full tiles leave through a TMA store, partial ones through plain stores), a
 whole-prompt prefill, chunks that start mid-context, single-token chunks, empty
 chunks, NaN in every pool slot no request owns, a sparse work list longer than
-one scan window per block, and the data errors the header documents."""
+one scan window per block, and the data errors the header documents.  With a
+shared prompt prefix the rows of all requests are packed into dense tiles; that
+mode must equal the per-request tiles bit for bit."""
 import numpy as np
 import pytest
 import torch
@@ -40,7 +42,7 @@ def assert_close(gpu_out, ref, what=""):
                              f"{i}: gpu {g[i]} ref {ref[i]} (max abs err {err.max():.3e})")
 
 
-def run_gpu(w, status=None, max_query_len=None, out=None, q=None):
+def run_gpu(w, status=None, max_query_len=None, out=None, q=None, shared=0):
     if out is None:
         out = torch.full((w.T, w.Hq, w.D), float("nan"), dtype=w.dtype, device="cuda")
     kvp.kvp_attention_prefill(out, (w.q if q is None else q).cuda(), w.k_pool.cuda(),
@@ -48,7 +50,7 @@ def run_gpu(w, status=None, max_query_len=None, out=None, q=None):
                               w.block_tables.cuda(), w.context_lens.cuda(),
                               w.query_start.cuda(),
                               w.max_query_len if max_query_len is None else max_query_len,
-                              w.scale, status=status)
+                              w.scale, shared_prefix_blocks=shared, status=status)
     torch.cuda.synchronize()
     return out
 
@@ -269,3 +271,89 @@ def test_sparse_work_list_spans_several_windows():
                                    w.query_start, w.scale, rows=rows)
     got = out.cpu()[torch.tensor(t).long(), torch.tensor(h).long()]
     assert_close(got, ref, "sparse work list")
+
+
+# --------------------------------------------------------------- shared prefix (dense tiles)
+def _same_bits(a, b):
+    return torch.equal(a.cpu().view(torch.int16), b.cpu().view(torch.int16))
+
+
+SHARED_CASES = [  # (context length, chunk length) with a 16-block (256-token) shared prefix
+    [(300, 40), (1100, 200), (260, 4), (520, 130), (256, 0), (700, 1), (1000, 300)],
+    # chunks that start inside the shared prefix (causal masking on shared chunks)
+    [(300, 100), (257, 257), (400, 150), (290, 64)],
+]
+
+
+@pytest.mark.parametrize("dtype", [torch.float16, torch.bfloat16])
+@pytest.mark.parametrize("Hq,Hkv,D", [(8, 8, 128), (16, 4, 64), (32, 4, 128), (8, 1, 64)])
+@pytest.mark.parametrize("case", [0, 1])
+def test_shared_prefix_dense_tiles_equal_per_request_tiles(dtype, Hq, Hkv, D, case):
+    """Dense tiles (rows of several requests in one 128-row tile, the shared
+    prefix's chunks read once per tile) against per-request tiles, bit for
+    bit, and against the oracle."""
+    lens = [n for n, _ in SHARED_CASES[case]]
+    qlens = [q for _, q in SHARED_CASES[case]]
+    w = workloads.make_prefill(B=len(lens), Hq=Hq, Hkv=Hkv, D=D, lens=lens, qlens=qlens,
+                               num_blocks=260, dtype=dtype, shared_blocks=16,
+                               seed=D + Hq + case, contiguous_p=0.5)
+    per_request = run_gpu(w)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    dense = run_gpu(w, status=status, shared=16)
+    assert kvp.kvp_read_status(status) == kvp.KVP_OK
+    assert _same_bits(dense, per_request), "dense tiles differ from per-request tiles"
+    ref = oracle.attention_prefill(w.q, w.k_pool, w.v_pool, w.block_tables, w.context_lens,
+                                   w.query_start, w.scale)
+    assert_close(dense, ref, f"dense {dtype} {Hq}/{Hkv} D{D} case {case}")
+
+
+def test_shared_prefix_disagreeing_table_sets_status_and_zeroes_its_tiles():
+    lens, qlens = [300, 400, 280, 350], [60, 300, 50, 90]
+    w = workloads.make_prefill(B=4, Hq=8, Hkv=2, D=64, lens=lens, qlens=qlens, num_blocks=120,
+                               dtype=torch.float16, shared_blocks=12, seed=4)
+    # request 2 names one of its private blocks inside the shared prefix
+    w.block_tables[2, 5] = int(w.block_tables[2, 17])
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out = run_gpu(w, status=status, shared=12)
+    assert kvp.kvp_read_status(status) == kvp.KVP_ERR_BAD_BLOCK
+    qs = w.query_start.tolist()
+    assert torch.count_nonzero(out[qs[2]:qs[3]].float()) == 0  # request 2's rows
+    # request 0 shares no 128-row tile with request 2 (G = 4: 32 tokens a tile)
+    ref = oracle.attention_prefill(w.q, w.k_pool, w.v_pool, w.block_tables, w.context_lens,
+                                   w.query_start, w.scale)
+    assert_close(out[:qs[1]], ref[:qs[1]], "rows of a request in good tiles")
+
+
+def test_shared_prefix_longer_than_a_context_sets_status():
+    w = workloads.make_prefill(B=2, Hq=8, Hkv=2, D=64, lens=[300, 260], qlens=[30, 20],
+                               num_blocks=60, dtype=torch.float16, shared_blocks=16, seed=6)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    run_gpu(w, status=status, shared=17)  # 17 blocks = 272 tokens > 260
+    assert kvp.kvp_read_status(status) == kvp.KVP_ERR_BAD_BLOCK
+
+
+def test_prefix_prefill_workload_dense_tiles_full_size():
+    """The benchmarked prompt pass with its 64 shared prefix blocks: dense
+    tiles equal per-request tiles bit for bit at full size (33 098 query
+    tokens of 128 requests), and every head of each request's first and last
+    rows matches the oracle."""
+    w = workloads.make_prefill_named("prefix_prefill", device="cuda", nan_sentinel=True)
+    S = w.info["shared_blocks"]
+    out_pr = torch.empty((w.T, w.Hq, w.D), dtype=w.dtype, device="cuda")
+    out_dn = torch.empty_like(out_pr)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    for out, shared in ((out_pr, 0), (out_dn, S)):
+        kvp.kvp_attention_prefill(out, w.q, w.k_pool, w.v_pool, w.block_tables, w.context_lens,
+                                  w.query_start, w.max_query_len, w.scale,
+                                  shared_prefix_blocks=shared, status=status)
+    assert kvp.kvp_read_status(status) == kvp.KVP_OK
+    assert _same_bits(out_dn, out_pr)
+    qs = w.query_start.cpu().numpy()
+    ends = np.unique(np.concatenate([qs[:-1], qs[1:] - 1]))
+    rows = np.stack([np.repeat(ends, w.Hq), np.tile(np.arange(w.Hq), len(ends))],
+                    axis=1).astype(np.int32)
+    ref = oracle.attention_prefill(w.q.cpu(), w.k_pool.cpu(), w.v_pool.cpu(),
+                                   w.block_tables.cpu(), w.context_lens.cpu(),
+                                   w.query_start.cpu(), w.scale, rows=rows)
+    got = out_dn.cpu()[torch.from_numpy(rows[:, 0]).long(), torch.from_numpy(rows[:, 1]).long()]
+    assert_close(got, ref, "prefix_prefill dense tiles")

@@ -168,7 +168,7 @@ def make_custom(*, B, Hq, Hkv, D, lens, num_blocks, dtype=torch.float16, kv_int8
                      lens, tables, seed, device, nan_sentinel)
 
 
-def _draw_tables(rng, nblk, num_blocks, p):
+def _draw_tables(rng, nblk, num_blocks, p, taken=()):
     free = np.ones(num_blocks, dtype=bool)
     free_list = list(range(num_blocks))
     pos = {b: i for i, b in enumerate(free_list)}
@@ -181,6 +181,8 @@ def _draw_tables(rng, nblk, num_blocks, p):
             free_list[i] = last
             pos[last] = i
 
+    for blk in taken:  # blocks already handed out elsewhere
+        take(int(blk))
     lists = []
     for n in nblk:
         row = []
@@ -398,9 +400,11 @@ class PrefillWorkload:
 
 def make_prefill(*, B, Hq, Hkv, D, lens, qlens, num_blocks, dtype=torch.float16, seed=11,
                  contiguous_p=0.0, max_blocks=None, device="cpu", name="prefill_custom",
-                 nan_sentinel=True) -> PrefillWorkload:
+                 nan_sentinel=True, shared_blocks=0) -> PrefillWorkload:
     """Request b: lens[b] cached tokens, its last qlens[b] are queries
-    (qlens[b] <= lens[b]).  Seeds base = seed * 100: k = 0 q, 1 K pool, 2 V
+    (qlens[b] <= lens[b]).  shared_blocks > 0: the first that many blocks of
+    every request are the same physical blocks (a cached prompt prefix; each
+    lens[b] must cover them).  Seeds base = seed * 100: k = 0 q, 1 K pool, 2 V
     pool, 5 tables.  Slots past every request's tokens hold NaN (16-bit)."""
     lens = [int(x) for x in lens]
     qlens = [int(x) for x in qlens]
@@ -408,10 +412,20 @@ def make_prefill(*, B, Hq, Hkv, D, lens, qlens, num_blocks, dtype=torch.float16,
         raise ValueError("lens and qlens need one entry per request")
     nblk = [-(-n // BLOCK_SIZE) for n in lens]
     mb = max_blocks if max_blocks is not None else max(1, max(nblk) if nblk else 1)
-    if sum(nblk) > num_blocks:
+    S = int(shared_blocks)
+    if S and any(n < S * BLOCK_SIZE for n in lens):
+        raise ValueError("every request must hold the whole shared prefix")
+    if S + sum(n - S for n in nblk) > num_blocks:
         raise ValueError("pool too small for the requested lengths")
     base = seed * 100
-    lists = _draw_tables(np.random.default_rng(base + 5), nblk, num_blocks, contiguous_p)
+    rng = np.random.default_rng(base + 5)
+    if S:
+        shared = _draw_tables(rng, [S], num_blocks, contiguous_p)[0]
+        rest = _draw_tables(rng, [n - S for n in nblk], num_blocks, contiguous_p,
+                            taken=shared)
+        lists = [shared + r for r in rest]
+    else:
+        lists = _draw_tables(rng, nblk, num_blocks, contiguous_p)
     tables = _tables_from_lists(lists, mb)
     T = sum(qlens)
     q = _randn((max(T, 1), Hq, D), dtype, base + 0, device)[:T]
@@ -469,4 +483,7 @@ def make_prefill_named(name: str, device="cpu", nan_sentinel=True,
                            context_lens=torch.tensor(lens, dtype=torch.int32).to(device),
                            query_start=torch.tensor(qs, dtype=torch.int32).to(device),
                            max_query_len=max(qlens),
-                           info={"prefix_tokens": prefix, "query_tokens": T})
+                           info={"prefix_tokens": prefix, "query_tokens": T,
+                                 # the prefix's full blocks are shared physically; its
+                                 # partial last block was copied per request on write
+                                 "shared_blocks": prefix // BLOCK_SIZE})
