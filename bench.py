@@ -241,12 +241,13 @@ class Step:
         desc = kvp.cache_desc(self.kp)
         self.pb_arg = partition_blocks
         nb = kvp.kvp_decode_workspace_bytes(w.B, w.Hq, desc, w.max_blocks, partition_blocks,
-                                            w.kv_int8)
+                                            w.kv_int8 and not w.kv_fp8, w.kv_fp8)
         self.ws = torch.empty(max(nb // 4, 1), dtype=torch.float32, device=dev) if nb else None
         self.split = nb > 0
         self.part_blocks = (min(partition_blocks, w.max_blocks) if partition_blocks else
                             kvp.kvp_decode_partition_blocks(w.B, w.Hq, desc, w.max_blocks,
-                                                            w.kv_int8))
+                                                            w.kv_int8 and not w.kv_fp8,
+                                                            w.kv_fp8))
 
     def _init_int8(self):
         """Quantise the fp16 source pools into the INT8 pools on the GPU: each

@@ -189,6 +189,8 @@ kvp_status kvp_copy_blocks(void* k_cache, void* v_cache, float* k_scale, float* 
  * Long contexts are split into partitions that run as independent CTAs and are
  * merged by a reduce pass (flash-decoding); a return value >= max_blocks_per_seq
  * means single-pass (no workspace needed).  Returns 0 on invalid sizes.
+ * kv_8bit: 0 for the fp16/bf16 decodes, 1 for the INT8 decode, 2 for the FP8
+ * decode (the decodes run differently shaped CTAs).
  */
 int32_t kvp_decode_partition_blocks(int32_t batch, int32_t num_q_heads, kvp_cache_desc cache,
                                     int32_t max_blocks_per_seq, int32_t kv_8bit);
@@ -199,7 +201,8 @@ int32_t kvp_decode_partition_blocks(int32_t batch, int32_t num_q_heads, kvp_cach
  * decode (0 = automatic).  The workspace holds, per (request, query head,
  * partition), the partition's running max, sum and unnormalised output in
  * float32; it needs no initialisation and is fully rewritten by each call.
- * kv_8bit: nonzero for the INT8 / FP8 decodes (their CTAs are shaped alike).
+ * kv_8bit: 0 for the fp16/bf16 decodes, 1 for the INT8 decode, 2 for the FP8
+ * decode; other values answer 0.
  */
 size_t kvp_decode_workspace_bytes(int32_t batch, int32_t num_q_heads, kvp_cache_desc cache,
                                   int32_t max_blocks_per_seq, int32_t partition_blocks,

@@ -246,17 +246,23 @@ def kvp_copy_blocks(k_cache, v_cache, pairs, *, k_scale=None, v_scale=None, stat
                                _ptr(status), _stream_ptr(stream)), "kvp_copy_blocks")
 
 
+def _kv_8bit(kv_int8, kv_fp8):
+    return 2 if kv_fp8 else (1 if kv_int8 else 0)
+
+
 def kvp_decode_partition_blocks(batch, num_q_heads, desc: kvp_cache_desc, max_blocks,
-                                kv_int8=False) -> int:
+                                kv_int8=False, kv_fp8=False) -> int:
+    """kv_int8 / kv_fp8: the pools hold INT8 / FP8 codes (their decodes are
+    shaped differently)."""
     return load_library().kvp_decode_partition_blocks(int(batch), int(num_q_heads), desc,
-                                                      int(max_blocks), int(bool(kv_int8)))
+                                                      int(max_blocks), _kv_8bit(kv_int8, kv_fp8))
 
 
 def kvp_decode_workspace_bytes(batch, num_q_heads, desc: kvp_cache_desc, max_blocks,
-                               partition_blocks=0, kv_int8=False) -> int:
+                               partition_blocks=0, kv_int8=False, kv_fp8=False) -> int:
     return int(load_library().kvp_decode_workspace_bytes(int(batch), int(num_q_heads), desc,
                                                          int(max_blocks), int(partition_blocks),
-                                                         int(bool(kv_int8))))
+                                                         _kv_8bit(kv_int8, kv_fp8)))
 
 
 def kvp_attention_decode(out, q, k_cache, v_cache, block_tables, context_lens, scale, *,

@@ -26,6 +26,7 @@ SOURCES = [
     "kvp_decode_mma.cu",
     "kvp_decode_int8.cu",
     "kvp_decode_fp8.cu",
+    "kvp_decode_fp8_umma.cu",
     "kvp_reduce.cu",
     "kvp_prefill.cu",
     "kvp_block_manager.cpp",

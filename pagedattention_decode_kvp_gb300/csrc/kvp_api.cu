@@ -145,7 +145,13 @@ constexpr int kSms = 152;
 constexpr double kCtaOverheadBlocks = 4.0;
 constexpr double kReduceCostBlocks = 2.0;
 
-int resident_ctas(DecodePath path) { return path == DecodePath::kMmaInt8 ? 4 : 3; }
+int resident_ctas(DecodePath path) {
+  switch (path) {
+    case DecodePath::kMmaInt8: return 4;
+    case DecodePath::kUmmaFp8: return 2;
+    default: return 3;
+  }
+}
 
 int auto_partition(DecodePath path, long long units, int max_blocks) {
   const long long slots = static_cast<long long>(kSms) * resident_ctas(path);
@@ -168,8 +174,9 @@ int auto_partition(DecodePath path, long long units, int max_blocks) {
   return best_pb;
 }
 
+// kv_8bit: 0 for 16-bit pools, 1 for INT8 codes, 2 for FP8 (E4M3) codes.
 kvp_status shape_decode(int batch, int num_q_heads, const kvp_cache_desc& c, int max_blocks,
-                        int partition_blocks, bool kv_8bit, DecodeShape* out) {
+                        int partition_blocks, int kv_8bit, DecodeShape* out) {
   if (batch < 0 || num_q_heads <= 0 || max_blocks <= 0) return KVP_ERR_INVALID_ARG;
   const kvp_status ds = check_desc(c);
   if (ds != KVP_OK) return ds;
@@ -177,8 +184,11 @@ kvp_status shape_decode(int batch, int num_q_heads, const kvp_cache_desc& c, int
   if (partition_blocks < 0 || partition_blocks > kMaxPartBlocks) return KVP_ERR_INVALID_ARG;
   const int G = num_q_heads / c.num_kv_heads;
   DecodeShape s;
-  if (kv_8bit) {
-    s.path = DecodePath::kMmaInt8;  // INT8 and FP8 share the shape (8-bit tiles)
+  if (kv_8bit == 2 && c.head_dim == 128) {
+    s.path = DecodePath::kUmmaFp8;  // FP8 codes straight into the tensor core
+    s.heads_per_cta = G < kHeadsPerCta ? G : kHeadsPerCta;
+  } else if (kv_8bit) {
+    s.path = DecodePath::kMmaInt8;  // INT8, and FP8 at head_dim 64 (8-bit tiles)
     s.heads_per_cta = G < kHeadsPerCta ? G : kHeadsPerCta;
   } else if (G <= 2) {
     s.path = DecodePath::kSimt;
@@ -209,7 +219,8 @@ kvp_status decode_common(void* out, const void* q, bool q_bf16, int kv_kind, con
                          const void* new_k = nullptr, const void* new_v = nullptr) {
   const bool int8 = kv_kind >= 2;  // 8-bit codes with scales: INT8 (2) or FP8 E4M3 (3)
   DecodeShape sh;
-  const kvp_status st = shape_decode(batch, hq, c, max_blocks, partition_blocks, int8, &sh);
+  const kvp_status st =
+      shape_decode(batch, hq, c, max_blocks, partition_blocks, int8 ? kv_kind - 1 : 0, &sh);
   if (st != KVP_OK) return st;
   const bool merge_runs = (phases & KVP_DECODE_MERGE_RUNS) != 0;
   phases &= ~KVP_DECODE_MERGE_RUNS;
@@ -261,9 +272,9 @@ kvp_status decode_common(void* out, const void* q, bool q_bf16, int kv_kind, con
   if (phases & KVP_PHASE_PARTIAL) {
     const int eb = int8 ? 1 : 2;
     DecodeMaps maps;
-    maps.merged = merge_runs;
+    maps.merged = merge_runs && sh.path != DecodePath::kUmmaFp8;  // (per-block fetch only)
     kvp_status r = KVP_OK;
-    if (merge_runs) {
+    if (maps.merged) {
       const int runs[3] = {1, 2, 4};
       for (int i = 0; i < 3 && r == KVP_OK; ++i) {
         r = make_pool_run_map(&maps.runs.k[i], kc, c, eb, runs[i]);
@@ -281,6 +292,9 @@ kvp_status decode_common(void* out, const void* q, bool q_bf16, int kv_kind, con
         break;
       case DecodePath::kMma:
         e = launch_decode_mma(p, maps, kv_kind == 1, sh.max_parts, s);
+        break;
+      case DecodePath::kUmmaFp8:
+        e = launch_decode_fp8_umma(p, maps.k, maps.v, sh.max_parts, s);
         break;
       default:
         e = kv_kind == 3 ? launch_decode_mma_fp8(p, maps, sh.max_parts, s)
@@ -417,7 +431,8 @@ kvp_status kvp_copy_blocks(void* k_cache, void* v_cache, float* k_scale, float* 
 int32_t kvp_decode_partition_blocks(int32_t batch, int32_t num_q_heads, kvp_cache_desc cache,
                                     int32_t max_blocks_per_seq, int32_t kv_int8) {
   DecodeShape sh;
-  if (shape_decode(batch, num_q_heads, cache, max_blocks_per_seq, 0, kv_int8 != 0, &sh) != KVP_OK)
+  if (kv_int8 < 0 || kv_int8 > 2 ||
+      shape_decode(batch, num_q_heads, cache, max_blocks_per_seq, 0, kv_int8, &sh) != KVP_OK)
     return 0;
   return sh.part_blocks;
 }
@@ -426,7 +441,8 @@ size_t kvp_decode_workspace_bytes(int32_t batch, int32_t num_q_heads, kvp_cache_
                                   int32_t max_blocks_per_seq, int32_t partition_blocks,
                                   int32_t kv_int8) {
   DecodeShape sh;
-  if (shape_decode(batch, num_q_heads, cache, max_blocks_per_seq, partition_blocks, kv_int8 != 0,
+  if (kv_int8 < 0 || kv_int8 > 2 ||
+      shape_decode(batch, num_q_heads, cache, max_blocks_per_seq, partition_blocks, kv_int8,
                    &sh) != KVP_OK)
     return 0;
   return sh.ws_bytes;

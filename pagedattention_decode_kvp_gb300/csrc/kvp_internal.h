@@ -32,7 +32,7 @@ constexpr int kHeadsPerCta = 8;      // query heads one tensor-core CTA serves
 constexpr int kMaxPartBlocks = 1024;  // table slice staged per CTA (4 KB)
 
 // Decode kernel family.
-enum class DecodePath : int { kSimt = 0, kMma = 1, kMmaInt8 = 2, kMmaFp8 = 3 };
+enum class DecodePath : int { kSimt = 0, kMma = 1, kMmaInt8 = 2, kMmaFp8 = 3, kUmmaFp8 = 4 };
 
 // Everything a decode launch needs besides the two tensor maps.
 struct DecodeParams {
@@ -109,6 +109,9 @@ cudaError_t launch_decode_mma_int8(const DecodeParams& p, const DecodeMaps& m, i
                                    cudaStream_t s);
 cudaError_t launch_decode_mma_fp8(const DecodeParams& p, const DecodeMaps& m, int grid_x,
                                   cudaStream_t s);
+// FP8 pools, head_dim 128, on tcgen05 (kind::f8f6f4); per-block 2-D pool maps.
+cudaError_t launch_decode_fp8_umma(const DecodeParams& p, const CUtensorMap& tk,
+                                   const CUtensorMap& tv, int grid_x, cudaStream_t s);
 cudaError_t launch_decode_reduce(const DecodeParams& p, cudaStream_t s);
 // Self-test of the bounded wait: one block waits on a barrier nothing arrives
 // on, for at most limit_ns, and records kErrTimeout when it gives up.

@@ -131,20 +131,6 @@ __device__ __forceinline__ void bulk_wait_all() {
   asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
 }
 
-// Named barrier over `nthreads` threads that also ANDs a flag across them.
-__device__ __forceinline__ bool named_bar_and(uint32_t id, uint32_t nthreads, bool v) {
-  uint32_t r;
-  asm volatile(
-      "{\n\t.reg .pred p, q;\n\t"
-      "setp.ne.u32 p, %1, 0;\n\t"
-      "bar.red.and.pred q, %2, %3, p;\n\t"
-      "selp.u32 %0, 1, 0, q;\n\t}"
-      : "=r"(r)
-      : "r"(static_cast<uint32_t>(v)), "r"(id), "r"(nthreads)
-      : "memory");
-  return r != 0;
-}
-
 // One work item.  Per-request tiles (no shared prefix): tokens t0 ..
 // t0 + ntok - 1 of request b's query chunk against kv head kvh.  Dense tiles
 // (a prefix of shared_blocks blocks that every request's table names alike):

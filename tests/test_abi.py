@@ -70,6 +70,13 @@ def test_workspace_sizing_rules(lib):
     # many short requests stay single pass; one very long one is split
     assert kvp.kvp_decode_workspace_bytes(128, 32, _desc(8192, 32, 16, 128), 97) == 0
     assert kvp.kvp_decode_partition_blocks(4, 64, _desc(40000, 8, 16, 128), 8192, 1) <= 1024
+    # the FP8 decode (kv_8bit = 2) runs fewer, larger CTAs per SM than the INT8
+    # one, so it cuts long contexts into fewer partitions; other kinds answer 0
+    d8 = _desc(40000, 8, 16, 128)
+    int8_pb = kvp.kvp_decode_partition_blocks(4, 64, d8, 8192, kv_int8=True)
+    fp8_pb = kvp.kvp_decode_partition_blocks(4, 64, d8, 8192, kv_fp8=True)
+    assert 16 <= int8_pb <= fp8_pb <= 1024
+    assert lib.kvp_decode_workspace_bytes(4, 64, d8, 8192, 0, 3) == 0
     # invalid sizes answer 0
     assert kvp.kvp_decode_workspace_bytes(4, 6, _desc(hkv=4), 16) == 0      # 6 % 4 != 0
     assert kvp.kvp_decode_workspace_bytes(4, 8, _desc(d=96), 16) == 0       # head_dim 96

@@ -39,10 +39,10 @@ def assert_attn_close(gpu_out, ref, what=""):
                              f"{i}: gpu {g[i]} ref {ref[i]} (max abs err {err.max():.3e})")
 
 
-def workspace_for(w, partition_blocks=0):
+def workspace_for(w, partition_blocks=0, fp8=False):
     d = kvp.kvp_cache_desc(w.num_blocks, w.Hkv, 16, w.D)
     nbytes = kvp.kvp_decode_workspace_bytes(w.B, w.Hq, d, w.max_blocks, partition_blocks,
-                                            w.kv_int8)
+                                            w.kv_int8 and not fp8, fp8)
     if nbytes == 0:
         return None
     return torch.empty(nbytes // 4 + 4, dtype=torch.float32, device="cuda")
@@ -459,7 +459,7 @@ def test_decode_fp8_parity(q_dtype, D, Hq, Hkv, partition_blocks):
     out = torch.full_like(w.q, float("nan"), device="cuda")
     kvp.kvp_attention_decode_fp8(out, w.q.cuda(), gkc, gvc, gks, gvs, w.block_tables.cuda(),
                                  w.context_lens.cuda(), w.scale,
-                                 workspace=workspace_for(w, partition_blocks),
+                                 workspace=workspace_for(w, partition_blocks, fp8=True),
                                  partition_blocks=partition_blocks)
     torch.cuda.synchronize()
     okc, oks = oracle.append_fp8(kc.view(torch.float8_e4m3fn), ks, w.new_k, w.slot_mapping)
@@ -528,7 +528,7 @@ def test_merged_run_fetch_equals_per_block_fetch(kind, dtype, D, Hq, Hkv, p_run,
     w = workloads.make_custom(B=len(lens), Hq=Hq, Hkv=Hkv, D=D, lens=lens, num_blocks=200,
                               dtype=dtype, kv_int8=kind != "16", contiguous_p=p_run,
                               seed=D + Hq + int(10 * p_run), max_blocks=48)
-    ws = workspace_for(w, partition_blocks)
+    ws = workspace_for(w, partition_blocks, fp8=kind == "fp8")
     outs = []
     if kind == "16":
         kp, vp = w.k_pool.cuda(), w.v_pool.cuda()
