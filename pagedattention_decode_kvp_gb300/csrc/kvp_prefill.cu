@@ -57,9 +57,43 @@ constexpr int kMmaWarp = kSoftmaxWarps;               // issues the tensor-core 
 constexpr int kProducerWarps = 2;
 constexpr int kThreads = kSoftmaxThreads + 32 + kProducerWarps * 32;
 constexpr int kSmemPerSm = 233472;                    // shared memory of one SM (bytes)
-// Work items are scanned in windows of kWindow candidates (one per softmax
-// thread); only those with rows are visited
-constexpr int kWindow = kSoftmaxThreads;
+// Work items are decoded by the K producer (32 candidates at a time, one per
+// lane) and handed to the other roles through a ring of kTileSlots slots in
+// shared memory, together with the checks of the block ids they read and, for
+// dense tiles, the lengths of up to kSlotReqs requests with rows in the tile.
+constexpr int kTileSlots = 4;
+constexpr int kSlotReqs = 8;
+
+// One work item.  Per-request tiles (no shared prefix): tokens t0 ..
+// t0 + ntok - 1 of request b's query chunk against kv head kvh.  Dense tiles
+// (a prefix of shared_blocks blocks that every request's table names alike):
+// 128 / G consecutive query tokens of the whole batch -- possibly of several
+// requests, b .. r1 -- against kv head kvh.  t0 is a row of q / out.
+struct Tile {
+  int kvh;
+  int t0, ntok;     // first query token (global row) and tokens in the tile
+  int b, r1;        // first and last request with rows in the tile
+  int nchunks;      // 128-key chunks the tile streams
+  int pos0, nkeys;  // per-request tiles: first token's position; keys needed
+  bool lens_bad;    // lengths out of range: rows are zeroed, nothing is read
+  int32_t status;   // error to record for this item (0 = none)
+};
+
+// The request lengths a per-request work item needs, loaded ahead of its turn.
+struct ItemLens {
+  int q0, q1, n;
+};
+
+// A decoded work item as the K producer hands it to the other roles.
+struct TileSlot {
+  Tile t;
+  int32_t bad;   // a block id the tile reads is out of range, or (dense) a
+                 // request's table names other prefix blocks than the first's
+  int32_t nreq;  // dense: requests b .. b + nreq - 1 listed below (0: too many)
+  int32_t end;   // no more work items
+  int32_t q0[kSlotReqs], q1[kSlotReqs], n[kSlotReqs];  // query_start[r], [r + 1], context_lens[r]
+};
+constexpr uint32_t kSlotBytes = (sizeof(TileSlot) + 15) / 16 * 16;
 
 template <bool kBf16, int D>
 struct PrefillLayout {
@@ -78,10 +112,11 @@ struct PrefillLayout {
   // and conflict-free for one-row-per-lane 16-byte writes
   static constexpr uint32_t kStgOff = kVOff + kVStages * kKV;
   static constexpr uint32_t kRedOff = kStgOff + kKV;  // [kRows] row sums
-  static constexpr uint32_t kMaskOff = kRedOff + kRows * 4;  // [kWindow / 32] work-item bits
-  static constexpr uint32_t kBarOff = kMaskOff + kWindow / 8;
-  // kfull[], vfull[], kempty[], vempty[], s[], p[], pv[2], q in TMEM, MMA done
-  static constexpr int kBars = 2 * (kKStages + kVStages) + 2 * kSBufs + 4;
+  static constexpr uint32_t kSlotOff = kRedOff + kRows * 4;  // [kTileSlots] decoded work items
+  static constexpr uint32_t kBarOff = kSlotOff + kTileSlots * kSlotBytes;
+  // kfull[], vfull[], kempty[], vempty[], s[], p[], pv[2], q in TMEM, MMA
+  // done, slot full[], slot empty[]
+  static constexpr int kBars = 2 * (kKStages + kVStages) + 2 * kSBufs + 4 + 2 * kTileSlots;
   // + the barriers and the TMEM address slot.  The swizzled tiles need a
   // 1024-byte aligned base, which the kernel checks instead of reserving slack.
   static constexpr size_t kSmem = kBarOff + kBars * 8 + 16;
@@ -131,25 +166,6 @@ __device__ __forceinline__ void bulk_wait_all() {
   asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
 }
 
-// One work item.  Per-request tiles (no shared prefix): tokens t0 ..
-// t0 + ntok - 1 of request b's query chunk against kv head kvh.  Dense tiles
-// (a prefix of shared_blocks blocks that every request's table names alike):
-// 128 / G consecutive query tokens of the whole batch -- possibly of several
-// requests, b .. r1 -- against kv head kvh.  t0 is a row of q / out.
-struct Tile {
-  int kvh;
-  int t0, ntok;     // first query token (global row) and tokens in the tile
-  int b, r1;        // first and last request with rows in the tile
-  int nchunks;      // 128-key chunks the tile streams
-  int pos0, nkeys;  // per-request tiles: first token's position; keys needed
-  bool lens_bad;    // lengths out of range: rows are zeroed, nothing is read
-  int32_t status;   // error to record for this item (0 = none)
-};
-
-// The request lengths a per-request work item needs, loaded ahead of its turn.
-struct ItemLens {
-  int q0, q1, n;
-};
 
 // Work item `id`.  Per-request tiles: of tiles_x * batch * num_kv_heads, the
 // last query tiles of every request first (they attend to the most keys),
@@ -332,6 +348,64 @@ __device__ __forceinline__ void row_info(const PrefillParams& p, const Tile& t, 
   pos = p.context_lens[r] - (q1 - q0) + (tok - q0);
 }
 
+// Row `row` of a dense tile from the request lengths its slot carries (the
+// same answer as row_info, without global loads); falls back to row_info when
+// the slot lists none.
+template <bool kDense>
+__device__ __forceinline__ void row_info_slot(const PrefillParams& p, const Tile& t,
+                                              const TileSlot& ts, int row, bool& valid, int& req,
+                                              int& pos) {
+  if (!kDense || ts.nreq == 0) {
+    row_info<kDense>(p, t, row, valid, req, pos);
+    return;
+  }
+  const int tk = row / p.group;
+  valid = tk < t.ntok;
+  const int tok = t.t0 + min(tk, t.ntok - 1);
+  int i = 0;
+  while (i + 1 < ts.nreq && ts.q1[i] <= tok) ++i;
+  req = t.b + i;
+  pos = ts.n[i] - (ts.q1[i] - ts.q0[i]) + (tok - ts.q0[i]);
+}
+
+// Whether a tile reads a block id out of range (every segment's ids), or --
+// dense tiles -- a request with rows in it names other blocks for the shared
+// prefix than the tile's first request, whose table the prefix is read
+// through.  The whole warp runs it (lane-strided); the answer is warp-uniform.
+template <bool kDense>
+__device__ bool tile_ids_bad(const PrefillParams& p, const Tile& t, int lane) {
+  bool bad = false;
+  if constexpr (kDense) {
+    if (t.r1 > t.b) {
+      const int32_t* t0 = p.block_tables + static_cast<size_t>(t.b) * p.max_blocks;
+      for (int k = lane; k < (t.r1 - t.b) * p.shared_blocks; k += 32) {
+        const int r = t.b + 1 + k / p.shared_blocks, i = k % p.shared_blocks;
+        if (p.query_start[r + 1] > p.query_start[r])
+          bad |= p.block_tables[static_cast<size_t>(r) * p.max_blocks + i] != t0[i];
+      }
+    }
+    ChunkWalk cw;
+    walk_start(p, t, cw);
+    int k;
+    while ((k = walk_next(p, t, cw)) >= 0) {
+      const int b0 = k / kBlockSize, b1 = (cw.end + kBlockSize - 1) / kBlockSize;
+      for (int i = b0 + lane; i < b1; i += 32) {
+        const int id = cw.tbl[i];
+        bad |= (id < 0) || (id >= p.num_blocks);
+      }
+      cw.key = cw.end;  // the rest of this segment is covered
+    }
+  } else {
+    const int32_t* tbl = p.block_tables + static_cast<size_t>(t.b) * p.max_blocks;
+    const int nblk = (t.nkeys + kBlockSize - 1) / kBlockSize;
+    for (int i = lane; i < nblk; i += 32) {
+      const int id = tbl[i];
+      bad |= (id < 0) || (id >= p.num_blocks);
+    }
+  }
+  return __any_sync(0xffffffffu, bad);
+}
+
 // Warp roles: warps 0-7 run the softmax -- warp w serves query rows
 // 32*(w%4) + 16*(w/4) .. +15 (within the TMEM lanes it may access), all keys
 // of each chunk and all O columns, and warps 0-3 move each tile's Q from
@@ -385,10 +459,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* pv_bar = p_bar + kSBufs;                                 // [2]
   uint64_t* qt_bar = pv_bar + 2;     // the tile's Q copied into TMEM
   uint64_t* done_bar = qt_bar + 1;   // every tensor-core op of the CTA complete
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done_bar + 1);
+  uint64_t* tf_bar = done_bar + 1;   // [kTileSlots] slot written (K producer, 32 arrivals)
+  uint64_t* te_bar = tf_bar + kTileSlots;  // [kTileSlots] slot read by every other role
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(te_bar + kTileSlots);
   uint8_t* stg = sm + L::kStgOff;                                    // output staging
   float* red = reinterpret_cast<float*>(sm + L::kRedOff);            // row sums
-  uint32_t* mask = reinterpret_cast<uint32_t*>(sm + L::kMaskOff);    // items with rows
+  auto slot_at = [&](uint32_t i) {
+    return reinterpret_cast<TileSlot*>(sm + L::kSlotOff + (i % kTileSlots) * kSlotBytes);
+  };
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const bool mma_warp = warp == kMmaWarp;
@@ -409,6 +487,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(smem_addr(pv_bar + 1), 1);
     mbar_init(smem_addr(qt_bar), 1);
     mbar_init(smem_addr(done_bar), 1);
+    for (int i = 0; i < kTileSlots; ++i) {
+      mbar_init(smem_addr(tf_bar + i), 32);
+      mbar_init(smem_addr(te_bar + i), 32 * (kSoftmaxWarps + 2));
+    }
     fence_barrier_init();
   }
   if (mma_warp) umma::alloc(smem_addr(tmem_slot), L::kTmemCols);
@@ -620,9 +702,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   };
 
   // ---- softmax warps: one work item
-  auto softmax_item = [&](const Tile& t) {
+  // (the slot `ts` is released -- its empty barrier arrived on -- once its
+  // contents are read)
+  auto softmax_item = [&](const Tile& t, const TileSlot& ts, uint64_t* slot_empty) {
     if (t.status != 0 && tid == 0) set_status(p.status, t.status);
     if (t.nchunks == 0) {
+      __syncwarp();
+      mbar_arrive(smem_addr(slot_empty));
       if (t.lens_bad) zero_tile_rows<D>(p, t, kSoftmaxThreads);
       return;
     }
@@ -630,34 +716,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     // this thread's two rows: valid (a token of the tile), request, position
     bool va, vb;
     int qa, qb, qpa, qpb;
-    row_info<kDense>(p, t, ra, va, qa, qpa);
-    row_info<kDense>(p, t, rb, vb, qb, qpb);
-    bool bad = false;
-    // per-request tiles: the block ids the tile reads, loaded now and range-
-    // checked at its end (ids past the first 128 are checked there directly)
-    int bid_pre[4] = {0, 0, 0, 0};
-    if constexpr (!kDense) {
-      const int32_t* tbl = p.block_tables + static_cast<size_t>(t.b) * p.max_blocks;
-      const int nblk = (t.nkeys + kBlockSize - 1) / kBlockSize;
-#pragma unroll
-      for (int u = 0; u < 4; ++u) bid_pre[u] = lane + 32 * u < nblk ? tbl[lane + 32 * u] : 0;
-    }
-    // dense tiles: every request with rows here must name the shared prefix's
-    // blocks as the first one does (each warp checks for itself); and this
-    // warp's valid rows are reduced once per tile so that every chunk's mask
-    // decision is warp-uniform: the smallest position, and the range of
-    // requests (a chunk of request R needs masks unless all rows are R's and
-    // lie at or past its last key)
+    row_info_slot<kDense>(p, t, ts, ra, va, qa, qpa);
+    row_info_slot<kDense>(p, t, ts, rb, vb, qb, qpb);
+    // the block ids the tile reads, checked by the K producer
+    const bool bad = ts.bad != 0;
+    __syncwarp();
+    mbar_arrive(smem_addr(slot_empty));
+    // dense tiles: this warp's valid rows are reduced once per tile so that
+    // every chunk's mask decision is warp-uniform: the smallest position, and
+    // the range of requests (a chunk of request R needs masks unless all rows
+    // are R's and lie at or past its last key)
     int wq = INT_MAX, wr0 = INT_MAX, wr1 = -1;
     if constexpr (kDense) {
-      if (t.r1 > t.b) {
-        const int32_t* t0 = p.block_tables + static_cast<size_t>(t.b) * p.max_blocks;
-        for (int k = lane; k < (t.r1 - t.b) * p.shared_blocks; k += 32) {
-          const int r = t.b + 1 + k / p.shared_blocks, i = k % p.shared_blocks;
-          if (p.query_start[r + 1] > p.query_start[r])
-            bad |= p.block_tables[static_cast<size_t>(r) * p.max_blocks + i] != t0[i];
-        }
-      }
       if (va) { wq = qpa; wr0 = qa; wr1 = qa; }
       if (vb) { wq = min(wq, qpb); wr0 = min(wr0, qb); wr1 = max(wr1, qb); }
 #pragma unroll
@@ -854,17 +924,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int ck = ck0; ck < end && j < n && ok; ck += kKeys, ++j)
           chunk(j, ck, min(kKeys, end - ck), mixed || ck + kKeys - 1 > wq, qea, qeb);
       }
-      // every block id the tile read, range-checked segment by segment
-      walk_start(p, t, cw);
-      int k;
-      while ((k = walk_next(p, t, cw)) >= 0) {
-        const int b0 = k / kBlockSize, b1 = (cw.end + kBlockSize - 1) / kBlockSize;
-        for (int i = b0 + lane; i < b1; i += 32) {
-          const int id = cw.tbl[i];
-          bad |= (id < 0) || (id >= p.num_blocks);
-        }
-        cw.key = cw.end;  // the rest of this segment is covered
-      }
     } else {
       // one request: chunk j holds keys 128 j ..; a chunk needs masks once it
       // reaches past the tile's first position (rows past the tile's tokens
@@ -872,25 +931,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int j = 0; j < n && ok; ++j)
         chunk(j, j * kKeys, min(kKeys, t.nkeys - j * kKeys), j * kKeys + kKeys - 1 > t.pos0,
               va ? qpa : -1, vb ? qpb : -1);
-      const int32_t* tbl = p.block_tables + static_cast<size_t>(t.b) * p.max_blocks;
-      const int nblk = (t.nkeys + kBlockSize - 1) / kBlockSize;
-#pragma unroll
-      for (int u = 0; u < 4; ++u)
-        bad |= lane + 32 * u < nblk && (bid_pre[u] < 0 || bid_pre[u] >= p.num_blocks);
-      for (int i = lane + 128; i < nblk; i += 32) {
-        const int bid = tbl[i];
-        bad |= (bid < 0) || (bid >= p.num_blocks);
-      }
     }
-    // ---- out = O / l.  A tile that met an out-of-range block id (each warp
-    // checked every chunk's ids, and the shared prefix's, for itself) writes
-    // zeros.  Every softmax warp gets here, even after a failed wait, so that
+    // ---- out = O / l.  A tile that met an out-of-range block id (or prefix
+    // tables that disagree) writes zeros.  Every softmax warp gets here, even after a failed wait, so that
     // the named barriers below always complete; the first one also agrees on
     // whether all waits succeeded.
     const uint32_t gl = gc + n - 1;
     if (ok) ok = mbar_wait_bounded(smem_addr(pv_bar + (gl & 1)), (gl >> 1) & 1);
     umma::fence_after_sync();
-    bad = __any_sync(0xffffffffu, bad);
     if (bad && tid == 0) set_status(p.status, kErrBadBlock);
     // row sums: the four lanes of a row, then through shared memory to the
     // thread that writes the row out
@@ -973,57 +1021,98 @@ __global__ void __launch_bounds__(kThreads, 1)
     gc += n;
   };
 
-  // ---- every role walks the same work items: the candidates id =
-  // blockIdx.x + k * gridDim.x, a window of kWindow at a time; the softmax
-  // warps mark those with rows, and each role visits the marked ones in
-  // order, loading the next item's lengths while it works on the current one
+  // ---- work items: the candidates id = blockIdx.x + k * gridDim.x.  The K
+  // producer decodes them 32 at a time (one per lane), checks the block ids
+  // of each one with rows, and hands it through the slot ring to the other
+  // roles, which take the items in the same order; a slot marked `end`
+  // closes the list.
   const int ncand = (items - static_cast<int>(blockIdx.x) + static_cast<int>(gridDim.x) - 1) /
                     static_cast<int>(gridDim.x);
-  for (int w0 = 0; w0 < ncand; w0 += kWindow) {
-    if (warp < kSoftmaxWarps) {
-      bool has = false;
-      const int k = w0 + tid;
-      if (k < ncand) {
-        Tile t;
-        const int id = static_cast<int>(blockIdx.x) + k * static_cast<int>(gridDim.x);
-        has = decode_tile<kDense>(p, tiles_x, id, load_lens<kDense>(p, id), t);
-      }
-      const uint32_t bits = __ballot_sync(0xffffffffu, has);
-      if (lane == 0) mask[warp] = bits;
-    }
-    __syncthreads();
-    // next marked candidate after k (-1: none)
-    auto next_item = [&](int k) {
-      for (int wd = (k + 1) >> 5; wd < kWindow / 32; ++wd) {
-        uint32_t m = mask[wd];
-        if (wd == ((k + 1) >> 5)) m &= 0xffffffffu << ((k + 1) & 31);
-        if (m) return wd * 32 + __ffs(m) - 1;
-      }
-      return -1;
-    };
-    auto id_of = [&](int k) {
-      return static_cast<int>(blockIdx.x) + (w0 + k) * static_cast<int>(gridDim.x);
-    };
-    int k = next_item(-1);
-    ItemLens lens = k >= 0 ? load_lens<kDense>(p, id_of(k)) : ItemLens{0, 0, 0};
-    while (k >= 0) {
-      const int kn = next_item(k);
-      const ItemLens cur = lens;
-      if (kn >= 0) lens = load_lens<kDense>(p, id_of(kn));  // in flight meanwhile
-      Tile t;
-      decode_tile<kDense>(p, tiles_x, id_of(k), cur, t);
-      if (ok) {
-        if (producer) {
-          if (t.nchunks > 0) produce_item(t);
-        } else if (mma_warp) {
-          if (t.nchunks > 0) mma_item(t);
-        } else {
-          softmax_item(t);
+  uint32_t item = 0;  // slots written (K producer) or taken (the other roles)
+  if (producer && is_k) {
+    // (the whole warp: lane-strided checks and lists, then every lane writes
+    // its part of the slot and arrives on its full barrier)
+    auto publish = [&](const Tile& t, bool end) {
+      bool bad = false;
+      int nreq = 0, q0 = 0, q1 = 0, nn = 0;
+      if (!end && t.nchunks > 0) {
+        bad = tile_ids_bad<kDense>(p, t, lane);
+        if constexpr (kDense) {
+          nreq = t.r1 - t.b + 1 <= kSlotReqs ? t.r1 - t.b + 1 : 0;
+          if (lane < nreq) {
+            q0 = p.query_start[t.b + lane];
+            q1 = p.query_start[t.b + lane + 1];
+            nn = p.context_lens[t.b + lane];
+          }
         }
       }
-      k = kn;
+      if (item >= static_cast<uint32_t>(kTileSlots))
+        ok &= mbar_wait_bounded(smem_addr(te_bar + item % kTileSlots),
+                                ((item / kTileSlots) - 1) & 1);
+      if (!ok) return;
+      TileSlot* ts = slot_at(item);
+      if (lane == 0) {
+        ts->t = t;
+        ts->bad = bad ? 1 : 0;
+        ts->nreq = nreq;
+        ts->end = end ? 1 : 0;
+      }
+      if (lane < nreq) {
+        ts->q0[lane] = q0;
+        ts->q1[lane] = q1;
+        ts->n[lane] = nn;
+      }
+      mbar_arrive(smem_addr(tf_bar + item % kTileSlots));
+      ++item;
+    };
+    for (int w0 = 0; w0 < ncand && ok; w0 += 32) {
+      Tile mine{};
+      bool has = false;
+      if (w0 + lane < ncand) {
+        const int id = static_cast<int>(blockIdx.x) + (w0 + lane) * static_cast<int>(gridDim.x);
+        has = decode_tile<kDense>(p, tiles_x, id, load_lens<kDense>(p, id), mine);
+      }
+      uint32_t bits = __ballot_sync(0xffffffffu, has);
+      while (bits != 0 && ok) {
+        const int src = __ffs(bits) - 1;
+        bits &= bits - 1;
+        Tile t;
+        t.kvh = __shfl_sync(0xffffffffu, mine.kvh, src);
+        t.t0 = __shfl_sync(0xffffffffu, mine.t0, src);
+        t.ntok = __shfl_sync(0xffffffffu, mine.ntok, src);
+        t.b = __shfl_sync(0xffffffffu, mine.b, src);
+        t.r1 = __shfl_sync(0xffffffffu, mine.r1, src);
+        t.nchunks = __shfl_sync(0xffffffffu, mine.nchunks, src);
+        t.pos0 = __shfl_sync(0xffffffffu, mine.pos0, src);
+        t.nkeys = __shfl_sync(0xffffffffu, mine.nkeys, src);
+        t.lens_bad = __shfl_sync(0xffffffffu, mine.lens_bad ? 1 : 0, src) != 0;
+        t.status = __shfl_sync(0xffffffffu, mine.status, src);
+        publish(t, false);
+        if (ok && t.nchunks > 0) produce_item(t);
+      }
     }
-    __syncthreads();  // the mask is rewritten for the next window
+    publish(Tile{}, true);
+  } else {
+    while (true) {
+      const uint32_t si = item % kTileSlots;
+      ok &= mbar_wait_bounded(smem_addr(tf_bar + si), (item / kTileSlots) & 1);
+      if (!ok) break;
+      const TileSlot& ts = *slot_at(item);
+      ++item;
+      const Tile t = ts.t;
+      const bool end = ts.end != 0;
+      if (warp < kSoftmaxWarps && !end) {
+        softmax_item(t, ts, te_bar + si);  // (releases the slot)
+      } else {
+        __syncwarp();
+        mbar_arrive(smem_addr(te_bar + si));
+        if (end) break;
+        if (t.nchunks > 0) {
+          if (producer) produce_item(t);
+          else mma_item(t);
+        }
+      }
+    }
   }
 
   if (producer) {
