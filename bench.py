@@ -49,7 +49,8 @@ PREFILL_METRIC = ("paged-attention prefill of prefix-cached prompts: achieved te
                   "(causal attention FLOPs) and query tokens/s")
 L2_BYTES = 129 * 1024 * 1024
 KERNEL_SOURCES = ["kvp_decode.cuh", "kvp_device.cuh", "kvp_decode_simt.cu", "kvp_decode_mma.cu",
-                  "kvp_decode_int8.cu", "kvp_internal.h"]
+                  "kvp_decode_int8.cu", "kvp_decode_fp8.cu", "kvp_decode_fp8_umma.cu",
+                  "kvp_umma.cuh", "kvp_internal.h"]
 PREFILL_SOURCES = ["kvp_prefill.cu", "kvp_umma.cuh", "kvp_device.cuh", "kvp_internal.h"]
 
 
