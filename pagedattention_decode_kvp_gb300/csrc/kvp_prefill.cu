@@ -362,8 +362,11 @@ __device__ __forceinline__ void row_info_slot(const PrefillParams& p, const Tile
   const int tk = row / p.group;
   valid = tk < t.ntok;
   const int tok = t.t0 + min(tk, t.ntok - 1);
+  // (query_start is non-decreasing: the index is the count of listed ends at
+  // or before the token, all compared at once)
   int i = 0;
-  while (i + 1 < ts.nreq && ts.q1[i] <= tok) ++i;
+#pragma unroll
+  for (int k = 0; k + 1 < kSlotReqs; ++k) i += (k + 1 < ts.nreq && ts.q1[k] <= tok) ? 1 : 0;
   req = t.b + i;
   pos = ts.n[i] - (ts.q1[i] - ts.q0[i]) + (tok - ts.q0[i]);
 }
@@ -937,6 +940,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     // the named barriers below always complete; the first one also agrees on
     // whether all waits succeeded.
     const uint32_t gl = gc + n - 1;
+    // the previous tile's staged rows have been read: by every thread (it
+    // passed the barrier below only after its own reads) and by the TMA
+    // store thread 0 issued (checked while the last P V completes)
+    if (tid == 0) bulk_wait_read();
     if (ok) ok = mbar_wait_bounded(smem_addr(pv_bar + (gl & 1)), (gl >> 1) & 1);
     umma::fence_after_sync();
     if (bad && tid == 0) set_status(p.status, kErrBadBlock);
@@ -954,10 +961,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       red[ra] = la;
       red[rb] = lb;
     }
-    // the previous tile's staged rows have been read: by every thread (it
-    // passed the barrier below only after its own reads) and by the TMA
-    // store thread 0 issued
-    if (tid == 0) bulk_wait_read();
     ok = named_bar_and(1, kSoftmaxThreads, ok);
     // thread (warp w, lane) finishes columns [D/2 (w / 4), +D/2) of row
     // 32 (w % 4) + lane: O read with the one-lane-per-row TMEM shape, scaled,
