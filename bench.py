@@ -485,7 +485,8 @@ def measure_decode(name, args, kvp, world, dev, local, headline):
         "step_bytes": sbytes,
         "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak,
                      "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": traffic,
-                     "kernel": "decode_partial_kernel", "peak_source": peak_src,
+                     "kernel": ("decode_fp8_umma_kernel" if w.kv_fp8 and w.D == 128
+                                else "decode_partial_kernel"), "peak_source": peak_src,
                      "algorithmic_bytes_per_launch": partial_bytes,
                      "launch_ms": round(partial_ms, 5),
                      "timing": "kernel events in a separate pass of the same steps"},
