@@ -391,12 +391,15 @@ kvp_status kvp_attention_decode_noalloc(void* out, const void* q, const void* k_
 
 /*
  * kvp_selftest_wait_timeout -- a diagnostic (the pages have no counterpart):
- * launches one block that waits, through the same bounded mbarrier wait every
- * pipeline of this library uses, on a barrier that nothing arrives on, and
- * gives up after `limit_ns` nanoseconds of wall-clock time (1e3 .. 5e9), as
- * the kernels do after 2 s when a copy or a hand-off never comes.  The wait
- * records KVP_ERR_TIMEOUT in *dev_status (if it still holds KVP_OK); nothing
- * faults and the stream stays usable.  Returns KVP_ERR_INVALID_ARG for a null
+ * launches one block whose two warps wait, through the same bounded mbarrier
+ * wait every pipeline of this library uses, on barriers that nothing arrives
+ * on: the first gives up after `limit_ns` nanoseconds of wall-clock time
+ * (1e3 .. 5e9), as the kernels do after 2 s when a copy or a hand-off never
+ * comes, and sets the block's abort flag; the second, waiting with the
+ * default 2 s limit, sees the flag and gives up within 16 tries (about a
+ * third of a millisecond), as every wait that polls the flag does.  The
+ * waits record KVP_ERR_TIMEOUT in *dev_status (if it still holds KVP_OK);
+ * nothing faults and the stream stays usable.  Returns KVP_ERR_INVALID_ARG for a null
  * status or a limit outside the range, KVP_ERR_CUDA if the launch fails.
  */
 kvp_status kvp_selftest_wait_timeout(int32_t* dev_status, int64_t limit_ns, kvp_stream_t stream);

@@ -146,22 +146,30 @@ __device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parit
 // complete -- is one try_wait; the waiting loop is out of line and sleeps
 // between tries (20 us hint), so a warp that waits leaves the issue slots to
 // the warps that share its scheduler (measured 2.7% on the prefill, whose
-// softmax warps are issue-bound).
+// softmax warps are issue-bound).  `abort` (optional, shared memory): a wait
+// that gives up sets it, and every wait polling the same flag gives up
+// within 16 tries of seeing it, so one lost transfer ends all of a CTA's
+// roles in about a third of a millisecond instead of 2 s per pending wait.
 constexpr uint64_t kWaitTimeoutNs = 2000000000ull;
 constexpr uint32_t kWaitHintNs = 20000;
 static __device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity,
-                                                  uint64_t limit_ns) {
+                                                  uint64_t limit_ns, volatile int* abort) {
   const uint64_t t0 = global_timer_ns();
   for (uint32_t i = 0; i < (1u << 26); ++i) {
     if (mbar_try_wait_sleep(bar, parity, kWaitHintNs)) return true;
-    if ((i & 15u) == 15u && global_timer_ns() - t0 > limit_ns) return false;
+    if ((i & 15u) == 15u) {
+      if (abort != nullptr && *abort != 0) return false;
+      if (global_timer_ns() - t0 > limit_ns) break;
+    }
   }
+  if (abort != nullptr) *abort = 1;
   return false;
 }
 __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
-                                                  uint64_t limit_ns = kWaitTimeoutNs) {
+                                                  uint64_t limit_ns = kWaitTimeoutNs,
+                                                  volatile int* abort = nullptr) {
   if (mbar_try_wait(bar, parity)) return true;
-  return mbar_wait_slow(bar, parity, limit_ns);
+  return mbar_wait_slow(bar, parity, limit_ns, abort);
 }
 
 // ----------------------------------------------------------------- TMA

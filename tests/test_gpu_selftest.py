@@ -30,7 +30,9 @@ def test_bounded_wait_gives_up_and_reports_timeout():
     kvp.kvp_selftest_wait_timeout(status, 20_000_000)  # 20 ms
     assert kvp.kvp_read_status(status) == kvp.KVP_ERR_TIMEOUT
     elapsed = time.perf_counter() - t0
-    assert 0.015 < elapsed < 2.0, elapsed
+    # the second warp waits with the default 2 s limit but stops on the
+    # abort flag the first one sets: the launch ends well before 2 s
+    assert 0.015 < elapsed < 0.5, elapsed
     # the first error stays: a second timeout leaves the word as it is
     kvp.kvp_selftest_wait_timeout(status, 1_000_000)
     assert kvp.kvp_read_status(status) == kvp.KVP_ERR_TIMEOUT
