@@ -218,8 +218,12 @@ class ClockSampler:
 class Step:
     """Device buffers of one workload and the step through the public API."""
 
-    def __init__(self, w, kvp, dev, partition_blocks=0, fused=False, merge_runs=False):
+    def __init__(self, w, kvp, dev, partition_blocks=0, fused=False, merge_runs=False,
+                 shared_prefix=0):
         self.w, self.kvp, self.dev = w, kvp, dev
+        # > 0: the requests' first `shared_prefix` table entries are the same
+        # physical blocks, decoded by kvp_attention_decode_shared_prefix
+        self.shared = shared_prefix if not w.kv_int8 else 0
         # the run-merged fetch rides on the phases argument of every decode call
         self.flags = kvp.KVP_DECODE_MERGE_RUNS if merge_runs else 0
         # the fused step needs one new token per request at position n - 1
@@ -243,6 +247,9 @@ class Step:
         self.pb_arg = partition_blocks
         nb = kvp.kvp_decode_workspace_bytes(w.B, w.Hq, desc, w.max_blocks, partition_blocks,
                                             w.kv_int8 and not w.kv_fp8, w.kv_fp8)
+        if self.shared:
+            nb = kvp.kvp_decode_shared_prefix_workspace_bytes(w.B, w.Hq, desc, w.max_blocks,
+                                                              self.shared, partition_blocks)
         self.ws = torch.empty(max(nb // 4, 1), dtype=torch.float32, device=dev) if nb else None
         self.split = nb > 0
         self.part_blocks = (min(partition_blocks, w.max_blocks) if partition_blocks else
@@ -288,7 +295,8 @@ class Step:
 
     def launches_per_step(self) -> int:
         append = 0 if self.fused else 1
-        return (1 if self.pairs is not None else 0) + append + 1 + (1 if self.split else 0)
+        decode = 3 if self.shared else 1 + (1 if self.split else 0)  # (prefix pass, split, reduce)
+        return (1 if self.pairs is not None else 0) + append + decode
 
     def run(self, ev=None):
         """One step; ev = (e_decode_start, e_partial_end) events to record."""
@@ -318,6 +326,14 @@ class Step:
                            status=self.status)
         if ev is not None:
             ev[0].record()
+        if self.shared:
+            kvp.kvp_attention_decode_shared_prefix(self.out, self.q, self.kp, self.vp, self.tables,
+                                                   self.lens, w.scale, self.shared,
+                                                   workspace=self.ws, status=self.status,
+                                                   partition_blocks=self.pb_arg)
+            if ev is not None:
+                ev[1].record()
+            return
         phases = [kvp.KVP_PHASE_PARTIAL, kvp.KVP_PHASE_REDUCE] if self.split else [kvp.KVP_PHASE_ALL]
         for i, ph in enumerate(phases):
             if w.kv_int8:
@@ -441,8 +457,12 @@ def measure_decode(name, args, kvp, world, dev, local, headline):
     w = workloads.make(name, device=dev, nan_sentinel=False,
                        batch=args.batch if headline else None,
                        contiguity=args.contiguity if headline else None)
+    # the prefix-sharing workload's first 64 table entries are the shared
+    # prefix's full blocks (its partial last block is copied per request)
+    shared = (w.info["prefix_tokens"] // 16 if w.cow_pairs is not None and
+              not (headline and args.no_shared_prefix) else 0)
     step = Step(w, kvp, dev, args.partition_blocks if headline else 0, fused=not args.unfused,
-                merge_runs=headline and args.merge_runs)
+                merge_runs=headline and args.merge_runs, shared_prefix=shared)
     lens = [int(x) for x in w.context_lens]
     dbytes = decode_bytes(w, lens)
     sbytes = dbytes["call"] + append_bytes(w) + copy_bytes(w)
@@ -476,6 +496,7 @@ def measure_decode(name, args, kvp, world, dev, local, headline):
                    "max_context": max(lens), "new_tokens": int(w.slot_mapping.numel()),
                    "cow_pairs": int(w.cow_pairs.shape[0]) if w.cow_pairs is not None else 0,
                    "partition_blocks": step.part_blocks,
+                   "shared_prefix_blocks": step.shared,
                    "append": "fused into the decode" if step.fused else "separate kernel",
                    "fetch": "runs of consecutive blocks" if step.flags else "per block",
                    "l2": ("inputs larger than L2: {:.2f} GB of K/V per step vs 129 MB L2"
@@ -485,7 +506,8 @@ def measure_decode(name, args, kvp, world, dev, local, headline):
         "step_bytes": sbytes,
         "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak,
                      "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": traffic,
-                     "kernel": ("decode_fp8_umma_kernel" if w.kv_fp8 and w.D == 128
+                     "kernel": ("decode_fp8_umma_kernel" if w.kv_fp8 and w.D == 128 else
+                                "prefix pass + decode_partial_kernel + reduce" if step.shared
                                 else "decode_partial_kernel"), "peak_source": peak_src,
                      "algorithmic_bytes_per_launch": partial_bytes,
                      "launch_ms": round(partial_ms, 5),
@@ -952,6 +974,9 @@ def main():
                     help="time only the named workload (default for llama7b: also gqa70b, "
                          "int8long, fp8long, prefix and prefix_prefill, each in its own "
                          "timed region, reported under \"workloads\")")
+    ap.add_argument("--no-shared-prefix", action="store_true",
+                    help="decode the prefix-sharing workload per request instead of with its "
+                         "shared prefix attended once per kv head")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()

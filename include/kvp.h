@@ -350,6 +350,43 @@ kvp_status kvp_attention_prefill(void* out, const void* q, const void* k_cache,
                                  kvp_stream_t stream);
 
 /*
+ * kvp_decode_shared_prefix_workspace_bytes -- bytes of workspace
+ * kvp_attention_decode_shared_prefix needs for these sizes (0 for invalid
+ * sizes).  Same layout as the decode's workspace, with one more partition per
+ * (request, query head): the shared prefix's part.
+ */
+size_t kvp_decode_shared_prefix_workspace_bytes(int32_t batch, int32_t num_q_heads,
+                                                kvp_cache_desc cache, int32_t max_blocks_per_seq,
+                                                int32_t shared_prefix_blocks,
+                                                int32_t partition_blocks);
+
+/*
+ * kvp_attention_decode_shared_prefix -- kvp_attention_decode for a batch whose
+ * requests share a cached prompt prefix: the first shared_prefix_blocks table
+ * entries of every request name the same physical blocks ("ATB KV Cache
+ * management", "Prefix Caching": the shared prefix's K/V is cached once and
+ * reused by every request).  The result is the decode's (same definition, same
+ * tolerance); only the order of the sums differs.  The prefix's whole 128-token
+ * chunks are attended once per kv head for every request's query together, on
+ * the tensor cores, instead of once per request; the rest of each context runs
+ * as the ordinary split-context decode; a reduce merges the two.  Every
+ * context_lens[b] must cover the shared prefix (>= 16 * shared_prefix_blocks),
+ * and every request's table must name the first request's prefix blocks:
+ * otherwise the rows of the 128-row tile holding that request (128 / G
+ * requests of one kv head, G = Hq / Hkv) are zeros and *dev_status gets
+ * KVP_ERR_BAD_BLOCK.  A prefix shorter than 128 tokens, or a query group that
+ * does not divide 128, runs the ordinary decode.  fp16/bf16 pools only;
+ * workspace: >= kvp_decode_shared_prefix_workspace_bytes(...) bytes, 16-byte
+ * aligned (required).  Other arguments as kvp_attention_decode.
+ */
+kvp_status kvp_attention_decode_shared_prefix(
+    void* out, const void* q, const void* k_cache, const void* v_cache,
+    const int32_t* block_tables, int32_t max_blocks_per_seq, const int32_t* context_lens,
+    int32_t batch, int32_t num_q_heads, float scale, kvp_cache_desc cache, kvp_dtype dtype,
+    int32_t shared_prefix_blocks, int32_t partition_blocks, void* workspace,
+    size_t workspace_bytes, int32_t* dev_status, kvp_stream_t stream);
+
+/*
  * kvp_attention_decode_noalloc -- kvp_attention_decode for callers that cannot
  * allocate device memory.  (The pages have no counterpart: this entry point
  * exists for integration, not for the method.)

@@ -85,6 +85,9 @@ SIGNATURES = {
                                             _I32, _I32, _P, _P]),
     "kvp_attention_prefill": (_I32, [_P, _P, _P, _P, _P, _I32, _P, _P, _I32, _I32, _I32, _I32,
                                      _I32, _F, _D, _I32, _P, _P]),
+    "kvp_decode_shared_prefix_workspace_bytes": (_SZ, [_I32, _I32, _D, _I32, _I32, _I32]),
+    "kvp_attention_decode_shared_prefix": (_I32, [_P, _P, _P, _P, _P, _I32, _P, _I32, _I32, _F,
+                                                  _D, _I32, _I32, _I32, _P, _SZ, _P, _P]),
     "kvp_read_status": (_I32, [_P, _P]),
     "kvp_selftest_wait_timeout": (_I32, [_P, _I64, _P]),
     "kvp_bm_create": (_P, [_I32, _I32, _I64]),
@@ -280,6 +283,32 @@ def kvp_attention_decode(out, q, k_cache, v_cache, block_tables, context_lens, s
         int(block_tables.shape[1]), _ptr(context_lens), B, Hq, float(scale), cache_desc(k_cache),
         _dtype_code(q), int(partition_blocks), _ptr(workspace), ws_bytes, int(phases),
         _ptr(status), _stream_ptr(stream)), "kvp_attention_decode")
+
+
+def kvp_decode_shared_prefix_workspace_bytes(batch, num_q_heads, desc: kvp_cache_desc, max_blocks,
+                                             shared_prefix_blocks, partition_blocks=0) -> int:
+    return int(load_library().kvp_decode_shared_prefix_workspace_bytes(
+        int(batch), int(num_q_heads), desc, int(max_blocks), int(shared_prefix_blocks),
+        int(partition_blocks)))
+
+
+def kvp_attention_decode_shared_prefix(out, q, k_cache, v_cache, block_tables, context_lens,
+                                       scale, shared_prefix_blocks, *, workspace,
+                                       partition_blocks=0, status=None, stream=None) -> None:
+    """kvp_attention_decode for requests whose first shared_prefix_blocks table
+    entries name the same physical blocks (the prefix part runs once per kv
+    head for all requests)."""
+    lib = load_library()
+    _need_cuda(out, q, k_cache, v_cache, block_tables, context_lens, workspace, status)
+    if q.dtype != k_cache.dtype or out.dtype != q.dtype:
+        raise TypeError("q, out and the pools must share one dtype")
+    B, Hq, _ = (int(x) for x in q.shape)
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    _check(lib.kvp_attention_decode_shared_prefix(
+        _ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
+        int(block_tables.shape[1]), _ptr(context_lens), B, Hq, float(scale), cache_desc(k_cache),
+        _dtype_code(q), int(shared_prefix_blocks), int(partition_blocks), _ptr(workspace),
+        ws_bytes, _ptr(status), _stream_ptr(stream)), "kvp_attention_decode_shared_prefix")
 
 
 def kvp_append_attention_decode(key, value, out, q, k_cache, v_cache, block_tables, context_lens,

@@ -309,6 +309,48 @@ kvp_status decode_common(void* out, const void* q, bool q_bf16, int kv_kind, con
   return KVP_OK;
 }
 
+// A decode whose requests share their first `shared` table entries: the
+// prefix's full 128-token chunks (skip = 8 * floor(shared / 8) blocks) are one
+// dense pass per kv head over every request's query (tensor cores), written
+// as partition 0 of the workspace; the rest of each context is the ordinary
+// split decode over blocks skip .. n - 1, written as partitions 1 ...; the
+// reduce merges them.  skip == 0 (a prefix shorter than one chunk) or a group
+// that does not divide the 128-row tile: the ordinary decode.
+struct PrefixShape {
+  int skip;          // blocks covered by the prefix pass (0: ordinary decode)
+  DecodeShape suf;   // the split decode over the suffix (max_parts: its partitions)
+  int max_parts;     // workspace partitions per row: 1 + suf.max_parts
+  size_t ws_bytes;
+};
+
+kvp_status shape_prefix_decode(int batch, int hq, const kvp_cache_desc& c, int max_blocks,
+                               int shared, int partition_blocks, PrefixShape* out) {
+  if (shared < 0 || shared > max_blocks) return KVP_ERR_INVALID_ARG;
+  const kvp_status ds = check_desc(c);
+  if (ds != KVP_OK) return ds;
+  if (hq <= 0 || hq % c.num_kv_heads != 0) return KVP_ERR_INVALID_ARG;
+  const int group = hq / c.num_kv_heads;
+  PrefixShape s{};
+  s.skip = (128 % group == 0) ? shared / 8 * 8 : 0;
+  if (s.skip == max_blocks) s.skip -= 8;  // keep a suffix width of at least one block
+  if (s.skip <= 0) {
+    s.skip = 0;
+    const kvp_status r = shape_decode(batch, hq, c, max_blocks, partition_blocks, 0, &s.suf);
+    if (r != KVP_OK) return r;
+    s.max_parts = s.suf.max_parts;
+    s.ws_bytes = s.suf.ws_bytes;
+  } else {
+    const kvp_status r =
+        shape_decode(batch, hq, c, max_blocks - s.skip, partition_blocks, 0, &s.suf);
+    if (r != KVP_OK) return r;
+    s.max_parts = 1 + s.suf.max_parts;
+    s.ws_bytes = static_cast<size_t>(batch) * hq * s.max_parts *
+                 (static_cast<size_t>(c.head_dim) + 2) * sizeof(float);
+  }
+  *out = s;
+  return KVP_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -583,6 +625,127 @@ kvp_status kvp_attention_prefill(void* out, const void* q, const void* k_cache,
   p.prefix_chunks = shared_prefix_blocks * kBlockSize / 128;
   return from_cuda(launch_prefill(p, tq, tk, tv, to, dtype == KVP_BF16, static_cast<int>(tiles),
                                   reinterpret_cast<cudaStream_t>(stream)));
+}
+
+size_t kvp_decode_shared_prefix_workspace_bytes(int32_t batch, int32_t num_q_heads,
+                                                kvp_cache_desc cache, int32_t max_blocks_per_seq,
+                                                int32_t shared_prefix_blocks,
+                                                int32_t partition_blocks) {
+  PrefixShape sh;
+  if (batch < 0 || shape_prefix_decode(batch, num_q_heads, cache, max_blocks_per_seq,
+                                       shared_prefix_blocks, partition_blocks, &sh) != KVP_OK)
+    return 0;
+  return sh.ws_bytes;
+}
+
+kvp_status kvp_attention_decode_shared_prefix(
+    void* out, const void* q, const void* k_cache, const void* v_cache,
+    const int32_t* block_tables, int32_t max_blocks_per_seq, const int32_t* context_lens,
+    int32_t batch, int32_t num_q_heads, float scale, kvp_cache_desc cache, kvp_dtype dtype,
+    int32_t shared_prefix_blocks, int32_t partition_blocks, void* workspace,
+    size_t workspace_bytes, int32_t* dev_status, kvp_stream_t stream) {
+  KVP_NVTX_RANGE("kvp_attention_decode_shared_prefix");
+  if (dtype != KVP_F16 && dtype != KVP_BF16) return KVP_ERR_INVALID_ARG;
+  if (batch < 0 || max_blocks_per_seq <= 0) return KVP_ERR_INVALID_ARG;
+  PrefixShape sh;
+  kvp_status r = shape_prefix_decode(batch, num_q_heads, cache, max_blocks_per_seq,
+                                     shared_prefix_blocks, partition_blocks, &sh);
+  if (r != KVP_OK) return r;
+  if (sh.skip == 0)  // no whole chunk of shared prefix: the ordinary decode
+    return decode_common(out, q, dtype == KVP_BF16, dtype == KVP_BF16 ? 1 : 0, k_cache,
+                         v_cache, nullptr, nullptr, block_tables, max_blocks_per_seq,
+                         context_lens, batch, num_q_heads, scale, cache, partition_blocks,
+                         workspace, workspace_bytes, KVP_PHASE_PARTIAL | KVP_PHASE_REDUCE,
+                         dev_status, stream);
+  if (!std::isfinite(scale)) return KVP_ERR_INVALID_ARG;
+  if (batch == 0) return KVP_OK;
+  if (!out || !q || !k_cache || !v_cache || !block_tables || !context_lens)
+    return KVP_ERR_INVALID_ARG;
+  if (!aligned(out, 16) || !aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16))
+    return KVP_ERR_INVALID_ARG;
+  if (workspace == nullptr || workspace_bytes < sh.ws_bytes || !aligned(workspace, 16))
+    return KVP_ERR_INVALID_ARG;
+  const int group = num_q_heads / cache.num_kv_heads;
+  if (static_cast<long long>(cache.num_kv_heads) * sh.suf.qgroups > 65535 || batch > 65535)
+    return KVP_ERR_UNSUPPORTED;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  float* ws_o = static_cast<float*>(workspace);
+  float* ws_ml = ws_o + static_cast<size_t>(batch) * num_q_heads * sh.max_parts * cache.head_dim;
+
+  // 1. the prefix part: dense tiles of 128 (request, head) rows per kv head,
+  // the prefix's full chunks only, into partition 0
+  const int box_tokens = std::min(128 / group, static_cast<int>(batch));
+  CUtensorMap tq, tk, tv;
+  r = make_q_map(&tq, q, batch, num_q_heads, cache.head_dim, group, box_tokens);
+  if (r != KVP_OK) return r;
+  r = make_pool_map(&tk, k_cache, cache, 2);
+  if (r != KVP_OK) return r;
+  r = make_pool_map(&tv, v_cache, cache, 2);
+  if (r != KVP_OK) return r;
+  PrefillParams pp{};
+  pp.q = q;
+  pp.block_tables = block_tables;
+  pp.context_lens = context_lens;
+  pp.query_start = nullptr;  // one query per request
+  pp.status = dev_status;
+  pp.batch = batch;
+  pp.num_q_heads = num_q_heads;
+  pp.num_kv_heads = cache.num_kv_heads;
+  pp.head_dim = cache.head_dim;
+  pp.num_blocks = cache.num_blocks;
+  pp.max_blocks = max_blocks_per_seq;
+  pp.group = group;
+  pp.num_tokens = batch;
+  pp.q_box_tokens = box_tokens;
+  pp.scale_log2 = scale * 1.4426950408889634f;
+  pp.shared_blocks = shared_prefix_blocks;
+  pp.prefix_chunks = sh.skip / 8;
+  pp.partial = 1;
+  pp.part_stride = sh.max_parts;
+  pp.part_o = ws_o;
+  pp.part_ml = ws_ml;
+  const long long tiles = (static_cast<long long>(batch) * group + 127) / 128;
+  if (launch_prefill(pp, tq, tk, tv, tq, dtype == KVP_BF16, static_cast<int>(tiles), s) !=
+      cudaSuccess)
+    return KVP_ERR_CUDA;
+
+  // 2. the rest of every context: the split decode over blocks skip .. n - 1,
+  // into partitions 1 ...
+  DecodeParams p{};
+  p.out = out;
+  p.q = q;
+  p.block_tables = block_tables;
+  p.context_lens = context_lens;
+  p.ws_o = ws_o;
+  p.ws_ml = ws_ml;
+  p.status = dev_status;
+  p.batch = batch;
+  p.num_q_heads = num_q_heads;
+  p.num_kv_heads = cache.num_kv_heads;
+  p.head_dim = cache.head_dim;
+  p.num_blocks = cache.num_blocks;
+  p.max_blocks = max_blocks_per_seq;
+  p.group = group;
+  p.qgroups = sh.suf.qgroups;
+  p.heads_per_cta = sh.suf.heads_per_cta;
+  p.part_blocks = sh.suf.part_blocks;
+  p.max_parts = sh.max_parts;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  p.q_bf16 = dtype == KVP_BF16 ? 1 : 0;
+  p.k_pool = k_cache;
+  p.v_pool = v_cache;
+  p.skip_blocks = sh.skip;
+  DecodeMaps maps;
+  maps.merged = false;
+  maps.k = tk;
+  maps.v = tv;
+  cudaError_t e = sh.suf.path == DecodePath::kSimt
+                      ? launch_decode_simt(p, maps, dtype == KVP_BF16, sh.suf.max_parts, s)
+                      : launch_decode_mma(p, maps, dtype == KVP_BF16, sh.suf.max_parts, s);
+  if (e != cudaSuccess) return KVP_ERR_CUDA;
+  // 3. merge
+  if (launch_decode_reduce(p, s) != cudaSuccess) return KVP_ERR_CUDA;
+  return KVP_OK;
 }
 
 kvp_status kvp_selftest_wait_timeout(int32_t* dev_status, int64_t limit_ns,

@@ -690,8 +690,8 @@ __device__ __forceinline__ bool decode_prologue(const DecodeParams& p, const Dec
     return false;
   }
   const int nblk_seq = (c.n + kBlockSize - 1) / kBlockSize;
-  c.nparts = (nblk_seq + p.part_blocks - 1) / p.part_blocks;
-  const int blk0 = c.part * p.part_blocks;
+  c.nparts = (nblk_seq - p.skip_blocks + p.part_blocks - 1) / p.part_blocks;
+  const int blk0 = p.skip_blocks + c.part * p.part_blocks;
   if (blk0 >= nblk_seq) return false;
   c.nb = min(p.part_blocks, nblk_seq - blk0);
   c.last_part = blk0 + c.nb == nblk_seq;
@@ -759,7 +759,7 @@ __device__ __forceinline__ void decode_epilogue(const DecodeParams& p, const Dec
   __syncthreads();
 
   const size_t rowbase = static_cast<size_t>(c.b) * p.num_q_heads + c.head0;
-  if (c.nparts == 1) {
+  if (c.nparts == 1 && p.skip_blocks == 0) {
     uint16_t* out = static_cast<uint16_t*>(p.out) + rowbase * D;
     for (int idx = threadIdx.x; idx < c.nheads * D; idx += blockDim.x) {
       const int hh = idx / D, d = idx % D;
@@ -794,7 +794,7 @@ __device__ __forceinline__ void decode_epilogue(const DecodeParams& p, const Dec
           acc = fmaf(f, mo[(w * H + hh) * D + d], acc);
         }
       }
-      const size_t prow = (rowbase + hh) * p.max_parts + c.part;
+      const size_t prow = (rowbase + hh) * p.max_parts + c.part + (p.skip_blocks > 0 ? 1 : 0);
       p.ws_o[prow * D + d] = acc;
       if (d == 0) {
         p.ws_ml[2 * prow] = M;

@@ -57,6 +57,9 @@ struct DecodeParams {
   const void* new_v;
   const void* k_pool;           // pool base pointers (the fused append writes through them)
   const void* v_pool;
+  int32_t skip_blocks;          // > 0: blocks [0, skip) are partition 0 of the workspace,
+                                // written by another kernel (a shared prefix); this launch's
+                                // partitions cover [skip, n) and are written as 1, 2, ...
 };
 
 // Everything a multi-query (prefill / chunked-prefill) launch needs besides the
@@ -77,6 +80,14 @@ struct PrefillParams {
   int32_t shared_blocks;         // > 0: leading table entries shared by all requests
                                  // (dense tiles over the whole batch's rows)
   int32_t prefix_chunks;         // full 128-key chunks inside the shared prefix
+  // Decode over a shared prefix: query_start is null (one query per request,
+  // rows of q / out are requests), only the prefix chunks are read, and each
+  // row's unnormalised (o, m, l) goes to partition 0 of a decode workspace
+  // (part_o [rows, part_stride, D], part_ml [rows, part_stride, 2]) instead of out.
+  int32_t partial;
+  int32_t part_stride;
+  float* part_o;
+  float* part_ml;
 };
 
 // Pool maps of the run-merged decode fetch: 5-D views {row piece (<= 128

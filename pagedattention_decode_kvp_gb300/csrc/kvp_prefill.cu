@@ -79,6 +79,12 @@ struct Tile {
   int32_t status;   // error to record for this item (0 = none)
 };
 
+// query_start[r]; a decode over a shared prefix passes none: one query per
+// request, so request r's row is r.
+__device__ __forceinline__ int qstart(const PrefillParams& p, int r) {
+  return p.query_start != nullptr ? p.query_start[r] : r;
+}
+
 // The request lengths a per-request work item needs, loaded ahead of its turn.
 struct ItemLens {
   int q0, q1, n;
@@ -112,7 +118,8 @@ struct PrefillLayout {
   // and conflict-free for one-row-per-lane 16-byte writes
   static constexpr uint32_t kStgOff = kVOff + kVStages * kKV;
   static constexpr uint32_t kRedOff = kStgOff + kKV;  // [kRows] row sums
-  static constexpr uint32_t kSlotOff = kRedOff + kRows * 4;  // [kTileSlots] decoded work items
+  static constexpr uint32_t kMaxOff = kRedOff + kRows * 4;   // [kRows] row maxima (partial output)
+  static constexpr uint32_t kSlotOff = kMaxOff + kRows * 4;  // [kTileSlots] decoded work items
   static constexpr uint32_t kBarOff = kSlotOff + kTileSlots * kSlotBytes;
   // kfull[], vfull[], kempty[], vempty[], s[], p[], pv[2], q in TMEM, MMA
   // done, slot full[], slot empty[]
@@ -178,7 +185,7 @@ __device__ __forceinline__ ItemLens load_lens(const PrefillParams& p, int id) {
   if constexpr (kDense) return ItemLens{0, 0, 0};  // dense tiles load their own
   const int per_x = p.batch * p.num_kv_heads;
   const int b = (id % per_x) / p.num_kv_heads;
-  return ItemLens{p.query_start[b], p.query_start[b + 1], p.context_lens[b]};
+  return ItemLens{qstart(p, b), qstart(p, b + 1), p.context_lens[b]};
 }
 
 // The request whose query rows hold token t (query_start is non-decreasing,
@@ -188,7 +195,7 @@ __device__ __forceinline__ int request_of(const PrefillParams& p, int t) {
   int lo = 0, hi = p.batch;  // answer in [lo, hi]
   while (lo < hi) {
     const int mid = (lo + hi + 1) >> 1;
-    if (p.query_start[mid] <= t) lo = mid; else hi = mid - 1;
+    if (qstart(p, mid) <= t) lo = mid; else hi = mid - 1;
   }
   return lo;
 }
@@ -211,8 +218,8 @@ struct ChunkWalk {
 __device__ __forceinline__ void walk_prefetch(const PrefillParams& p, const Tile& t,
                                               ChunkWalk& w) {
   if (w.r <= t.r1) {
-    w.nq0 = p.query_start[w.r];
-    w.nq1 = p.query_start[w.r + 1];
+    w.nq0 = qstart(p, w.r);
+    w.nq1 = qstart(p, w.r + 1);
     w.nn = p.context_lens[w.r];
   }
 }
@@ -234,7 +241,7 @@ __device__ __forceinline__ void walk_start(const PrefillParams& p, const Tile& t
 // chunks: empty).
 __device__ __forceinline__ int walk_next(const PrefillParams& p, const Tile& t, ChunkWalk& w) {
   while (w.key >= w.end) {
-    if (w.r > t.r1) return -1;
+    if (w.r > t.r1 || p.partial) return -1;  // (a decode's prefix part: the prefix only)
     const int r = w.r++;
     const int q0 = w.nq0, q1 = w.nq1, n = w.nn;
     walk_prefetch(p, t, w);
@@ -262,7 +269,7 @@ __device__ __forceinline__ bool decode_tile(const PrefillParams& p, int tiles_x,
     const int x = id / p.num_kv_heads;
     t.kvh = id % p.num_kv_heads;
     t.t0 = x * tok_per_tile;
-    const int rows_end = p.query_start[p.batch];  // tokens past it belong to no request
+    const int rows_end = qstart(p, p.batch);  // tokens past it belong to no request
     if (x == 0 && t.kvh == 0 && rows_end > p.num_tokens) t.status = kErrBadBlock;
     if (rows_end > p.num_tokens || t.t0 >= rows_end) {  // rows outside q / out: touch nothing
       t.ntok = 0;
@@ -273,7 +280,7 @@ __device__ __forceinline__ bool decode_tile(const PrefillParams& p, int tiles_x,
     t.r1 = request_of(p, t.t0 + t.ntok - 1);
     // every request with rows here: lengths in range, the whole shared prefix cached
     for (int r = t.b; r <= t.r1; ++r) {
-      const int q0 = p.query_start[r], q1 = p.query_start[r + 1], n = p.context_lens[r];
+      const int q0 = qstart(p, r), q1 = qstart(p, r + 1), n = p.context_lens[r];
       if (q1 <= q0) continue;
       if (q1 - q0 > n || n > p.max_blocks * kBlockSize || n < p.shared_blocks * kBlockSize)
         t.lens_bad = true;
@@ -342,8 +349,8 @@ __device__ __forceinline__ void row_info(const PrefillParams& p, const Tile& t, 
   }
   const int tok = t.t0 + min(tk, t.ntok - 1);
   int r = t.b;
-  while (r < t.r1 && p.query_start[r + 1] <= tok) ++r;  // tiles span few requests
-  const int q0 = p.query_start[r], q1 = p.query_start[r + 1];
+  while (r < t.r1 && qstart(p, r + 1) <= tok) ++r;  // tiles span few requests
+  const int q0 = qstart(p, r), q1 = qstart(p, r + 1);
   req = r;
   pos = p.context_lens[r] - (q1 - q0) + (tok - q0);
 }
@@ -383,7 +390,7 @@ __device__ bool tile_ids_bad(const PrefillParams& p, const Tile& t, int lane) {
       const int32_t* t0 = p.block_tables + static_cast<size_t>(t.b) * p.max_blocks;
       for (int k = lane; k < (t.r1 - t.b) * p.shared_blocks; k += 32) {
         const int r = t.b + 1 + k / p.shared_blocks, i = k % p.shared_blocks;
-        if (p.query_start[r + 1] > p.query_start[r])
+        if (qstart(p, r + 1) > qstart(p, r))
           bad |= p.block_tables[static_cast<size_t>(r) * p.max_blocks + i] != t0[i];
       }
     }
@@ -467,6 +474,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(te_bar + kTileSlots);
   uint8_t* stg = sm + L::kStgOff;                                    // output staging
   float* red = reinterpret_cast<float*>(sm + L::kRedOff);            // row sums
+  float* mred = reinterpret_cast<float*>(sm + L::kMaxOff);           // row maxima
   auto slot_at = [&](uint32_t i) {
     return reinterpret_cast<TileSlot*>(sm + L::kSlotOff + (i % kTileSlots) * kSlotBytes);
   };
@@ -712,7 +720,21 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (t.nchunks == 0) {
       __syncwarp();
       mbar_arrive(smem_addr(slot_empty));
-      if (t.lens_bad) zero_tile_rows<D>(p, t, kSoftmaxThreads);
+      if (t.lens_bad) {
+        if (p.partial) {
+          // a decode's prefix part: the rows' partition 0 marked failed (the
+          // reduce writes them as zeros)
+          for (int r = tid; r < t.ntok * G; r += kSoftmaxThreads) {
+            const size_t prow =
+                (static_cast<size_t>(t.t0 + r / G) * p.num_q_heads + t.kvh * G + r % G) *
+                p.part_stride;
+            p.part_ml[2 * prow] = 0.f;
+            p.part_ml[2 * prow + 1] = -1.f;
+          }
+        } else {
+          zero_tile_rows<D>(p, t, kSoftmaxThreads);
+        }
+      }
       return;
     }
     const int n = t.nchunks;
@@ -960,8 +982,45 @@ __global__ void __launch_bounds__(kThreads, 1)
     if ((lane & 3) == 0) {
       red[ra] = la;
       red[rb] = lb;
+      mred[ra] = ma;
+      mred[rb] = mb;
     }
     ok = named_bar_and(1, kSoftmaxThreads, ok);
+    if (p.partial) {
+      // a decode's prefix part: row r of the tile is request t0 + r / G, head
+      // kvh * G + r % G; its unnormalised O, running max (log2 units) and row
+      // sum go to partition 0 of the decode workspace (a bad tile marks l < 0)
+      const int r = quarter * 32 + lane;
+      const int hf = warp >> 2;
+      if (ok) {  // (warp-uniform: the TMEM load is a whole-warp instruction)
+        const uint32_t tOr =
+            tmem + L::kOCol + hf * (D / 2) + (static_cast<uint32_t>(quarter * 32) << 16);
+        float o[D / 2];
+#pragma unroll
+        for (int c = 0; c < D / 64; ++c)
+          umma::ld32(tOr + c * 32, *reinterpret_cast<float(*)[32]>(o + c * 32));
+        umma::wait_ld();
+        if (r < t.ntok * G) {
+          const size_t prow =
+              (static_cast<size_t>(t.t0 + r / G) * p.num_q_heads + t.kvh * G + r % G) *
+              p.part_stride;
+          float4* dst = reinterpret_cast<float4*>(p.part_o + prow * D + hf * (D / 2));
+#pragma unroll
+          for (int c = 0; c < D / 8; ++c)
+            dst[c] = make_float4(o[4 * c], o[4 * c + 1], o[4 * c + 2], o[4 * c + 3]);
+          if (hf == 0) {
+            p.part_ml[2 * prow] = mred[r];
+            p.part_ml[2 * prow + 1] = bad ? -1.f : red[r];
+          }
+        }
+      }
+      // the next tile's first P V overwrites O: every thread has read its part
+      umma::fence_before_sync();
+      named_bar_sync(1, kSoftmaxThreads);
+      vc += n;
+      gc += n;
+      return;
+    }
     // thread (warp w, lane) finishes columns [D/2 (w / 4), +D/2) of row
     // 32 (w % 4) + lane: O read with the one-lane-per-row TMEM shape, scaled,
     // packed and staged
@@ -1043,8 +1102,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         if constexpr (kDense) {
           nreq = t.r1 - t.b + 1 <= kSlotReqs ? t.r1 - t.b + 1 : 0;
           if (lane < nreq) {
-            q0 = p.query_start[t.b + lane];
-            q1 = p.query_start[t.b + lane + 1];
+            q0 = qstart(p, t.b + lane);
+            q1 = qstart(p, t.b + lane + 1);
             nn = p.context_lens[t.b + lane];
           }
         }

@@ -31,8 +31,12 @@ __global__ void __launch_bounds__(256) decode_reduce_kernel(const DecodeParams p
   const int n = p.context_lens[b];
   if (n <= 0 || n > p.max_blocks * kBlockSize) return;  // written by the partition pass
   const int nblk = (n + kBlockSize - 1) / kBlockSize;
-  const int nparts = (nblk + p.part_blocks - 1) / p.part_blocks;
-  if (nparts <= 1) return;
+  // with a shared prefix (skip_blocks > 0) partition 0 holds the prefix part
+  // and the rest cover blocks skip .. nblk - 1; the row is always merged here
+  const int nparts = p.skip_blocks > 0
+                         ? 1 + (max(nblk - p.skip_blocks, 0) + p.part_blocks - 1) / p.part_blocks
+                         : (nblk + p.part_blocks - 1) / p.part_blocks;
+  if (nparts <= 1 && p.skip_blocks == 0) return;
 
   const float* ml = p.ws_ml + static_cast<size_t>(row) * p.max_parts * 2;
   const float* wo = p.ws_o + static_cast<size_t>(row) * p.max_parts * D + lane * E;
