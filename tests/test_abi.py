@@ -170,3 +170,28 @@ def test_prefill_invalid_arguments_fail_before_any_launch(lib):
     assert big == kvp.KVP_ERR_UNSUPPORTED
     assert call(mql=0) == kvp.KVP_OK
     assert call(T=0) == kvp.KVP_OK
+
+
+def test_shared_prefix_decode_sizing_and_validation(lib):
+    d = _desc(8192, 32, 16, 128)
+    # 64 shared blocks of a 97-block table: the prefix pass covers 64, the split
+    # decode the remaining 33 (one partition): two partitions per row
+    wsb = kvp.kvp_decode_shared_prefix_workspace_bytes(128, 32, d, 97, 64)
+    assert wsb == 128 * 32 * 2 * (128 + 2) * 4
+    # a prefix shorter than one 128-token chunk sizes the ordinary decode
+    assert kvp.kvp_decode_shared_prefix_workspace_bytes(128, 32, d, 97, 7) == \
+        kvp.kvp_decode_workspace_bytes(128, 32, d, 97)
+    # invalid sizes answer 0
+    assert kvp.kvp_decode_shared_prefix_workspace_bytes(128, 32, d, 97, 98) == 0
+    assert kvp.kvp_decode_shared_prefix_workspace_bytes(128, 32, d, 97, -1) == 0
+    P = None
+    A = ctypes.c_void_p(1 << 20)
+
+    def call(shared=64, dtype=0, ws_bytes=wsb, ws=A, batch=128, mb=97):
+        return lib.kvp_attention_decode_shared_prefix(A, A, A, A, A, mb, A, batch, 32, 0.125, d,
+                                                      dtype, shared, 0, ws, ws_bytes, P, P)
+    assert call(dtype=2) == kvp.KVP_ERR_INVALID_ARG          # 8-bit codes: not this call
+    assert call(shared=98) == kvp.KVP_ERR_INVALID_ARG        # more than the table
+    assert call(ws_bytes=wsb - 16) == kvp.KVP_ERR_INVALID_ARG
+    assert call(ws=P) == kvp.KVP_ERR_INVALID_ARG
+    assert call(batch=0) == kvp.KVP_OK
