@@ -680,7 +680,12 @@ __device__ __forceinline__ bool decode_prologue(const DecodeParams& p, const Dec
   c.head0 = c.kvh * p.group + qg * p.heads_per_cta;
   c.nheads = min(p.heads_per_cta, p.group - qg * p.heads_per_cta);
 
-  grid_dependency_wait();  // the previous kernel (e.g. the append) has landed
+  // the previous kernel (e.g. the append) has landed.  Behind a shared
+  // prefix's pass (skip_blocks > 0) the wait moves to the CTA's end instead:
+  // that pass -- a plain launch, so the append had landed before it began --
+  // writes only partition 0, which this kernel never reads, so the two run
+  // side by side; the reduce after this kernel then finds both written
+  if (p.skip_blocks == 0) grid_dependency_wait();
   c.n = p.context_lens[c.b];
   if (c.n <= 0 || c.n > p.max_blocks * kBlockSize) {
     if (c.part == 0) {
@@ -837,8 +842,10 @@ __global__ void __launch_bounds__(kWarps * 32)
         prefetch_tensormap(&tmv);
 #pragma unroll
         for (int s = 0; s < S; ++s) mbar_init(smem_addr(sm.bars + s), 1);
-      }))
+      })) {
+    if (p.skip_blocks > 0) grid_dependency_wait();  // (see decode_prologue)
     return;
+  }
 
   const float* ksrc = p.k_scale;
   const float* vsrc = p.v_scale;
@@ -911,6 +918,7 @@ __global__ void __launch_bounds__(kWarps * 32)
     set_status(p.status, kErrBadBlock);
   }
 
+  if (p.skip_blocks > 0) grid_dependency_wait();  // (see decode_prologue)
   launch_dependents();
   __syncthreads();
   decode_epilogue<Path>(p, sm, c, st, any_bad || cta_flag != 0);
@@ -964,8 +972,10 @@ __global__ void __launch_bounds__(kWarps * 32)
           mbar_init(smem_addr(full + s), 1);
           mbar_init(smem_addr(empty + s), kWarps);
         }
-      }))
+      })) {
+    if (p.skip_blocks > 0) grid_dependency_wait();  // (see decode_prologue)
     return;
+  }
 
   const int ngroups = (c.nb + kWarps - 1) / kWarps;
   // thread 0: fetch group g into group stage g % kGS
@@ -1054,6 +1064,7 @@ __global__ void __launch_bounds__(kWarps * 32)
     set_status(p.status, kErrBadBlock);
   }
 
+  if (p.skip_blocks > 0) grid_dependency_wait();  // (see decode_prologue)
   launch_dependents();
   __syncthreads();
   decode_epilogue<Path>(p, sm, c, st, any_bad || cta_flag != 0);

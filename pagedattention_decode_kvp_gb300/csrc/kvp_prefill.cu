@@ -510,6 +510,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   umma::fence_after_sync();
   const uint32_t tmem = *tmem_slot;
   grid_dependency_wait();
+  // a decode's prefix pass: the split decode behind it reads nothing this
+  // kernel writes, so it may start at once (it waits for this kernel before
+  // it exits, so the reduce after it finds partition 0 written)
+  if (p.partial) launch_dependents();
   bool ok = true;
 
   // ---- per-role state, kept across work items
