@@ -571,16 +571,29 @@ def decode_cpu_baseline(w, step, rows_all, rows_one):
 
 def run_e2e(step, host_keys, args, world, dev, unit_total, unit_scale, unit):
     """The same steps end to end through the public API: every step copies its
-    inputs in from pinned host memory and its output back, then waits."""
-    host = {k: getattr(step, k).cpu().pin_memory() for k in host_keys
-            if getattr(step, k, None) is not None}
+    inputs in from pinned host memory and its output back, then waits.  The
+    inputs sit in one pinned host buffer (each 256-byte aligned) and the step's
+    device inputs are views of one device buffer, so a step's inputs travel in
+    one copy."""
+    keys = [k for k in host_keys if getattr(step, k, None) is not None]
+    offs, total = {}, 0
+    for k in keys:
+        t = getattr(step, k)
+        offs[k] = total
+        total += (t.numel() * t.element_size() + 255) // 256 * 256
+    host_buf = torch.zeros(max(total, 256), dtype=torch.uint8).pin_memory()
+    dev_buf = torch.empty(max(total, 256), dtype=torch.uint8, device=dev)
+    for k in keys:
+        t = getattr(step, k).contiguous()
+        nb = t.numel() * t.element_size()
+        host_buf[offs[k]:offs[k] + nb].copy_(t.reshape(-1).view(torch.uint8).cpu())
+        setattr(step, k, dev_buf[offs[k]:offs[k] + nb].view(t.dtype).view(t.shape))
     out_host = torch.empty(step.out.shape, dtype=step.out.dtype).pin_memory()
-    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    h2d = int(host_buf.numel())
     d2h = out_host.numel() * out_host.element_size()
 
     def e2e_step():
-        for k, t in host.items():
-            getattr(step, k).copy_(t, non_blocking=True)
+        dev_buf.copy_(host_buf, non_blocking=True)
         step.run()
         out_host.copy_(step.out, non_blocking=True)
         torch.cuda.current_stream().synchronize()
