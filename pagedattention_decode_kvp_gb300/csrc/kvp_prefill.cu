@@ -278,12 +278,23 @@ __device__ __forceinline__ bool decode_tile(const PrefillParams& p, int tiles_x,
     t.ntok = min(tok_per_tile, rows_end - t.t0);
     t.b = request_of(p, t.t0);
     t.r1 = request_of(p, t.t0 + t.ntok - 1);
-    // every request with rows here: lengths in range, the whole shared prefix cached
-    for (int r = t.b; r <= t.r1; ++r) {
-      const int q0 = qstart(p, r), q1 = qstart(p, r + 1), n = p.context_lens[r];
-      if (q1 <= q0) continue;
-      if (q1 - q0 > n || n > p.max_blocks * kBlockSize || n < p.shared_blocks * kBlockSize)
-        t.lens_bad = true;
+    // every request with rows here: lengths in range, the whole shared prefix
+    // cached (eight requests' lengths loaded before any is compared: a tile of
+    // a decode's prefix pass holds up to 128 requests)
+    for (int r0 = t.b; r0 <= t.r1; r0 += 8) {
+      int q0[8], q1[8], nn[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const bool in = r0 + u <= t.r1;
+        q0[u] = in ? qstart(p, r0 + u) : 0;
+        q1[u] = in ? qstart(p, r0 + u + 1) : 0;
+        nn[u] = in ? p.context_lens[r0 + u] : 0;
+      }
+#pragma unroll
+      for (int u = 0; u < 8; ++u)
+        if (q1[u] > q0[u] && (q1[u] - q0[u] > nn[u] || nn[u] > p.max_blocks * kBlockSize ||
+                              nn[u] < p.shared_blocks * kBlockSize))
+          t.lens_bad = true;
     }
     if (t.lens_bad) {
       t.status = kErrBadBlock;
@@ -387,11 +398,25 @@ __device__ bool tile_ids_bad(const PrefillParams& p, const Tile& t, int lane) {
   bool bad = false;
   if constexpr (kDense) {
     if (t.r1 > t.b) {
+      // entries lane-strided, 16 requests' loaded before any is compared: a
+      // tile of a decode's prefix pass holds up to 128 requests, and one
+      // dependent load per request would take tens of microseconds
       const int32_t* t0 = p.block_tables + static_cast<size_t>(t.b) * p.max_blocks;
-      for (int k = lane; k < (t.r1 - t.b) * p.shared_blocks; k += 32) {
-        const int r = t.b + 1 + k / p.shared_blocks, i = k % p.shared_blocks;
-        if (qstart(p, r + 1) > qstart(p, r))
-          bad |= p.block_tables[static_cast<size_t>(r) * p.max_blocks + i] != t0[i];
+      constexpr int kU = 16;
+      for (int i = lane; i < p.shared_blocks; i += 32) {
+        const int want = t0[i];
+        for (int r0 = t.b + 1; r0 <= t.r1; r0 += kU) {
+          int got[kU];
+          bool live[kU];
+#pragma unroll
+          for (int u = 0; u < kU; ++u) {
+            const int r = r0 + u;
+            live[u] = r <= t.r1 && qstart(p, r + 1) > qstart(p, r);
+            got[u] = live[u] ? p.block_tables[static_cast<size_t>(r) * p.max_blocks + i] : want;
+          }
+#pragma unroll
+          for (int u = 0; u < kU; ++u) bad |= got[u] != want;
+        }
       }
     }
     ChunkWalk cw;
