@@ -52,6 +52,8 @@ KERNEL_SOURCES = ["kvp_decode.cuh", "kvp_device.cuh", "kvp_decode_simt.cu", "kvp
                   "kvp_decode_int8.cu", "kvp_decode_fp8.cu", "kvp_decode_fp8_umma.cu",
                   "kvp_umma.cuh", "kvp_internal.h"]
 PREFILL_SOURCES = ["kvp_prefill.cu", "kvp_umma.cuh", "kvp_device.cuh", "kvp_internal.h"]
+# the shared-prefix decode runs the prefill kernel's prefix pass and the reduce too
+SHARED_DECODE_SOURCES = KERNEL_SOURCES + ["kvp_prefill.cu", "kvp_reduce.cu"]
 
 
 # ------------------------------------------------------------------ byte model
@@ -482,7 +484,8 @@ def measure_decode(name, args, kvp, world, dev, local, headline):
     achieved = partial_bytes / (partial_ms / 1e3) / 1e9
     # the committed counters are for the full-size workloads only
     full_size = not (headline and (args.batch or args.contiguity is not None))
-    traffic = profiled_traffic(name) if full_size else None
+    traffic = (profiled_traffic(name, SHARED_DECODE_SOURCES if step.shared else None)
+               if full_size else None)
     m = {
         "value": round(value, 2),
         "unit": "GB/s",
