@@ -257,6 +257,30 @@ __device__ __forceinline__ int walk_next(const PrefillParams& p, const Tile& t, 
   return key;
 }
 
+// Whether a request among r0 .. r1 (those with query rows) has lengths out of
+// range for a dense tile: kB requests' lengths are loaded before any is
+// compared, so each batch waits one global-load latency.
+template <int kB>
+__device__ __forceinline__ bool lens_out_of_range(const PrefillParams& p, int r0, int r1) {
+  bool bad = false;
+  for (; r0 <= r1; r0 += kB) {
+    int q0[kB], q1[kB], nn[kB];
+#pragma unroll
+    for (int u = 0; u < kB; ++u) {
+      const bool in = r0 + u <= r1;
+      q0[u] = in ? qstart(p, r0 + u) : 0;
+      q1[u] = in ? qstart(p, r0 + u + 1) : 0;
+      nn[u] = in ? p.context_lens[r0 + u] : 0;
+    }
+#pragma unroll
+    for (int u = 0; u < kB; ++u)
+      if (q1[u] > q0[u] && (q1[u] - q0[u] > nn[u] || nn[u] > p.max_blocks * kBlockSize ||
+                            nn[u] < p.shared_blocks * kBlockSize))
+        bad = true;
+  }
+  return bad;
+}
+
 // Returns false when the item has no rows.
 template <bool kDense>
 __device__ __forceinline__ bool decode_tile(const PrefillParams& p, int tiles_x, int id,
@@ -279,23 +303,10 @@ __device__ __forceinline__ bool decode_tile(const PrefillParams& p, int tiles_x,
     t.b = request_of(p, t.t0);
     t.r1 = request_of(p, t.t0 + t.ntok - 1);
     // every request with rows here: lengths in range, the whole shared prefix
-    // cached (eight requests' lengths loaded before any is compared: a tile of
-    // a decode's prefix pass holds up to 128 requests)
-    for (int r0 = t.b; r0 <= t.r1; r0 += 8) {
-      int q0[8], q1[8], nn[8];
-#pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        const bool in = r0 + u <= t.r1;
-        q0[u] = in ? qstart(p, r0 + u) : 0;
-        q1[u] = in ? qstart(p, r0 + u + 1) : 0;
-        nn[u] = in ? p.context_lens[r0 + u] : 0;
-      }
-#pragma unroll
-      for (int u = 0; u < 8; ++u)
-        if (q1[u] > q0[u] && (q1[u] - q0[u] > nn[u] || nn[u] > p.max_blocks * kBlockSize ||
-                              nn[u] < p.shared_blocks * kBlockSize))
-          t.lens_bad = true;
-    }
+    // cached (a prompt tile holds a few requests; a tile of a decode's prefix
+    // pass up to 128: checked in batches of 32)
+    t.lens_bad = t.r1 - t.b < 8 ? lens_out_of_range<8>(p, t.b, t.r1)
+                                : lens_out_of_range<32>(p, t.b, t.r1);
     if (t.lens_bad) {
       t.status = kErrBadBlock;
       return true;
@@ -389,6 +400,31 @@ __device__ __forceinline__ void row_info_slot(const PrefillParams& p, const Tile
   pos = ts.n[i] - (ts.q1[i] - ts.q0[i]) + (tok - ts.q0[i]);
 }
 
+// (dense tiles) Whether a request b + 1 .. r1 with rows in tile t names other
+// blocks for the shared prefix than request b: the lane's entries, kU
+// requests' loaded at a time.
+template <int kU>
+__device__ __forceinline__ bool prefix_tables_differ(const PrefillParams& p, const Tile& t,
+                                                     int lane) {
+  bool bad = false;
+  const int32_t* t0 = p.block_tables + static_cast<size_t>(t.b) * p.max_blocks;
+  for (int i = lane; i < p.shared_blocks; i += 32) {
+    const int want = t0[i];
+    for (int r0 = t.b + 1; r0 <= t.r1; r0 += kU) {
+      int got[kU];
+#pragma unroll
+      for (int u = 0; u < kU; ++u) {
+        const int r = r0 + u;
+        const bool live = r <= t.r1 && qstart(p, r + 1) > qstart(p, r);
+        got[u] = live ? p.block_tables[static_cast<size_t>(r) * p.max_blocks + i] : want;
+      }
+#pragma unroll
+      for (int u = 0; u < kU; ++u) bad |= got[u] != want;
+    }
+  }
+  return bad;
+}
+
 // Whether a tile reads a block id out of range (every segment's ids), or --
 // dense tiles -- a request with rows in it names other blocks for the shared
 // prefix than the tile's first request, whose table the prefix is read
@@ -398,26 +434,12 @@ __device__ bool tile_ids_bad(const PrefillParams& p, const Tile& t, int lane) {
   bool bad = false;
   if constexpr (kDense) {
     if (t.r1 > t.b) {
-      // entries lane-strided, 16 requests' loaded before any is compared: a
-      // tile of a decode's prefix pass holds up to 128 requests, and one
-      // dependent load per request would take tens of microseconds
-      const int32_t* t0 = p.block_tables + static_cast<size_t>(t.b) * p.max_blocks;
-      constexpr int kU = 16;
-      for (int i = lane; i < p.shared_blocks; i += 32) {
-        const int want = t0[i];
-        for (int r0 = t.b + 1; r0 <= t.r1; r0 += kU) {
-          int got[kU];
-          bool live[kU];
-#pragma unroll
-          for (int u = 0; u < kU; ++u) {
-            const int r = r0 + u;
-            live[u] = r <= t.r1 && qstart(p, r + 1) > qstart(p, r);
-            got[u] = live[u] ? p.block_tables[static_cast<size_t>(r) * p.max_blocks + i] : want;
-          }
-#pragma unroll
-          for (int u = 0; u < kU; ++u) bad |= got[u] != want;
-        }
-      }
+      // entries lane-strided, a batch of requests' loaded before any is
+      // compared (4 for a prompt tile's few requests, 32 for the up to 128 of
+      // a decode's prefix pass): one dependent load per request would take
+      // tens of microseconds
+      bad = t.r1 - t.b < 8 ? prefix_tables_differ<4>(p, t, lane)
+                           : prefix_tables_differ<32>(p, t, lane);
     }
     ChunkWalk cw;
     walk_start(p, t, cw);

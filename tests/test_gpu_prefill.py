@@ -8,9 +8,10 @@ Cases span several 128-row query tiles and 128-key chunks with ragged tails
 (full tiles leave through a TMA store, partial ones through plain stores), a
 whole-prompt prefill, chunks that start mid-context, single-token chunks, empty
 chunks, NaN in every pool slot no request owns, a sparse work list longer than
-one scan window per block, and the data errors the header documents.  With a
-shared prompt prefix the rows of all requests are packed into dense tiles; that
-mode must equal the per-request tiles bit for bit."""
+one scan window per block, rows whose running maximum jumps between chunks (the
+lazy rescale of O and the row sums), and the data errors the header documents.
+With a shared prompt prefix the rows of all requests are packed into dense
+tiles; that mode must equal the per-request tiles bit for bit."""
 import numpy as np
 import pytest
 import torch
@@ -127,6 +128,41 @@ def test_prefill_is_deterministic():
     a = run_gpu(w)
     b = run_gpu(w)
     assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+
+
+def _plant_score_jumps(w, amp=8.0, step=12.0, period=5):
+    """Scores that jump between chunks: K's first component is step * (c % period)
+    at the keys of chunk c (positions 128 c .. 128 c + 127, through each
+    request's table), q's first component +amp for even heads and -amp for odd
+    ones.  An even head's scores then rise by amp * step * scale = 8.5 (12.2 in
+    log2 units, past the 2^8 the running maximum may lag by) at each chunk of a
+    period, so O and the row sums are rescaled chunk after chunk; an odd head
+    keeps its first chunk's maximum."""
+    k = w.k_pool.clone()
+    tables = w.block_tables.cpu()
+    for b in range(w.B):
+        pos = torch.arange(int(w.context_lens[b]))
+        blk = tables[b, pos // 16].long()
+        k[blk, :, pos % 16, 0] = (step * ((pos // 128) % period)).to(k.dtype)[:, None]
+    q = w.q.clone()
+    q[:, 0::2, 0] = amp
+    q[:, 1::2, 0] = -amp
+    w.k_pool, w.q = k, q
+
+
+@pytest.mark.parametrize("dtype", [torch.float16, torch.bfloat16])
+@pytest.mark.parametrize("D,shared", [(128, 0), (64, 0), (128, 16)])
+def test_rows_whose_maximum_jumps_between_chunks(dtype, D, shared):
+    lens, qlens = [1100, 900, 700, 300], [1100, 300, 64, 300]
+    w = workloads.make_prefill(B=4, Hq=8, Hkv=2, D=D, lens=lens, qlens=qlens, num_blocks=220,
+                               dtype=dtype, seed=41 + D + shared, shared_blocks=shared)
+    _plant_score_jumps(w)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out = run_gpu(w, status=status, shared=shared)
+    assert kvp.kvp_read_status(status) == kvp.KVP_OK
+    ref = oracle.attention_prefill(w.q, w.k_pool, w.v_pool, w.block_tables, w.context_lens,
+                                   w.query_start, w.scale)
+    assert_close(out, ref, f"max jumps {dtype} D{D} shared {shared}")
 
 
 def test_chunk_longer_than_context_sets_status_and_zeroes_rows():
