@@ -660,6 +660,13 @@ __device__ __forceinline__ DecodeSmem decode_smem(uint8_t* smem_raw) {
   return m;
 }
 
+// Behind a shared prefix's pass: the grid's first CTA waits for that pass
+// before it exits (see decode_prologue).
+__device__ __forceinline__ void shared_prefix_exit_wait(const DecodeParams& p) {
+  if (p.skip_blocks > 0 && blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0)
+    dev::grid_dependency_wait();
+}
+
 // Prologue shared by both pipelines: which work this CTA has, the partition's
 // block ids staged in shared memory and range-checked ("踩坑一": the page table
 // is copied on chip once, not looked up in HBM per page), and the fused
@@ -681,10 +688,12 @@ __device__ __forceinline__ bool decode_prologue(const DecodeParams& p, const Dec
   c.nheads = min(p.heads_per_cta, p.group - qg * p.heads_per_cta);
 
   // the previous kernel (e.g. the append) has landed.  Behind a shared
-  // prefix's pass (skip_blocks > 0) the wait moves to the CTA's end instead:
-  // that pass -- a plain launch, so the append had landed before it began --
-  // writes only partition 0, which this kernel never reads, so the two run
-  // side by side; the reduce after this kernel then finds both written
+  // prefix's pass (skip_blocks > 0) the two run side by side instead: that
+  // pass -- a plain launch, so the append had landed before it began --
+  // writes only partition 0, which this kernel never reads; the grid's first
+  // CTA waits for it before it exits (shared_prefix_exit_wait), so this grid
+  // completes after it and the reduce behind finds both written, while every
+  // other CTA leaves its SM as soon as it is done
   if (p.skip_blocks == 0) grid_dependency_wait();
   c.n = p.context_lens[c.b];
   if (c.n <= 0 || c.n > p.max_blocks * kBlockSize) {
@@ -843,7 +852,7 @@ __global__ void __launch_bounds__(kWarps * 32)
 #pragma unroll
         for (int s = 0; s < S; ++s) mbar_init(smem_addr(sm.bars + s), 1);
       })) {
-    if (p.skip_blocks > 0) grid_dependency_wait();  // (see decode_prologue)
+    shared_prefix_exit_wait(p);
     return;
   }
 
@@ -918,7 +927,7 @@ __global__ void __launch_bounds__(kWarps * 32)
     set_status(p.status, kErrBadBlock);
   }
 
-  if (p.skip_blocks > 0) grid_dependency_wait();  // (see decode_prologue)
+  shared_prefix_exit_wait(p);
   launch_dependents();
   __syncthreads();
   decode_epilogue<Path>(p, sm, c, st, any_bad || cta_flag != 0);
@@ -973,7 +982,7 @@ __global__ void __launch_bounds__(kWarps * 32)
           mbar_init(smem_addr(empty + s), kWarps);
         }
       })) {
-    if (p.skip_blocks > 0) grid_dependency_wait();  // (see decode_prologue)
+    shared_prefix_exit_wait(p);
     return;
   }
 
@@ -1064,7 +1073,7 @@ __global__ void __launch_bounds__(kWarps * 32)
     set_status(p.status, kErrBadBlock);
   }
 
-  if (p.skip_blocks > 0) grid_dependency_wait();  // (see decode_prologue)
+  shared_prefix_exit_wait(p);
   launch_dependents();
   __syncthreads();
   decode_epilogue<Path>(p, sm, c, st, any_bad || cta_flag != 0);
