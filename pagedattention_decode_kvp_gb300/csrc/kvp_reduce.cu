@@ -97,9 +97,86 @@ __global__ void __launch_bounds__(256) decode_reduce_kernel(const DecodeParams p
   }
 }
 
+// One warp per row, for splits of at most 8 partitions (most rows of a
+// short or medium context), eight rows per CTA: a block of 256 threads per row
+// would spend its time being scheduled and synchronised.  Lane i holds
+// partition i's (m, l); every lane accumulates its D/32 output elements over
+// the partitions in order (independent loads), multiplying and adding
+// separately, so a row comes out bit for bit as decode_reduce_kernel writes
+// it (one partition per warp there, summed in warp order).
+template <int D, bool kBf16Out>
+__global__ void __launch_bounds__(256) decode_reduce_warp_kernel(const DecodeParams p) {
+  constexpr int E = D / 32;  // output elements per lane
+  constexpr int kMaxParts = 8;
+  dev::grid_dependency_wait();  // the partition pass has written the workspace
+  dev::launch_dependents();
+  const int lane = threadIdx.x & 31;
+  const int row = blockIdx.x * 8 + (threadIdx.x >> 5);  // (b, h) flattened
+  if (row >= p.batch * p.num_q_heads) return;
+  const int b = row / p.num_q_heads;
+  const int n = p.context_lens[b];
+  if (n <= 0 || n > p.max_blocks * kBlockSize) return;  // written by the partition pass
+  const int nblk = (n + kBlockSize - 1) / kBlockSize;
+  const int nparts = p.skip_blocks > 0
+                         ? 1 + (max(nblk - p.skip_blocks, 0) + p.part_blocks - 1) / p.part_blocks
+                         : (nblk + p.part_blocks - 1) / p.part_blocks;
+  if (nparts <= 1 && p.skip_blocks == 0) return;
+
+  const float* ml = p.ws_ml + static_cast<size_t>(row) * p.max_parts * 2;
+  const float* wo = p.ws_o + static_cast<size_t>(row) * p.max_parts * D + lane * E;
+  float2 v = make_float2(-INFINITY, 0.f);
+  if (lane < nparts) v = *reinterpret_cast<const float2*>(ml + 2 * lane);
+  const float M = dev::warp_max(v.x);
+  const bool bad = __any_sync(0xffffffffu, lane < nparts && v.y < 0.f);
+
+  float acc[E];
+#pragma unroll
+  for (int e = 0; e < E; ++e) acc[e] = 0.f;
+  float L = 0.f;
+  if (!bad) {
+#pragma unroll
+    for (int i = 0; i < kMaxParts; ++i) {
+      if (i < nparts) {
+        const float f = exp2f(__shfl_sync(0xffffffffu, v.x, i) - M);
+        L = __fadd_rn(L, __fmul_rn(f, __shfl_sync(0xffffffffu, v.y, i)));
+        float x[E];
+        if constexpr (E == 4) {
+          const float4 t = *reinterpret_cast<const float4*>(wo + static_cast<size_t>(i) * D);
+          x[0] = t.x;
+          x[1] = t.y;
+          x[2] = t.z;
+          x[3] = t.w;
+        } else {
+          const float2 t = *reinterpret_cast<const float2*>(wo + static_cast<size_t>(i) * D);
+          x[0] = t.x;
+          x[1] = t.y;
+        }
+#pragma unroll
+        for (int e = 0; e < E; ++e) acc[e] = __fadd_rn(acc[e], __fmul_rn(f, x[e]));
+      }
+    }
+  }
+  uint16_t* out = static_cast<uint16_t*>(p.out) + static_cast<size_t>(row) * D + lane * E;
+#pragma unroll
+  for (int e = 0; e < E; ++e)
+    out[e] = dev::from_float<kBf16Out>((!bad && L > 0.f) ? acc[e] / L : 0.f);
+}
+
 cudaError_t launch_decode_reduce(const DecodeParams& p, cudaStream_t s) {
-  const dim3 grid(p.batch * p.num_q_heads);
   const dim3 block(256);
+  if (p.max_parts <= 8) {  // every row has at most 8 partitions: a warp per row
+    const dim3 grid((p.batch * p.num_q_heads + 7) / 8);
+    if (p.head_dim == 64) {
+      return p.q_bf16 ? launch_pdl(decode_reduce_warp_kernel<64, true>, grid, block, 0, s, p)
+                      : launch_pdl(decode_reduce_warp_kernel<64, false>, grid, block, 0, s, p);
+    }
+    if (p.head_dim == 128) {
+      return p.q_bf16 ? launch_pdl(decode_reduce_warp_kernel<128, true>, grid, block, 0, s, p)
+                      : launch_pdl(decode_reduce_warp_kernel<128, false>, grid, block, 0, s, p);
+    }
+    return cudaErrorInvalidValue;
+  }
+  const dim3 grid(p.batch * p.num_q_heads);
   if (p.head_dim == 64) {
     return p.q_bf16 ? launch_pdl(decode_reduce_kernel<64, true>, grid, block, 0, s, p)
                     : launch_pdl(decode_reduce_kernel<64, false>, grid, block, 0, s, p);
