@@ -150,6 +150,26 @@ def test_split_phases_equal_single_call():
     assert same_bits(out, out_all)
 
 
+@pytest.mark.parametrize("dtype", [torch.float16, torch.bfloat16])
+@pytest.mark.parametrize("D", [64, 128])
+def test_warp_reduce_equals_cta_reduce(dtype, D):
+    """Rows are merged by one warp each when no row can have more than 8
+    partitions (max_blocks / partition_blocks <= 8), by a CTA each otherwise;
+    both write the same bits, so the same workload with its table padded past
+    8 partitions' width gives the same output."""
+    lens = [1024, 1000, 513, 17, 129, 0, 777]
+    w = workloads.make_custom(B=len(lens), Hq=16, Hkv=2, D=D, lens=lens, num_blocks=400,
+                              dtype=dtype, seed=D + 13, max_blocks=64)
+    out_warp, _, _ = gpu_decode_16(w, 8)
+    w.block_tables = torch.cat([w.block_tables, torch.zeros((w.B, 8), dtype=torch.int32)], 1)
+    assert w.max_blocks == 72
+    out_cta, kp, vp = gpu_decode_16(w, 8)
+    assert same_bits(out_warp, out_cta)
+    okp, ovp = oracle_pools_16(w)
+    ref = oracle.attention_decode(w.q, okp, ovp, w.block_tables, w.context_lens, w.scale)
+    assert_attn_close(out_warp, ref, f"warp reduce {dtype} D{D}")
+
+
 def test_decode_is_deterministic():
     w = workloads.make_custom(B=4, Hq=8, Hkv=8, D=128, lens=[4000, 10, 2500, 1234],
                               num_blocks=700, dtype=torch.float16, seed=8)
