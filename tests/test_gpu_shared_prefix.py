@@ -128,6 +128,28 @@ def test_prefix_tables_that_disagree_set_status_and_zero_rows():
     assert (g[2] == 0).all()
 
 
+@pytest.mark.parametrize("bad_req", [1, 9, 33, 39])
+def test_wide_tile_checks_find_a_disagreeing_table_or_short_length(bad_req):
+    """A prefix tile of 40 requests (checked 32 requests per batch of loads):
+    a disagreeing prefix entry, or a length that does not cover the prefix, in
+    the first or a later batch sets the status; no NaN reaches any row."""
+    w = shared_case(40, 4, 4, 64, 16, [5 + 3 * i for i in range(40)], torch.float16, seed=23)
+    tables = w.block_tables.clone()
+    tables[bad_req, 7] = tables[bad_req, int(w.context_lens[bad_req]) // 16]
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out = run(w, 16, status, tables=tables)
+    assert kvp.kvp_read_status(status) == kvp.KVP_ERR_BAD_BLOCK
+    g = out.double().cpu().numpy()
+    assert np.isfinite(g).all()
+    assert (g[bad_req] == 0).all()
+    lens = w.context_lens.clone()
+    lens[bad_req] = 16 * 16 - 3
+    status.zero_()
+    out = run(w, 16, status, lens=lens)
+    assert kvp.kvp_read_status(status) == kvp.KVP_ERR_BAD_BLOCK
+    assert np.isfinite(out.double().cpu().numpy()).all()
+
+
 def test_lengths_that_do_not_cover_the_prefix_set_status():
     w = shared_case(3, 8, 8, 64, 16, [10, 20, 30], torch.float16, seed=22)
     lens = w.context_lens.clone()
